@@ -1,0 +1,39 @@
+"""Float64 CPU oracle of the tensor-parallel decoder linear block.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product path imports this package:
+only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg (``--impl reference`` and the ``cpu_baseline`` object) may call it. It
+shares no code with the CUDA library; the only common dependency is the
+seeded input generator in ``workloads/``, which holds no block arithmetic.
+
+Sources, cited by page title and section throughout:
+
+* [UC]  "Tensor & pipeline parallelism" (Undercurrent internals, vLLM
+        parallelism page): what the capture hooks see and how records are
+        keyed and ordered.
+* [VCR] "vLLM Code Reading (Section 5): GPUWorker.execute_model 与 PP/TP 通信",
+        sections 11-14: column/row split identities, attention and MLP TP
+        data flow.
+* [VSC] "vLLM 源码完全拆解（十一）：模型并行与 Worker 层", sections on the
+        linear-layer split, ColumnParallelLinear, MergedColumnParallelLinear /
+        QkvParallelLinear, RowParallelLinear and the column-row block.
+* [MLX] mlxcel manual "Tensor Parallelism": Weight Sharding Strategies,
+        GQA-Aware Attention Sharding.
+
+Every function computes in float64 from bf16 inputs converted exactly. Where
+the block has a plain definition (the unsharded Y = XW, SiLU, RMSNorm, row
+selection) the oracle is that definition; the sharded variants
+(``column_parallel``, ``row_parallel``, ``mlp_block_tp``, ``qkv_parallel``,
+``o_proj_parallel``) restate the pages' split algebra and exist to pin the
+invariants the pages fix.
+
+Parity status: every function here is pinned by tests in
+``tests/test_oracle.py`` (brute force, closed forms, library routines,
+page-printed head counts in ``tests/golden/``). None is "parity unpinned".
+"""
+from .tp_block import (  # noqa: F401
+    bf16_to_f64, linear, column_parallel, row_parallel, silu, silu_mul, rms_norm,
+    add_rms_norm, mlp_block, mlp_block_tp, mlp_layer, gqa_partition, qkv_shard_rows,
+    qkv_parallel, o_proj_parallel, divide,
+)
+from .capture import capture_rows, pack_key  # noqa: F401
