@@ -1,0 +1,197 @@
+/*
+ * tp_linear.h -- C ABI of libtplinear.so: a Megatron-style tensor-parallel
+ * decoder linear block on one GB300 (sm_103a).
+ *
+ * The block is the column-parallel / row-parallel pair the pages describe:
+ *   - "vLLM 源码完全拆解（十一）：模型并行与 Worker 层" (sections on the split
+ *     of one matmul, ColumnParallelLinear, MergedColumnParallelLinear /
+ *     QkvParallelLinear, RowParallelLinear and the column-row block);
+ *   - "vLLM Code Reading (Section 5)", sections 11-14 (column/row split
+ *     identities; attention and MLP TP data flow);
+ *   - "Tensor & pipeline parallelism" (Undercurrent internals): what the
+ *     capture hooks see (post-reduce, full tensors) and how records are keyed.
+ *
+ * The t tensor-parallel shards are a logical weight layout held on one GPU.
+ * The all-reduce that follows a row-parallel layer on t GPUs becomes an
+ * on-chip reduction of the t per-shard partial sums (tensor-memory
+ * accumulation across the shards' K ranges, or a deterministic split-K fix-up
+ * in fp32); there is no inter-GPU collective.
+ *
+ * Conventions shared by every call:
+ *   - Weights are bf16 in nn.Linear layout [out_features, in_features],
+ *     row-major; activations are bf16 row-major. All GEMMs multiply bf16,
+ *     accumulate in fp32 and round the result to bf16 (nearest-even).
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise,
+ *     and must be 16-byte aligned (tensor-memory-access copies need it).
+ *   - The library never allocates, frees or synchronises. Calls only enqueue
+ *     work on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *     Errors found on the host are returned; errors found by a kernel are
+ *     written to the workspace status word (see tp_workspace_size) and
+ *     become visible after the caller synchronises.
+ *   - Return value: TP_OK (0) or a negative TP_ERR_* code; tp_last_error()
+ *     then holds a message (thread-local).
+ *   - T = 0 tokens is legal everywhere and enqueues nothing (a step with no
+ *     scheduled tokens runs no forward pass).
+ */
+#ifndef TP_LINEAR_H
+#define TP_LINEAR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TP_OK 0
+#define TP_ERR_ARG (-1)         /* null / misaligned pointer, bad enum, workspace too small */
+#define TP_ERR_SHAPE (-2)       /* a size that does not divide (the pages' divide()), T < 0 */
+#define TP_ERR_UNSUPPORTED (-3) /* legal per the pages but not built (e.g. t not a power of 2) */
+#define TP_ERR_CUDA (-4)        /* a CUDA runtime/driver call failed */
+#define TP_ERR_CAPACITY (-5)    /* device status: capture records exceeded capacity */
+#define TP_ERR_TIMEOUT (-6)     /* device status: a bounded on-chip wait gave up */
+
+typedef struct tp_linear tp_linear_t; /* opaque handle: metadata + prebuilt weight tensor maps */
+typedef void* tp_stream_t;            /* cudaStream_t */
+
+enum { TP_BLOCK_MLP = 0, TP_BLOCK_ATTN_PROJ = 1 };
+enum { TP_FLAG_HAS_NORM = 1 };        /* MLP: fused residual add + RMSNorm in front of gate_up */
+
+typedef struct {
+  int32_t kind;          /* TP_BLOCK_MLP or TP_BLOCK_ATTN_PROJ */
+  int32_t t;             /* logical tensor-parallel size: 1, 2, 4 or 8 */
+  int64_t hidden;        /* H */
+  int64_t intermediate;  /* MLP: I, I % t == 0, (I / t) % 8 == 0 */
+  int32_t n_q_heads;     /* ATTN: nq % t == 0 */
+  int32_t n_kv_heads;    /* ATTN: nkv % t == 0, or t % nkv == 0 (kv heads replicated) */
+  int32_t head_dim;      /* ATTN: hd % 8 == 0 */
+  float rms_eps;         /* MLP with TP_FLAG_HAS_NORM */
+  int32_t flags;         /* TP_FLAG_* */
+  int32_t reserved;      /* must be 0 */
+} tp_config_t;
+
+/*
+ * Sizes of the two packed weight buffers the caller allocates for a handle.
+ *   MLP : col = gate_up  [t][2][I/t][H]   (shard r: its gate rows, then its up rows)
+ *         row = down     [t][H][I/t]      (shard r: input columns r*I/t .. of W_down)
+ *   ATTN: col = qkv      [t][w_s][H]      (shard r: its q heads | k heads | v heads,
+ *                                          w_s = (nq/t + 2*kv_per_shard) * hd)
+ *         row = o_proj   [t][H][nq*hd/t]
+ * "MergedColumnParallelLinear" / "QkvParallelLinear" / "RowParallelLinear"
+ * (weight_loader: narrow(dim, rank * shard, shard)).
+ */
+int tp_packed_weight_bytes(const tp_config_t* cfg, int64_t* col_bytes, int64_t* row_bytes);
+
+/*
+ * Validate `cfg`, pack the unsharded weights into the shard layout above (on
+ * `stream`) and return a handle. w_full: MLP {W_gate [I,H], W_up [I,H],
+ * W_down [H,I]}, n_w = 3; ATTN {W_q [nq*hd,H], W_k [nkv*hd,H], W_v [nkv*hd,H],
+ * W_o [H,nq*hd]}, n_w = 4. gamma: RMSNorm weight [H] bf16 (MLP with
+ * TP_FLAG_HAS_NORM), else NULL. The handle borrows w_col_packed, w_row_packed
+ * and gamma for its lifetime; w_full may be freed once `stream` has passed the
+ * packing. The shard count follows divide(): a remainder is TP_ERR_SHAPE.
+ */
+int tp_linear_create(const tp_config_t* cfg, const void* const* w_full, int32_t n_w,
+                     void* w_col_packed, void* w_row_packed, const void* gamma,
+                     tp_stream_t stream, tp_linear_t** out);
+int tp_linear_destroy(tp_linear_t* h);
+
+/*
+ * Workspace bytes a forward call with at most `max_tokens` tokens needs.
+ * The workspace is caller-owned device memory that must be ZERO-FILLED before
+ * its first use with a handle; afterwards the kernels leave it consistent
+ * (split-K arrival counters reset themselves). Bytes [0, 4) are the device
+ * status word: int32, 0 = ok, else a TP_ERR_* code written by a kernel
+ * (sticky until the caller clears it). Holds the normalised input, the
+ * shard-major intermediate h [t][T][I/t] and fp32 split-K partials.
+ * One workspace must not be used by two calls that may run concurrently.
+ */
+int tp_workspace_size(const tp_linear_t* h, int64_t max_tokens, int64_t* bytes);
+
+/*
+ * MLP half of a decoder layer ("Tensor & pipeline parallelism": mlp_out,
+ * residual_stream; "vLLM Code Reading (Section 5)" §14):
+ *   with TP_FLAG_HAS_NORM: r = x_in + residual_in; x = RMSNorm(r) * gamma
+ *   else:                  x = x_in;  r = residual_in (may be NULL)
+ *   h_r = silu(x W_gate,r^T) * (x W_up,r^T)            (column-parallel, per shard)
+ *   mlp_out = sum_r h_r W_down,r^T                      (row-parallel, reduced on chip)
+ *   residual_stream = mlp_out + r                       (if residual_stream != NULL)
+ * x_in, residual_in, residual_out, mlp_out, residual_stream: [T, H] bf16.
+ * residual_out (required with norm, ignored without) receives r in bf16.
+ */
+int tp_mlp_forward(tp_linear_t* h, int64_t T, const void* x_in, const void* residual_in,
+                   void* residual_out, void* mlp_out, void* residual_stream,
+                   void* workspace, int64_t workspace_bytes, tp_stream_t stream);
+
+/*
+ * The steps of tp_mlp_forward, one call each (same semantics, same kernels):
+ *   tp_add_rms_norm : residual_out = a + residual_in; x_out = RMSNorm(residual_out) * gamma.
+ *                     a, residual_in, residual_out, x_out [T, H]; gamma [H]. Any H % 8 == 0.
+ *   tp_gate_up_forward: h_out [t][T][I/t] = silu(x W_gate,r^T) * (x W_up,r^T) per shard r.
+ *   tp_down_forward : mlp_out = sum_r h_in[r] W_down,r^T; residual_stream = mlp_out + residual.
+ */
+int tp_add_rms_norm(int64_t T, int64_t H, const void* a, const void* residual_in, const void* gamma,
+                    float eps, void* residual_out, void* x_out, tp_stream_t stream);
+int tp_gate_up_forward(tp_linear_t* h, int64_t T, const void* x, void* h_out,
+                       void* workspace, int64_t workspace_bytes, tp_stream_t stream);
+int tp_down_forward(tp_linear_t* h, int64_t T, const void* h_in, const void* residual,
+                    void* mlp_out, void* residual_stream,
+                    void* workspace, int64_t workspace_bytes, tp_stream_t stream);
+
+/*
+ * Attention projections ("vLLM Code Reading (Section 5)" §13;
+ * "Tensor & pipeline parallelism": attn_out):
+ *   qkv_out [t][T][w_s] = per shard r: x [Wq_r; Wk_r; Wv_r]^T    (not gathered)
+ *   o_out   [T, H]      = sum_r attn_in[r] Wo_r^T                 (reduced on chip)
+ * x [T, H]; attn_in [t][T][nq*hd/t] (shard r's local heads). Either half may be
+ * skipped by passing NULL for both of its pointers.
+ */
+int tp_attn_proj_forward(tp_linear_t* h, int64_t T, const void* x, void* qkv_out,
+                         const void* attn_in, void* o_out,
+                         void* workspace, int64_t workspace_bytes, tp_stream_t stream);
+
+/*
+ * Activation capture ("Tensor & pipeline parallelism": What the adapter hooks,
+ * Duplicate records across TP ranks, Merging records): records every row i of
+ * each tensor whose key (row_req[i] << 32) | (uint32)row_pos[i] is among the
+ * n_sel selector keys (any order; duplicates give one record; keys that match
+ * no row give none). Records are grouped by tensor in the order given, rows
+ * ascending within a tensor. Record j: hdr_out[j] = {request_id, token_pos,
+ * tensor_type, layer, row, 0} and rows_out[j] = tensors[k][row] (H bf16,
+ * bit-exact). *n_out_dev (device int64) receives the total number of records
+ * n_tensors * n_match, even when it exceeds `capacity`; only records with
+ * j < capacity are written, and TP_ERR_CAPACITY is written to the status word
+ * (workspace bytes [0,4)) when it overflows. Call it after the reducing layer
+ * has been enqueued: stream order makes it read the reduced tensors.
+ * row_req, row_pos: [T] int32; sel_keys: [n_sel] int64; tensors: HOST array
+ * of n_tensors device pointers to [T, H] bf16; tensor_types: HOST array.
+ */
+typedef struct {
+  int32_t request_id, token_pos, tensor_type, layer, row, pad;
+} tp_record_hdr_t;
+
+int tp_capture_workspace_size(int64_t T, int64_t n_sel, int64_t* bytes);
+int tp_capture_rows(int64_t T, int64_t H, const int32_t* row_req, const int32_t* row_pos,
+                    const int64_t* sel_keys, int64_t n_sel, int32_t n_tensors,
+                    const void* const* tensors, const int32_t* tensor_types, int32_t layer,
+                    tp_record_hdr_t* hdr_out, void* rows_out, int64_t capacity,
+                    int64_t* n_out_dev, void* workspace, int64_t workspace_bytes,
+                    tp_stream_t stream);
+
+/* Thread-local message describing the last non-zero return on this thread. */
+const char* tp_last_error(void);
+
+/*
+ * Plan of the GEMM launches a forward call with T tokens would make, for
+ * inspection and benchmarks: writes up to 2 entries of
+ * {swap_ab, block_n, splits, units, grid} for the column-parallel and the
+ * row-parallel GEMM. Returns the number written.
+ */
+typedef struct {
+  int32_t swap_ab, block_n, splits, units, grid, stages;
+} tp_gemm_plan_t;
+int tp_describe_plan(const tp_linear_t* h, int64_t T, tp_gemm_plan_t* plans, int32_t max_plans);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TP_LINEAR_H */

@@ -1,0 +1,273 @@
+"""Thin ctypes binding of libtplinear.so (include/tp_linear.h).
+
+Argument marshalling only: torch tensors become device pointers and the
+current CUDA stream becomes the stream argument; torch allocates the outputs,
+packed weights and workspaces. Every step of the block runs in the library's
+CUDA kernels. There is no fallback: if the library is missing or cannot load,
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtplinear.so")
+
+TP_OK = 0
+TP_ERR_ARG, TP_ERR_SHAPE, TP_ERR_UNSUPPORTED, TP_ERR_CUDA, TP_ERR_CAPACITY, TP_ERR_TIMEOUT = (
+    -1, -2, -3, -4, -5, -6)
+TP_BLOCK_MLP, TP_BLOCK_ATTN_PROJ = 0, 1
+TP_FLAG_HAS_NORM = 1
+
+ABI_SYMBOLS = (
+    "tp_packed_weight_bytes", "tp_linear_create", "tp_linear_destroy", "tp_workspace_size",
+    "tp_mlp_forward", "tp_add_rms_norm", "tp_gate_up_forward", "tp_down_forward",
+    "tp_attn_proj_forward", "tp_capture_workspace_size", "tp_capture_rows", "tp_last_error",
+    "tp_describe_plan",
+)
+
+
+class TPError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"tp_linear error {code}: {msg}")
+        self.code = code
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("t", ctypes.c_int32), ("hidden", ctypes.c_int64),
+                ("intermediate", ctypes.c_int64), ("n_q_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("rms_eps", ctypes.c_float), ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class GemmPlan(ctypes.Structure):
+    _fields_ = [("swap_ab", ctypes.c_int32), ("block_n", ctypes.c_int32), ("splits", ctypes.c_int32),
+                ("units", ctypes.c_int32), ("grid", ctypes.c_int32), ("stages", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load the in-tree library once (raises if it is not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    PI64 = ctypes.POINTER(ctypes.c_int64)
+    sig = {
+        "tp_packed_weight_bytes": [ctypes.POINTER(Config), PI64, PI64],
+        "tp_linear_create": [ctypes.POINTER(Config), ctypes.POINTER(P), I32, P, P, P, P,
+                             ctypes.POINTER(P)],
+        "tp_linear_destroy": [P],
+        "tp_workspace_size": [P, I64, PI64],
+        "tp_mlp_forward": [P, I64, P, P, P, P, P, P, I64, P],
+        "tp_add_rms_norm": [I64, I64, P, P, P, F, P, P, P],
+        "tp_gate_up_forward": [P, I64, P, P, P, I64, P],
+        "tp_down_forward": [P, I64, P, P, P, P, P, I64, P],
+        "tp_attn_proj_forward": [P, I64, P, P, P, P, P, I64, P],
+        "tp_capture_workspace_size": [I64, I64, PI64],
+        "tp_capture_rows": [I64, I64, P, P, P, I64, I32, ctypes.POINTER(P), ctypes.POINTER(I32),
+                            I32, P, P, I64, P, P, I64, P],
+        "tp_describe_plan": [P, I64, ctypes.POINTER(GemmPlan), I32],
+    }
+    for name, args in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    L.tp_last_error.argtypes = []
+    L.tp_last_error.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _check(rc: int) -> int:
+    if rc < 0:
+        raise TPError(rc, lib().tp_last_error().decode(errors="replace"))
+    return rc
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _bf16(t: torch.Tensor, name: str) -> torch.Tensor:
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor")
+    return t
+
+
+def make_config(kind: int, t: int, hidden: int, intermediate: int = 0, n_q_heads: int = 0,
+                n_kv_heads: int = 0, head_dim: int = 0, rms_eps: float = 1e-5, flags: int = 0) -> Config:
+    return Config(kind, t, hidden, intermediate, n_q_heads, n_kv_heads, head_dim, rms_eps, flags, 0)
+
+
+def packed_weight_bytes(cfg: Config):
+    a, b = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().tp_packed_weight_bytes(ctypes.byref(cfg), ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def capture_workspace_size(T: int, n_sel: int) -> int:
+    b = ctypes.c_int64()
+    _check(lib().tp_capture_workspace_size(T, n_sel, ctypes.byref(b)))
+    return b.value
+
+
+class TPLinear:
+    """One tensor-parallel block (MLP or attention projections) on the current GPU.
+
+    ``weights``: MLP (w_gate [I,H], w_up [I,H], w_down [H,I]); attention
+    (w_q, w_k, w_v, w_o), all bf16 CUDA tensors in nn.Linear layout. The
+    packed shard buffers are allocated here and owned by this object.
+    """
+
+    def __init__(self, cfg: Config, weights: Sequence[torch.Tensor], gamma: Optional[torch.Tensor] = None,
+                 stream=None):
+        L = lib()
+        self.cfg = cfg
+        col, row = packed_weight_bytes(cfg)
+        dev = weights[0].device
+        self.w_col = torch.empty(col // 2, dtype=torch.bfloat16, device=dev)
+        self.w_row = torch.empty(row // 2, dtype=torch.bfloat16, device=dev)
+        self.gamma = None if gamma is None else _bf16(gamma, "gamma")
+        ws = [_bf16(w, "weight") for w in weights]
+        arr = (ctypes.c_void_p * len(ws))(*[w.data_ptr() for w in ws])
+        h = ctypes.c_void_p()
+        _check(L.tp_linear_create(ctypes.byref(cfg), arr, len(ws), _ptr(self.w_col), _ptr(self.w_row),
+                                  _ptr(self.gamma), _stream(stream), ctypes.byref(h)))
+        self.handle = h
+        self._ws = None
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            lib().tp_linear_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ------------------------------------------------------------------ workspace
+    def workspace_size(self, max_tokens: int) -> int:
+        b = ctypes.c_int64()
+        _check(lib().tp_workspace_size(self.handle, max_tokens, ctypes.byref(b)))
+        return b.value
+
+    def workspace(self, max_tokens: int) -> torch.Tensor:
+        """A zero-filled workspace for calls of up to max_tokens tokens (cached, grows on demand)."""
+        need = self.workspace_size(max_tokens)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.zeros(need, dtype=torch.uint8, device=self.w_col.device)
+        return self._ws
+
+    def plan(self, T: int):
+        arr = (GemmPlan * 2)()
+        n = _check(lib().tp_describe_plan(self.handle, T, arr, 2))
+        return [{k: getattr(arr[i], k) for k, _ in GemmPlan._fields_} for i in range(n)]
+
+    # ------------------------------------------------------------------ MLP
+    def mlp_forward(self, x: torch.Tensor, residual: Optional[torch.Tensor] = None,
+                    residual_stream: bool = True, out: Optional[dict] = None, ws: Optional[torch.Tensor] = None,
+                    stream=None) -> dict:
+        T, H = x.shape
+        norm = bool(self.cfg.flags & TP_FLAG_HAS_NORM)
+        o = out if out is not None else {}
+        if "mlp_out" not in o:
+            o["mlp_out"] = torch.empty_like(x)
+        if norm and "residual_out" not in o:
+            o["residual_out"] = torch.empty_like(x)
+        if residual_stream and residual is not None and "residual_stream" not in o:
+            o["residual_stream"] = torch.empty_like(x)
+        ws = self.workspace(T) if ws is None else ws
+        _check(lib().tp_mlp_forward(self.handle, T, _ptr(_bf16(x, "x")), _ptr(residual), _ptr(o.get("residual_out")),
+                                    _ptr(o["mlp_out"]), _ptr(o.get("residual_stream")), _ptr(ws), ws.numel(),
+                                    _stream(stream)))
+        return o
+
+    def gate_up(self, x: torch.Tensor, h_out: Optional[torch.Tensor] = None, ws=None, stream=None) -> torch.Tensor:
+        T = x.shape[0]
+        t, Is = self.cfg.t, self.cfg.intermediate // self.cfg.t
+        h_out = torch.empty(t, T, Is, dtype=torch.bfloat16, device=x.device) if h_out is None else h_out
+        ws = self.workspace(T) if ws is None else ws
+        _check(lib().tp_gate_up_forward(self.handle, T, _ptr(_bf16(x, "x")), _ptr(h_out), _ptr(ws), ws.numel(),
+                                        _stream(stream)))
+        return h_out
+
+    def down(self, h_in: torch.Tensor, residual: Optional[torch.Tensor] = None, out=None, stream_out=None,
+             ws=None, stream=None):
+        T = h_in.shape[1]
+        H = self.cfg.hidden
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=h_in.device) if out is None else out
+        if residual is not None and stream_out is None:
+            stream_out = torch.empty_like(out)
+        ws = self.workspace(T) if ws is None else ws
+        _check(lib().tp_down_forward(self.handle, T, _ptr(_bf16(h_in, "h_in")), _ptr(residual), _ptr(out),
+                                     _ptr(stream_out), _ptr(ws), ws.numel(), _stream(stream)))
+        return out, stream_out
+
+    # ------------------------------------------------------------------ attention projections
+    def attn_proj_forward(self, x: Optional[torch.Tensor], attn_in: Optional[torch.Tensor],
+                          qkv_out=None, o_out=None, ws=None, stream=None):
+        c = self.cfg
+        T = (x if x is not None else attn_in[0]).shape[0]
+        q_per = c.n_q_heads // c.t
+        kv_per = 1 if c.t >= c.n_kv_heads else c.n_kv_heads // c.t
+        w_s = (q_per + 2 * kv_per) * c.head_dim
+        dev = self.w_col.device
+        if x is not None and qkv_out is None:
+            qkv_out = torch.empty(c.t, T, w_s, dtype=torch.bfloat16, device=dev)
+        if attn_in is not None and o_out is None:
+            o_out = torch.empty(T, c.hidden, dtype=torch.bfloat16, device=dev)
+        ws = self.workspace(T) if ws is None else ws
+        _check(lib().tp_attn_proj_forward(self.handle, T, _ptr(x), _ptr(qkv_out if x is not None else None),
+                                          _ptr(attn_in), _ptr(o_out if attn_in is not None else None),
+                                          _ptr(ws), ws.numel(), _stream(stream)))
+        return qkv_out, o_out
+
+
+def add_rms_norm(a: torch.Tensor, residual: torch.Tensor, gamma: torch.Tensor, eps: float,
+                 residual_out=None, x_out=None, stream=None):
+    T, H = a.shape
+    residual_out = torch.empty_like(a) if residual_out is None else residual_out
+    x_out = torch.empty_like(a) if x_out is None else x_out
+    _check(lib().tp_add_rms_norm(T, H, _ptr(_bf16(a, "a")), _ptr(_bf16(residual, "residual")),
+                                 _ptr(_bf16(gamma, "gamma")), eps, _ptr(residual_out), _ptr(x_out),
+                                 _stream(stream)))
+    return x_out, residual_out
+
+
+def capture_rows(row_req: torch.Tensor, row_pos: torch.Tensor, sel_keys: torch.Tensor,
+                 tensors: Sequence[torch.Tensor], tensor_types: Sequence[int], layer: int, capacity: int,
+                 ws: Optional[torch.Tensor] = None, stream=None):
+    """Returns (headers int32 [capacity, 6], rows [capacity, H], n_out int64 device scalar, ws)."""
+    T, H = tensors[0].shape
+    dev = tensors[0].device
+    hdr = torch.empty(max(capacity, 1), 6, dtype=torch.int32, device=dev)
+    rows = torch.empty(max(capacity, 1), H, dtype=torch.bfloat16, device=dev)
+    n_out = torch.zeros(1, dtype=torch.int64, device=dev)
+    need = capture_workspace_size(T, sel_keys.numel())
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev) if ws is None else ws
+    arr = (ctypes.c_void_p * len(tensors))(*[_bf16(t, "tensor").data_ptr() for t in tensors])
+    types = (ctypes.c_int32 * len(tensors))(*tensor_types)
+    _check(lib().tp_capture_rows(T, H, _ptr(row_req), _ptr(row_pos), _ptr(sel_keys), sel_keys.numel(),
+                                 len(tensors), arr, types, layer, _ptr(hdr), _ptr(rows), capacity,
+                                 _ptr(n_out), _ptr(ws), ws.numel(), _stream(stream)))
+    return hdr, rows, n_out, ws

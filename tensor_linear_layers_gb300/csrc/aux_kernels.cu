@@ -1,0 +1,301 @@
+// Memory-bound kernels of the block: fused residual add + RMSNorm, the
+// activation-capture gather, and create-time weight packing into the shard
+// layout.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace tpl {
+
+// ======================================================================= RMSNorm
+// One CTA per token row. r = a + residual (fp32, rounded to bf16 and stored as
+// the updated residual); x = r_bf16 * rsqrt(mean(r_bf16^2) + eps) * gamma.
+// "Tensor & pipeline parallelism", residual_stream: post_attention_layernorm
+// folds the residual add and the norm together and returns both tensors.
+constexpr int kNormThreads = 256;
+constexpr int kNormMaxVec = 8;  // 16-byte vectors per thread: H <= 8 * 8 * 256
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(b[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ uint4 f32_to_bf16x8(const float* f) {
+  uint4 v;
+  __nv_bfloat162* b = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) b[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return v;
+}
+
+__global__ void __launch_bounds__(kNormThreads)
+    add_rms_norm_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ res,
+                        const __nv_bfloat16* __restrict__ gamma, float eps, int H,
+                        __nv_bfloat16* __restrict__ res_out, __nv_bfloat16* __restrict__ x_out) {
+  const int row = blockIdx.x;
+  const int nvec = H >> 3;
+  const size_t roff = (size_t)row * H;
+  const uint4* av = reinterpret_cast<const uint4*>(a + roff);
+  const uint4* rv = reinterpret_cast<const uint4*>(res + roff);
+  uint4* ro = reinterpret_cast<uint4*>(res_out + roff);
+  float r[kNormMaxVec][8];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < kNormMaxVec; ++k) {
+    const int v = threadIdx.x + k * kNormThreads;
+    if (v < nvec) {
+      float fa[8], fr[8];
+      bf16x8_to_f32(__ldg(av + v), fa);
+      bf16x8_to_f32(__ldg(rv + v), fr);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) fa[i] += fr[i];
+      const uint4 packed = f32_to_bf16x8(fa);
+      ro[v] = packed;
+      bf16x8_to_f32(packed, r[k]);  // the stored (bf16) residual is what gets normalised
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss += r[k][i] * r[k][i];
+    }
+  }
+  __shared__ float red[kNormThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = threadIdx.x < kNormThreads / 32 ? red[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (threadIdx.x == 0) red[0] = t;
+  }
+  __syncthreads();
+  const float inv = rsqrtf(red[0] / (float)H + eps);
+  const uint4* gv = reinterpret_cast<const uint4*>(gamma);
+  uint4* xo = reinterpret_cast<uint4*>(x_out + roff);
+#pragma unroll
+  for (int k = 0; k < kNormMaxVec; ++k) {
+    const int v = threadIdx.x + k * kNormThreads;
+    if (v < nvec) {
+      float g[8], o[8];
+      bf16x8_to_f32(__ldg(gv + v), g);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = r[k][i] * inv * g[i];
+      xo[v] = f32_to_bf16x8(o);
+    }
+  }
+}
+
+cudaError_t launch_add_rms_norm(int T, int H, const void* a, const void* res, const void* gamma,
+                                float eps, void* res_out, void* x_out, cudaStream_t st) {
+  add_rms_norm_kernel<<<T, kNormThreads, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(a), static_cast<const __nv_bfloat16*>(res),
+      static_cast<const __nv_bfloat16*>(gamma), eps, H, static_cast<__nv_bfloat16*>(res_out),
+      static_cast<__nv_bfloat16*>(x_out));
+  return cudaGetLastError();
+}
+int max_norm_hidden() { return kNormMaxVec * 8 * kNormThreads; }
+
+// ======================================================================= capture
+// "Tensor & pipeline parallelism", What the adapter hooks / Duplicate records:
+// select rows whose (request_id, token_pos) key was registered, record them
+// per tensor in batch-row order; a key selected twice still yields one record.
+constexpr int kCapThreads = 1024;
+constexpr uint64_t kEmpty = 0xFFFFFFFFFFFFFFFFull;
+
+__device__ __forceinline__ uint64_t mix64(uint64_t k) {
+  // MurmurHash3 64-bit finaliser
+  k ^= k >> 33;
+  k *= 0xff51afd7ed558ccdull;
+  k ^= k >> 33;
+  k *= 0xc4ceb9fe1a85ec53ull;
+  k ^= k >> 33;
+  return k;
+}
+
+__device__ __forceinline__ uint64_t row_key(int req, int pos) {
+  return (static_cast<uint64_t>(static_cast<uint32_t>(req)) << 32) | static_cast<uint32_t>(pos);
+}
+
+__global__ void __launch_bounds__(kCapThreads)
+    capture_match_kernel(int T, const int32_t* __restrict__ row_req, const int32_t* __restrict__ row_pos,
+                         const int64_t* __restrict__ sel, int n_sel, uint64_t* gtable, int cap_log2,
+                         CaptureMeta meta, int64_t capacity, int64_t* n_out_dev,
+                         int32_t* match_rows, int32_t* n_match_ws, int* status) {
+  extern __shared__ uint64_t stable[];
+  uint64_t* table = gtable != nullptr ? gtable : stable;
+  const uint32_t cap = 1u << cap_log2;
+  const uint32_t mask = cap - 1u;
+  __shared__ int s_has_empty;
+  __shared__ int warp_cnt[kCapThreads / 32];
+  __shared__ int warp_off[kCapThreads / 32];
+  __shared__ int s_chunk;
+  __shared__ int s_running;
+  if (threadIdx.x == 0) {
+    s_has_empty = 0;
+    s_running = 0;
+  }
+  for (uint32_t i = threadIdx.x; i < cap; i += kCapThreads) table[i] = kEmpty;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n_sel; i += kCapThreads) {
+    const uint64_t key = static_cast<uint64_t>(sel[i]);
+    if (key == kEmpty) {
+      s_has_empty = 1;
+      continue;
+    }
+    uint32_t h = static_cast<uint32_t>(mix64(key)) & mask;
+    for (uint32_t probe = 0; probe < cap; ++probe) {
+      const unsigned long long prev =
+          atomicCAS(reinterpret_cast<unsigned long long*>(table + h), kEmpty, key);
+      if (prev == kEmpty || prev == key) break;
+      h = (h + 1u) & mask;
+    }
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  // rows in chunks of one CTA: flag, block-wide exclusive scan, order-preserving compaction
+  for (int base = 0; base < T; base += kCapThreads) {
+    const int i = base + threadIdx.x;
+    int hit = 0;
+    if (i < T) {
+      const uint64_t key = row_key(row_req[i], row_pos[i]);
+      if (key == kEmpty) {
+        hit = s_has_empty;
+      } else {
+        // volatile: the table was filled with atomics at L2 and must not be read from a stale L1 line
+        const volatile uint64_t* vt = table;
+        uint32_t h = static_cast<uint32_t>(mix64(key)) & mask;
+        for (uint32_t probe = 0; probe < cap; ++probe) {
+          const uint64_t v = vt[h];
+          if (v == key) {
+            hit = 1;
+            break;
+          }
+          if (v == kEmpty) break;
+          h = (h + 1u) & mask;
+        }
+      }
+    }
+    const unsigned ball = __ballot_sync(0xffffffffu, hit);
+    const int before = __popc(ball & ((1u << lane) - 1u));
+    if (lane == 0) warp_cnt[wid] = __popc(ball);
+    __syncthreads();
+    if (wid == 0) {
+      const int v = warp_cnt[lane];
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      warp_off[lane] = incl - v;
+      if (lane == 31) s_chunk = incl;
+    }
+    __syncthreads();
+    if (hit) match_rows[s_running + warp_off[wid] + before] = i;
+    __syncthreads();
+    if (threadIdx.x == 0) s_running += s_chunk;
+    __syncthreads();
+  }
+  const int n_match = s_running;
+  const int64_t n_rec = static_cast<int64_t>(meta.n_tensors) * n_match;
+  if (threadIdx.x == 0) {
+    *n_match_ws = n_match;
+    *n_out_dev = n_rec;
+    if (n_rec > capacity) atomicCAS(status, 0, kStatusCapacity);
+  }
+  const int64_t n_write = n_rec < capacity ? n_rec : capacity;
+  for (int64_t j = threadIdx.x; j < n_write; j += kCapThreads) {
+    const int k = static_cast<int>(j / n_match);
+    const int m = static_cast<int>(j - static_cast<int64_t>(k) * n_match);
+    const int row = match_rows[m];
+    int32_t* h = meta.hdr + j * 6;
+    h[0] = row_req[row];
+    h[1] = row_pos[row];
+    h[2] = meta.types[k];
+    h[3] = meta.layer;
+    h[4] = row;
+    h[5] = 0;
+  }
+}
+
+__global__ void __launch_bounds__(256)
+    capture_copy_kernel(int H, CaptureMeta meta, int64_t capacity, const int32_t* __restrict__ match_rows,
+                        const int32_t* __restrict__ n_match_ws, __nv_bfloat16* __restrict__ rows_out) {
+  const int n_match = *n_match_ws;
+  int64_t n_rec = static_cast<int64_t>(meta.n_tensors) * n_match;
+  if (n_rec > capacity) n_rec = capacity;
+  const int nvec = H >> 3;
+  for (int64_t j = blockIdx.x; j < n_rec; j += gridDim.x) {
+    const int k = static_cast<int>(j / n_match);
+    const int m = static_cast<int>(j - static_cast<int64_t>(k) * n_match);
+    const uint4* src = reinterpret_cast<const uint4*>(meta.tensors[k] + (size_t)match_rows[m] * H);
+    uint4* dst = reinterpret_cast<uint4*>(rows_out + (size_t)j * H);
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) dst[v] = __ldg(src + v);
+  }
+}
+
+cudaError_t launch_capture(int T, int H, const int32_t* row_req, const int32_t* row_pos,
+                           const int64_t* sel, int n_sel, uint64_t* gtable, int cap_log2,
+                           size_t table_smem, const CaptureMeta& meta, int64_t capacity,
+                           int64_t* n_out_dev, int32_t* match_rows, int32_t* n_match_ws, int* status,
+                           int copy_grid, cudaStream_t st) {
+  if (table_smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(capture_match_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(table_smem));
+    if (e != cudaSuccess) return e;
+  }
+  capture_match_kernel<<<1, kCapThreads, table_smem, st>>>(T, row_req, row_pos, sel, n_sel, gtable,
+                                                           cap_log2, meta, capacity, n_out_dev,
+                                                           match_rows, n_match_ws, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  capture_copy_kernel<<<copy_grid, 256, 0, st>>>(H, meta, capacity, match_rows, n_match_ws,
+                                                 static_cast<__nv_bfloat16*>(meta.rows_out));
+  return cudaGetLastError();
+}
+
+// ======================================================================= packing
+// Build the shard layout of a weight ("weight_loader": each rank narrows the
+// full checkpoint tensor to its shard). One CTA copies one packed row.
+__global__ void __launch_bounds__(128) pack_rows_kernel(PackSpec s, __nv_bfloat16* __restrict__ dst) {
+  const int64_t d = blockIdx.x;  // packed row
+  const __nv_bfloat16* src = nullptr;
+  if (s.mode == PACK_GATE_UP) {
+    // dst [t][2][Is][H]  <-  gate / up rows r*Is + i
+    const int64_t i = d % s.Is, g = (d / s.Is) % 2, r = d / (2 * s.Is);
+    src = s.src[g] + (r * s.Is + i) * s.width;
+  } else if (s.mode == PACK_ROW) {
+    // dst [t][N][Ks]  <-  W[n][r*Ks : (r+1)*Ks]   (W is [N][t*Ks])
+    const int64_t n = d % s.N, r = d / s.N;
+    src = s.src[0] + n * (s.t * s.width) + r * s.width;
+  } else {
+    // PACK_QKV: dst [t][ws][H], shard r = [q heads | k heads | v heads]
+    const int64_t c = d % s.ws, r = d / s.ws;
+    const int64_t qpart = (int64_t)s.q_per * s.hd, kvpart = (int64_t)s.kv_per * s.hd;
+    if (c < qpart) {
+      src = s.src[0] + (r * qpart + c) * s.width;
+    } else {
+      const int64_t cc = (c - qpart) % kvpart;
+      const int which = (c - qpart) < kvpart ? 1 : 2;
+      const int64_t head = (s.rep > 1) ? (r / s.rep) : (r * s.kv_per + cc / s.hd);
+      src = s.src[which] + (head * s.hd + cc % s.hd) * s.width;
+    }
+  }
+  const uint4* sv = reinterpret_cast<const uint4*>(src);
+  uint4* dv = reinterpret_cast<uint4*>(dst + d * s.width);
+  for (int v = threadIdx.x; v < s.width / 8; v += blockDim.x) dv[v] = sv[v];
+}
+
+cudaError_t launch_pack(const PackSpec& s, int64_t rows, void* dst, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  pack_rows_kernel<<<static_cast<unsigned>(rows), 128, 0, st>>>(s, static_cast<__nv_bfloat16*>(dst));
+  return cudaGetLastError();
+}
+
+}  // namespace tpl

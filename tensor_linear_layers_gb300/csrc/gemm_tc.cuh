@@ -1,0 +1,503 @@
+// Persistent, warp-specialised tcgen05 GEMM engine for the tensor-parallel
+// linear block.
+//
+//   warp 0      : TMA producer (one elected thread) filling a ring of shared-
+//                 memory stages, each guarded by a full/empty mbarrier pair
+//   warp 1      : tensor-memory allocator + MMA issuer (one elected thread)
+//   warps 2..5  : epilogue: tcgen05.ld from the fp32 accumulator, fused
+//                 SiLU*mul / residual add, bf16 stores; split-K fix-up
+//
+// The accumulator lives in tensor memory, double-buffered so the epilogue of
+// one tile overlaps the main loop of the next. Operand A feeds the UMMA M side
+// (128 rows per accumulator, NA accumulators), operand B the N side (BN rows).
+//
+//   SWAP = false (prefill): A = activations (128 tokens), B = weights (BN = 256).
+//   SWAP = true  (decode) : A = weights (NA x 128 rows), B = activations (BN >= tokens).
+//
+// Kinds:
+//   KIND_GATE_UP : column-parallel merged gate/up. A weight tile is 128 gate
+//                  rows + the matching 128 up rows of one shard, so one
+//                  thread holds g and u of the same intermediate feature and
+//                  applies silu(g) * u in registers. Output h [t][T][I/t].
+//   KIND_COL     : column-parallel plain store, output split per shard
+//                  [t][T][w_s] (QKV by head).
+//   KIND_ROW     : row-parallel: the K loop runs over all t shards in turn,
+//                  so the shards' partial sums add up in the accumulator (the
+//                  on-chip replacement of the all-reduce); with split-K the
+//                  fp32 partials of the splits are added by the last split to
+//                  arrive, in ascending split order (deterministic).
+//                  Output y [T][N], optional y + residual.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include "ptx.cuh"
+
+namespace tpl {
+
+enum GemmKind : int { KIND_GATE_UP = 0, KIND_COL = 1, KIND_ROW = 2 };
+
+// status codes written by kernels (mirror TP_ERR_* of the public header)
+constexpr int kStatusTimeout = -6;
+
+struct GemmParams {
+  int T;             // tokens
+  int m_tiles;       // tiles on the A (UMMA M) side
+  int n_tiles;       // tiles on the B (UMMA N) side
+  int splits;        // K splits per tile
+  int units;         // m_tiles * n_tiles * splits
+  int nkb;           // 64-wide k-blocks per tile (all shards for KIND_ROW)
+  int kbs;           // k-blocks per shard (KIND_ROW)
+  int nb;            // KIND_GATE_UP: 128-row blocks per shard
+  int group_m;       // raster group along M (SWAP = false)
+  int Is;            // KIND_GATE_UP: I / t
+  int n_out;         // KIND_COL / KIND_ROW: output features
+  int ws_out;        // KIND_COL: features per output shard (== n_out if unsplit)
+  __nv_bfloat16* out;
+  __nv_bfloat16* out2;         // KIND_ROW: y + resid (nullable)
+  const __nv_bfloat16* resid;  // KIND_ROW: residual [T][n_out]
+  float* partials;             // split-K fp32 partials
+  int* counters;               // split-K arrival counters, one per tile
+  int* status;                 // device status word
+  unsigned long long timeout_ns;
+};
+
+template <bool SWAP, int KIND, int BN, int NA>
+struct GemmShape {
+  static constexpr int kABytes = NA * 128 * 128;  // NA x 128 rows x 64 bf16
+  static constexpr int kBBytes = BN * 128;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kSmemBudget = 221 * 1024;
+  static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
+  static constexpr int kAccCols = NA * BN;  // tensor-memory columns per accumulator buffer
+  static constexpr int kTmemNeed = 2 * kAccCols;
+  static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
+                                   : kTmemNeed <= 256 ? 256 : 512;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  // epilogue column groups: GATE_UP pairs (g, u) at distance kUOff
+  static constexpr int kNG = (KIND == KIND_GATE_UP) ? (SWAP ? BN : 128) : BN;
+  static constexpr int kUOff = SWAP ? BN : 128;
+  static constexpr int kCh = kNG >= 32 ? 32 : 16;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
+  static_assert(KIND != KIND_GATE_UP || (SWAP ? NA == 2 : (NA == 1 && BN == 256)), "gate/up tile");
+  static_assert(kStages >= 2, "pipeline depth");
+  static_assert(kTmemNeed <= 512, "tensor memory");
+};
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <bool SWAP, int KIND, int BN, int NA>
+__global__ void __launch_bounds__(192, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_act,
+                   const __grid_constant__ CUtensorMap map_w, const GemmParams p) {
+  using S = GemmShape<SWAP, KIND, BN, NA>;
+  constexpr int STAGES = S::kStages;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_addr);
+  const uint32_t bar0 = base + STAGES * S::kStageBytes;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint8_t* misc = base_ptr + STAGES * S::kStageBytes + 8 * (2 * STAGES + 5);
+  volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(misc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 4);
+  volatile int* s_last = reinterpret_cast<volatile int*>(misc + 8);
+  volatile int* s_ok = reinterpret_cast<volatile int*>(misc + 12);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 4);
+    }
+    mbar_init(done_bar, 1);
+    *s_abort = 0;
+    *s_last = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&map_act);
+    prefetch_tensormap(&map_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(s_tmem)), S::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+
+  // unit -> (tile m, tile n, split)
+  auto decode_unit = [&](int u, int& tm, int& tn, int& sp) {
+    const int tile = u / p.splits;
+    sp = u - tile * p.splits;
+    if (!SWAP && p.group_m > 1) {
+      const int group_size = p.group_m * p.n_tiles;
+      const int g = tile / group_size;
+      const int first_m = g * p.group_m;
+      const int rem = p.m_tiles - first_m;
+      const int gm = rem < p.group_m ? rem : p.group_m;
+      const int in_g = tile - g * group_size;
+      tm = first_m + in_g % gm;
+      tn = in_g / gm;
+    } else {
+      tm = tile / p.n_tiles;
+      tn = tile - tm * p.n_tiles;
+    }
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_a = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, last_phase_bits = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        int tm, tn, sp;
+        decode_unit(u, tm, tn, sp);
+        const int kb0 = (int)((long long)sp * p.nkb / p.splits);
+        const int kb1 = (int)((long long)(sp + 1) * p.nkb / p.splits);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, p.timeout_ns)) {
+            if (!*s_abort) {
+              atomicExch(p.status, kStatusTimeout);
+              *s_abort = 1;
+            }
+            ok = false;
+            break;
+          }
+          const uint32_t sa = base + stage * S::kStageBytes;
+          const uint32_t sb = sa + S::kABytes;
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, S::kStageBytes);
+          int kx = kb * 64, shard = 0;
+          if (KIND == KIND_ROW) {
+            shard = kb / p.kbs;
+            kx = (kb - shard * p.kbs) * 64;
+          }
+          if (!SWAP) {
+            // A: 128 tokens of the activation
+            tma_load_4d(sa, &map_act, fb, kx, tm * 128, 0, shard, pol_a);
+            // B: weight rows
+            if (KIND == KIND_GATE_UP) {
+              const int r = tn / p.nb, blk = tn - r * p.nb;
+              tma_load_4d(sb, &map_w, fb, kx, blk * 128, 0, r, pol_w);
+              tma_load_4d(sb + 128 * 128, &map_w, fb, kx, blk * 128, 1, r, pol_w);
+            } else {
+              tma_load_4d(sb, &map_w, fb, kx, tn * BN, 0, shard, pol_w);
+            }
+          } else {
+            // A: weight rows (NA x 128)
+            if (KIND == KIND_GATE_UP) {
+              const int r = tm / p.nb, blk = tm - r * p.nb;
+              tma_load_4d(sa, &map_w, fb, kx, blk * 128, 0, r, pol_w);
+              tma_load_4d(sa + 128 * 128, &map_w, fb, kx, blk * 128, 1, r, pol_w);
+            } else {
+#pragma unroll
+              for (int a = 0; a < NA; ++a)
+                tma_load_4d(sa + a * 128 * 128, &map_w, fb, kx, (tm * NA + a) * 128, 0, shard, pol_w);
+            }
+            // B: BN tokens of the activation
+            tma_load_4d(sb, &map_act, fb, kx, tn * BN, 0, shard, pol_a);
+          }
+          issued_mask |= 1u << stage;
+          last_phase_bits = (last_phase_bits & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // drain: let copies already in flight land before the CTA exits
+        for (int s = 0; s < STAGES; ++s)
+          if (issued_mask & (1u << s))
+            mbar_wait_bounded(full_bar(s), (last_phase_bits >> s) & 1u, nullptr, 20000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int buf = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        int tm, tn, sp;
+        decode_unit(u, tm, tn, sp);
+        const int kb0 = (int)((long long)sp * p.nkb / p.splits);
+        const int kb1 = (int)((long long)(sp + 1) * p.nkb / p.splits);
+        if (!mbar_wait_bounded(tempty_bar(buf), acc_phase ^ 1u, s_abort, p.timeout_ns)) {
+          if (!*s_abort) {
+            atomicExch(p.status, kStatusTimeout);
+            *s_abort = 1;
+          }
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * S::kAccCols;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait_bounded(full_bar(stage), phase, s_abort, p.timeout_ns)) {
+            if (!*s_abort) {
+              atomicExch(p.status, kStatusTimeout);
+              *s_abort = 1;
+            }
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = base + stage * S::kStageBytes;
+          const uint32_t sb = sa + S::kABytes;
+          const uint64_t adesc = smem_desc_k128(sa);
+          const uint64_t bdesc = smem_desc_k128(sb);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+            for (int a = 0; a < NA; ++a) {
+              tc_mma_bf16(d_tmem + a * BN, adesc + (uint64_t)(a * (128 * 128 >> 4) + ks * 2),
+                          bdesc + (uint64_t)(ks * 2), S::kIdesc, (kb > kb0 || ks > 0) ? 1u : 0u);
+            }
+          }
+          tc_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar(buf));
+        if (++buf == 2) {
+          buf = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // all issued MMAs complete before tensor memory is released
+      tc_commit(done_bar);
+      mbar_wait_bounded(done_bar, 0, nullptr, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;              // tensor-memory lane quadrant of this warp
+    const int row = q * 32 + lane;       // row of the 128-row accumulator
+    const int et = threadIdx.x - 64;     // 0..127
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    int buf = 0;
+    uint32_t acc_phase = 0;
+    constexpr int CH = S::kCh;
+    constexpr int ACC = S::kAccCols;
+
+    // Apply the epilogue to one chunk of CH column groups starting at c0.
+    auto emit = [&](int tm, int tn, int c0, const float* g, const float* u) {
+      if (!SWAP) {
+        const int m = tm * 128 + row;
+        if (m >= p.T) return;
+        if (KIND == KIND_GATE_UP) {
+          const int r = tn / p.nb, blk = tn - r * p.nb;
+          const int i0 = blk * 128 + c0;
+          __nv_bfloat16* dst = p.out + ((size_t)r * p.T + m) * p.Is + i0;
+#pragma unroll
+          for (int j = 0; j < CH; j += 8) {
+            if (i0 + j < p.Is) {
+              uint4 v;
+              v.x = pack_bf16x2(silu_f(g[j + 0]) * u[j + 0], silu_f(g[j + 1]) * u[j + 1]);
+              v.y = pack_bf16x2(silu_f(g[j + 2]) * u[j + 2], silu_f(g[j + 3]) * u[j + 3]);
+              v.z = pack_bf16x2(silu_f(g[j + 4]) * u[j + 4], silu_f(g[j + 5]) * u[j + 5]);
+              v.w = pack_bf16x2(silu_f(g[j + 6]) * u[j + 6], silu_f(g[j + 7]) * u[j + 7]);
+              *reinterpret_cast<uint4*>(dst + j) = v;
+            }
+          }
+        } else if (KIND == KIND_COL) {
+#pragma unroll
+          for (int j = 0; j < CH; j += 8) {
+            const int n = tn * BN + c0 + j;
+            if (n < p.n_out) {
+              const int ro = n / p.ws_out, c = n - ro * p.ws_out;
+              uint4 v;
+              v.x = pack_bf16x2(g[j + 0], g[j + 1]);
+              v.y = pack_bf16x2(g[j + 2], g[j + 3]);
+              v.z = pack_bf16x2(g[j + 4], g[j + 5]);
+              v.w = pack_bf16x2(g[j + 6], g[j + 7]);
+              *reinterpret_cast<uint4*>(p.out + ((size_t)ro * p.T + m) * p.ws_out + c) = v;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < CH; j += 8) {
+            const int n = tn * BN + c0 + j;
+            if (n < p.n_out) {
+              const size_t off = (size_t)m * p.n_out + n;
+              uint4 v;
+              v.x = pack_bf16x2(g[j + 0], g[j + 1]);
+              v.y = pack_bf16x2(g[j + 2], g[j + 3]);
+              v.z = pack_bf16x2(g[j + 4], g[j + 5]);
+              v.w = pack_bf16x2(g[j + 6], g[j + 7]);
+              *reinterpret_cast<uint4*>(p.out + off) = v;
+              if (p.out2 != nullptr) {
+                const uint4 rv = *reinterpret_cast<const uint4*>(p.resid + off);
+                const __nv_bfloat162* rb = reinterpret_cast<const __nv_bfloat162*>(&rv);
+                float2 r0 = __bfloat1622float2(rb[0]), r1 = __bfloat1622float2(rb[1]);
+                float2 r2 = __bfloat1622float2(rb[2]), r3 = __bfloat1622float2(rb[3]);
+                uint4 w;
+                w.x = pack_bf16x2(g[j + 0] + r0.x, g[j + 1] + r0.y);
+                w.y = pack_bf16x2(g[j + 2] + r1.x, g[j + 3] + r1.y);
+                w.z = pack_bf16x2(g[j + 4] + r2.x, g[j + 5] + r2.y);
+                w.w = pack_bf16x2(g[j + 6] + r3.x, g[j + 7] + r3.y);
+                *reinterpret_cast<uint4*>(p.out2 + off) = w;
+              }
+            }
+          }
+        }
+      } else {
+        // rows are output features, columns are tokens
+        if (KIND == KIND_GATE_UP) {
+          const int r = tm / p.nb, blk = tm - r * p.nb;
+          const int i = blk * 128 + row;
+          if (i >= p.Is) return;
+          __nv_bfloat16* dst = p.out + (size_t)r * p.T * p.Is + i;
+#pragma unroll
+          for (int j = 0; j < CH; ++j) {
+            const int tok = tn * BN + c0 + j;
+            if (tok < p.T) dst[(size_t)tok * p.Is] = __float2bfloat16_rn(silu_f(g[j]) * u[j]);
+          }
+        } else if (KIND == KIND_COL) {
+          const int f = tm * 128 + row;
+          if (f >= p.n_out) return;
+          const int ro = f / p.ws_out, c = f - ro * p.ws_out;
+          __nv_bfloat16* dst = p.out + (size_t)ro * p.T * p.ws_out + c;
+#pragma unroll
+          for (int j = 0; j < CH; ++j) {
+            const int tok = tn * BN + c0 + j;
+            if (tok < p.T) dst[(size_t)tok * p.ws_out] = __float2bfloat16_rn(g[j]);
+          }
+        } else {
+          const int f = tm * 128 + row;
+          if (f >= p.n_out) return;
+#pragma unroll
+          for (int j = 0; j < CH; ++j) {
+            const int tok = tn * BN + c0 + j;
+            if (tok < p.T) {
+              const size_t off = (size_t)tok * p.n_out + f;
+              p.out[off] = __float2bfloat16_rn(g[j]);
+              if (p.out2 != nullptr)
+                p.out2[off] = __float2bfloat16_rn(g[j] + __bfloat162float(p.resid[off]));
+            }
+          }
+        }
+      }
+    };
+
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+      int tm, tn, sp;
+      decode_unit(u, tm, tn, sp);
+      // one thread waits and the decision is shared, so all 128 epilogue
+      // threads leave together and no named barrier is left half-joined
+      if (et == 0) {
+        const bool ok = mbar_wait_bounded(tfull_bar(buf), acc_phase, s_abort, p.timeout_ns);
+        if (!ok && !*s_abort) {
+          atomicExch(p.status, kStatusTimeout);
+          *s_abort = 1;
+        }
+        *s_ok = ok ? 1 : 0;
+      }
+      named_bar_sync(1, 128);
+      const int ok = *s_ok;
+      named_bar_sync(1, 128);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t acc = lane_addr + buf * ACC;
+      const int tile = tm * p.n_tiles + tn;
+      float g[CH], uu[CH];
+      if (p.splits == 1) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < S::kNG; c0 += CH) {
+          if (CH == 32) tmem_ld32(acc + c0, g); else tmem_ld16(acc + c0, g);
+          if (KIND == KIND_GATE_UP) {
+            if (CH == 32) tmem_ld32(acc + S::kUOff + c0, uu); else tmem_ld16(acc + S::kUOff + c0, uu);
+          }
+          tc_wait_ld();
+          emit(tm, tn, c0, g, uu);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(buf));
+      } else {
+        float* part = p.partials + ((size_t)tile * p.splits + sp) * ACC * 128;
+#pragma unroll 1
+        for (int c0 = 0; c0 < ACC; c0 += CH) {
+          if (CH == 32) tmem_ld32(acc + c0, g); else tmem_ld16(acc + c0, g);
+          tc_wait_ld();
+#pragma unroll
+          for (int j = 0; j < CH; ++j) __stcg(part + (size_t)(c0 + j) * 128 + row, g[j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(buf));
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (et == 0) {
+          const int old = atomicAdd(p.counters + tile, 1);
+          const int last = (old == p.splits - 1);
+          if (last) p.counters[tile] = 0;
+          *s_last = last;
+        }
+        named_bar_sync(1, 128);
+        const int last = *s_last;
+        named_bar_sync(1, 128);   // every thread has read s_last before it is rewritten
+        if (last) {
+          __threadfence();
+          const float* base_part = p.partials + (size_t)tile * p.splits * ACC * 128;
+#pragma unroll 1
+          for (int c0 = 0; c0 < S::kNG; c0 += CH) {
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+              float a = 0.f, b = 0.f;
+              for (int s = 0; s < p.splits; ++s) {
+                const float* ps = base_part + (size_t)s * ACC * 128;
+                a += __ldcg(ps + (size_t)(c0 + j) * 128 + row);
+                if (KIND == KIND_GATE_UP) b += __ldcg(ps + (size_t)(S::kUOff + c0 + j) * 128 + row);
+              }
+              g[j] = a;
+              uu[j] = b;
+            }
+            emit(tm, tn, c0, g, uu);
+          }
+        }
+      }
+      if (++buf == 2) {
+        buf = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, S::kTmemCols);
+  }
+}
+
+}  // namespace tpl

@@ -1,0 +1,56 @@
+// Declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+namespace tpl {
+
+constexpr int kStatusCapacity = -5;
+
+// ---------------------------------------------------------------- capture
+constexpr int kCaptureMaxTensors = 8;
+struct CaptureMeta {
+  const __nv_bfloat16* tensors[kCaptureMaxTensors];
+  int32_t types[kCaptureMaxTensors];
+  int32_t n_tensors;
+  int32_t layer;
+  int32_t* hdr;        // [capacity][6]
+  void* rows_out;      // [capacity][H] bf16
+};
+
+cudaError_t launch_capture(int T, int H, const int32_t* row_req, const int32_t* row_pos,
+                           const int64_t* sel, int n_sel, uint64_t* gtable, int cap_log2,
+                           size_t table_smem, const CaptureMeta& meta, int64_t capacity,
+                           int64_t* n_out_dev, int32_t* match_rows, int32_t* n_match_ws, int* status,
+                           int copy_grid, cudaStream_t st);
+
+// ---------------------------------------------------------------- RMSNorm
+cudaError_t launch_add_rms_norm(int T, int H, const void* a, const void* res, const void* gamma,
+                                float eps, void* res_out, void* x_out, cudaStream_t st);
+int max_norm_hidden();
+
+// ---------------------------------------------------------------- packing
+enum PackMode : int { PACK_GATE_UP = 0, PACK_ROW = 1, PACK_QKV = 2 };
+struct PackSpec {
+  int mode;
+  const __nv_bfloat16* src[3];
+  int64_t width;  // elements per packed row (H, or Ks for PACK_ROW)
+  int64_t Is;     // PACK_GATE_UP: I / t
+  int64_t N;      // PACK_ROW: output features
+  int64_t t;
+  int64_t ws;     // PACK_QKV: packed rows per shard
+  int q_per, kv_per, rep, hd;
+};
+cudaError_t launch_pack(const PackSpec& s, int64_t rows, void* dst, cudaStream_t st);
+
+// ---------------------------------------------------------------- GEMM
+struct GemmParams;
+// Launch the GEMM instantiation for (swap, kind, bn); returns cudaErrorInvalidValue
+// when no such instantiation exists.
+cudaError_t launch_gemm(bool swap, int kind, int bn, const CUtensorMap& map_act,
+                        const CUtensorMap& map_w, const GemmParams& p, int grid, cudaStream_t st);
+int gemm_stages(bool swap, int kind, int bn);
+
+}  // namespace tpl

@@ -1,0 +1,725 @@
+// Host side of libtplinear.so: argument validation, shard packing, tensor
+// maps, launch plans and the C ABI declared in include/tp_linear.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "gemm_tc.cuh"
+#include "internal.h"
+#include "tp_linear.h"
+
+namespace tpl {
+cudaError_t launch_gemm_prefill(int kind, const CUtensorMap& a, const CUtensorMap& w,
+                                const GemmParams& p, int grid, cudaStream_t st);
+cudaError_t launch_gemm_decode_gate_up(int bn, const CUtensorMap& a, const CUtensorMap& w,
+                                       const GemmParams& p, int grid, cudaStream_t st);
+cudaError_t launch_gemm_decode_col(int bn, const CUtensorMap& a, const CUtensorMap& w,
+                                   const GemmParams& p, int grid, cudaStream_t st);
+cudaError_t launch_gemm_decode_row(int bn, const CUtensorMap& a, const CUtensorMap& w,
+                                   const GemmParams& p, int grid, cudaStream_t st);
+int gemm_stages_prefill(int kind);
+int gemm_stages_decode_gate_up(int bn);
+int gemm_stages_decode_col(int bn);
+int gemm_stages_decode_row(int bn);
+
+cudaError_t launch_gemm(bool swap, int kind, int bn, const CUtensorMap& a, const CUtensorMap& w,
+                        const GemmParams& p, int grid, cudaStream_t st) {
+  if (!swap) return launch_gemm_prefill(kind, a, w, p, grid, st);
+  switch (kind) {
+    case KIND_GATE_UP: return launch_gemm_decode_gate_up(bn, a, w, p, grid, st);
+    case KIND_COL: return launch_gemm_decode_col(bn, a, w, p, grid, st);
+    case KIND_ROW: return launch_gemm_decode_row(bn, a, w, p, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+int gemm_stages(bool swap, int kind, int bn) {
+  if (!swap) return gemm_stages_prefill(kind);
+  switch (kind) {
+    case KIND_GATE_UP: return gemm_stages_decode_gate_up(bn);
+    case KIND_COL: return gemm_stages_decode_col(bn);
+    case KIND_ROW: return gemm_stages_decode_row(bn);
+    default: return 0;
+  }
+}
+}  // namespace tpl
+
+using namespace tpl;
+
+// ============================================================================ errors
+namespace {
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+int ok() {
+  g_err[0] = '\0';
+  return TP_OK;
+}
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(TP_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+constexpr int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
+
+// ============================================================================ driver entry
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 4-D bf16 tensor map: dims (d0 innermost .. d3), dense strides, box (64, box_rows, 1, 1),
+// 128-byte swizzle, out-of-bounds elements read as zero.
+int make_map(CUtensorMap* m, const void* ptr, int64_t d0, int64_t d1, int64_t d2, int64_t d3,
+             int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[4] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2, (cuuint64_t)d3};
+  const cuuint64_t strides[3] = {(cuuint64_t)(d0 * 2), (cuuint64_t)(d0 * d1 * 2),
+                                 (cuuint64_t)(d0 * d1 * d2 * 2)};
+  const cuuint32_t box[4] = {64u, (cuuint32_t)box_rows, 1u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for dims %lld x %lld x %lld x %lld",
+                (int)r, (long long)d0, (long long)d1, (long long)d2, (long long)d3);
+  return TP_OK;
+}
+
+// ============================================================================ workspace layout
+constexpr int64_t kHdrBytes = 256;
+constexpr int kMaxCounters = 4096;  // split-K tiles per GEMM
+constexpr int64_t kCountersColOff = kHdrBytes;
+constexpr int64_t kCountersRowOff = kCountersColOff + kMaxCounters * 4;
+constexpr int64_t kDynOff = align256(kCountersRowOff + kMaxCounters * 4);
+constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per on-chip wait
+
+}  // namespace
+
+// ============================================================================ handle
+struct tp_linear {
+  tp_config_t cfg;
+  int device;
+  int nsm;
+  int64_t H;
+  // MLP
+  int64_t I, Is;
+  // ATTN
+  int q_per, kv_per, rep;
+  int64_t ws_qkv;  // packed rows per QKV shard
+  int64_t Ks;      // row-parallel input features per shard (Is or nq*hd/t)
+  int64_t n_col;   // column-parallel output rows in total
+  void* w_col;
+  void* w_row;
+  const void* gamma;
+  CUtensorMap map_col_swap, map_col_wide, map_row_swap, map_row_wide;
+};
+
+namespace {
+
+struct Plan {
+  bool swap;
+  int kind;
+  int bn;
+  int m_tiles, n_tiles, splits, units, nkb, kbs, nb, grid, acc_cols;
+  int64_t partial_bytes;
+};
+
+// Pick the operand orientation, tile width and K split of one GEMM.
+Plan make_plan(const tp_linear* h, int which, int64_t T) {
+  Plan pl{};
+  const bool mlp = h->cfg.kind == TP_BLOCK_MLP;
+  pl.kind = which == 0 ? (mlp ? KIND_GATE_UP : KIND_COL) : KIND_ROW;
+  pl.swap = T <= 128;
+  pl.bn = pl.swap ? (T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128) : 256;
+  const int t = h->cfg.t;
+  int64_t w_tiles;
+  if (which == 0) {
+    pl.nkb = (int)ceil_div(h->H, 64);
+    pl.kbs = 0;
+    if (mlp) {
+      pl.nb = (int)ceil_div(h->Is, 128);
+      w_tiles = (int64_t)t * pl.nb;  // 128 gate + 128 up rows per tile
+    } else {
+      w_tiles = ceil_div(h->n_col, pl.swap ? 128 : 256);
+    }
+  } else {
+    pl.kbs = (int)ceil_div(h->Ks, 64);
+    pl.nkb = t * pl.kbs;
+    w_tiles = ceil_div(h->H, pl.swap ? 128 : 256);
+  }
+  if (pl.swap) {
+    pl.m_tiles = (int)w_tiles;
+    pl.n_tiles = (int)ceil_div(T, pl.bn);
+  } else {
+    pl.m_tiles = (int)ceil_div(T, 128);
+    pl.n_tiles = (int)w_tiles;
+  }
+  pl.acc_cols = (pl.swap && pl.kind == KIND_GATE_UP) ? 2 * pl.bn : pl.bn;
+  const int64_t tiles = (int64_t)pl.m_tiles * pl.n_tiles;
+  // time ~ waves * (k-blocks per unit + per-unit overhead); the overhead of a
+  // split unit includes writing and re-reading its fp32 partial tile
+  const double c1 = pl.swap ? 4.0 : 8.0;
+  const double cs = pl.swap ? 2.0 : 16.0;
+  int best = 1;
+  double best_cost = 1e30;
+  const int max_s = (tiles <= kMaxCounters) ? std::min(16, std::max(1, pl.nkb / 2)) : 1;
+  for (int s = 1; s <= max_s; ++s) {
+    const double waves = (double)ceil_div(tiles * s, h->nsm);
+    const double cost = waves * ((double)pl.nkb / s + c1 + (s > 1 ? cs : 0.0));
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  pl.splits = best;
+  pl.units = (int)(tiles * pl.splits);
+  pl.grid = (int)std::min<int64_t>(pl.units, h->nsm);
+  pl.partial_bytes = pl.splits > 1 ? tiles * pl.splits * pl.acc_cols * 128 * 4 : 0;
+  return pl;
+}
+
+struct Layout {
+  int64_t x_norm, h, part_col, part_row, total;
+};
+
+Layout make_layout(const tp_linear* h, int64_t T) {
+  Layout L{};
+  int64_t off = kDynOff;
+  const bool mlp = h->cfg.kind == TP_BLOCK_MLP;
+  if (mlp && (h->cfg.flags & TP_FLAG_HAS_NORM)) {
+    L.x_norm = off;
+    off = align256(off + T * h->H * 2);
+  }
+  if (mlp) {
+    L.h = off;
+    off = align256(off + (int64_t)h->cfg.t * T * h->Is * 2);
+  }
+  L.part_col = off;
+  off = align256(off + make_plan(h, 0, T).partial_bytes);
+  L.part_row = off;
+  off = align256(off + make_plan(h, 1, T).partial_bytes);
+  L.total = off;
+  return L;
+}
+
+int check_device(const tp_linear* h) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != h->device)
+    return fail(TP_ERR_ARG, "current device %d is not the handle's device %d", dev, h->device);
+  return TP_OK;
+}
+
+GemmParams base_params(const Plan& pl, int64_t T, void* ws, int64_t part_off, int64_t cnt_off) {
+  GemmParams p{};
+  p.T = (int)T;
+  p.m_tiles = pl.m_tiles;
+  p.n_tiles = pl.n_tiles;
+  p.splits = pl.splits;
+  p.units = pl.units;
+  p.nkb = pl.nkb;
+  p.kbs = pl.kbs;
+  p.nb = pl.nb;
+  p.group_m = 8;
+  char* w = static_cast<char*>(ws);
+  p.partials = reinterpret_cast<float*>(w + part_off);
+  p.counters = reinterpret_cast<int*>(w + cnt_off);
+  p.status = reinterpret_cast<int*>(w);
+  p.timeout_ns = kTimeoutNs;
+  return p;
+}
+
+// column-parallel GEMM: gate_up (MLP) or QKV (ATTN)
+int run_col(const tp_linear* h, int64_t T, const void* x, void* out, void* ws, const Layout& L,
+            cudaStream_t st) {
+  const Plan pl = make_plan(h, 0, T);
+  CUtensorMap map_x;
+  int rc = make_map(&map_x, x, h->H, T, 1, 1, pl.swap ? pl.bn : 128);
+  if (rc) return rc;
+  GemmParams p = base_params(pl, T, ws, L.part_col, kCountersColOff);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  if (h->cfg.kind == TP_BLOCK_MLP) {
+    p.Is = (int)h->Is;
+  } else {
+    p.n_out = (int)h->n_col;
+    p.ws_out = (int)h->ws_qkv;
+  }
+  const CUtensorMap& mw = pl.swap ? h->map_col_swap : h->map_col_wide;
+  cudaError_t e = launch_gemm(pl.swap, pl.kind, pl.bn, map_x, mw, p, pl.grid, st);
+  if (e != cudaSuccess) return cuda_fail(e, "column-parallel GEMM launch");
+  return TP_OK;
+}
+
+// row-parallel GEMM with the cross-shard reduction: down (MLP) or o_proj (ATTN)
+int run_row(const tp_linear* h, int64_t T, const void* in_shards, const void* resid, void* out,
+            void* out2, void* ws, const Layout& L, cudaStream_t st) {
+  const Plan pl = make_plan(h, 1, T);
+  CUtensorMap map_in;
+  int rc = make_map(&map_in, in_shards, h->Ks, T, 1, h->cfg.t, pl.swap ? pl.bn : 128);
+  if (rc) return rc;
+  GemmParams p = base_params(pl, T, ws, L.part_row, kCountersRowOff);
+  p.n_out = (int)h->H;
+  p.ws_out = (int)h->H;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.out2 = static_cast<__nv_bfloat16*>(out2);
+  p.resid = static_cast<const __nv_bfloat16*>(resid);
+  const CUtensorMap& mw = pl.swap ? h->map_row_swap : h->map_row_wide;
+  cudaError_t e = launch_gemm(pl.swap, pl.kind, pl.bn, map_in, mw, p, pl.grid, st);
+  if (e != cudaSuccess) return cuda_fail(e, "row-parallel GEMM launch");
+  return TP_OK;
+}
+
+int check_ws(const tp_linear* h, int64_t T, const void* ws, int64_t ws_bytes, Layout* L) {
+  if (ws == nullptr || !aligned16(ws)) return fail(TP_ERR_ARG, "workspace is null or not 16-byte aligned");
+  *L = make_layout(h, T);
+  if (ws_bytes < L->total)
+    return fail(TP_ERR_ARG, "workspace too small: %lld bytes, %lld needed for T=%lld",
+                (long long)ws_bytes, (long long)L->total, (long long)T);
+  return TP_OK;
+}
+
+int check_T(int64_t T) {
+  if (T < 0) return fail(TP_ERR_SHAPE, "T must be >= 0 (got %lld)", (long long)T);
+  if (T > (1 << 24)) return fail(TP_ERR_UNSUPPORTED, "T > 16777216 tokens in one call");
+  return TP_OK;
+}
+
+#define TP_CHECK_PTR(p, name)                                                        \
+  do {                                                                               \
+    if ((p) == nullptr) return fail(TP_ERR_ARG, "%s is null", name);                \
+    if (!aligned16(p)) return fail(TP_ERR_ARG, "%s is not 16-byte aligned", name);  \
+  } while (0)
+
+int validate_cfg(const tp_config_t* c) {
+  if (c == nullptr) return fail(TP_ERR_ARG, "config is null");
+  if (c->kind != TP_BLOCK_MLP && c->kind != TP_BLOCK_ATTN_PROJ)
+    return fail(TP_ERR_ARG, "unknown block kind %d", c->kind);
+  if (c->reserved != 0) return fail(TP_ERR_ARG, "reserved field must be 0");
+  if (c->t <= 0) return fail(TP_ERR_SHAPE, "t must be positive (got %d)", c->t);
+  if ((c->t & (c->t - 1)) != 0 || c->t > 8)
+    return fail(TP_ERR_UNSUPPORTED, "t must be a power of 2 in [1, 8] (got %d)", c->t);
+  if (c->hidden <= 0 || c->hidden > (1 << 20)) return fail(TP_ERR_SHAPE, "hidden out of range");
+  if (c->hidden % 8 != 0) return fail(TP_ERR_UNSUPPORTED, "hidden must be a multiple of 8");
+  if (c->kind == TP_BLOCK_MLP) {
+    if (c->intermediate <= 0 || c->intermediate > (1 << 22))
+      return fail(TP_ERR_SHAPE, "intermediate out of range");
+    if (c->intermediate % c->t != 0)
+      return fail(TP_ERR_SHAPE, "intermediate %lld is not divisible by t=%d",
+                  (long long)c->intermediate, c->t);
+    if ((c->intermediate / c->t) % 8 != 0)
+      return fail(TP_ERR_UNSUPPORTED, "intermediate / t must be a multiple of 8");
+    if (c->flags & ~TP_FLAG_HAS_NORM) return fail(TP_ERR_ARG, "unknown flags 0x%x", c->flags);
+    if ((c->flags & TP_FLAG_HAS_NORM) && !(c->rms_eps >= 0.0f))
+      return fail(TP_ERR_ARG, "rms_eps must be >= 0");
+    if ((c->flags & TP_FLAG_HAS_NORM) && c->hidden > max_norm_hidden())
+      return fail(TP_ERR_UNSUPPORTED, "hidden > %d with the fused norm", max_norm_hidden());
+  } else {
+    if (c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0)
+      return fail(TP_ERR_SHAPE, "head counts must be positive");
+    if (c->n_q_heads % c->t != 0)
+      return fail(TP_ERR_SHAPE, "n_q_heads %d is not divisible by t=%d", c->n_q_heads, c->t);
+    if (c->n_kv_heads % c->t != 0 && c->t % c->n_kv_heads != 0)
+      return fail(TP_ERR_SHAPE, "n_kv_heads %d and t=%d: neither divides the other", c->n_kv_heads, c->t);
+    if (c->n_q_heads % c->n_kv_heads != 0)
+      return fail(TP_ERR_SHAPE, "n_q_heads must be a multiple of n_kv_heads");
+    if (c->head_dim % 8 != 0) return fail(TP_ERR_UNSUPPORTED, "head_dim must be a multiple of 8");
+    if (c->flags != 0) return fail(TP_ERR_ARG, "flags must be 0 for the attention projections");
+  }
+  return TP_OK;
+}
+
+void derive(tp_linear* h) {
+  const tp_config_t& c = h->cfg;
+  h->H = c.hidden;
+  const int t = c.t;
+  if (c.kind == TP_BLOCK_MLP) {
+    h->I = c.intermediate;
+    h->Is = c.intermediate / t;
+    h->Ks = h->Is;
+    h->n_col = 2 * h->I;
+  } else {
+    h->q_per = c.n_q_heads / t;
+    if (t >= c.n_kv_heads) {
+      h->kv_per = 1;
+      h->rep = t / c.n_kv_heads;
+    } else {
+      h->kv_per = c.n_kv_heads / t;
+      h->rep = 1;
+    }
+    h->ws_qkv = (int64_t)(h->q_per + 2 * h->kv_per) * c.head_dim;
+    h->n_col = t * h->ws_qkv;
+    h->Ks = (int64_t)c.n_q_heads * c.head_dim / t;
+  }
+}
+
+}  // namespace
+
+// ============================================================================ C ABI
+extern "C" {
+
+const char* tp_last_error(void) { return g_err; }
+
+int tp_packed_weight_bytes(const tp_config_t* cfg, int64_t* col_bytes, int64_t* row_bytes) {
+  int rc = validate_cfg(cfg);
+  if (rc) return rc;
+  if (col_bytes == nullptr || row_bytes == nullptr) return fail(TP_ERR_ARG, "null output pointer");
+  tp_linear tmp{};
+  tmp.cfg = *cfg;
+  derive(&tmp);
+  *col_bytes = tmp.n_col * tmp.H * 2;
+  *row_bytes = tmp.H * tmp.Ks * cfg->t * 2;
+  return ok();
+}
+
+int tp_linear_create(const tp_config_t* cfg, const void* const* w_full, int32_t n_w,
+                     void* w_col_packed, void* w_row_packed, const void* gamma, tp_stream_t stream,
+                     tp_linear_t** out) {
+  if (out == nullptr) return fail(TP_ERR_ARG, "out is null");
+  *out = nullptr;
+  int rc = validate_cfg(cfg);
+  if (rc) return rc;
+  const bool mlp = cfg->kind == TP_BLOCK_MLP;
+  const int need = mlp ? 3 : 4;
+  if (w_full == nullptr || n_w != need)
+    return fail(TP_ERR_ARG, "expected %d full weight pointers, got %d", need, n_w);
+  for (int i = 0; i < need; ++i) TP_CHECK_PTR(w_full[i], "w_full[i]");
+  TP_CHECK_PTR(w_col_packed, "w_col_packed");
+  TP_CHECK_PTR(w_row_packed, "w_row_packed");
+  if (mlp && (cfg->flags & TP_FLAG_HAS_NORM)) TP_CHECK_PTR(gamma, "gamma");
+
+  tp_linear* h = new (std::nothrow) tp_linear();
+  if (h == nullptr) return fail(TP_ERR_ARG, "out of host memory");
+  h->cfg = *cfg;
+  derive(h);
+  h->w_col = w_col_packed;
+  h->w_row = w_row_packed;
+  h->gamma = (mlp && (cfg->flags & TP_FLAG_HAS_NORM)) ? gamma : nullptr;
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->nsm, cudaDevAttrMultiProcessorCount, h->device);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(e, "device query");
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int t = cfg->t;
+  // pack the shards ("weight_loader": narrow the full tensor to each rank's slice)
+  PackSpec pc{}, pr{};
+  if (mlp) {
+    pc.mode = PACK_GATE_UP;
+    pc.src[0] = static_cast<const __nv_bfloat16*>(w_full[0]);
+    pc.src[1] = static_cast<const __nv_bfloat16*>(w_full[1]);
+    pc.width = h->H;
+    pc.Is = h->Is;
+    pr.mode = PACK_ROW;
+    pr.src[0] = static_cast<const __nv_bfloat16*>(w_full[2]);
+  } else {
+    pc.mode = PACK_QKV;
+    for (int i = 0; i < 3; ++i) pc.src[i] = static_cast<const __nv_bfloat16*>(w_full[i]);
+    pc.width = h->H;
+    pc.ws = h->ws_qkv;
+    pc.q_per = h->q_per;
+    pc.kv_per = h->kv_per;
+    pc.rep = h->rep;
+    pc.hd = cfg->head_dim;
+    pr.mode = PACK_ROW;
+    pr.src[0] = static_cast<const __nv_bfloat16*>(w_full[3]);
+  }
+  pc.t = t;
+  pr.width = h->Ks;
+  pr.N = h->H;
+  pr.t = t;
+  e = launch_pack(pc, h->n_col, w_col_packed, st);
+  if (e == cudaSuccess) e = launch_pack(pr, (int64_t)t * h->H, w_row_packed, st);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(e, "weight packing");
+  }
+  // weight tensor maps, one per operand orientation
+  if (mlp) {
+    rc = make_map(&h->map_col_swap, w_col_packed, h->H, h->Is, 2, t, 128);
+    if (!rc) rc = make_map(&h->map_col_wide, w_col_packed, h->H, h->Is, 2, t, 128);
+  } else {
+    rc = make_map(&h->map_col_swap, w_col_packed, h->H, h->n_col, 1, 1, 128);
+    if (!rc) rc = make_map(&h->map_col_wide, w_col_packed, h->H, h->n_col, 1, 1, 256);
+  }
+  if (!rc) rc = make_map(&h->map_row_swap, w_row_packed, h->Ks, h->H, 1, t, 128);
+  if (!rc) rc = make_map(&h->map_row_wide, w_row_packed, h->Ks, h->H, 1, t, 256);
+  if (rc) {
+    delete h;
+    return rc;
+  }
+  *out = h;
+  return ok();
+}
+
+int tp_linear_destroy(tp_linear_t* h) {
+  delete h;
+  return ok();
+}
+
+int tp_workspace_size(const tp_linear_t* h, int64_t max_tokens, int64_t* bytes) {
+  if (h == nullptr || bytes == nullptr) return fail(TP_ERR_ARG, "null argument");
+  int rc = check_T(max_tokens);
+  if (rc) return rc;
+  int64_t best = kDynOff;
+  for (int64_t T = 1; T <= max_tokens; ++T) best = std::max(best, make_layout(h, T).total);
+  *bytes = best;
+  return ok();
+}
+
+int tp_describe_plan(const tp_linear_t* h, int64_t T, tp_gemm_plan_t* plans, int32_t max_plans) {
+  if (h == nullptr || plans == nullptr || max_plans < 0) return fail(TP_ERR_ARG, "null argument");
+  if (check_T(T) || T == 0) return 0;
+  int n = 0;
+  for (int which = 0; which < 2 && n < max_plans; ++which, ++n) {
+    const Plan pl = make_plan(h, which, T);
+    plans[n].swap_ab = pl.swap;
+    plans[n].block_n = pl.bn;
+    plans[n].splits = pl.splits;
+    plans[n].units = pl.units;
+    plans[n].grid = pl.grid;
+    plans[n].stages = gemm_stages(pl.swap, pl.kind, pl.bn);
+  }
+  g_err[0] = '\0';
+  return n;
+}
+
+int tp_add_rms_norm(int64_t T, int64_t H, const void* a, const void* residual_in, const void* gamma,
+                    float eps, void* residual_out, void* x_out, tp_stream_t stream) {
+  int rc = check_T(T);
+  if (rc) return rc;
+  if (H <= 0 || H % 8 != 0) return fail(TP_ERR_UNSUPPORTED, "H must be a positive multiple of 8");
+  if (H > max_norm_hidden()) return fail(TP_ERR_UNSUPPORTED, "H > %d", max_norm_hidden());
+  if (!(eps >= 0.0f)) return fail(TP_ERR_ARG, "eps must be >= 0");
+  TP_CHECK_PTR(a, "a");
+  TP_CHECK_PTR(residual_in, "residual_in");
+  TP_CHECK_PTR(gamma, "gamma");
+  TP_CHECK_PTR(residual_out, "residual_out");
+  TP_CHECK_PTR(x_out, "x_out");
+  if (T == 0) return ok();
+  cudaError_t e = launch_add_rms_norm((int)T, (int)H, a, residual_in, gamma, eps, residual_out,
+                                      x_out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "add_rms_norm launch");
+  return ok();
+}
+
+int tp_gate_up_forward(tp_linear_t* h, int64_t T, const void* x, void* h_out, void* workspace,
+                       int64_t workspace_bytes, tp_stream_t stream) {
+  if (h == nullptr) return fail(TP_ERR_ARG, "handle is null");
+  if (h->cfg.kind != TP_BLOCK_MLP) return fail(TP_ERR_ARG, "not an MLP handle");
+  int rc = check_T(T);
+  if (rc) return rc;
+  TP_CHECK_PTR(x, "x");
+  TP_CHECK_PTR(h_out, "h_out");
+  Layout L;
+  if ((rc = check_ws(h, T, workspace, workspace_bytes, &L))) return rc;
+  if ((rc = check_device(h))) return rc;
+  if (T == 0) return ok();
+  if ((rc = run_col(h, T, x, h_out, workspace, L, static_cast<cudaStream_t>(stream)))) return rc;
+  return ok();
+}
+
+int tp_down_forward(tp_linear_t* h, int64_t T, const void* h_in, const void* residual,
+                    void* mlp_out, void* residual_stream, void* workspace, int64_t workspace_bytes,
+                    tp_stream_t stream) {
+  if (h == nullptr) return fail(TP_ERR_ARG, "handle is null");
+  if (h->cfg.kind != TP_BLOCK_MLP) return fail(TP_ERR_ARG, "not an MLP handle");
+  int rc = check_T(T);
+  if (rc) return rc;
+  TP_CHECK_PTR(h_in, "h_in");
+  TP_CHECK_PTR(mlp_out, "mlp_out");
+  if (residual_stream != nullptr) {
+    TP_CHECK_PTR(residual_stream, "residual_stream");
+    TP_CHECK_PTR(residual, "residual");
+  }
+  Layout L;
+  if ((rc = check_ws(h, T, workspace, workspace_bytes, &L))) return rc;
+  if ((rc = check_device(h))) return rc;
+  if (T == 0) return ok();
+  if ((rc = run_row(h, T, h_in, residual, mlp_out, residual_stream, workspace, L,
+                    static_cast<cudaStream_t>(stream))))
+    return rc;
+  return ok();
+}
+
+int tp_mlp_forward(tp_linear_t* h, int64_t T, const void* x_in, const void* residual_in,
+                   void* residual_out, void* mlp_out, void* residual_stream, void* workspace,
+                   int64_t workspace_bytes, tp_stream_t stream) {
+  if (h == nullptr) return fail(TP_ERR_ARG, "handle is null");
+  if (h->cfg.kind != TP_BLOCK_MLP) return fail(TP_ERR_ARG, "not an MLP handle");
+  int rc = check_T(T);
+  if (rc) return rc;
+  const bool norm = (h->cfg.flags & TP_FLAG_HAS_NORM) != 0;
+  TP_CHECK_PTR(x_in, "x_in");
+  TP_CHECK_PTR(mlp_out, "mlp_out");
+  if (norm) {
+    TP_CHECK_PTR(residual_in, "residual_in");
+    TP_CHECK_PTR(residual_out, "residual_out");
+  }
+  if (residual_in != nullptr) TP_CHECK_PTR(residual_in, "residual_in");
+  if (residual_stream != nullptr) {
+    TP_CHECK_PTR(residual_stream, "residual_stream");
+    if (residual_in == nullptr) return fail(TP_ERR_ARG, "residual_stream needs a residual");
+  }
+  Layout L;
+  if ((rc = check_ws(h, T, workspace, workspace_bytes, &L))) return rc;
+  if ((rc = check_device(h))) return rc;
+  if (T == 0) return ok();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  const void* x = x_in;
+  const void* resid = residual_in;
+  if (norm) {
+    cudaError_t e = launch_add_rms_norm((int)T, (int)h->H, x_in, residual_in, h->gamma,
+                                        h->cfg.rms_eps, residual_out, ws + L.x_norm, st);
+    if (e != cudaSuccess) return cuda_fail(e, "add_rms_norm launch");
+    x = ws + L.x_norm;
+    resid = residual_out;
+  }
+  void* hbuf = ws + L.h;
+  if ((rc = run_col(h, T, x, hbuf, workspace, L, st))) return rc;
+  if ((rc = run_row(h, T, hbuf, resid, mlp_out, residual_stream, workspace, L, st))) return rc;
+  return ok();
+}
+
+int tp_attn_proj_forward(tp_linear_t* h, int64_t T, const void* x, void* qkv_out,
+                         const void* attn_in, void* o_out, void* workspace, int64_t workspace_bytes,
+                         tp_stream_t stream) {
+  if (h == nullptr) return fail(TP_ERR_ARG, "handle is null");
+  if (h->cfg.kind != TP_BLOCK_ATTN_PROJ) return fail(TP_ERR_ARG, "not an attention handle");
+  int rc = check_T(T);
+  if (rc) return rc;
+  const bool do_qkv = x != nullptr || qkv_out != nullptr;
+  const bool do_o = attn_in != nullptr || o_out != nullptr;
+  if (do_qkv) {
+    TP_CHECK_PTR(x, "x");
+    TP_CHECK_PTR(qkv_out, "qkv_out");
+  }
+  if (do_o) {
+    TP_CHECK_PTR(attn_in, "attn_in");
+    TP_CHECK_PTR(o_out, "o_out");
+  }
+  Layout L;
+  if ((rc = check_ws(h, T, workspace, workspace_bytes, &L))) return rc;
+  if ((rc = check_device(h))) return rc;
+  if (T == 0) return ok();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (do_qkv && (rc = run_col(h, T, x, qkv_out, workspace, L, st))) return rc;
+  if (do_o && (rc = run_row(h, T, attn_in, nullptr, o_out, nullptr, workspace, L, st))) return rc;
+  return ok();
+}
+
+// ---------------------------------------------------------------------------- capture
+namespace {
+constexpr int kSmemTableMaxLog2 = 13;  // 8192 slots = 64 KB of shared memory
+struct CaptureLayout {
+  int cap_log2;
+  bool global_table;
+  int64_t n_match, rows, table, total;
+};
+CaptureLayout capture_layout(int64_t T, int64_t n_sel) {
+  CaptureLayout c{};
+  int lg = 6;
+  while ((int64_t(1) << lg) < 2 * n_sel) ++lg;
+  c.cap_log2 = lg;
+  c.global_table = lg > kSmemTableMaxLog2;
+  c.n_match = kDynOff;
+  c.rows = kDynOff + 256;
+  c.table = align256(c.rows + 4 * std::max<int64_t>(T, 1));
+  c.total = c.global_table ? align256(c.table + (int64_t(8) << lg)) : c.table;
+  return c;
+}
+}  // namespace
+
+int tp_capture_workspace_size(int64_t T, int64_t n_sel, int64_t* bytes) {
+  if (bytes == nullptr) return fail(TP_ERR_ARG, "bytes is null");
+  int rc = check_T(T);
+  if (rc) return rc;
+  if (n_sel < 0 || n_sel > (int64_t(1) << 26)) return fail(TP_ERR_SHAPE, "n_sel out of range");
+  *bytes = capture_layout(T, n_sel).total;
+  return ok();
+}
+
+int tp_capture_rows(int64_t T, int64_t H, const int32_t* row_req, const int32_t* row_pos,
+                    const int64_t* sel_keys, int64_t n_sel, int32_t n_tensors,
+                    const void* const* tensors, const int32_t* tensor_types, int32_t layer,
+                    tp_record_hdr_t* hdr_out, void* rows_out, int64_t capacity, int64_t* n_out_dev,
+                    void* workspace, int64_t workspace_bytes, tp_stream_t stream) {
+  int rc = check_T(T);
+  if (rc) return rc;
+  if (H <= 0 || H % 8 != 0) return fail(TP_ERR_UNSUPPORTED, "H must be a positive multiple of 8");
+  if (n_sel < 0 || n_sel > (int64_t(1) << 26)) return fail(TP_ERR_SHAPE, "n_sel out of range");
+  if (n_tensors < 1 || n_tensors > kCaptureMaxTensors)
+    return fail(TP_ERR_UNSUPPORTED, "n_tensors must be in [1, %d]", kCaptureMaxTensors);
+  if (capacity < 0) return fail(TP_ERR_SHAPE, "capacity must be >= 0");
+  if (tensors == nullptr || tensor_types == nullptr) return fail(TP_ERR_ARG, "tensor list is null");
+  TP_CHECK_PTR(row_req, "row_req");
+  TP_CHECK_PTR(row_pos, "row_pos");
+  if (n_sel > 0) TP_CHECK_PTR(sel_keys, "sel_keys");
+  TP_CHECK_PTR(n_out_dev, "n_out_dev");
+  if (capacity > 0) {
+    TP_CHECK_PTR(hdr_out, "hdr_out");
+    TP_CHECK_PTR(rows_out, "rows_out");
+  }
+  CaptureMeta meta{};
+  for (int k = 0; k < n_tensors; ++k) {
+    TP_CHECK_PTR(tensors[k], "tensors[k]");
+    meta.tensors[k] = static_cast<const __nv_bfloat16*>(tensors[k]);
+    meta.types[k] = tensor_types[k];
+  }
+  meta.n_tensors = n_tensors;
+  meta.layer = layer;
+  meta.hdr = reinterpret_cast<int32_t*>(hdr_out);
+  meta.rows_out = rows_out;
+  if (workspace == nullptr || !aligned16(workspace))
+    return fail(TP_ERR_ARG, "workspace is null or not 16-byte aligned");
+  const CaptureLayout c = capture_layout(T, n_sel);
+  if (workspace_bytes < c.total)
+    return fail(TP_ERR_ARG, "capture workspace too small: %lld < %lld", (long long)workspace_bytes,
+                (long long)c.total);
+  if (T == 0) return ok();
+  int dev = 0, nsm = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  char* ws = static_cast<char*>(workspace);
+  const int64_t recs = std::min<int64_t>(capacity, (int64_t)n_tensors * T);
+  const int copy_grid = (int)std::max<int64_t>(1, std::min<int64_t>(recs, 4 * nsm));
+  cudaError_t e = launch_capture(
+      (int)T, (int)H, row_req, row_pos, sel_keys, (int)n_sel,
+      c.global_table ? reinterpret_cast<uint64_t*>(ws + c.table) : nullptr, c.cap_log2,
+      c.global_table ? 0 : (size_t(8) << c.cap_log2), meta, capacity, n_out_dev,
+      reinterpret_cast<int32_t*>(ws + c.rows), reinterpret_cast<int32_t*>(ws + c.n_match),
+      reinterpret_cast<int*>(ws), copy_grid, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "capture launch");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,131 @@
+"""The C ABI without a GPU: the library loads, exports what the header declares,
+and rejects bad arguments on the host (the pages' divide() rule, the power-of-2
+shard count, null and misaligned pointers) before touching the device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import tensor_linear_layers_gb300 as tl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tp_linear.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from tensor_linear_layers_gb300 import _build
+    _build.build()
+    return tl.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tp_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert set(declared_functions()) == set(tl.ABI_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_symbols_have_c_linkage():
+    out = os.popen(f"nm -D --defined-only {tl.LIB_PATH}").read()
+    exported = set(re.findall(r"\bT (tp_[a-z_0-9]+)\b", out))
+    assert set(declared_functions()) <= exported
+
+
+def cfg_mlp(t=2, H=512, I=1408, flags=0):
+    return tl.make_config(tl.TP_BLOCK_MLP, t, H, I, flags=flags)
+
+
+def test_packed_bytes_mlp(L):
+    col, row = tl.packed_weight_bytes(cfg_mlp())
+    assert col == 2 * 1408 * 512 * 2 and row == 512 * 1408 * 2
+
+
+def test_packed_bytes_attention_gqa(L):
+    # 32 q heads, 8 kv heads, hd 128, t=4: shard = 8 q + 2 k + 2 v heads
+    cfg = tl.make_config(tl.TP_BLOCK_ATTN_PROJ, 4, 4096, n_q_heads=32, n_kv_heads=8, head_dim=128)
+    col, row = tl.packed_weight_bytes(cfg)
+    assert col == 4 * 12 * 128 * 4096 * 2
+    assert row == 4096 * 4096 * 2
+    # t=8 with 4 kv heads: kv heads replicated, one per shard
+    cfg = tl.make_config(tl.TP_BLOCK_ATTN_PROJ, 8, 4096, n_q_heads=32, n_kv_heads=4, head_dim=128)
+    col, _ = tl.packed_weight_bytes(cfg)
+    assert col == 8 * (4 + 2) * 128 * 4096 * 2
+
+
+@pytest.mark.parametrize("cfg,code", [
+    (cfg_mlp(t=4, I=1410), tl.TP_ERR_SHAPE),              # divide(): I % t != 0
+    (cfg_mlp(t=3, I=1410), tl.TP_ERR_UNSUPPORTED),        # t not a power of 2
+    (cfg_mlp(t=16, I=4096), tl.TP_ERR_UNSUPPORTED),
+    (cfg_mlp(t=0), tl.TP_ERR_SHAPE),
+    (cfg_mlp(H=500), tl.TP_ERR_UNSUPPORTED),
+    (cfg_mlp(t=8, I=1416), tl.TP_ERR_UNSUPPORTED),        # I/t = 177, not a multiple of 8
+    (cfg_mlp(flags=4), tl.TP_ERR_ARG),
+    (tl.make_config(tl.TP_BLOCK_ATTN_PROJ, 4, 4096, n_q_heads=30, n_kv_heads=6, head_dim=128),
+     tl.TP_ERR_SHAPE),
+    (tl.make_config(tl.TP_BLOCK_ATTN_PROJ, 4, 4096, n_q_heads=24, n_kv_heads=3, head_dim=128),
+     tl.TP_ERR_SHAPE),
+    (tl.make_config(7, 4, 4096), tl.TP_ERR_ARG),
+])
+def test_bad_configs_rejected(L, cfg, code):
+    with pytest.raises(tl.TPError) as e:
+        tl.packed_weight_bytes(cfg)
+    assert e.value.code == code
+
+
+def test_create_rejects_null_and_misaligned_pointers(L):
+    cfg = cfg_mlp()
+    h = ctypes.c_void_p()
+    arr = (ctypes.c_void_p * 3)(0x1000, 0x2000, 0x3000)
+    rc = L.tp_linear_create(ctypes.byref(cfg), arr, 2, ctypes.c_void_p(0x4000), ctypes.c_void_p(0x5000),
+                            None, None, ctypes.byref(h))
+    assert rc == tl.TP_ERR_ARG and b"expected 3" in L.tp_last_error()
+    arr_bad = (ctypes.c_void_p * 3)(0x1000, 0x2008, 0x3000)
+    rc = L.tp_linear_create(ctypes.byref(cfg), arr_bad, 3, ctypes.c_void_p(0x4000), ctypes.c_void_p(0x5000),
+                            None, None, ctypes.byref(h))
+    assert rc == tl.TP_ERR_ARG and b"aligned" in L.tp_last_error()
+    rc = L.tp_linear_create(ctypes.byref(cfg), arr, 3, None, ctypes.c_void_p(0x5000), None, None,
+                            ctypes.byref(h))
+    assert rc == tl.TP_ERR_ARG
+    cfg_n = cfg_mlp(flags=tl.TP_FLAG_HAS_NORM)
+    rc = L.tp_linear_create(ctypes.byref(cfg_n), arr, 3, ctypes.c_void_p(0x4000), ctypes.c_void_p(0x5000),
+                            None, None, ctypes.byref(h))
+    assert rc == tl.TP_ERR_ARG and b"gamma" in L.tp_last_error()
+    assert not h.value
+
+
+def test_null_handle_and_negative_tokens(L):
+    assert L.tp_mlp_forward(None, 4, None, None, None, None, None, None, 0, None) == tl.TP_ERR_ARG
+    assert L.tp_add_rms_norm(-1, 512, None, None, None, 1e-5, None, None, None) == tl.TP_ERR_SHAPE
+    assert L.tp_add_rms_norm(4, 500, None, None, None, 1e-5, None, None, None) == tl.TP_ERR_UNSUPPORTED
+
+
+def test_zero_tokens_enqueue_nothing(L):
+    # T == 0 is a step with no forward pass: valid pointers, nothing launched, TP_OK
+    p = ctypes.c_void_p(0x10000)
+    assert L.tp_add_rms_norm(0, 512, p, p, p, 1e-5, p, p, None) == tl.TP_OK
+
+
+def test_capture_argument_checks(L):
+    b = ctypes.c_int64()
+    assert L.tp_capture_workspace_size(2048, 205, ctypes.byref(b)) == tl.TP_OK and b.value > 0
+    assert L.tp_capture_workspace_size(-1, 1, ctypes.byref(b)) == tl.TP_ERR_SHAPE
+    p = ctypes.c_void_p(0x10000)
+    arr = (ctypes.c_void_p * 1)(0x10000)
+    types = (ctypes.c_int32 * 1)(2)
+    rc = L.tp_capture_rows(16, 512, p, p, p, 4, 9, arr, types, 0, p, p, 8, p, p, 1 << 20, None)
+    assert rc == tl.TP_ERR_UNSUPPORTED     # more than 8 tensors
+    rc = L.tp_capture_rows(16, 512, None, p, p, 4, 1, arr, types, 0, p, p, 8, p, p, 1 << 20, None)
+    assert rc == tl.TP_ERR_ARG
+    rc = L.tp_capture_rows(16, 512, p, p, p, 4, 1, arr, types, 0, p, p, 8, p, p, 16, None)
+    assert rc == tl.TP_ERR_ARG and b"too small" in L.tp_last_error()
