@@ -1,0 +1,508 @@
+"""Benchmark of the tensor-parallel MLP block on GB300 (one JSON line on rank 0).
+
+Default workload: Llama-3-8B-shaped MLP decode (32 tokens, hidden 4096,
+intermediate 14336, t = 8 logical shards, residual add + RMSNorm). A step is
+one pass of the whole block: add + RMSNorm, column-parallel gate_up GEMM with
+SiLU*mul, row-parallel down GEMM with the on-chip shard reduction and the
+residual-stream epilogue. The metric for decode is weight GB/s (weight bytes
+streamed per second); prefill workloads report TFLOP/s.
+
+L2: every step uses one of 4 rotating copies of the weights (4 x 352 MB for
+the decode workload), so no step finds its weights in the 129 MB L2.
+
+--impl reference runs the float64 CPU oracle on the host cores instead (the
+reference arm of this build: there is no other implementation of the
+pages' method to run), each step a bounded sample of the same workload.
+
+Multi-GPU: replicas only. Each rank runs its own copy of the block on its own
+token batch (weak scaling); there is no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+import workloads  # noqa: E402
+
+METRIC = "TP-layout MLP block TFLOP/s (prefill) & weight GB/s (decode) vs GB300 roofline"
+DEFAULT_WORKLOAD = "llama3_8b_mlp_decode"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--rotate", type=int, default=4, help="weight copies rotated across steps")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={','.join(self.FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.15)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, parts[2:]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- distributed
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, ws: int) -> float:
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------- work model
+def work_model(w: workloads.Workload):
+    decode = w.kind == "mlp" and w.T <= 128
+    flops = w.flops()
+    wbytes = w.weight_bytes()
+    abytes = w.activation_bytes()
+    return decode, flops, wbytes, abytes
+
+
+def dominant_kernel_bytes(w: workloads.Workload) -> float:
+    """Algorithmic bytes of one gate_up launch: weights read once, x read, h written."""
+    return 2.0 * (2 * w.I * w.H + w.T * w.H + w.T * w.I)
+
+
+def dominant_kernel_flops(w: workloads.Workload) -> float:
+    if w.kind == "mlp":
+        return 2.0 * w.T * w.H * 2 * w.I
+    return 2.0 * w.T * w.H * (w.nq + 2 * w.nkv) * w.hd
+
+
+# ---------------------------------------------------------------------------- CPU oracle timing
+class OracleSample:
+    """A bounded sample of the workload run through the float64 oracle on the host cores.
+
+    MLP: the first ``rows`` tokens and ``feat`` of the I intermediate features
+    (the block's output is a sum over intermediate features, so the slice is a
+    proportional part of the work and of the weight bytes). Attention: the first
+    ``rows`` tokens through both projections.
+    """
+
+    def __init__(self, w: workloads.Workload, feat: int, rows: int = 32, seed: int = 0):
+        import oracle
+        self.oracle = oracle
+        self.w = w
+        f = oracle.bf16_to_f64
+        rng = np.random.default_rng(seed)
+        self.rows = min(w.T, rows)
+        small = workloads.Workload(**{**w.__dict__, "T": self.rows})
+        if w.kind == "mlp":
+            self.feat = max(8, min(w.I, feat))
+            d = workloads.mlp_inputs(small, T=self.rows)
+            cols = np.sort(rng.choice(w.I, self.feat, replace=False))
+            self.args = (f(d["x"]), f(d["w_gate"])[cols], f(d["w_up"])[cols], f(d["w_down"])[:, cols])
+            self.kw = dict(residual=None if d["residual"] is None else f(d["residual"]),
+                           gamma=None if d["gamma"] is None else f(d["gamma"]), eps=w.eps, norm=w.norm)
+            self.wbytes = 3.0 * w.H * self.feat * 2
+            self.flops = 2.0 * self.rows * w.H * 2 * self.feat + 2.0 * self.rows * self.feat * w.H
+        else:
+            self.feat = 0
+            d = workloads.attn_inputs(small, T=self.rows)
+            self.args = tuple(f(d[k]) for k in ("x", "w_q", "w_k", "w_v", "w_o", "attn"))
+            self.wbytes = float(w.weight_bytes())
+            self.flops = w.flops() * self.rows / w.T
+
+    def run(self):
+        w, o = self.w, self.oracle
+        if w.kind == "mlp":
+            o.mlp_layer(*self.args, **self.kw)
+        else:
+            x, wq, wk, wv, wo, A = self.args
+            o.qkv_parallel(x, wq, wk, wv, w.nq, w.nkv, w.hd, w.t)
+            o.o_proj_parallel(A, wo, w.t)
+
+    def describe(self, n, el):
+        w = self.w
+        if w.kind == "mlp":
+            what = f"{self.rows} of {w.T} tokens x {self.feat} of {w.I} intermediate features (hidden {w.H})"
+        else:
+            what = f"{self.rows} of {w.T} tokens through QKV and o_proj"
+        return f"float64 NumPy oracle, {what}, {n} repetitions in {el:.2f} s"
+
+    def value(self, per_s, decode):
+        return (self.wbytes / per_s / 1e9, "GB/s") if decode else (self.flops / per_s / 1e12, "TFLOP/s")
+
+
+def time_reps(sample: OracleSample, n: int) -> float:
+    t0 = time.perf_counter()
+    for _ in range(n):
+        sample.run()
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w: workloads.Workload, budget_s: float = 12.0):
+    decode = work_model(w)[0]
+    s = OracleSample(w, feat=2048)
+    s.run()
+    per1 = time_reps(s, 1)
+    n = max(1, int(budget_s / max(per1, 1e-6)))
+    el = time_reps(s, n)
+    v, unit = s.value(el / n, decode)
+    return {"value": v, "unit": unit, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": s.describe(n, el)}
+
+
+def config_obj(w: workloads.Workload, n: int, rotate: int, decode: bool):
+    c = {"workload": w.name, "desc": w.desc, "tokens": w.T, "hidden": w.H, "t": w.t}
+    if w.kind == "mlp":
+        c["intermediate"] = w.I
+        c["fused_add_rmsnorm"] = w.norm
+    else:
+        c.update({"n_q_heads": w.nq, "n_kv_heads": w.nkv, "head_dim": w.hd})
+    c["l2"] = f"{rotate} rotating weight copies ({rotate * w.weight_bytes() / 1e9:.2f} GB) > 129 MB L2"
+    c["parallelism"] = f"replicas x{n}" if n > 1 else "single GPU (t shards on one GPU)"
+    return c
+
+
+# ---------------------------------------------------------------------------- reference arm
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    w = workloads.WORKLOADS[args.workload]
+    decode = work_model(w)[0]
+    K = args.steps if args.steps is not None else 20
+    W = args.warmup if args.warmup is not None else 3
+    # size one step so that warm-up + K steps take about two minutes in total
+    target = max(0.002, min(2.0, 120.0 / max(1, K + W)))
+    s = OracleSample(w, feat=2048)
+    s.run()
+    per = time_reps(s, 1)
+    if w.kind == "mlp":
+        feat = int(min(w.I, max(8, 2048 * target / max(per, 1e-6))) // 8 * 8)
+        s = OracleSample(w, feat=max(8, feat))
+    time_reps(s, W)
+    el = time_reps(s, K)
+    value, unit = s.value(el / K, decode)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
+        "steps": K, "warmup": W, "ms_per_step": el / K * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_obj(w, args.gpus, args.rotate, decode),
+        "cpu_baseline": {"value": value, "unit": unit, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                         "sample": s.describe(K, el)},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------- our arm
+def run_ours(args, ws, rank, local):
+    import tensor_linear_layers_gb300 as tl
+    from tensor_linear_layers_gb300 import _build
+    if rank == 0 or ws == 1:
+        _build.build()
+    barrier(ws)
+    tl.lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workloads.WORKLOADS[args.workload]
+    decode, flops, wbytes, abytes = work_model(w)
+    R = max(1, args.rotate)
+    if decode:
+        K = args.steps if args.steps is not None else 10000
+        W = args.warmup if args.warmup is not None else 100
+    else:
+        K = args.steps if args.steps is not None else 50
+        W = args.warmup if args.warmup is not None else 5
+    W = max(W, 3)
+
+    # ---- inputs: same weights on every rank, rank-specific activations (replicas)
+    if w.kind == "mlp":
+        d = workloads.mlp_inputs(w)
+        cfg = tl.make_config(tl.TP_BLOCK_MLP, w.t, w.H, w.I, rms_eps=w.eps,
+                             flags=tl.TP_FLAG_HAS_NORM if w.norm else 0)
+        wl = [d["w_gate"].to(dev), d["w_up"].to(dev), d["w_down"].to(dev)]
+        gamma = None if d["gamma"] is None else d["gamma"].to(dev)
+        blocks = []
+        for r in range(R):
+            blocks.append(tl.TPLinear(cfg, wl, gamma=gamma))
+        del wl
+        xs = [workloads.draw((w.T, w.H), 1000 + rank * R + r, 0).to(dev) for r in range(R)]
+        rs = [workloads.draw((w.T, w.H), 1000 + rank * R + r, 1).to(dev) for r in range(R)] if w.norm else [None] * R
+        outs = [{"mlp_out": torch.empty_like(xs[0]), "residual_out": torch.empty_like(xs[0]) if w.norm else None,
+                 "residual_stream": torch.empty_like(xs[0]) if w.norm else None} for _ in range(R)]
+        for o in outs:
+            for k in [k for k, v in o.items() if v is None]:
+                del o[k]
+        wss = [b.workspace(w.T) for b in blocks]
+        launches_per_step = (1 if w.norm else 0) + 2
+
+        def step(i):
+            j = i % R
+            blocks[j].mlp_forward(xs[j], residual=rs[j], out=outs[j], ws=wss[j])
+
+        def dominant(i):
+            j = i % R
+            blocks[j].gate_up(xs[j], h_out=hbufs[j], ws=wss[j])
+        hbufs = [torch.empty(w.t, w.T, w.I // w.t, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    else:
+        d = workloads.attn_inputs(w)
+        cfg = tl.make_config(tl.TP_BLOCK_ATTN_PROJ, w.t, w.H, n_q_heads=w.nq, n_kv_heads=w.nkv, head_dim=w.hd)
+        wl = [d[k].to(dev) for k in ("w_q", "w_k", "w_v", "w_o")]
+        blocks = [tl.TPLinear(cfg, wl) for _ in range(R)]
+        del wl
+        xs = [workloads.draw((w.T, w.H), 1000 + rank * R + r, 0).to(dev) for r in range(R)]
+        As = [workloads.draw((w.t, w.T, w.nq * w.hd // w.t), 1000 + rank * R + r, 1).to(dev) for r in range(R)]
+        wss = [b.workspace(w.T) for b in blocks]
+        q_per = w.nq // w.t
+        kv_per = 1 if w.t >= w.nkv else w.nkv // w.t
+        qkvs = [torch.empty(w.t, w.T, (q_per + 2 * kv_per) * w.hd, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        oos = [torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        launches_per_step = 2
+
+        def step(i):
+            j = i % R
+            blocks[j].attn_proj_forward(xs[j], As[j], qkv_out=qkvs[j], o_out=oos[j], ws=wss[j])
+
+        def dominant(i):
+            j = i % R
+            blocks[j].attn_proj_forward(xs[j], None, qkv_out=qkvs[j], ws=wss[j])
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    # ---- warm-up
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize()
+    for b, wsb in zip(blocks, wss):
+        st = int(wsb[:4].view(torch.int32).item())
+        if st != 0:
+            raise RuntimeError(f"device status {st} after warm-up")
+
+    # ---- timed region: K whole steps, device-timed with events on the launching stream
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / K
+    ms = max_over_ranks(ms, ws)
+    sec = ms / 1e3
+
+    # ---- dominant kernel alone (column-parallel GEMM), same stream, events around K2 launches
+    K2 = min(K, 2000 if decode else 20)
+    for i in range(3):
+        dominant(i)
+    torch.cuda.synchronize()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for i in range(K2):
+        dominant(i)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dom_s = d0.elapsed_time(d1) / K2 / 1e3
+
+    # ---- end to end through the public API from pinned host buffers
+    K3 = min(K, 500 if decode else 10)
+    if w.kind == "mlp":
+        hx = [xs[j].cpu().pin_memory() for j in range(R)]
+        hr = [rs[j].cpu().pin_memory() if rs[j] is not None else None for j in range(R)]
+        ho = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs[j].items()} for j in range(R)]
+        h2d = sum(t.numel() * 2 for t in (hx[0], hr[0]) if t is not None)
+        d2h = sum(v.numel() * 2 for v in ho[0].values())
+
+        def e2e_step(i):
+            j = i % R
+            xs[j].copy_(hx[j], non_blocking=True)
+            if hr[j] is not None:
+                rs[j].copy_(hr[j], non_blocking=True)
+            blocks[j].mlp_forward(xs[j], residual=rs[j], out=outs[j], ws=wss[j])
+            for k, v in outs[j].items():
+                ho[j][k].copy_(v, non_blocking=True)
+    else:
+        hx = [xs[j].cpu().pin_memory() for j in range(R)]
+        hA = [As[j].cpu().pin_memory() for j in range(R)]
+        hq = [torch.empty(qkvs[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
+        hoo = [torch.empty(oos[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
+        h2d = hx[0].numel() * 2 + hA[0].numel() * 2
+        d2h = hq[0].numel() * 2 + hoo[0].numel() * 2
+
+        def e2e_step(i):
+            j = i % R
+            xs[j].copy_(hx[j], non_blocking=True)
+            As[j].copy_(hA[j], non_blocking=True)
+            blocks[j].attn_proj_forward(xs[j], As[j], qkv_out=qkvs[j], o_out=oos[j], ws=wss[j])
+            hq[j].copy_(qkvs[j], non_blocking=True)
+            hoo[j].copy_(oos[j], non_blocking=True)
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(ws)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for i in range(K3):
+        e2e_step(i)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(f0.elapsed_time(f1) / K3, ws) / 1e3
+
+    for b, wsb in zip(blocks, wss):
+        st = int(wsb[:4].view(torch.int32).item())
+        if st != 0:
+            raise RuntimeError(f"device status {st} after the timed region")
+
+    pk = peaks()
+    if decode:
+        unit = "GB/s"
+        value = ws * wbytes / sec / 1e9
+        e2e_value = ws * wbytes / e2e_s / 1e9
+        dom_alg = dominant_kernel_bytes(w)
+        achieved = dom_alg / dom_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                "kernel": "gate_up column-parallel GEMM (tc_gemm_kernel<swap, GATE_UP>)",
+                "algorithmic_bytes_per_launch": dom_alg, "avg_launch_us": dom_s * 1e6,
+                "peak_source": pk["source"] + " hbm_gbs (copy, burst)"}
+    else:
+        unit = "TFLOP/s"
+        value = ws * flops / sec / 1e12
+        e2e_value = ws * flops / e2e_s / 1e12
+        dom_alg = dominant_kernel_flops(w)
+        achieved = dom_alg / dom_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16_tflops"], "traffic": None,
+                "kernel": "column-parallel GEMM (tc_gemm_kernel<noswap>)",
+                "algorithmic_flops_per_launch": dom_alg, "avg_launch_us": dom_s * 1e6,
+                "peak_source": pk["source"] + " bf16_tflops (cuBLAS burst)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": ws, "steps": K, "warmup": W,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic", "config": config_obj(w, ws, R, decode),
+        "roofline": roof, "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": K * launches_per_step,
+        "detail": {
+            "block_tflops": ws * flops / sec / 1e12,
+            "block_gbs_weights_plus_activations": ws * (wbytes + abytes) / sec / 1e9,
+            "tokens_per_s": ws * w.T / sec,
+            "frac_hbm_measured_weights": (wbytes / sec / 1e9) / pk["hbm_gbs"],
+            "frac_hbm_nominal_8tbs_weights": (wbytes / sec / 1e9) / 8000.0,
+            "frac_bf16_measured": (flops / sec / 1e12) / pk["bf16_tflops"],
+            "plans": blocks[0].plan(w.T),
+        },
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

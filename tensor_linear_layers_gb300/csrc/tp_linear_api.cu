@@ -520,6 +520,7 @@ int tp_add_rms_norm(int64_t T, int64_t H, const void* a, const void* residual_in
   if (H <= 0 || H % 8 != 0) return fail(TP_ERR_UNSUPPORTED, "H must be a positive multiple of 8");
   if (H > max_norm_hidden()) return fail(TP_ERR_UNSUPPORTED, "H > %d", max_norm_hidden());
   if (!(eps >= 0.0f)) return fail(TP_ERR_ARG, "eps must be >= 0");
+  if (T == 0) return ok();
   TP_CHECK_PTR(a, "a");
   TP_CHECK_PTR(residual_in, "residual_in");
   TP_CHECK_PTR(gamma, "gamma");
@@ -538,6 +539,7 @@ int tp_gate_up_forward(tp_linear_t* h, int64_t T, const void* x, void* h_out, vo
   if (h->cfg.kind != TP_BLOCK_MLP) return fail(TP_ERR_ARG, "not an MLP handle");
   int rc = check_T(T);
   if (rc) return rc;
+  if (T == 0) return ok();
   TP_CHECK_PTR(x, "x");
   TP_CHECK_PTR(h_out, "h_out");
   Layout L;
@@ -555,6 +557,7 @@ int tp_down_forward(tp_linear_t* h, int64_t T, const void* h_in, const void* res
   if (h->cfg.kind != TP_BLOCK_MLP) return fail(TP_ERR_ARG, "not an MLP handle");
   int rc = check_T(T);
   if (rc) return rc;
+  if (T == 0) return ok();
   TP_CHECK_PTR(h_in, "h_in");
   TP_CHECK_PTR(mlp_out, "mlp_out");
   if (residual_stream != nullptr) {
@@ -578,6 +581,7 @@ int tp_mlp_forward(tp_linear_t* h, int64_t T, const void* x_in, const void* resi
   if (h->cfg.kind != TP_BLOCK_MLP) return fail(TP_ERR_ARG, "not an MLP handle");
   int rc = check_T(T);
   if (rc) return rc;
+  if (T == 0) return ok();
   const bool norm = (h->cfg.flags & TP_FLAG_HAS_NORM) != 0;
   TP_CHECK_PTR(x_in, "x_in");
   TP_CHECK_PTR(mlp_out, "mlp_out");
@@ -618,6 +622,7 @@ int tp_attn_proj_forward(tp_linear_t* h, int64_t T, const void* x, void* qkv_out
   if (h->cfg.kind != TP_BLOCK_ATTN_PROJ) return fail(TP_ERR_ARG, "not an attention handle");
   int rc = check_T(T);
   if (rc) return rc;
+  if (T == 0) return ok();
   const bool do_qkv = x != nullptr || qkv_out != nullptr;
   const bool do_o = attn_in != nullptr || o_out != nullptr;
   if (do_qkv) {
@@ -681,6 +686,7 @@ int tp_capture_rows(int64_t T, int64_t H, const int32_t* row_req, const int32_t*
   if (n_tensors < 1 || n_tensors > kCaptureMaxTensors)
     return fail(TP_ERR_UNSUPPORTED, "n_tensors must be in [1, %d]", kCaptureMaxTensors);
   if (capacity < 0) return fail(TP_ERR_SHAPE, "capacity must be >= 0");
+  if (T == 0) return ok();
   if (tensors == nullptr || tensor_types == nullptr) return fail(TP_ERR_ARG, "tensor list is null");
   TP_CHECK_PTR(row_req, "row_req");
   TP_CHECK_PTR(row_pos, "row_pos");
