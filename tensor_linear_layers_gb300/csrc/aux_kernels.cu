@@ -3,6 +3,7 @@
 // layout.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <algorithm>
 #include <cstdint>
 
 #include "internal.h"
@@ -262,39 +263,55 @@ cudaError_t launch_capture(int T, int H, const int32_t* row_req, const int32_t* 
 
 // ======================================================================= packing
 // Build the shard layout of a weight ("weight_loader": each rank narrows the
-// full checkpoint tensor to its shard). One CTA copies one packed row.
-__global__ void __launch_bounds__(128) pack_rows_kernel(PackSpec s, __nv_bfloat16* __restrict__ dst) {
-  const int64_t d = blockIdx.x;  // packed row
-  const __nv_bfloat16* src = nullptr;
-  if (s.mode == PACK_GATE_UP) {
-    // dst [t][2][Is][H]  <-  gate / up rows r*Is + i
-    const int64_t i = d % s.Is, g = (d / s.Is) % 2, r = d / (2 * s.Is);
-    src = s.src[g] + (r * s.Is + i) * s.width;
-  } else if (s.mode == PACK_ROW) {
-    // dst [t][N][Ks]  <-  W[n][r*Ks : (r+1)*Ks]   (W is [N][t*Ks])
-    const int64_t n = d % s.N, r = d / s.N;
-    src = s.src[0] + n * (s.t * s.width) + r * s.width;
-  } else {
-    // PACK_QKV: dst [t][ws][H], shard r = [q heads | k heads | v heads]
-    const int64_t c = d % s.ws, r = d / s.ws;
-    const int64_t qpart = (int64_t)s.q_per * s.hd, kvpart = (int64_t)s.kv_per * s.hd;
-    if (c < qpart) {
-      src = s.src[0] + (r * qpart + c) * s.width;
+// full checkpoint tensor to its shard), tiled into 32 KB blocks of 256 rows x
+// 64 K elements, each 16-byte chunk stored at its 128-byte-swizzled position:
+// within a row rr of a block, logical chunk c sits at physical chunk
+// c ^ (rr % 8). One thread writes one 16-byte chunk.
+__global__ void __launch_bounds__(256) pack_tiles_kernel(PackSpec s, int64_t n_chunks, uint4* __restrict__ dst) {
+  for (int64_t id = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; id < n_chunks;
+       id += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t blk = id >> 11;          // 2048 chunks per block
+    const int rr = (int)((id >> 3) & 255);
+    const int c = (int)(id & 7) ^ (rr & 7);
+    const int64_t wt = blk / s.nkb, kb = blk - wt * s.nkb;
+    const __nv_bfloat16* src = nullptr;
+    if (s.mode == PACK_GATE_UP) {
+      // block = [128 gate rows | 128 up rows] of shard r, feature block b
+      const int64_t r = wt / s.nb, b = wt - r * s.nb;
+      const int64_t i = b * 128 + (rr & 127), k = kb * 64 + c * 8;
+      if (i < s.Is && k < s.H) src = s.src[rr >> 7] + (r * s.Is + i) * s.H + k;
+    } else if (s.mode == PACK_QKV) {
+      // packed row n = [shard r: q heads | k heads | v heads]
+      const int64_t n = wt * 256 + rr, k = kb * 64 + c * 8;
+      if (n < s.n_col && k < s.H) {
+        const int64_t r = n / s.ws, cc = n - r * s.ws;
+        const int64_t qpart = (int64_t)s.q_per * s.hd, kvpart = (int64_t)s.kv_per * s.hd;
+        if (cc < qpart) {
+          src = s.src[0] + (r * qpart + cc) * s.H + k;
+        } else {
+          const int64_t e = cc - qpart;
+          const int which = e < kvpart ? 1 : 2;
+          const int64_t ek = e < kvpart ? e : e - kvpart;
+          const int64_t head = (s.rep > 1) ? (r / s.rep) : (r * s.kv_per + ek / s.hd);
+          src = s.src[which] + (head * s.hd + ek % s.hd) * s.H + k;
+        }
+      }
     } else {
-      const int64_t cc = (c - qpart) % kvpart;
-      const int which = (c - qpart) < kvpart ? 1 : 2;
-      const int64_t head = (s.rep > 1) ? (r / s.rep) : (r * s.kv_per + cc / s.hd);
-      src = s.src[which] + (head * s.hd + cc % s.hd) * s.width;
+      // PACK_ROW: output row n, global k-block kb = shard r, local k-block kk
+      const int64_t n = wt * 256 + rr;
+      const int64_t r = kb / s.kbs, kk = kb - r * s.kbs;
+      const int64_t k = kk * 64 + c * 8;
+      if (n < s.H && k < s.Is) src = s.src[0] + n * (s.t * s.Is) + r * s.Is + k;
     }
+    dst[id] = src != nullptr ? *reinterpret_cast<const uint4*>(src) : make_uint4(0u, 0u, 0u, 0u);
   }
-  const uint4* sv = reinterpret_cast<const uint4*>(src);
-  uint4* dv = reinterpret_cast<uint4*>(dst + d * s.width);
-  for (int v = threadIdx.x; v < s.width / 8; v += blockDim.x) dv[v] = sv[v];
 }
 
-cudaError_t launch_pack(const PackSpec& s, int64_t rows, void* dst, cudaStream_t st) {
-  if (rows <= 0) return cudaSuccess;
-  pack_rows_kernel<<<static_cast<unsigned>(rows), 128, 0, st>>>(s, static_cast<__nv_bfloat16*>(dst));
+cudaError_t launch_pack(const PackSpec& s, int64_t n_blocks, void* dst, cudaStream_t st) {
+  if (n_blocks <= 0) return cudaSuccess;
+  const int64_t n_chunks = n_blocks * 2048;
+  const int64_t grid = std::min<int64_t>((n_chunks + 255) / 256, 1 << 16);
+  pack_tiles_kernel<<<(unsigned)grid, 256, 0, st>>>(s, n_chunks, static_cast<uint4*>(dst));
   return cudaGetLastError();
 }
 

@@ -1,26 +1,26 @@
-// Decode-shaped (swapped operand) instantiations of KIND_COL: A = weight rows,
-// B = the step's tokens (N = 16 .. 128).
+// Decode-shaped (swapped operand) instantiations of KIND_COL: A = 256 weight
+// rows, B = the step's tokens (N = 16 .. 128).
 #include "gemm_launch.cuh"
 
 namespace tpl {
 
-cudaError_t launch_gemm_decode_col(int bn, const CUtensorMap& a, const CUtensorMap& w,
-                                  const GemmParams& p, int grid, cudaStream_t st) {
+cudaError_t launch_gemm_decode_col(int bn, const CUtensorMap& a, const GemmParams& p, int grid,
+                                  cudaStream_t st) {
   switch (bn) {
-    case 16: return launch_one<true, KIND_COL, 16, 1>(a, w, p, grid, st);
-    case 32: return launch_one<true, KIND_COL, 32, 1>(a, w, p, grid, st);
-    case 64: return launch_one<true, KIND_COL, 64, 1>(a, w, p, grid, st);
-    case 128: return launch_one<true, KIND_COL, 128, 1>(a, w, p, grid, st);
+    case 16: return launch_one<true, KIND_COL, 16>(a, p, grid, st);
+    case 32: return launch_one<true, KIND_COL, 32>(a, p, grid, st);
+    case 64: return launch_one<true, KIND_COL, 64>(a, p, grid, st);
+    case 128: return launch_one<true, KIND_COL, 128>(a, p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 int gemm_stages_decode_col(int bn) {
   switch (bn) {
-    case 16: return GemmShape<true, KIND_COL, 16, 1>::kStages;
-    case 32: return GemmShape<true, KIND_COL, 32, 1>::kStages;
-    case 64: return GemmShape<true, KIND_COL, 64, 1>::kStages;
-    case 128: return GemmShape<true, KIND_COL, 128, 1>::kStages;
+    case 16: return GemmShape<true, KIND_COL, 16>::kStages;
+    case 32: return GemmShape<true, KIND_COL, 32>::kStages;
+    case 64: return GemmShape<true, KIND_COL, 64>::kStages;
+    case 128: return GemmShape<true, KIND_COL, 128>::kStages;
     default: return 0;
   }
 }

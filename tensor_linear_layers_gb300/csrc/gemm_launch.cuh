@@ -6,11 +6,10 @@
 
 namespace tpl {
 
-template <bool SWAP, int KIND, int BN, int NA>
-cudaError_t launch_one(const CUtensorMap& map_act, const CUtensorMap& map_w, const GemmParams& p,
-                       int grid, cudaStream_t st) {
-  using S = GemmShape<SWAP, KIND, BN, NA>;
-  auto kernel = tc_gemm_kernel<SWAP, KIND, BN, NA>;
+template <bool SWAP, int KIND, int BN>
+cudaError_t launch_one(const CUtensorMap& map_act, const GemmParams& p, int grid, cudaStream_t st) {
+  using S = GemmShape<SWAP, KIND, BN>;
+  auto kernel = tc_gemm_kernel<SWAP, KIND, BN>;
   static std::atomic<uint64_t> attr_done{0};  // one bit per device ordinal
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -21,8 +20,22 @@ cudaError_t launch_one(const CUtensorMap& map_act, const CUtensorMap& map_w, con
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit, std::memory_order_acq_rel);
   }
-  kernel<<<grid, 192, S::kSmemBytes, st>>>(map_act, map_w, p);
-  return cudaGetLastError();
+  if (p.splits == 1) {
+    kernel<<<grid, 192, S::kSmemBytes, st>>>(map_act, p);
+    return cudaGetLastError();
+  }
+  // split-K ends in a grid-wide barrier: launch cooperatively so every CTA is resident
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = S::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, map_act, p);
 }
 
 }  // namespace tpl

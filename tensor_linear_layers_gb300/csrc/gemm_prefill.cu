@@ -3,21 +3,21 @@
 
 namespace tpl {
 
-cudaError_t launch_gemm_prefill(int kind, const CUtensorMap& a, const CUtensorMap& w,
-                                const GemmParams& p, int grid, cudaStream_t st) {
+cudaError_t launch_gemm_prefill(int kind, const CUtensorMap& a, const GemmParams& p, int grid,
+                                cudaStream_t st) {
   switch (kind) {
-    case KIND_GATE_UP: return launch_one<false, KIND_GATE_UP, 256, 1>(a, w, p, grid, st);
-    case KIND_COL: return launch_one<false, KIND_COL, 256, 1>(a, w, p, grid, st);
-    case KIND_ROW: return launch_one<false, KIND_ROW, 256, 1>(a, w, p, grid, st);
+    case KIND_GATE_UP: return launch_one<false, KIND_GATE_UP, 256>(a, p, grid, st);
+    case KIND_COL: return launch_one<false, KIND_COL, 256>(a, p, grid, st);
+    case KIND_ROW: return launch_one<false, KIND_ROW, 256>(a, p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 int gemm_stages_prefill(int kind) {
   switch (kind) {
-    case KIND_GATE_UP: return GemmShape<false, KIND_GATE_UP, 256, 1>::kStages;
-    case KIND_COL: return GemmShape<false, KIND_COL, 256, 1>::kStages;
-    case KIND_ROW: return GemmShape<false, KIND_ROW, 256, 1>::kStages;
+    case KIND_GATE_UP: return GemmShape<false, KIND_GATE_UP, 256>::kStages;
+    case KIND_COL: return GemmShape<false, KIND_COL, 256>::kStages;
+    case KIND_ROW: return GemmShape<false, KIND_ROW, 256>::kStages;
     default: return 0;
   }
 }

@@ -1,32 +1,42 @@
 // Persistent, warp-specialised tcgen05 GEMM engine for the tensor-parallel
 // linear block.
 //
-//   warp 0      : TMA producer (one elected thread) filling a ring of shared-
-//                 memory stages, each guarded by a full/empty mbarrier pair
+//   warp 0      : producer (one elected thread): the weight block of a stage
+//                 is one contiguous 32 KB bulk copy, the activation tile a
+//                 TMA tensor copy; a ring of shared-memory stages guarded by
+//                 full/empty mbarrier pairs
 //   warp 1      : tensor-memory allocator + MMA issuer (one elected thread)
 //   warps 2..5  : epilogue: tcgen05.ld from the fp32 accumulator, fused
 //                 SiLU*mul / residual add, bf16 stores; split-K fix-up
 //
-// The accumulator lives in tensor memory, double-buffered so the epilogue of
-// one tile overlaps the main loop of the next. Operand A feeds the UMMA M side
-// (128 rows per accumulator, NA accumulators), operand B the N side (BN rows).
+// Weights are packed once, at create time, as blocks of 256 rows x 64 K
+// elements (32 KB), already in the 128-byte-swizzled K-major image that the
+// MMA reads from shared memory; block (w_tile, kb) lives at
+// w_packed + (w_tile * nkb + kb) * 32 KB, so a unit of work streams one
+// contiguous stretch of memory.
 //
-//   SWAP = false (prefill): A = activations (128 tokens), B = weights (BN = 256).
-//   SWAP = true  (decode) : A = weights (NA x 128 rows), B = activations (BN >= tokens).
+// Operand A feeds the UMMA M side (128 rows per accumulator, NA
+// accumulators), operand B the N side (BN rows):
+//   SWAP = false (prefill): A = 128 tokens, B = 256 weight rows (BN = 256).
+//   SWAP = true  (decode) : A = 256 weight rows (two M=128 accumulators),
+//                           B = the step's tokens (BN = 16 .. 128).
 //
 // Kinds:
-//   KIND_GATE_UP : column-parallel merged gate/up. A weight tile is 128 gate
-//                  rows + the matching 128 up rows of one shard, so one
-//                  thread holds g and u of the same intermediate feature and
-//                  applies silu(g) * u in registers. Output h [t][T][I/t].
+//   KIND_GATE_UP : column-parallel merged gate/up. A weight block holds 128
+//                  gate rows and the matching 128 up rows of one shard, so
+//                  one thread holds g and u of the same intermediate feature
+//                  and applies silu(g) * u in registers. Output h [t][T][I/t].
 //   KIND_COL     : column-parallel plain store, output split per shard
 //                  [t][T][w_s] (QKV by head).
 //   KIND_ROW     : row-parallel: the K loop runs over all t shards in turn,
 //                  so the shards' partial sums add up in the accumulator (the
-//                  on-chip replacement of the all-reduce); with split-K the
-//                  fp32 partials of the splits are added by the last split to
-//                  arrive, in ascending split order (deterministic).
-//                  Output y [T][N], optional y + residual.
+//                  on-chip replacement of the all-reduce). Output y [T][N],
+//                  optional y + residual.
+//
+// Split-K (splits > 1, few tiles): every unit writes its fp32 partial tile;
+// after a grid-wide barrier (cooperative launch, so all CTAs are resident;
+// the wait is bounded) all CTAs together add the partials of each tile in
+// ascending split order (deterministic) and apply the epilogue.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -36,8 +46,9 @@ namespace tpl {
 
 enum GemmKind : int { KIND_GATE_UP = 0, KIND_COL = 1, KIND_ROW = 2 };
 
-// status codes written by kernels (mirror TP_ERR_* of the public header)
-constexpr int kStatusTimeout = -6;
+constexpr int kStatusTimeout = -6;     // mirrors TP_ERR_TIMEOUT
+constexpr int kWBlockRows = 256;       // rows of one packed weight block
+constexpr int kWBlockBytes = kWBlockRows * 128;  // 256 rows x 64 bf16
 
 struct GemmParams {
   int T;             // tokens
@@ -47,23 +58,25 @@ struct GemmParams {
   int units;         // m_tiles * n_tiles * splits
   int nkb;           // 64-wide k-blocks per tile (all shards for KIND_ROW)
   int kbs;           // k-blocks per shard (KIND_ROW)
-  int nb;            // KIND_GATE_UP: 128-row blocks per shard
+  int nb;            // KIND_GATE_UP: 128-row gate blocks per shard
   int group_m;       // raster group along M (SWAP = false)
   int Is;            // KIND_GATE_UP: I / t
   int n_out;         // KIND_COL / KIND_ROW: output features
   int ws_out;        // KIND_COL: features per output shard (== n_out if unsplit)
+  const uint8_t* w_packed;     // packed weight blocks
   __nv_bfloat16* out;
   __nv_bfloat16* out2;         // KIND_ROW: y + resid (nullable)
   const __nv_bfloat16* resid;  // KIND_ROW: residual [T][n_out]
-  float* partials;             // split-K fp32 partials
-  int* counters;               // split-K arrival counters, one per tile
+  float* partials;             // split-K fp32 partials [tile][split][col][128 rows]
+  unsigned* gbar;              // grid barrier {arrivals, generation}
   int* status;                 // device status word
   unsigned long long timeout_ns;
 };
 
-template <bool SWAP, int KIND, int BN, int NA>
+template <bool SWAP, int KIND, int BN>
 struct GemmShape {
-  static constexpr int kABytes = NA * 128 * 128;  // NA x 128 rows x 64 bf16
+  static constexpr int NA = SWAP ? 2 : 1;                // accumulators (128 rows each)
+  static constexpr int kABytes = NA * 128 * 128;          // A tile: NA x 128 rows x 64 bf16
   static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kSmemBudget = 221 * 1024;
@@ -75,13 +88,15 @@ struct GemmShape {
                                    : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
-  // epilogue column groups: GATE_UP pairs (g, u) at distance kUOff
-  static constexpr int kNG = (KIND == KIND_GATE_UP) ? (SWAP ? BN : 128) : BN;
+  // epilogue segments: a segment is a run of kNG accumulator columns; GATE_UP
+  // pairs each gate column with the up column kUOff further on
+  static constexpr int kSeg = (SWAP && KIND != KIND_GATE_UP) ? 2 : 1;
+  static constexpr int kNG = (KIND == KIND_GATE_UP && !SWAP) ? 128 : BN;
   static constexpr int kUOff = SWAP ? BN : 128;
   static constexpr int kCh = kNG >= 32 ? 32 : 16;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
-  static_assert(KIND != KIND_GATE_UP || (SWAP ? NA == 2 : (NA == 1 && BN == 256)), "gate/up tile");
+  static_assert(SWAP || BN == 256, "prefill tiles are 128 x 256");
   static_assert(kStages >= 2, "pipeline depth");
   static_assert(kTmemNeed <= 512, "tensor memory");
 };
@@ -93,12 +108,139 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <bool SWAP, int KIND, int BN, int NA>
+// Epilogue of N (multiple of 8) accumulator columns c0 .. c0+N-1 of segment
+// `seg` in accumulator row `row`; g = values (gate for GATE_UP), u = up values.
+template <bool SWAP, int KIND, int BN, int N>
+__device__ __forceinline__ void emit_vals(const GemmParams& p, int tm, int tn, int seg, int row, int c0,
+                                          const float* g, const float* u) {
+    if (!SWAP) {
+      const int m = tm * 128 + row;
+      if (m >= p.T) return;
+      if (KIND == KIND_GATE_UP) {
+        const int r = tn / p.nb, blk = tn - r * p.nb;
+        const int i0 = blk * 128 + c0;
+        __nv_bfloat16* dst = p.out + ((size_t)r * p.T + m) * p.Is + i0;
+#pragma unroll
+        for (int j = 0; j < N; j += 8) {
+          if (i0 + j < p.Is) {
+            uint4 v;
+            v.x = pack_bf16x2(silu_f(g[j + 0]) * u[j + 0], silu_f(g[j + 1]) * u[j + 1]);
+            v.y = pack_bf16x2(silu_f(g[j + 2]) * u[j + 2], silu_f(g[j + 3]) * u[j + 3]);
+            v.z = pack_bf16x2(silu_f(g[j + 4]) * u[j + 4], silu_f(g[j + 5]) * u[j + 5]);
+            v.w = pack_bf16x2(silu_f(g[j + 6]) * u[j + 6], silu_f(g[j + 7]) * u[j + 7]);
+            *reinterpret_cast<uint4*>(dst + j) = v;
+          }
+        }
+      } else if (KIND == KIND_COL) {
+#pragma unroll
+        for (int j = 0; j < N; j += 8) {
+          const int n = tn * BN + c0 + j;
+          if (n < p.n_out) {
+            const int ro = n / p.ws_out, c = n - ro * p.ws_out;
+            uint4 v;
+            v.x = pack_bf16x2(g[j + 0], g[j + 1]);
+            v.y = pack_bf16x2(g[j + 2], g[j + 3]);
+            v.z = pack_bf16x2(g[j + 4], g[j + 5]);
+            v.w = pack_bf16x2(g[j + 6], g[j + 7]);
+            *reinterpret_cast<uint4*>(p.out + ((size_t)ro * p.T + m) * p.ws_out + c) = v;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < N; j += 8) {
+          const int n = tn * BN + c0 + j;
+          if (n < p.n_out) {
+            const size_t off = (size_t)m * p.n_out + n;
+            uint4 v;
+            v.x = pack_bf16x2(g[j + 0], g[j + 1]);
+            v.y = pack_bf16x2(g[j + 2], g[j + 3]);
+            v.z = pack_bf16x2(g[j + 4], g[j + 5]);
+            v.w = pack_bf16x2(g[j + 6], g[j + 7]);
+            *reinterpret_cast<uint4*>(p.out + off) = v;
+            if (p.out2 != nullptr) {
+              const uint4 rv = *reinterpret_cast<const uint4*>(p.resid + off);
+              const __nv_bfloat162* rb = reinterpret_cast<const __nv_bfloat162*>(&rv);
+              const float2 r0 = __bfloat1622float2(rb[0]), r1 = __bfloat1622float2(rb[1]);
+              const float2 r2 = __bfloat1622float2(rb[2]), r3 = __bfloat1622float2(rb[3]);
+              uint4 w;
+              w.x = pack_bf16x2(g[j + 0] + r0.x, g[j + 1] + r0.y);
+              w.y = pack_bf16x2(g[j + 2] + r1.x, g[j + 3] + r1.y);
+              w.z = pack_bf16x2(g[j + 4] + r2.x, g[j + 5] + r2.y);
+              w.w = pack_bf16x2(g[j + 6] + r3.x, g[j + 7] + r3.y);
+              *reinterpret_cast<uint4*>(p.out2 + off) = w;
+            }
+          }
+        }
+      }
+    } else {
+      // accumulator rows are output features, columns are tokens
+      if (KIND == KIND_GATE_UP) {
+        const int r = tm / p.nb, blk = tm - r * p.nb;
+        const int i = blk * 128 + row;
+        if (i >= p.Is) return;
+        __nv_bfloat16* dst = p.out + (size_t)r * p.T * p.Is + i;
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+          const int tok = tn * BN + c0 + j;
+          if (tok < p.T) dst[(size_t)tok * p.Is] = __float2bfloat16_rn(silu_f(g[j]) * u[j]);
+        }
+      } else if (KIND == KIND_COL) {
+        const int f = tm * 256 + seg * 128 + row;
+        if (f >= p.n_out) return;
+        const int ro = f / p.ws_out, c = f - ro * p.ws_out;
+        __nv_bfloat16* dst = p.out + (size_t)ro * p.T * p.ws_out + c;
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+          const int tok = tn * BN + c0 + j;
+          if (tok < p.T) dst[(size_t)tok * p.ws_out] = __float2bfloat16_rn(g[j]);
+        }
+      } else {
+        const int f = tm * 256 + seg * 128 + row;
+        if (f >= p.n_out) return;
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+          const int tok = tn * BN + c0 + j;
+          if (tok < p.T) {
+            const size_t off = (size_t)tok * p.n_out + f;
+            p.out[off] = __float2bfloat16_rn(g[j]);
+            if (p.out2 != nullptr)
+              p.out2[off] = __float2bfloat16_rn(g[j] + __bfloat162float(p.resid[off]));
+          }
+        }
+      }
+    }
+}
+
+// Grid-wide barrier for a cooperative launch, called by one thread per CTA.
+// gbar[0] counts arrivals and is reset by the last CTA to arrive, which then
+// bumps the generation gbar[1] that the others wait on. Bounded: returns
+// false after timeout_ns.
+__device__ __forceinline__ bool grid_barrier(unsigned* gbar, unsigned nblocks, unsigned long long timeout_ns) {
+  volatile unsigned* vgen = gbar + 1;
+  const unsigned gen = *vgen;
+  __threadfence();
+  const unsigned old = atomicAdd(gbar, 1u);
+  if (old == nblocks - 1) {
+    atomicExch(gbar, 0u);
+    __threadfence();
+    atomicAdd(gbar + 1, 1u);
+    return true;
+  }
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; *vgen == gen; ++it) {
+    __nanosleep(64);
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+  __threadfence();
+  return true;
+}
+
+template <bool SWAP, int KIND, int BN>
 __global__ void __launch_bounds__(192, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_act,
-                   const __grid_constant__ CUtensorMap map_w, const GemmParams p) {
-  using S = GemmShape<SWAP, KIND, BN, NA>;
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_act, const GemmParams p) {
+  using S = GemmShape<SWAP, KIND, BN>;
   constexpr int STAGES = S::kStages;
+  constexpr int NA = S::NA;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -113,7 +255,6 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* misc = base_ptr + STAGES * S::kStageBytes + 8 * (2 * STAGES + 5);
   volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(misc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 4);
-  volatile int* s_last = reinterpret_cast<volatile int*>(misc + 8);
   volatile int* s_ok = reinterpret_cast<volatile int*>(misc + 12);
 
   const int warp = threadIdx.x >> 5;
@@ -130,10 +271,8 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(done_bar, 1);
     *s_abort = 0;
-    *s_last = 0;
     fence_barrier_init();
     prefetch_tensormap(&map_act);
-    prefetch_tensormap(&map_w);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(s_tmem)), S::kTmemCols);
@@ -166,7 +305,9 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
+      // decode streams each weight byte once: keep it out of L2's way;
+      // prefill re-reads weight blocks from L2 across token tiles
+      const uint64_t pol_w = SWAP ? policy_evict_first() : policy_evict_normal();
       const uint64_t pol_a = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
@@ -177,6 +318,8 @@ __global__ void __launch_bounds__(192, 1)
         decode_unit(u, tm, tn, sp);
         const int kb0 = (int)((long long)sp * p.nkb / p.splits);
         const int kb1 = (int)((long long)(sp + 1) * p.nkb / p.splits);
+        const int wt = SWAP ? tm : tn;
+        const uint8_t* wsrc = p.w_packed + (size_t)wt * p.nkb * kWBlockBytes;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, p.timeout_ns)) {
             if (!*s_abort) {
@@ -195,30 +338,13 @@ __global__ void __launch_bounds__(192, 1)
             shard = kb / p.kbs;
             kx = (kb - shard * p.kbs) * 64;
           }
+          const uint8_t* wblk = wsrc + (size_t)kb * kWBlockBytes;
           if (!SWAP) {
-            // A: 128 tokens of the activation
-            tma_load_4d(sa, &map_act, fb, kx, tm * 128, 0, shard, pol_a);
-            // B: weight rows
-            if (KIND == KIND_GATE_UP) {
-              const int r = tn / p.nb, blk = tn - r * p.nb;
-              tma_load_4d(sb, &map_w, fb, kx, blk * 128, 0, r, pol_w);
-              tma_load_4d(sb + 128 * 128, &map_w, fb, kx, blk * 128, 1, r, pol_w);
-            } else {
-              tma_load_4d(sb, &map_w, fb, kx, tn * BN, 0, shard, pol_w);
-            }
+            tma_load_4d(sa, &map_act, fb, kx, tm * 128, 0, shard, pol_a);   // 128 tokens
+            bulk_load(sb, wblk, kWBlockBytes, fb, pol_w);                   // 256 weight rows
           } else {
-            // A: weight rows (NA x 128)
-            if (KIND == KIND_GATE_UP) {
-              const int r = tm / p.nb, blk = tm - r * p.nb;
-              tma_load_4d(sa, &map_w, fb, kx, blk * 128, 0, r, pol_w);
-              tma_load_4d(sa + 128 * 128, &map_w, fb, kx, blk * 128, 1, r, pol_w);
-            } else {
-#pragma unroll
-              for (int a = 0; a < NA; ++a)
-                tma_load_4d(sa + a * 128 * 128, &map_w, fb, kx, (tm * NA + a) * 128, 0, shard, pol_w);
-            }
-            // B: BN tokens of the activation
-            tma_load_4d(sb, &map_act, fb, kx, tn * BN, 0, shard, pol_a);
+            bulk_load(sa, wblk, kWBlockBytes, fb, pol_w);                   // 256 weight rows
+            tma_load_4d(sb, &map_act, fb, kx, tn * BN, 0, shard, pol_a);    // BN tokens
           }
           issued_mask |= 1u << stage;
           last_phase_bits = (last_phase_bits & ~(1u << stage)) | (phase << stage);
@@ -309,106 +435,6 @@ __global__ void __launch_bounds__(192, 1)
     constexpr int CH = S::kCh;
     constexpr int ACC = S::kAccCols;
 
-    // Apply the epilogue to one chunk of CH column groups starting at c0.
-    auto emit = [&](int tm, int tn, int c0, const float* g, const float* u) {
-      if (!SWAP) {
-        const int m = tm * 128 + row;
-        if (m >= p.T) return;
-        if (KIND == KIND_GATE_UP) {
-          const int r = tn / p.nb, blk = tn - r * p.nb;
-          const int i0 = blk * 128 + c0;
-          __nv_bfloat16* dst = p.out + ((size_t)r * p.T + m) * p.Is + i0;
-#pragma unroll
-          for (int j = 0; j < CH; j += 8) {
-            if (i0 + j < p.Is) {
-              uint4 v;
-              v.x = pack_bf16x2(silu_f(g[j + 0]) * u[j + 0], silu_f(g[j + 1]) * u[j + 1]);
-              v.y = pack_bf16x2(silu_f(g[j + 2]) * u[j + 2], silu_f(g[j + 3]) * u[j + 3]);
-              v.z = pack_bf16x2(silu_f(g[j + 4]) * u[j + 4], silu_f(g[j + 5]) * u[j + 5]);
-              v.w = pack_bf16x2(silu_f(g[j + 6]) * u[j + 6], silu_f(g[j + 7]) * u[j + 7]);
-              *reinterpret_cast<uint4*>(dst + j) = v;
-            }
-          }
-        } else if (KIND == KIND_COL) {
-#pragma unroll
-          for (int j = 0; j < CH; j += 8) {
-            const int n = tn * BN + c0 + j;
-            if (n < p.n_out) {
-              const int ro = n / p.ws_out, c = n - ro * p.ws_out;
-              uint4 v;
-              v.x = pack_bf16x2(g[j + 0], g[j + 1]);
-              v.y = pack_bf16x2(g[j + 2], g[j + 3]);
-              v.z = pack_bf16x2(g[j + 4], g[j + 5]);
-              v.w = pack_bf16x2(g[j + 6], g[j + 7]);
-              *reinterpret_cast<uint4*>(p.out + ((size_t)ro * p.T + m) * p.ws_out + c) = v;
-            }
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < CH; j += 8) {
-            const int n = tn * BN + c0 + j;
-            if (n < p.n_out) {
-              const size_t off = (size_t)m * p.n_out + n;
-              uint4 v;
-              v.x = pack_bf16x2(g[j + 0], g[j + 1]);
-              v.y = pack_bf16x2(g[j + 2], g[j + 3]);
-              v.z = pack_bf16x2(g[j + 4], g[j + 5]);
-              v.w = pack_bf16x2(g[j + 6], g[j + 7]);
-              *reinterpret_cast<uint4*>(p.out + off) = v;
-              if (p.out2 != nullptr) {
-                const uint4 rv = *reinterpret_cast<const uint4*>(p.resid + off);
-                const __nv_bfloat162* rb = reinterpret_cast<const __nv_bfloat162*>(&rv);
-                float2 r0 = __bfloat1622float2(rb[0]), r1 = __bfloat1622float2(rb[1]);
-                float2 r2 = __bfloat1622float2(rb[2]), r3 = __bfloat1622float2(rb[3]);
-                uint4 w;
-                w.x = pack_bf16x2(g[j + 0] + r0.x, g[j + 1] + r0.y);
-                w.y = pack_bf16x2(g[j + 2] + r1.x, g[j + 3] + r1.y);
-                w.z = pack_bf16x2(g[j + 4] + r2.x, g[j + 5] + r2.y);
-                w.w = pack_bf16x2(g[j + 6] + r3.x, g[j + 7] + r3.y);
-                *reinterpret_cast<uint4*>(p.out2 + off) = w;
-              }
-            }
-          }
-        }
-      } else {
-        // rows are output features, columns are tokens
-        if (KIND == KIND_GATE_UP) {
-          const int r = tm / p.nb, blk = tm - r * p.nb;
-          const int i = blk * 128 + row;
-          if (i >= p.Is) return;
-          __nv_bfloat16* dst = p.out + (size_t)r * p.T * p.Is + i;
-#pragma unroll
-          for (int j = 0; j < CH; ++j) {
-            const int tok = tn * BN + c0 + j;
-            if (tok < p.T) dst[(size_t)tok * p.Is] = __float2bfloat16_rn(silu_f(g[j]) * u[j]);
-          }
-        } else if (KIND == KIND_COL) {
-          const int f = tm * 128 + row;
-          if (f >= p.n_out) return;
-          const int ro = f / p.ws_out, c = f - ro * p.ws_out;
-          __nv_bfloat16* dst = p.out + (size_t)ro * p.T * p.ws_out + c;
-#pragma unroll
-          for (int j = 0; j < CH; ++j) {
-            const int tok = tn * BN + c0 + j;
-            if (tok < p.T) dst[(size_t)tok * p.ws_out] = __float2bfloat16_rn(g[j]);
-          }
-        } else {
-          const int f = tm * 128 + row;
-          if (f >= p.n_out) return;
-#pragma unroll
-          for (int j = 0; j < CH; ++j) {
-            const int tok = tn * BN + c0 + j;
-            if (tok < p.T) {
-              const size_t off = (size_t)tok * p.n_out + f;
-              p.out[off] = __float2bfloat16_rn(g[j]);
-              if (p.out2 != nullptr)
-                p.out2[off] = __float2bfloat16_rn(g[j] + __bfloat162float(p.resid[off]));
-            }
-          }
-        }
-      }
-    };
-
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
       int tm, tn, sp;
       decode_unit(u, tm, tn, sp);
@@ -432,13 +458,17 @@ __global__ void __launch_bounds__(192, 1)
       float g[CH], uu[CH];
       if (p.splits == 1) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < S::kNG; c0 += CH) {
-          if (CH == 32) tmem_ld32(acc + c0, g); else tmem_ld16(acc + c0, g);
-          if (KIND == KIND_GATE_UP) {
-            if (CH == 32) tmem_ld32(acc + S::kUOff + c0, uu); else tmem_ld16(acc + S::kUOff + c0, uu);
+        for (int seg = 0; seg < S::kSeg; ++seg) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < S::kNG; c0 += CH) {
+            const uint32_t col = seg * BN + c0;
+            if (CH == 32) tmem_ld32(acc + col, g); else tmem_ld16(acc + col, g);
+            if (KIND == KIND_GATE_UP) {
+              if (CH == 32) tmem_ld32(acc + S::kUOff + col, uu); else tmem_ld16(acc + S::kUOff + col, uu);
+            }
+            tc_wait_ld();
+            emit_vals<SWAP, KIND, BN, CH>(p, tm, tn, seg, row, c0, g, uu);
           }
-          tc_wait_ld();
-          emit(tm, tn, c0, g, uu);
         }
         tc_fence_before();
         __syncwarp();
@@ -455,36 +485,6 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty_bar(buf));
-        __threadfence();
-        named_bar_sync(1, 128);
-        if (et == 0) {
-          const int old = atomicAdd(p.counters + tile, 1);
-          const int last = (old == p.splits - 1);
-          if (last) p.counters[tile] = 0;
-          *s_last = last;
-        }
-        named_bar_sync(1, 128);
-        const int last = *s_last;
-        named_bar_sync(1, 128);   // every thread has read s_last before it is rewritten
-        if (last) {
-          __threadfence();
-          const float* base_part = p.partials + (size_t)tile * p.splits * ACC * 128;
-#pragma unroll 1
-          for (int c0 = 0; c0 < S::kNG; c0 += CH) {
-#pragma unroll
-            for (int j = 0; j < CH; ++j) {
-              float a = 0.f, b = 0.f;
-              for (int s = 0; s < p.splits; ++s) {
-                const float* ps = base_part + (size_t)s * ACC * 128;
-                a += __ldcg(ps + (size_t)(c0 + j) * 128 + row);
-                if (KIND == KIND_GATE_UP) b += __ldcg(ps + (size_t)(S::kUOff + c0 + j) * 128 + row);
-              }
-              g[j] = a;
-              uu[j] = b;
-            }
-            emit(tm, tn, c0, g, uu);
-          }
-        }
       }
       if (++buf == 2) {
         buf = 0;
@@ -497,6 +497,52 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, S::kTmemCols);
+  }
+  if (p.splits > 1) {
+    // ---------------------------------------------------------- split-K reduction
+    __threadfence();
+    if (threadIdx.x == 0) {
+      bool ok = !*s_abort && grid_barrier(p.gbar, gridDim.x, p.timeout_ns);
+      if (!ok && !*s_abort) atomicExch(p.status, kStatusTimeout);
+      *s_ok = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (!*s_ok) return;
+    constexpr int G = 8;
+    constexpr int ACC = S::kAccCols;
+    constexpr int NCOL = (KIND == KIND_GATE_UP) ? S::kNG : ACC;  // columns that own an output
+    constexpr int NCG = NCOL / G;
+    const long long total = (long long)p.m_tiles * p.n_tiles * NCG * 128;
+    for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+         it += (long long)gridDim.x * blockDim.x) {
+      const int row = (int)(it & 127);
+      const long long rest = it >> 7;
+      const int cg = (int)(rest % NCG);
+      const int tile = (int)(rest / NCG);
+      const int c0 = cg * G;
+      const float* base_part = p.partials + (size_t)tile * p.splits * ACC * 128 + row;
+      float g[G], u[G];
+#pragma unroll
+      for (int j = 0; j < G; ++j) g[j] = u[j] = 0.f;
+#pragma unroll 2
+      for (int s = 0; s < p.splits; ++s) {
+        const float* ps = base_part + (size_t)s * ACC * 128;
+        float gv[G], uv[G];
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          gv[j] = __ldcg(ps + (size_t)(c0 + j) * 128);
+          if (KIND == KIND_GATE_UP) uv[j] = __ldcg(ps + (size_t)(S::kUOff + c0 + j) * 128);
+        }
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          g[j] += gv[j];
+          if (KIND == KIND_GATE_UP) u[j] += uv[j];
+        }
+      }
+      const int tm = tile / p.n_tiles, tn = tile - tm * p.n_tiles;
+      const int seg = (SWAP && KIND != KIND_GATE_UP) ? c0 / BN : 0;
+      emit_vals<SWAP, KIND, BN, G>(p, tm, tn, seg, row, c0 - seg * BN, g, u);
+    }
   }
 }
 

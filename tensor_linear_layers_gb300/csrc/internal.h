@@ -32,25 +32,31 @@ cudaError_t launch_add_rms_norm(int T, int H, const void* a, const void* res, co
 int max_norm_hidden();
 
 // ---------------------------------------------------------------- packing
+// Weights are packed as blocks of 256 rows x 64 K elements (32 KB) in the
+// 128-byte-swizzled K-major image the MMA reads; block (w_tile, kb) sits at
+// (w_tile * nkb + kb) * 32 KB. Rows or K past the end are zero.
 enum PackMode : int { PACK_GATE_UP = 0, PACK_ROW = 1, PACK_QKV = 2 };
 struct PackSpec {
   int mode;
   const __nv_bfloat16* src[3];
-  int64_t width;  // elements per packed row (H, or Ks for PACK_ROW)
-  int64_t Is;     // PACK_GATE_UP: I / t
-  int64_t N;      // PACK_ROW: output features
+  int64_t H;       // hidden: K of the column kinds, output rows of PACK_ROW
+  int64_t Is;      // PACK_GATE_UP: rows per shard; PACK_ROW: K per shard
   int64_t t;
-  int64_t ws;     // PACK_QKV: packed rows per shard
+  int64_t nb;      // PACK_GATE_UP: 128-row blocks per shard
+  int64_t nkb;     // k-blocks per weight tile
+  int64_t kbs;     // PACK_ROW: k-blocks per shard
+  int64_t n_col;   // PACK_QKV: packed rows in total
+  int64_t ws;      // PACK_QKV: packed rows per shard
   int q_per, kv_per, rep, hd;
 };
-cudaError_t launch_pack(const PackSpec& s, int64_t rows, void* dst, cudaStream_t st);
+cudaError_t launch_pack(const PackSpec& s, int64_t n_blocks, void* dst, cudaStream_t st);
 
 // ---------------------------------------------------------------- GEMM
 struct GemmParams;
-// Launch the GEMM instantiation for (swap, kind, bn); returns cudaErrorInvalidValue
+// Launch the GEMM instantiation for (swap, kind, bn); cudaErrorInvalidValue
 // when no such instantiation exists.
-cudaError_t launch_gemm(bool swap, int kind, int bn, const CUtensorMap& map_act,
-                        const CUtensorMap& map_w, const GemmParams& p, int grid, cudaStream_t st);
+cudaError_t launch_gemm(bool swap, int kind, int bn, const CUtensorMap& map_act, const GemmParams& p,
+                        int grid, cudaStream_t st);
 int gemm_stages(bool swap, int kind, int bn);
 
 }  // namespace tpl

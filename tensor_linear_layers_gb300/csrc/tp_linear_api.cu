@@ -15,26 +15,26 @@
 #include "tp_linear.h"
 
 namespace tpl {
-cudaError_t launch_gemm_prefill(int kind, const CUtensorMap& a, const CUtensorMap& w,
-                                const GemmParams& p, int grid, cudaStream_t st);
-cudaError_t launch_gemm_decode_gate_up(int bn, const CUtensorMap& a, const CUtensorMap& w,
-                                       const GemmParams& p, int grid, cudaStream_t st);
-cudaError_t launch_gemm_decode_col(int bn, const CUtensorMap& a, const CUtensorMap& w,
-                                   const GemmParams& p, int grid, cudaStream_t st);
-cudaError_t launch_gemm_decode_row(int bn, const CUtensorMap& a, const CUtensorMap& w,
-                                   const GemmParams& p, int grid, cudaStream_t st);
+cudaError_t launch_gemm_prefill(int kind, const CUtensorMap& a, const GemmParams& p, int grid,
+                                cudaStream_t st);
+cudaError_t launch_gemm_decode_gate_up(int bn, const CUtensorMap& a, const GemmParams& p, int grid,
+                                       cudaStream_t st);
+cudaError_t launch_gemm_decode_col(int bn, const CUtensorMap& a, const GemmParams& p, int grid,
+                                   cudaStream_t st);
+cudaError_t launch_gemm_decode_row(int bn, const CUtensorMap& a, const GemmParams& p, int grid,
+                                   cudaStream_t st);
 int gemm_stages_prefill(int kind);
 int gemm_stages_decode_gate_up(int bn);
 int gemm_stages_decode_col(int bn);
 int gemm_stages_decode_row(int bn);
 
-cudaError_t launch_gemm(bool swap, int kind, int bn, const CUtensorMap& a, const CUtensorMap& w,
-                        const GemmParams& p, int grid, cudaStream_t st) {
-  if (!swap) return launch_gemm_prefill(kind, a, w, p, grid, st);
+cudaError_t launch_gemm(bool swap, int kind, int bn, const CUtensorMap& a, const GemmParams& p,
+                        int grid, cudaStream_t st) {
+  if (!swap) return launch_gemm_prefill(kind, a, p, grid, st);
   switch (kind) {
-    case KIND_GATE_UP: return launch_gemm_decode_gate_up(bn, a, w, p, grid, st);
-    case KIND_COL: return launch_gemm_decode_col(bn, a, w, p, grid, st);
-    case KIND_ROW: return launch_gemm_decode_row(bn, a, w, p, grid, st);
+    case KIND_GATE_UP: return launch_gemm_decode_gate_up(bn, a, p, grid, st);
+    case KIND_COL: return launch_gemm_decode_col(bn, a, p, grid, st);
+    case KIND_ROW: return launch_gemm_decode_row(bn, a, p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -114,11 +114,11 @@ int make_map(CUtensorMap* m, const void* ptr, int64_t d0, int64_t d1, int64_t d2
 }
 
 // ============================================================================ workspace layout
-constexpr int64_t kHdrBytes = 256;
-constexpr int kMaxCounters = 4096;  // split-K tiles per GEMM
-constexpr int64_t kCountersColOff = kHdrBytes;
-constexpr int64_t kCountersRowOff = kCountersColOff + kMaxCounters * 4;
-constexpr int64_t kDynOff = align256(kCountersRowOff + kMaxCounters * 4);
+// header: [0] status word; [64] grid barrier of the column-parallel GEMM;
+// [128] grid barrier of the row-parallel GEMM; T-dependent buffers from kDynOff
+constexpr int64_t kGbarColOff = 64;
+constexpr int64_t kGbarRowOff = 128;
+constexpr int64_t kDynOff = 256;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per on-chip wait
 
 }  // namespace
@@ -136,10 +136,12 @@ struct tp_linear {
   int64_t ws_qkv;  // packed rows per QKV shard
   int64_t Ks;      // row-parallel input features per shard (Is or nq*hd/t)
   int64_t n_col;   // column-parallel output rows in total
+  // packed weight blocks (256 rows x 64 K each)
+  int nb;          // MLP: 128-row gate blocks per shard
+  int wt_col, nkb_col, wt_row, nkb_row, kbs_row;
   void* w_col;
   void* w_row;
   const void* gamma;
-  CUtensorMap map_col_swap, map_col_wide, map_row_swap, map_row_wide;
 };
 
 namespace {
@@ -160,20 +162,17 @@ Plan make_plan(const tp_linear* h, int which, int64_t T) {
   pl.swap = T <= 128;
   pl.bn = pl.swap ? (T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128) : 256;
   const int t = h->cfg.t;
+  (void)t;
   int64_t w_tiles;
   if (which == 0) {
-    pl.nkb = (int)ceil_div(h->H, 64);
+    pl.nkb = h->nkb_col;
     pl.kbs = 0;
-    if (mlp) {
-      pl.nb = (int)ceil_div(h->Is, 128);
-      w_tiles = (int64_t)t * pl.nb;  // 128 gate + 128 up rows per tile
-    } else {
-      w_tiles = ceil_div(h->n_col, pl.swap ? 128 : 256);
-    }
+    pl.nb = h->nb;
+    w_tiles = h->wt_col;   // MLP: 128 gate + 128 up rows per tile
   } else {
-    pl.kbs = (int)ceil_div(h->Ks, 64);
-    pl.nkb = t * pl.kbs;
-    w_tiles = ceil_div(h->H, pl.swap ? 128 : 256);
+    pl.kbs = h->kbs_row;
+    pl.nkb = h->nkb_row;
+    w_tiles = h->wt_row;
   }
   if (pl.swap) {
     pl.m_tiles = (int)w_tiles;
@@ -182,7 +181,7 @@ Plan make_plan(const tp_linear* h, int which, int64_t T) {
     pl.m_tiles = (int)ceil_div(T, 128);
     pl.n_tiles = (int)w_tiles;
   }
-  pl.acc_cols = (pl.swap && pl.kind == KIND_GATE_UP) ? 2 * pl.bn : pl.bn;
+  pl.acc_cols = pl.swap ? 2 * pl.bn : pl.bn;
   const int64_t tiles = (int64_t)pl.m_tiles * pl.n_tiles;
   // time ~ waves * (k-blocks per unit + per-unit overhead); the overhead of a
   // split unit includes writing and re-reading its fp32 partial tile
@@ -190,7 +189,7 @@ Plan make_plan(const tp_linear* h, int which, int64_t T) {
   const double cs = pl.swap ? 2.0 : 16.0;
   int best = 1;
   double best_cost = 1e30;
-  const int max_s = (tiles <= kMaxCounters) ? std::min(16, std::max(1, pl.nkb / 2)) : 1;
+  const int max_s = std::min(16, std::max(1, pl.nkb / 2));
   for (int s = 1; s <= max_s; ++s) {
     const double waves = (double)ceil_div(tiles * s, h->nsm);
     const double cost = waves * ((double)pl.nkb / s + c1 + (s > 1 ? cs : 0.0));
@@ -201,7 +200,7 @@ Plan make_plan(const tp_linear* h, int which, int64_t T) {
   }
   pl.splits = best;
   pl.units = (int)(tiles * pl.splits);
-  pl.grid = (int)std::min<int64_t>(pl.units, h->nsm);
+  pl.grid = (int)std::min<int64_t>(pl.units, h->nsm);   // one CTA per SM (shared memory)
   pl.partial_bytes = pl.splits > 1 ? tiles * pl.splits * pl.acc_cols * 128 * 4 : 0;
   return pl;
 }
@@ -239,7 +238,7 @@ int check_device(const tp_linear* h) {
   return TP_OK;
 }
 
-GemmParams base_params(const Plan& pl, int64_t T, void* ws, int64_t part_off, int64_t cnt_off) {
+GemmParams base_params(const Plan& pl, int64_t T, void* ws, int64_t part_off, int64_t gbar_off) {
   GemmParams p{};
   p.T = (int)T;
   p.m_tiles = pl.m_tiles;
@@ -252,7 +251,7 @@ GemmParams base_params(const Plan& pl, int64_t T, void* ws, int64_t part_off, in
   p.group_m = 8;
   char* w = static_cast<char*>(ws);
   p.partials = reinterpret_cast<float*>(w + part_off);
-  p.counters = reinterpret_cast<int*>(w + cnt_off);
+  p.gbar = reinterpret_cast<unsigned*>(w + gbar_off);
   p.status = reinterpret_cast<int*>(w);
   p.timeout_ns = kTimeoutNs;
   return p;
@@ -265,7 +264,7 @@ int run_col(const tp_linear* h, int64_t T, const void* x, void* out, void* ws, c
   CUtensorMap map_x;
   int rc = make_map(&map_x, x, h->H, T, 1, 1, pl.swap ? pl.bn : 128);
   if (rc) return rc;
-  GemmParams p = base_params(pl, T, ws, L.part_col, kCountersColOff);
+  GemmParams p = base_params(pl, T, ws, L.part_col, kGbarColOff);
   p.out = static_cast<__nv_bfloat16*>(out);
   if (h->cfg.kind == TP_BLOCK_MLP) {
     p.Is = (int)h->Is;
@@ -273,8 +272,8 @@ int run_col(const tp_linear* h, int64_t T, const void* x, void* out, void* ws, c
     p.n_out = (int)h->n_col;
     p.ws_out = (int)h->ws_qkv;
   }
-  const CUtensorMap& mw = pl.swap ? h->map_col_swap : h->map_col_wide;
-  cudaError_t e = launch_gemm(pl.swap, pl.kind, pl.bn, map_x, mw, p, pl.grid, st);
+  p.w_packed = static_cast<const uint8_t*>(h->w_col);
+  cudaError_t e = launch_gemm(pl.swap, pl.kind, pl.bn, map_x, p, pl.grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "column-parallel GEMM launch");
   return TP_OK;
 }
@@ -286,14 +285,14 @@ int run_row(const tp_linear* h, int64_t T, const void* in_shards, const void* re
   CUtensorMap map_in;
   int rc = make_map(&map_in, in_shards, h->Ks, T, 1, h->cfg.t, pl.swap ? pl.bn : 128);
   if (rc) return rc;
-  GemmParams p = base_params(pl, T, ws, L.part_row, kCountersRowOff);
+  GemmParams p = base_params(pl, T, ws, L.part_row, kGbarRowOff);
   p.n_out = (int)h->H;
   p.ws_out = (int)h->H;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.out2 = static_cast<__nv_bfloat16*>(out2);
   p.resid = static_cast<const __nv_bfloat16*>(resid);
-  const CUtensorMap& mw = pl.swap ? h->map_row_swap : h->map_row_wide;
-  cudaError_t e = launch_gemm(pl.swap, pl.kind, pl.bn, map_in, mw, p, pl.grid, st);
+  p.w_packed = static_cast<const uint8_t*>(h->w_row);
+  cudaError_t e = launch_gemm(pl.swap, pl.kind, pl.bn, map_in, p, pl.grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "row-parallel GEMM launch");
   return TP_OK;
 }
@@ -379,6 +378,17 @@ void derive(tp_linear* h) {
     h->n_col = t * h->ws_qkv;
     h->Ks = (int64_t)c.n_q_heads * c.head_dim / t;
   }
+  h->nkb_col = (int)ceil_div(h->H, 64);
+  if (c.kind == TP_BLOCK_MLP) {
+    h->nb = (int)ceil_div(h->Is, 128);
+    h->wt_col = t * h->nb;
+  } else {
+    h->nb = 0;
+    h->wt_col = (int)ceil_div(h->n_col, 256);
+  }
+  h->kbs_row = (int)ceil_div(h->Ks, 64);
+  h->nkb_row = t * h->kbs_row;
+  h->wt_row = (int)ceil_div(h->H, 256);
 }
 
 }  // namespace
@@ -395,8 +405,8 @@ int tp_packed_weight_bytes(const tp_config_t* cfg, int64_t* col_bytes, int64_t* 
   tp_linear tmp{};
   tmp.cfg = *cfg;
   derive(&tmp);
-  *col_bytes = tmp.n_col * tmp.H * 2;
-  *row_bytes = tmp.H * tmp.Ks * cfg->t * 2;
+  *col_bytes = (int64_t)tmp.wt_col * tmp.nkb_col * kWBlockBytes;
+  *row_bytes = (int64_t)tmp.wt_row * tmp.nkb_row * kWBlockBytes;
   return ok();
 }
 
@@ -431,51 +441,39 @@ int tp_linear_create(const tp_config_t* cfg, const void* const* w_full, int32_t 
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int t = cfg->t;
-  // pack the shards ("weight_loader": narrow the full tensor to each rank's slice)
+  // pack the shards ("weight_loader": narrow the full tensor to each rank's slice),
+  // tiled into swizzled 32 KB blocks
   PackSpec pc{}, pr{};
+  pc.t = pr.t = t;
+  pc.H = pr.H = h->H;
+  pc.nkb = h->nkb_col;
   if (mlp) {
     pc.mode = PACK_GATE_UP;
     pc.src[0] = static_cast<const __nv_bfloat16*>(w_full[0]);
     pc.src[1] = static_cast<const __nv_bfloat16*>(w_full[1]);
-    pc.width = h->H;
     pc.Is = h->Is;
-    pr.mode = PACK_ROW;
+    pc.nb = h->nb;
     pr.src[0] = static_cast<const __nv_bfloat16*>(w_full[2]);
   } else {
     pc.mode = PACK_QKV;
     for (int i = 0; i < 3; ++i) pc.src[i] = static_cast<const __nv_bfloat16*>(w_full[i]);
-    pc.width = h->H;
+    pc.n_col = h->n_col;
     pc.ws = h->ws_qkv;
     pc.q_per = h->q_per;
     pc.kv_per = h->kv_per;
     pc.rep = h->rep;
     pc.hd = cfg->head_dim;
-    pr.mode = PACK_ROW;
     pr.src[0] = static_cast<const __nv_bfloat16*>(w_full[3]);
   }
-  pc.t = t;
-  pr.width = h->Ks;
-  pr.N = h->H;
-  pr.t = t;
-  e = launch_pack(pc, h->n_col, w_col_packed, st);
-  if (e == cudaSuccess) e = launch_pack(pr, (int64_t)t * h->H, w_row_packed, st);
+  pr.mode = PACK_ROW;
+  pr.Is = h->Ks;
+  pr.kbs = h->kbs_row;
+  pr.nkb = h->nkb_row;
+  e = launch_pack(pc, (int64_t)h->wt_col * h->nkb_col, w_col_packed, st);
+  if (e == cudaSuccess) e = launch_pack(pr, (int64_t)h->wt_row * h->nkb_row, w_row_packed, st);
   if (e != cudaSuccess) {
     delete h;
     return cuda_fail(e, "weight packing");
-  }
-  // weight tensor maps, one per operand orientation
-  if (mlp) {
-    rc = make_map(&h->map_col_swap, w_col_packed, h->H, h->Is, 2, t, 128);
-    if (!rc) rc = make_map(&h->map_col_wide, w_col_packed, h->H, h->Is, 2, t, 128);
-  } else {
-    rc = make_map(&h->map_col_swap, w_col_packed, h->H, h->n_col, 1, 1, 128);
-    if (!rc) rc = make_map(&h->map_col_wide, w_col_packed, h->H, h->n_col, 1, 1, 256);
-  }
-  if (!rc) rc = make_map(&h->map_row_swap, w_row_packed, h->Ks, h->H, 1, t, 128);
-  if (!rc) rc = make_map(&h->map_row_wide, w_row_packed, h->Ks, h->H, 1, t, 256);
-  if (rc) {
-    delete h;
-    return rc;
   }
   *out = h;
   return ok();

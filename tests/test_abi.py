@@ -46,16 +46,27 @@ def cfg_mlp(t=2, H=512, I=1408, flags=0):
     return tl.make_config(tl.TP_BLOCK_MLP, t, H, I, flags=flags)
 
 
+BLOCK = 256 * 64 * 2     # packed weight block: 256 rows x 64 K elements, bf16
+
+
+def cdiv(a, b):
+    return -(-a // b)
+
+
 def test_packed_bytes_mlp(L):
+    # gate_up: t shards x ceil(I/t / 128) blocks of [128 gate | 128 up] rows x ceil(H/64) k-blocks
     col, row = tl.packed_weight_bytes(cfg_mlp())
-    assert col == 2 * 1408 * 512 * 2 and row == 512 * 1408 * 2
+    assert col == 2 * cdiv(704, 128) * cdiv(512, 64) * BLOCK
+    # down: ceil(H/256) row tiles x t shards x ceil(I/t / 64) k-blocks
+    assert row == cdiv(512, 256) * 2 * cdiv(704, 64) * BLOCK
+    assert col >= 2 * 1408 * 512 * 2 and row >= 512 * 1408 * 2
 
 
 def test_packed_bytes_attention_gqa(L):
-    # 32 q heads, 8 kv heads, hd 128, t=4: shard = 8 q + 2 k + 2 v heads
+    # 32 q heads, 8 kv heads, hd 128, t=4: shard = 8 q + 2 k + 2 v heads = 1536 rows
     cfg = tl.make_config(tl.TP_BLOCK_ATTN_PROJ, 4, 4096, n_q_heads=32, n_kv_heads=8, head_dim=128)
     col, row = tl.packed_weight_bytes(cfg)
-    assert col == 4 * 12 * 128 * 4096 * 2
+    assert col == cdiv(4 * 1536, 256) * 64 * BLOCK == 4 * 12 * 128 * 4096 * 2
     assert row == 4096 * 4096 * 2
     # t=8 with 4 kv heads: kv heads replicated, one per shard
     cfg = tl.make_config(tl.TP_BLOCK_ATTN_PROJ, 8, 4096, n_q_heads=32, n_kv_heads=4, head_dim=128)
