@@ -73,6 +73,21 @@ struct GemmParams {
   unsigned long long timeout_ns;
 };
 
+// Parameters of the fused decode-shaped MLP block (mlp_decode.cu).
+struct MlpDecodeParams {
+  GemmParams g1;                 // KIND_GATE_UP, swapped operands
+  GemmParams g2;                 // KIND_ROW, swapped operands
+  const __nv_bfloat16* x_in;     // [T, H] (a, with the norm)
+  const __nv_bfloat16* res_in;   // [T, H] or null
+  const __nv_bfloat16* gamma;    // [H] (norm)
+  __nv_bfloat16* res_out;        // [T, H] (norm)
+  __nv_bfloat16* x_norm;         // [T, H] workspace (norm)
+  unsigned* bars;                // 5 arrival counters, zero at launch; reset at exit
+  float eps;
+  int H;
+  int has_norm;
+};
+
 template <bool SWAP, int KIND, int BN>
 struct GemmShape {
   static constexpr int NA = SWAP ? 2 : 1;                // accumulators (128 rows each)
@@ -209,6 +224,94 @@ __device__ __forceinline__ void emit_vals(const GemmParams& p, int tm, int tn, i
         }
       }
     }
+}
+
+// Split-K reduction: adds the fp32 partials of every tile in ascending split
+// order and applies the epilogue. Work items (8 columns of one accumulator
+// row) are spread over `nthreads` threads, this one being `tid`.
+template <bool SWAP, int KIND, int BN>
+__device__ __forceinline__ void reduce_partials(const GemmParams& p, long long tid, long long nthreads) {
+  using S = GemmShape<SWAP, KIND, BN>;
+  // one item = 8 columns of one accumulator row; the loads of up to 8 splits
+  // are all issued before they are added (in ascending split order)
+  constexpr int G = 8;
+  constexpr int SC = (KIND == KIND_GATE_UP) ? 4 : 8;   // splits loaded per round
+  constexpr int ACC = S::kAccCols;
+  constexpr int NCOL = (KIND == KIND_GATE_UP) ? S::kNG : ACC;  // columns that own an output
+  constexpr int NCG = NCOL / G;
+  const long long total = (long long)p.m_tiles * p.n_tiles * NCG * 128;
+  for (long long it = tid; it < total; it += nthreads) {
+    const int row = (int)(it & 127);
+    const long long rest = it >> 7;
+    const int cg = (int)(rest % NCG);
+    const int tile = (int)(rest / NCG);
+    const int c0 = cg * G;
+    const float* base_part = p.partials + (size_t)tile * p.splits * ACC * 128 + row;
+    float g[G], u[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) g[j] = u[j] = 0.f;
+    for (int s0 = 0; s0 < p.splits; s0 += SC) {
+      float gv[SC][G], uv[SC][G];
+#pragma unroll
+      for (int s = 0; s < SC; ++s) {
+        if (s0 + s < p.splits) {
+          const float* ps = base_part + (size_t)(s0 + s) * ACC * 128;
+#pragma unroll
+          for (int j = 0; j < G; ++j) {
+            gv[s][j] = __ldcg(ps + (size_t)(c0 + j) * 128);
+            if (KIND == KIND_GATE_UP) uv[s][j] = __ldcg(ps + (size_t)(S::kUOff + c0 + j) * 128);
+          }
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < SC; ++s) {
+        if (s0 + s < p.splits) {
+#pragma unroll
+          for (int j = 0; j < G; ++j) {
+            g[j] += gv[s][j];
+            if (KIND == KIND_GATE_UP) u[j] += uv[s][j];
+          }
+        }
+      }
+    }
+    const int tm = tile / p.n_tiles, tn = tile - tm * p.n_tiles;
+    const int seg = (SWAP && KIND != KIND_GATE_UP) ? c0 / BN : 0;
+    emit_vals<SWAP, KIND, BN, G>(p, tm, tn, seg, row, c0 - seg * BN, g, u);
+  }
+}
+
+// Arrival counters used as grid-wide barriers between the phases of one
+// launch. bar_arrive: one thread per CTA, after the CTA's writes (the
+// fence makes them visible device-wide first). bar_wait: spin (with sleeps)
+// until `n` CTAs have arrived; gives up after timeout_ns or when *abort is set.
+__device__ __forceinline__ void bar_arrive(unsigned* c) {
+  __threadfence();
+  atomicAdd(c, 1u);
+}
+__device__ __forceinline__ bool bar_wait(const unsigned* c, unsigned n, unsigned long long timeout_ns,
+                                         const volatile int* abort) {
+  const volatile unsigned* v = c;
+  if (*v >= n) {
+    __threadfence();
+    return true;
+  }
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(32);
+    if (*v >= n) {
+      __threadfence();
+      return true;
+    }
+    if ((it & 31u) == 0) {
+      if (abort != nullptr && *abort) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+  }
+}
+// Order this thread's generic-proxy global writes before later async-proxy
+// (TMA) reads of the same memory by other CTAs.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // Grid-wide barrier for a cooperative launch, called by one thread per CTA.
@@ -508,41 +611,8 @@ __global__ void __launch_bounds__(192, 1)
     }
     __syncthreads();
     if (!*s_ok) return;
-    constexpr int G = 8;
-    constexpr int ACC = S::kAccCols;
-    constexpr int NCOL = (KIND == KIND_GATE_UP) ? S::kNG : ACC;  // columns that own an output
-    constexpr int NCG = NCOL / G;
-    const long long total = (long long)p.m_tiles * p.n_tiles * NCG * 128;
-    for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
-         it += (long long)gridDim.x * blockDim.x) {
-      const int row = (int)(it & 127);
-      const long long rest = it >> 7;
-      const int cg = (int)(rest % NCG);
-      const int tile = (int)(rest / NCG);
-      const int c0 = cg * G;
-      const float* base_part = p.partials + (size_t)tile * p.splits * ACC * 128 + row;
-      float g[G], u[G];
-#pragma unroll
-      for (int j = 0; j < G; ++j) g[j] = u[j] = 0.f;
-#pragma unroll 2
-      for (int s = 0; s < p.splits; ++s) {
-        const float* ps = base_part + (size_t)s * ACC * 128;
-        float gv[G], uv[G];
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-          gv[j] = __ldcg(ps + (size_t)(c0 + j) * 128);
-          if (KIND == KIND_GATE_UP) uv[j] = __ldcg(ps + (size_t)(S::kUOff + c0 + j) * 128);
-        }
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-          g[j] += gv[j];
-          if (KIND == KIND_GATE_UP) u[j] += uv[j];
-        }
-      }
-      const int tm = tile / p.n_tiles, tn = tile - tm * p.n_tiles;
-      const int seg = (SWAP && KIND != KIND_GATE_UP) ? c0 / BN : 0;
-      emit_vals<SWAP, KIND, BN, G>(p, tm, tn, seg, row, c0 - seg * BN, g, u);
-    }
+    reduce_partials<SWAP, KIND, BN>(p, (long long)blockIdx.x * blockDim.x + threadIdx.x,
+                                    (long long)gridDim.x * blockDim.x);
   }
 }
 

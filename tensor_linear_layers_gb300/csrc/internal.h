@@ -58,5 +58,9 @@ struct GemmParams;
 cudaError_t launch_gemm(bool swap, int kind, int bn, const CUtensorMap& map_act, const GemmParams& p,
                         int grid, cudaStream_t st);
 int gemm_stages(bool swap, int kind, int bn);
+struct MlpDecodeParams;
+// The fused decode-shaped MLP block (T <= 128): one cooperative launch.
+cudaError_t launch_mlp_decode(int bn, const CUtensorMap& map_x, const CUtensorMap& map_h,
+                              const MlpDecodeParams& P, int grid, cudaStream_t st);
 
 }  // namespace tpl

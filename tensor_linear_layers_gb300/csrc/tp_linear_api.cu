@@ -115,9 +115,12 @@ int make_map(CUtensorMap* m, const void* ptr, int64_t d0, int64_t d1, int64_t d2
 
 // ============================================================================ workspace layout
 // header: [0] status word; [64] grid barrier of the column-parallel GEMM;
-// [128] grid barrier of the row-parallel GEMM; T-dependent buffers from kDynOff
+// [128] grid barrier of the row-parallel GEMM; [192] the 5 phase counters of
+// the fused decode block; T-dependent buffers from kDynOff
 constexpr int64_t kGbarColOff = 64;
 constexpr int64_t kGbarRowOff = 128;
+constexpr int64_t kDecodeBarsOff = 192;
+constexpr int64_t kFusedMaxT = 128;
 constexpr int64_t kDynOff = 256;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per on-chip wait
 
@@ -601,13 +604,47 @@ int tp_mlp_forward(tp_linear_t* h, int64_t T, const void* x_in, const void* resi
   const void* x = x_in;
   const void* resid = residual_in;
   if (norm) {
-    cudaError_t e = launch_add_rms_norm((int)T, (int)h->H, x_in, residual_in, h->gamma,
-                                        h->cfg.rms_eps, residual_out, ws + L.x_norm, st);
-    if (e != cudaSuccess) return cuda_fail(e, "add_rms_norm launch");
     x = ws + L.x_norm;
     resid = residual_out;
   }
   void* hbuf = ws + L.h;
+  if (T <= kFusedMaxT) {
+    // decode-shaped step: norm, gate_up, h, down and both reductions in one launch
+    const Plan p1 = make_plan(h, 0, T), p2 = make_plan(h, 1, T);
+    const void* xsrc = norm ? static_cast<const void*>(ws + L.x_norm) : x_in;
+    CUtensorMap map_x, map_h;
+    if ((rc = make_map(&map_x, xsrc, h->H, T, 1, 1, p1.bn))) return rc;
+    if ((rc = make_map(&map_h, hbuf, h->Ks, T, 1, h->cfg.t, p2.bn))) return rc;
+    MlpDecodeParams P{};
+    P.g1 = base_params(p1, T, workspace, L.part_col, kGbarColOff);
+    P.g1.out = static_cast<__nv_bfloat16*>(hbuf);
+    P.g1.Is = (int)h->Is;
+    P.g1.w_packed = static_cast<const uint8_t*>(h->w_col);
+    P.g2 = base_params(p2, T, workspace, L.part_row, kGbarRowOff);
+    P.g2.n_out = (int)h->H;
+    P.g2.ws_out = (int)h->H;
+    P.g2.out = static_cast<__nv_bfloat16*>(mlp_out);
+    P.g2.out2 = static_cast<__nv_bfloat16*>(residual_stream);
+    P.g2.resid = static_cast<const __nv_bfloat16*>(norm ? residual_out : residual_in);
+    P.g2.w_packed = static_cast<const uint8_t*>(h->w_row);
+    P.x_in = static_cast<const __nv_bfloat16*>(x_in);
+    P.res_in = static_cast<const __nv_bfloat16*>(residual_in);
+    P.gamma = static_cast<const __nv_bfloat16*>(h->gamma);
+    P.res_out = static_cast<__nv_bfloat16*>(residual_out);
+    P.x_norm = reinterpret_cast<__nv_bfloat16*>(ws + L.x_norm);
+    P.bars = reinterpret_cast<unsigned*>(ws + kDecodeBarsOff);
+    P.eps = h->cfg.rms_eps;
+    P.H = (int)h->H;
+    P.has_norm = norm ? 1 : 0;
+    cudaError_t e = launch_mlp_decode(p1.bn, map_x, map_h, P, h->nsm, st);
+    if (e != cudaSuccess) return cuda_fail(e, "fused decode MLP launch");
+    return ok();
+  }
+  if (norm) {
+    cudaError_t e = launch_add_rms_norm((int)T, (int)h->H, x_in, residual_in, h->gamma,
+                                        h->cfg.rms_eps, residual_out, ws + L.x_norm, st);
+    if (e != cudaSuccess) return cuda_fail(e, "add_rms_norm launch");
+  }
   if ((rc = run_col(h, T, x, hbuf, workspace, L, st))) return rc;
   if ((rc = run_row(h, T, hbuf, resid, mlp_out, residual_stream, workspace, L, st))) return rc;
   return ok();
