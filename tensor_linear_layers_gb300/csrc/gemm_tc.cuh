@@ -82,7 +82,10 @@ struct MlpDecodeParams {
   const __nv_bfloat16* gamma;    // [H] (norm)
   __nv_bfloat16* res_out;        // [T, H] (norm)
   __nv_bfloat16* x_norm;         // [T, H] workspace (norm)
-  unsigned* bars;                // 5 arrival counters, zero at launch; reset at exit
+  unsigned* bars;                // [0] norm arrivals, [1] CTAs finished, [2] gate_up partials written
+  unsigned* cnt1;                // per gate_up tile: splits whose partial is written
+  unsigned* hready;              // per gate_up tile: 1 once its h columns are written
+  unsigned* cnt2;                // per down tile: splits whose partial is written
   float eps;
   int H;
   int has_norm;
@@ -226,27 +229,24 @@ __device__ __forceinline__ void emit_vals(const GemmParams& p, int tm, int tn, i
     }
 }
 
-// Split-K reduction: adds the fp32 partials of every tile in ascending split
-// order and applies the epilogue. Work items (8 columns of one accumulator
-// row) are spread over `nthreads` threads, this one being `tid`.
+// Split-K reduction of one tile's items [it_lo, it_hi): an item is 8 columns
+// of one accumulator row (rows fastest). Adds the fp32 partials in ascending
+// split order and applies the epilogue. Items are spread over `nthreads`
+// threads, this one being `tid`; the loads of up to SC splits are all issued
+// before they are added.
 template <bool SWAP, int KIND, int BN>
-__device__ __forceinline__ void reduce_partials(const GemmParams& p, long long tid, long long nthreads) {
+__device__ __forceinline__ void reduce_tile_items(const GemmParams& p, int tile, int it_lo, int it_hi,
+                                                  int tid, int nthreads) {
   using S = GemmShape<SWAP, KIND, BN>;
-  // one item = 8 columns of one accumulator row; the loads of up to 8 splits
-  // are all issued before they are added (in ascending split order)
   constexpr int G = 8;
-  constexpr int SC = (KIND == KIND_GATE_UP) ? 4 : 8;   // splits loaded per round
+  constexpr int SC = (KIND == KIND_GATE_UP) ? 4 : 8;
   constexpr int ACC = S::kAccCols;
-  constexpr int NCOL = (KIND == KIND_GATE_UP) ? S::kNG : ACC;  // columns that own an output
-  constexpr int NCG = NCOL / G;
-  const long long total = (long long)p.m_tiles * p.n_tiles * NCG * 128;
-  for (long long it = tid; it < total; it += nthreads) {
-    const int row = (int)(it & 127);
-    const long long rest = it >> 7;
-    const int cg = (int)(rest % NCG);
-    const int tile = (int)(rest / NCG);
-    const int c0 = cg * G;
-    const float* base_part = p.partials + (size_t)tile * p.splits * ACC * 128 + row;
+  const float* tile_part = p.partials + (size_t)tile * p.splits * ACC * 128;
+  const int tm = tile / p.n_tiles, tn = tile - tm * p.n_tiles;
+  for (int it = it_lo + tid; it < it_hi; it += nthreads) {
+    const int row = it & 127;
+    const int c0 = (it >> 7) * G;
+    const float* base_part = tile_part + row;
     float g[G], u[G];
 #pragma unroll
     for (int j = 0; j < G; ++j) g[j] = u[j] = 0.f;
@@ -274,9 +274,26 @@ __device__ __forceinline__ void reduce_partials(const GemmParams& p, long long t
         }
       }
     }
-    const int tm = tile / p.n_tiles, tn = tile - tm * p.n_tiles;
     const int seg = (SWAP && KIND != KIND_GATE_UP) ? c0 / BN : 0;
     emit_vals<SWAP, KIND, BN, G>(p, tm, tn, seg, row, c0 - seg * BN, g, u);
+  }
+}
+// Items of one tile: 8-column groups of the columns that own an output, x 128 rows.
+template <bool SWAP, int KIND, int BN>
+__host__ __device__ constexpr int tile_items() {
+  using S = GemmShape<SWAP, KIND, BN>;
+  return ((KIND == KIND_GATE_UP) ? S::kNG : S::kAccCols) / 8 * 128;
+}
+
+// Split-K reduction of every tile, spread over all threads of the grid.
+template <bool SWAP, int KIND, int BN>
+__device__ __forceinline__ void reduce_partials(const GemmParams& p, long long tid, long long nthreads) {
+  constexpr int ITEMS = tile_items<SWAP, KIND, BN>();
+  const long long total = (long long)p.m_tiles * p.n_tiles * ITEMS;
+  for (long long it = tid; it < total; it += nthreads) {
+    const int tile = (int)(it / ITEMS);
+    const int i = (int)(it - (long long)tile * ITEMS);
+    reduce_tile_items<SWAP, KIND, BN>(p, tile, i, i + 1, 0, 1);
   }
 }
 

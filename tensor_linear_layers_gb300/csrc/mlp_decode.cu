@@ -1,24 +1,25 @@
 // Fused decode-shaped MLP block: one persistent cooperative launch runs the
 // whole step for T <= 128 tokens.
 //
-//   phase 0  residual add + RMSNorm of the T rows (epilogue warps; rows
-//            spread over CTAs)                                -> bars[0]
-//   phase 1  column-parallel gate_up: units of 256 weight rows (128 gate +
-//            128 up of one shard) x a K range; fp32 partials
-//                                                              -> bars[1]
-//   phase 1b the partials of every tile are added in split order and
-//            silu(g) * u is written to h [t][T][I/t]          -> bars[2]
-//   phase 2  row-parallel down: K runs over the t shards in turn, so the
-//            shards' partial sums meet in the accumulator; fp32 partials
-//                                                              -> bars[3]
-//   phase 2b partials added in split order; mlp_out = y, residual_stream =
-//            y + residual
+//   norm     residual add + RMSNorm of the T rows by the epilogue warps (rows
+//            spread over CTAs); every CTA arrives on bars[0]
+//   gate_up  column-parallel units of 256 weight rows (128 gate + 128 up of
+//            one shard) x a K range; with split-K every split writes its fp32
+//            partial. After one grid-wide wait the CTAs add the partials tile
+//            by tile (split order), in the order the down splits will read h,
+//            write silu(g) * u to h [t][T][I/t] and count finished items in
+//            hready[tile]
+//   down     row-parallel units: K runs over the t shards in turn, so the
+//            shards' partial sums meet in the accumulator. The producer loads
+//            the h columns of a k-block as soon as the gate_up tile that
+//            wrote them is complete, streaming weight blocks meanwhile. The
+//            splits of a down tile (resident together) each add their slice
+//            of the tile; mlp_out = y, residual_stream = y + residual
 //
-// The producer never waits for a phase boundary before it has to: it streams
-// the next phase's weight blocks into free stages and only defers the
-// activation half of those stages until the barrier that makes the
-// activation valid has passed. All waits are bounded (status word on
-// timeout); the cooperative launch guarantees every CTA is resident.
+// Between the GEMMs, work flows through per-tile counters and flags in the
+// workspace. Every wait is bounded (status word on
+// timeout) and the cooperative launch makes every CTA resident. The last CTA
+// to finish resets the counters and flags for the next launch.
 #include "gemm_launch.cuh"
 
 namespace tpl {
@@ -35,6 +36,7 @@ __global__ void __launch_bounds__(192, 1)
   constexpr int STAGES = S::kStages;
   constexpr int ACC = S::kAccCols;
   constexpr int CH = S::kCh;
+  constexpr int kItems1 = tile_items<true, KIND_GATE_UP, BN>();  // h of a gate_up tile is complete at this count
   const unsigned grid = gridDim.x;
 
   extern __shared__ uint8_t smem_raw[];
@@ -87,6 +89,9 @@ __global__ void __launch_bounds__(192, 1)
       *s_abort = 1;
     }
   };
+  // gate_up units go to CTAs 0, 1, ...; down units to CTAs grid-1, grid-2, ...,
+  // so CTAs without gate_up work start down (and its weight stream) at once
+  auto first_unit = [&](int ph) -> int { return ph == 0 ? (int)blockIdx.x : (int)(grid - 1 - blockIdx.x); };
   auto krange = [](const GemmParams& p, int u, int& tm, int& kb0, int& kb1) {
     const int tile = u / p.splits;
     const int sp = u - tile * p.splits;
@@ -100,29 +105,53 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_a = policy_evict_last();
+      constexpr int kPreX = 3;  // weight stages issued before the normalised x exists
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, last_phase_bits = 0;
-      int pend_stage[STAGES], pend_kx[STAGES], pend_sh[STAGES];
-      int npend = 0;
+      // activation halves waiting for their producer: FIFO of (stage, kx, shard, gate_up tile or -1)
+      int q_stage[STAGES], q_kx[STAGES], q_sh[STAGES], q_dep[STAGES];
+      int q_head = 0, q_n = 0;
+      bool x_ready = !P.has_norm;
       bool ok = true;
+      auto dep_ready = [&](int dep) -> bool {
+        if (dep < 0) {
+          if (!x_ready) x_ready = *reinterpret_cast<const volatile unsigned*>(P.bars) >= grid;
+          return x_ready;
+        }
+        return *reinterpret_cast<const volatile unsigned*>(P.hready + dep) >= (unsigned)kItems1;
+      };
+      auto issue_front = [&]() {
+        const int i = q_head;
+        const uint32_t sb = base + q_stage[i] * S::kStageBytes + S::kABytes;
+        fence_proxy_async_global();
+        if (q_dep[i] < 0)
+          tma_load_4d(sb, &map_x, full_bar(q_stage[i]), q_kx[i], 0, 0, 0, pol_a);
+        else
+          tma_load_4d(sb, &map_h, full_bar(q_stage[i]), q_kx[i], 0, 0, q_sh[i], pol_a);
+        q_head = (q_head + 1) % STAGES;
+        --q_n;
+      };
+      // issue every queued activation copy whose data is ready; block (bounded) on the
+      // oldest one while more than `keep` entries remain queued
+      auto drain = [&](int keep) -> bool {
+        while (q_n > 0) {
+          if (dep_ready(q_dep[q_head])) {
+            issue_front();
+            continue;
+          }
+          if (q_n <= keep) return true;
+          const int dep = q_dep[q_head];
+          const unsigned* c = dep < 0 ? P.bars : P.hready + dep;
+          if (!bar_wait(c, dep < 0 ? grid : (unsigned)kItems1, timeout, s_abort)) return false;
+          if (dep < 0) x_ready = true;
+          issue_front();
+        }
+        return true;
+      };
       for (int ph = 0; ph < 2 && ok; ++ph) {
         const GemmParams& p = ph == 0 ? P.g1 : P.g2;
-        const CUtensorMap* map = ph == 0 ? &map_x : &map_h;
-        const unsigned* flag = ph == 0 ? P.bars + 0 : P.bars + 2;
-        bool ready = (ph == 0) ? !P.has_norm : false;
-        auto flush = [&]() -> bool {
-          if (!bar_wait(flag, grid, timeout, s_abort)) return false;
-          fence_proxy_async_global();
-          for (int i = 0; i < npend; ++i) {
-            const uint32_t sb = base + pend_stage[i] * S::kStageBytes + S::kABytes;
-            tma_load_4d(sb, map, full_bar(pend_stage[i]), pend_kx[i], 0, 0, pend_sh[i], pol_a);
-          }
-          npend = 0;
-          ready = true;
-          return true;
-        };
-        for (int u = blockIdx.x; u < p.units && ok; u += grid) {
+        for (int u = first_unit(ph); u < p.units && ok; u += grid) {
           int tm, kb0, kb1;
           krange(p, u, tm, kb0, kb1);
           const uint8_t* wsrc = p.w_packed + (size_t)tm * p.nkb * kWBlockBytes;
@@ -136,30 +165,24 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t fb = full_bar(stage);
             mbar_arrive_expect_tx(fb, S::kStageBytes);
             bulk_load(sa, wsrc + (size_t)kb * kWBlockBytes, kWBlockBytes, fb, pol_w);
-            int kx = kb * 64, shard = 0;
+            int kx = kb * 64, shard = 0, dep = -1;
             if (ph == 1) {
               shard = kb / p.kbs;
-              kx = (kb - shard * p.kbs) * 64;
+              const int kk = kb - shard * p.kbs;
+              kx = kk * 64;
+              dep = shard * P.g1.nb + (kk * 64) / 128;   // gate_up tile that wrote these h columns
             }
-            if (!ready) {
-              const volatile unsigned* vf = flag;
-              if (*vf >= grid && !flush()) {
-                set_abort();
-                ok = false;
-                break;
-              }
-            }
-            if (ready) {
-              tma_load_4d(sa + S::kABytes, map, fb, kx, 0, 0, shard, pol_a);
-            } else {
-              pend_stage[npend] = stage;
-              pend_kx[npend] = kx;
-              pend_sh[npend] = shard;
-              if (++npend == STAGES && !flush()) {
-                set_abort();
-                ok = false;
-                break;
-              }
+            const int slot = (q_head + q_n) % STAGES;
+            q_stage[slot] = stage;
+            q_kx[slot] = kx;
+            q_sh[slot] = shard;
+            q_dep[slot] = dep;
+            ++q_n;
+            const int keep = (!x_ready && ph == 0) ? kPreX - 1 : STAGES - 1;
+            if (!drain(keep)) {
+              set_abort();
+              ok = false;
+              break;
             }
             issued_mask |= 1u << stage;
             last_phase_bits = (last_phase_bits & ~(1u << stage)) | (phase << stage);
@@ -169,10 +192,10 @@ __global__ void __launch_bounds__(192, 1)
             }
           }
         }
-        if (ok && npend > 0 && !flush()) {
-          set_abort();
-          ok = false;
-        }
+      }
+      if (ok && !drain(0)) {
+        set_abort();
+        ok = false;
       }
       if (!ok) {
         for (int s = 0; s < STAGES; ++s)
@@ -191,7 +214,7 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       for (int ph = 0; ph < 2 && ok; ++ph) {
         const GemmParams& p = ph == 0 ? P.g1 : P.g2;
-        for (int u = blockIdx.x; u < p.units && ok; u += grid) {
+        for (int u = first_unit(ph); u < p.units && ok; u += grid) {
           int tm, kb0, kb1;
           krange(p, u, tm, kb0, kb1);
           if (!mbar_wait_bounded(tempty_bar(buf), acc_phase ^ 1u, s_abort, timeout)) {
@@ -255,20 +278,6 @@ __global__ void __launch_bounds__(192, 1)
       named_bar_sync(1, 128);
       return r;
     };
-    // All 128 epilogue threads: make this CTA's writes visible, arrive, wait for every CTA.
-    auto grid_sync = [&](unsigned* c, bool proxy) -> bool {
-      if (proxy) fence_proxy_async_global();
-      __threadfence();
-      named_bar_sync(1, 128);
-      bool r = true;
-      if (et == 0) {
-        bar_arrive(c);
-        r = bar_wait(c, grid, timeout, s_abort);
-        if (!r) set_abort();
-      }
-      return agree(r);
-    };
-
     // ---- phase 0: residual add + RMSNorm, one row per CTA in turn
     if (P.has_norm) {
       const int H = P.H, nvec = H >> 3;
@@ -323,10 +332,10 @@ __global__ void __launch_bounds__(192, 1)
     }
 
     float g[CH], uu[CH];
-    // ---- phases 1 and 2: units of the two GEMMs
+    // ---- gate_up units, then down units
     for (int ph = 0; ph < 2 && ok; ++ph) {
       const GemmParams& p = ph == 0 ? P.g1 : P.g2;
-      for (int u = blockIdx.x; u < p.units && ok; u += grid) {
+      for (int u = first_unit(ph); u < p.units && ok; u += grid) {
         int tm, kb0, kb1;
         krange(p, u, tm, kb0, kb1);
         const int sp = u - tm * p.splits;
@@ -361,6 +370,16 @@ __global__ void __launch_bounds__(192, 1)
               }
             }
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(buf));
+          if (ph == 0) {
+            // this tile's h columns are complete
+            fence_proxy_async_global();
+            __threadfence();
+            named_bar_sync(1, 128);
+            if (et == 0) atomicAdd(P.hready + tm, (unsigned)kItems1);
+          }
         } else {
           float* part = p.partials + ((size_t)tm * p.splits + sp) * ACC * 128;
 #pragma unroll 1
@@ -370,29 +389,92 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int j = 0; j < CH; ++j) __stcg(part + (size_t)(c0 + j) * 128 + row, g[j]);
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(buf));
+          if (ph == 1) {
+            // down: the splits of a tile are resident at the same time when the
+            // tile's units fall in one wave; each waits for the tile's partials
+            // and adds its own slice. Otherwise the last split to arrive adds
+            // the whole tile.
+            __threadfence();
+            named_bar_sync(1, 128);
+            unsigned* cnt = P.cnt2 + tm;
+            constexpr int items = tile_items<true, KIND_ROW, BN>();
+            const bool together = (p.units <= (int)grid) || ((int)grid % p.splits == 0);
+            unsigned old = 0;
+            if (et == 0) old = atomicAdd(cnt, 1u);
+            int lo = 0, hi = 0;
+            if (together) {
+              bool w2 = true;
+              if (et == 0) {
+                w2 = bar_wait(cnt, (unsigned)p.splits, timeout, s_abort);
+                if (!w2) set_abort();
+              }
+              if (!agree(w2)) {
+                ok = false;
+                break;
+              }
+              lo = (int)((long long)sp * items / p.splits);
+              hi = (int)((long long)(sp + 1) * items / p.splits);
+            } else if (agree(old == (unsigned)(p.splits - 1))) {
+              __threadfence();
+              hi = items;
+            }
+            if (hi > lo) reduce_tile_items<true, KIND_ROW, BN>(p, tm, lo, hi, et, 128);
+          }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar(buf));
         if (++buf == 2) {
           buf = 0;
           acc_phase ^= 1u;
         }
       }
-      if (!ok) break;
-      if (ph == 0) {
-        if (P.g1.splits > 1) {
-          if (!grid_sync(P.bars + 1, false)) { ok = false; break; }
-          reduce_partials<true, KIND_GATE_UP, BN>(P.g1, etid, ethreads);
-        }
-        // h is read by the tensor copies of phase 2 (async proxy)
-        fence_proxy_async_global();
+      if (ph == 0 && ok && P.g1.splits > 1) {
+        // every CTA's gate_up partials are written: wait for all CTAs, then add
+        // them up tile by tile, in the order the down splits will read h
+        // (round-robin over the down splits, nearest k-block first), counting
+        // finished items per tile so that down can start on a tile at once
         __threadfence();
         named_bar_sync(1, 128);
-        if (et == 0) bar_arrive(P.bars + 2);
-      } else if (P.g2.splits > 1) {
-        if (!grid_sync(P.bars + 3, false)) { ok = false; break; }
-        reduce_partials<true, KIND_ROW, BN>(P.g2, etid, ethreads);
+        bool w1 = true;
+        if (et == 0) {
+          bar_arrive(P.bars + 2);
+          w1 = bar_wait(P.bars + 2, grid, timeout, s_abort);
+          if (!w1) set_abort();
+        }
+        if (!agree(w1)) {
+          ok = false;
+          break;
+        }
+        const GemmParams& q1 = P.g1;
+        const GemmParams& q2 = P.g2;
+        const int n1 = q1.m_tiles;
+        auto dep_of = [&](int kb) {
+          const int sh = kb / q2.kbs, kk = kb - sh * q2.kbs;
+          return sh * q1.nb + (kk * 64) / 128;
+        };
+        auto t0 = [&](int s) { return dep_of((int)((long long)s * q2.nkb / q2.splits)); };
+        const int S2 = q2.splits;
+        const int R = n1 / S2 + 2;
+        constexpr int NCG = kItems1 / 128;
+        const long long total = (long long)S2 * R * NCG * 128;
+        for (long long it = (long long)blockIdx.x * 128 + et; it < total; it += (long long)grid * 128) {
+          const int row = (int)(it & 127);
+          const long long rest = it >> 7;
+          const int cg = (int)(rest % NCG);
+          const int n = (int)(rest / NCG);
+          const int r = n / S2, s = n - r * S2;
+          const int x = t0(s) + r;
+          const bool valid = x < n1 && (s == S2 - 1 || x < t0(s + 1));  // same for the whole warp
+          if (!valid) continue;
+          reduce_tile_items<true, KIND_GATE_UP, BN>(q1, x, cg * 128 + row, cg * 128 + row + 1, 0, 1);
+          fence_proxy_async_global();
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence();
+            atomicAdd(P.hready + x, 32u);
+          }
+        }
       }
     }
   }
@@ -402,12 +484,21 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, S::kTmemCols);
   }
-  // every wait of this CTA is behind it: the last CTA out resets the counters
+  // every wait of this CTA is behind it: the last CTA out resets counters and flags
   if (threadIdx.x == 0) {
     __threadfence();
-    const unsigned old = atomicAdd(P.bars + 4, 1u);
+    const unsigned old = atomicAdd(P.bars + 1, 1u);
     if (old == grid - 1) {
-      for (int i = 0; i < 5; ++i) atomicExch(P.bars + i, 0u);
+      const int n1 = P.g1.m_tiles, n2 = P.g2.m_tiles;
+      for (int i = 0; i < n1; ++i) {
+        P.hready[i] = 0u;
+        P.cnt1[i] = 0u;
+      }
+      for (int i = 0; i < n2; ++i) P.cnt2[i] = 0u;
+      P.bars[0] = 0u;
+      P.bars[2] = 0u;
+      __threadfence();
+      atomicExch(P.bars + 1, 0u);
     }
   }
 }

@@ -115,13 +115,15 @@ int make_map(CUtensorMap* m, const void* ptr, int64_t d0, int64_t d1, int64_t d2
 
 // ============================================================================ workspace layout
 // header: [0] status word; [64] grid barrier of the column-parallel GEMM;
-// [128] grid barrier of the row-parallel GEMM; [192] the 5 phase counters of
-// the fused decode block; T-dependent buffers from kDynOff
+// [128] grid barrier of the row-parallel GEMM; [192] counters of the fused
+// decode block. Then the fused block's per-tile counters and flags (fixed size
+// per handle), then the buffers whose size depends on T.
 constexpr int64_t kGbarColOff = 64;
 constexpr int64_t kGbarRowOff = 128;
 constexpr int64_t kDecodeBarsOff = 192;
+constexpr int64_t kTileCountersOff = 256;
 constexpr int64_t kFusedMaxT = 128;
-constexpr int64_t kDynOff = 256;
+constexpr int64_t kCaptureOff = 256;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per on-chip wait
 
 }  // namespace
@@ -149,6 +151,13 @@ struct tp_linear {
 
 namespace {
 
+// start of the T-dependent part of a forward workspace: after the header and
+// the fused block's per-tile counters (cnt1 and hready per gate_up tile, cnt2
+// per down tile)
+int64_t dyn_off(const tp_linear* h) {
+  return align256(kTileCountersOff + 4 * (2 * (int64_t)h->wt_col + (int64_t)h->wt_row));
+}
+
 struct Plan {
   bool swap;
   int kind;
@@ -158,7 +167,8 @@ struct Plan {
 };
 
 // Pick the operand orientation, tile width and K split of one GEMM.
-Plan make_plan(const tp_linear* h, int which, int64_t T) {
+// force_splits > 0 overrides the split count.
+Plan make_plan(const tp_linear* h, int which, int64_t T, int force_splits = 0) {
   Plan pl{};
   const bool mlp = h->cfg.kind == TP_BLOCK_MLP;
   pl.kind = which == 0 ? (mlp ? KIND_GATE_UP : KIND_COL) : KIND_ROW;
@@ -201,7 +211,7 @@ Plan make_plan(const tp_linear* h, int which, int64_t T) {
       best = s;
     }
   }
-  pl.splits = best;
+  pl.splits = force_splits > 0 ? std::min(force_splits, std::max(1, pl.nkb)) : best;
   pl.units = (int)(tiles * pl.splits);
   pl.grid = (int)std::min<int64_t>(pl.units, h->nsm);   // one CTA per SM (shared memory)
   pl.partial_bytes = pl.splits > 1 ? tiles * pl.splits * pl.acc_cols * 128 * 4 : 0;
@@ -212,9 +222,18 @@ struct Layout {
   int64_t x_norm, h, part_col, part_row, total;
 };
 
+// Split count of the gate_up GEMM inside the fused decode block. Decode streams
+// weights from HBM, and a few more than half the SMs keep it busy, so a unit
+// takes a tile's whole K (h comes straight out of the accumulator, no partials)
+// unless there are too few tiles for that.
+int fused_gate_up_splits(const tp_linear* h) {
+  const int tiles = h->wt_col;
+  return tiles * 2 >= h->nsm ? 1 : std::max(1, h->nsm / tiles);
+}
+
 Layout make_layout(const tp_linear* h, int64_t T) {
   Layout L{};
-  int64_t off = kDynOff;
+  int64_t off = dyn_off(h);
   const bool mlp = h->cfg.kind == TP_BLOCK_MLP;
   if (mlp && (h->cfg.flags & TP_FLAG_HAS_NORM)) {
     L.x_norm = off;
@@ -225,7 +244,9 @@ Layout make_layout(const tp_linear* h, int64_t T) {
     off = align256(off + (int64_t)h->cfg.t * T * h->Is * 2);
   }
   L.part_col = off;
-  off = align256(off + make_plan(h, 0, T).partial_bytes);
+  int64_t pc = make_plan(h, 0, T).partial_bytes;
+  if (T <= kFusedMaxT) pc = std::max(pc, make_plan(h, 0, T, fused_gate_up_splits(h)).partial_bytes);
+  off = align256(off + pc);
   L.part_row = off;
   off = align256(off + make_plan(h, 1, T).partial_bytes);
   L.total = off;
@@ -491,7 +512,7 @@ int tp_workspace_size(const tp_linear_t* h, int64_t max_tokens, int64_t* bytes) 
   if (h == nullptr || bytes == nullptr) return fail(TP_ERR_ARG, "null argument");
   int rc = check_T(max_tokens);
   if (rc) return rc;
-  int64_t best = kDynOff;
+  int64_t best = dyn_off(h);
   for (int64_t T = 1; T <= max_tokens; ++T) best = std::max(best, make_layout(h, T).total);
   *bytes = best;
   return ok();
@@ -610,7 +631,7 @@ int tp_mlp_forward(tp_linear_t* h, int64_t T, const void* x_in, const void* resi
   void* hbuf = ws + L.h;
   if (T <= kFusedMaxT) {
     // decode-shaped step: norm, gate_up, h, down and both reductions in one launch
-    const Plan p1 = make_plan(h, 0, T), p2 = make_plan(h, 1, T);
+    const Plan p1 = make_plan(h, 0, T, fused_gate_up_splits(h)), p2 = make_plan(h, 1, T);
     const void* xsrc = norm ? static_cast<const void*>(ws + L.x_norm) : x_in;
     CUtensorMap map_x, map_h;
     if ((rc = make_map(&map_x, xsrc, h->H, T, 1, 1, p1.bn))) return rc;
@@ -633,6 +654,9 @@ int tp_mlp_forward(tp_linear_t* h, int64_t T, const void* x_in, const void* resi
     P.res_out = static_cast<__nv_bfloat16*>(residual_out);
     P.x_norm = reinterpret_cast<__nv_bfloat16*>(ws + L.x_norm);
     P.bars = reinterpret_cast<unsigned*>(ws + kDecodeBarsOff);
+    P.cnt1 = reinterpret_cast<unsigned*>(ws + kTileCountersOff);
+    P.hready = P.cnt1 + h->wt_col;
+    P.cnt2 = P.hready + h->wt_col;
     P.eps = h->cfg.rms_eps;
     P.H = (int)h->H;
     P.has_norm = norm ? 1 : 0;
@@ -692,8 +716,8 @@ CaptureLayout capture_layout(int64_t T, int64_t n_sel) {
   while ((int64_t(1) << lg) < 2 * n_sel) ++lg;
   c.cap_log2 = lg;
   c.global_table = lg > kSmemTableMaxLog2;
-  c.n_match = kDynOff;
-  c.rows = kDynOff + 256;
+  c.n_match = kCaptureOff;
+  c.rows = kCaptureOff + 256;
   c.table = align256(c.rows + 4 * std::max<int64_t>(T, 1));
   c.total = c.global_table ? align256(c.table + (int64_t(8) << lg)) : c.table;
   return c;
