@@ -1,4 +1,4 @@
-// Fused decode-shaped MLP block: one persistent cooperative launch runs the
+// Fused decode-shaped MLP block: one persistent launch runs the
 // whole step for T <= 128 tokens.
 //
 //   norm     residual add + RMSNorm of the T rows by the epilogue warps (rows
@@ -18,7 +18,7 @@
 //
 // Between the GEMMs, work flows through per-tile counters and flags in the
 // workspace. Every wait is bounded (status word on
-// timeout) and the cooperative launch makes every CTA resident. The last CTA
+// timeout); with one CTA per SM every CTA of the grid is resident. The last CTA
 // to finish resets the counters and flags for the next launch.
 #include "gemm_launch.cuh"
 
@@ -82,6 +82,9 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
   const unsigned long long timeout = P.g1.timeout_ns;
+  // A launch that follows on the same stream may be scheduled onto SMs this grid
+  // frees; it touches nothing but constant weights before its griddepcontrol.wait.
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
   auto set_abort = [&]() {
     if (!*s_abort) {
@@ -105,7 +108,10 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_a = policy_evict_last();
-      constexpr int kPreX = 3;  // weight stages issued before the normalised x exists
+      // weight blocks are constant: they stream before this launch waits for the one
+      // before it (griddepcontrol.wait), which comes first whenever an activation
+      // copy or a counter of the workspace is needed
+      bool dep_waited = false;
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, last_phase_bits = 0;
@@ -135,6 +141,11 @@ __global__ void __launch_bounds__(192, 1)
       // issue every queued activation copy whose data is ready; block (bounded) on the
       // oldest one while more than `keep` entries remain queued
       auto drain = [&](int keep) -> bool {
+        if (q_n <= keep && !dep_waited) return true;
+        if (!dep_waited) {
+          griddep_wait();
+          dep_waited = true;
+        }
         while (q_n > 0) {
           if (dep_ready(q_dep[q_head])) {
             issue_front();
@@ -178,8 +189,7 @@ __global__ void __launch_bounds__(192, 1)
             q_sh[slot] = shard;
             q_dep[slot] = dep;
             ++q_n;
-            const int keep = (!x_ready && ph == 0) ? kPreX - 1 : STAGES - 1;
-            if (!drain(keep)) {
+            if (!drain(STAGES - 1)) {
               set_abort();
               ok = false;
               break;
@@ -193,6 +203,7 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
+      if (!dep_waited) griddep_wait();
       if (ok && !drain(0)) {
         set_abort();
         ok = false;
@@ -278,29 +289,48 @@ __global__ void __launch_bounds__(192, 1)
       named_bar_sync(1, 128);
       return r;
     };
-    // ---- phase 0: residual add + RMSNorm, one row per CTA in turn
+    griddep_wait();
+    // ---- phase 0: residual add + RMSNorm, one row per CTA in turn. The loads of a
+    // chunk of up to 8 vectors per thread are issued together, and the rounded
+    // residual stays in registers for the second pass (H <= 8 * 8 * 128 = 8192
+    // in one chunk; longer rows loop).
     if (P.has_norm) {
       const int H = P.H, nvec = H >> 3;
+      constexpr int NV = 8;
       for (int r = blockIdx.x; r < P.g1.T; r += grid) {
         const size_t roff = (size_t)r * H;
         const uint4* av = reinterpret_cast<const uint4*>(P.x_in + roff);
         const uint4* rv = reinterpret_cast<const uint4*>(P.res_in + roff);
         uint4* ro = reinterpret_cast<uint4*>(P.res_out + roff);
         float ss = 0.f;
-        for (int v = et; v < nvec; v += 128) {
-          const uint4 a4 = __ldg(av + v), r4 = __ldg(rv + v);
-          const __nv_bfloat162* ab = reinterpret_cast<const __nv_bfloat162*>(&a4);
-          const __nv_bfloat162* rb = reinterpret_cast<const __nv_bfloat162*>(&r4);
-          uint4 o;
-          __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+        for (int v0 = 0; v0 < nvec; v0 += NV * 128) {
+          uint4 a4[NV], r4[NV];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 fa = __bfloat1622float2(ab[i]), fr = __bfloat1622float2(rb[i]);
-            ob[i] = __floats2bfloat162_rn(fa.x + fr.x, fa.y + fr.y);
-            const float2 q2 = __bfloat1622float2(ob[i]);  // the stored residual is what is normalised
-            ss += q2.x * q2.x + q2.y * q2.y;
+          for (int k = 0; k < NV; ++k) {
+            const int v = v0 + k * 128 + et;
+            if (v < nvec) {
+              a4[k] = __ldg(av + v);
+              r4[k] = __ldg(rv + v);
+            }
           }
-          ro[v] = o;
+#pragma unroll
+          for (int k = 0; k < NV; ++k) {
+            const int v = v0 + k * 128 + et;
+            if (v < nvec) {
+              const __nv_bfloat162* ab = reinterpret_cast<const __nv_bfloat162*>(&a4[k]);
+              const __nv_bfloat162* rb = reinterpret_cast<const __nv_bfloat162*>(&r4[k]);
+              uint4 o;
+              __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 fa = __bfloat1622float2(ab[i]), fr = __bfloat1622float2(rb[i]);
+                ob[i] = __floats2bfloat162_rn(fa.x + fr.x, fa.y + fr.y);
+                const float2 q2 = __bfloat1622float2(ob[i]);  // the stored residual is what is normalised
+                ss += q2.x * q2.x + q2.y * q2.y;
+              }
+              ro[v] = o;
+            }
+          }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -310,18 +340,32 @@ __global__ void __launch_bounds__(192, 1)
         named_bar_sync(1, 128);
         const uint4* gv = reinterpret_cast<const uint4*>(P.gamma);
         uint4* xo = reinterpret_cast<uint4*>(P.x_norm + roff);
-        for (int v = et; v < nvec; v += 128) {
-          const uint4 r4 = ro[v], g4 = __ldg(gv + v);
-          const __nv_bfloat162* rb = reinterpret_cast<const __nv_bfloat162*>(&r4);
-          const __nv_bfloat162* gb = reinterpret_cast<const __nv_bfloat162*>(&g4);
-          uint4 o;
-          __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+        for (int v0 = 0; v0 < nvec; v0 += NV * 128) {
+          uint4 r4[NV], g4[NV];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 fr = __bfloat1622float2(rb[i]), fg = __bfloat1622float2(gb[i]);
-            ob[i] = __floats2bfloat162_rn(fr.x * inv * fg.x, fr.y * inv * fg.y);
+          for (int k = 0; k < NV; ++k) {
+            const int v = v0 + k * 128 + et;
+            if (v < nvec) {
+              r4[k] = ro[v];   // written by this thread above
+              g4[k] = __ldg(gv + v);
+            }
           }
-          xo[v] = o;
+#pragma unroll
+          for (int k = 0; k < NV; ++k) {
+            const int v = v0 + k * 128 + et;
+            if (v < nvec) {
+              const __nv_bfloat162* rb = reinterpret_cast<const __nv_bfloat162*>(&r4[k]);
+              const __nv_bfloat162* gb = reinterpret_cast<const __nv_bfloat162*>(&g4[k]);
+              uint4 o;
+              __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 fr = __bfloat1622float2(rb[i]), fg = __bfloat1622float2(gb[i]);
+                ob[i] = __floats2bfloat162_rn(fr.x * inv * fg.x, fr.y * inv * fg.y);
+              }
+              xo[v] = o;
+            }
+          }
         }
       }
       // x_norm is read by the tensor copies of phase 1 (async proxy)
@@ -523,12 +567,20 @@ cudaError_t launch_mlp_decode_bn(const CUtensorMap& mx, const CUtensorMap& mh, c
   cfg.blockDim = dim3(192);
   cfg.dynamicSmemBytes = S::kSmemBytes;
   cfg.stream = st;
+  // One CTA per SM (shared memory) and grid == SM count: every CTA is resident
+  // while nothing else occupies the GPU. Programmatic serialisation lets the next
+  // launch on the stream be scheduled onto SMs this grid frees; it can only be
+  // scheduled once every CTA of this grid has started (griddepcontrol.launch_dependents
+  // is executed by all of them), so each grid still becomes fully resident. Waits
+  // between CTAs are bounded: a grid that could not become resident ends with
+  // TP_ERR_TIMEOUT in the status word instead of hanging.
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, mx, mh, P);
+  e = cudaLaunchKernelEx(&cfg, kernel, mx, mh, P);
+  return e;
 }
 
 cudaError_t launch_mlp_decode(int bn, const CUtensorMap& mx, const CUtensorMap& mh, const MlpDecodeParams& P,
