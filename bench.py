@@ -61,6 +61,34 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+# ---------------------------------------------------------------------------- ncu traffic
+def kernel_sources_hash() -> str:
+    import hashlib
+    csrc = os.path.join(ROOT, "tensor_linear_layers_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(key: str):
+    """DRAM bytes per launch from the committed ncu capture of this kernel and
+    workload, or None when there is none or the kernel sources changed since."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("csrc_sha256_16") != kernel_sources_hash():
+        return None
+    k = d.get("kernels", {}).get(key)
+    return None if k is None else float(k["traffic_bytes"])
+
+
 # ---------------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
@@ -460,7 +488,8 @@ def run_ours(args, ws, rank, local):
         dom_alg = float(wbytes + abytes) if fused else dominant_kernel_bytes(w)
         achieved = dom_alg / dom_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                "frac": achieved / pk["hbm_gbs"],
+                "traffic": ncu_traffic(("mlp_decode_kernel@" if fused else "tc_gemm_kernel<swap,GATE_UP>@") + w.name),
                 "kernel": ("fused decode MLP block (mlp_decode_kernel)" if fused
                            else "gate_up column-parallel GEMM (tc_gemm_kernel<swap, GATE_UP>)"),
                 "algorithmic_bytes_per_launch": dom_alg, "avg_launch_us": dom_s * 1e6,
@@ -472,7 +501,9 @@ def run_ours(args, ws, rank, local):
         dom_alg = dominant_kernel_flops(w)
         achieved = dom_alg / dom_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / pk["bf16_tflops"], "traffic": None,
+                "frac": achieved / pk["bf16_tflops"],
+                "traffic": ncu_traffic(("tc_gemm_kernel<noswap,GATE_UP>@" if w.kind == "mlp"
+                                        else "tc_gemm_kernel<noswap,COL>@") + w.name),
                 "kernel": "column-parallel GEMM (tc_gemm_kernel<noswap>)",
                 "algorithmic_flops_per_launch": dom_alg, "avg_launch_us": dom_s * 1e6,
                 "peak_source": pk["source"] + " bf16_tflops (cuBLAS burst)"}
