@@ -123,6 +123,32 @@ int tp_mlp_forward(tp_linear_t* h, int64_t T, const void* x_in, const void* resi
                    void* workspace, int64_t workspace_bytes, tp_stream_t stream);
 
 /*
+ * tp_mlp_forward for callers that cannot allocate device memory. The pages
+ * have no counterpart: it is a service of this library, not a step of the
+ * method. Some callers may not call cudaMalloc at all, or not at the moment
+ * they run the block: plug-ins whose host hands them only memory it planned
+ * ahead, runtimes whose own allocator owns all device memory, real-time loops
+ * that forbid allocation after start-up. This entry point allocates nothing; it
+ * runs the same fused decode-shaped block as tp_mlp_forward (same arguments,
+ * same results) with its scratch in a fixed 16 MiB array inside the library
+ * (each GPU that loads the library holds it until the process exits).
+ *   - T <= 128 only, and only shapes whose scratch fits in 16 MiB; anything
+ *     larger returns TP_ERR_UNSUPPORTED with the size in tp_last_error().
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents:
+ *     calls that may overlap on the GPU (two streams, two handles) race and
+ *     must be serialised by the caller. Each call clears the counters it needs
+ *     (a memset on `stream`, not an allocation).
+ *   - status_dev: optional device int32 the caller owns and zeroes; kernels
+ *     write a TP_ERR_* code there on a device-side failure. NULL: not reported.
+ * Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+int tp_mlp_forward_no_alloc(tp_linear_t* h, int64_t T, const void* x_in, const void* residual_in,
+                            void* residual_out, void* mlp_out, void* residual_stream,
+                            int32_t* status_dev, tp_stream_t stream);
+
+/*
  * The steps of tp_mlp_forward, one call each (same semantics, same kernels):
  *   tp_add_rms_norm : residual_out = a + residual_in; x_out = RMSNorm(residual_out) * gamma.
  *                     a, residual_in, residual_out, x_out [T, H]; gamma [H]. Any H % 8 == 0.

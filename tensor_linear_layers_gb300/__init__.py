@@ -27,7 +27,7 @@ ABI_SYMBOLS = (
     "tp_packed_weight_bytes", "tp_linear_create", "tp_linear_destroy", "tp_workspace_size",
     "tp_mlp_forward", "tp_add_rms_norm", "tp_gate_up_forward", "tp_down_forward",
     "tp_attn_proj_forward", "tp_capture_workspace_size", "tp_capture_rows", "tp_last_error",
-    "tp_describe_plan",
+    "tp_describe_plan", "tp_mlp_forward_no_alloc",
 )
 
 
@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
         "tp_capture_rows": [I64, I64, P, P, P, I64, I32, ctypes.POINTER(P), ctypes.POINTER(I32),
                             I32, P, P, I64, P, P, I64, P],
         "tp_describe_plan": [P, I64, ctypes.POINTER(GemmPlan), I32],
+        "tp_mlp_forward_no_alloc": [P, I64, P, P, P, P, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -200,6 +201,24 @@ class TPLinear:
         _check(lib().tp_mlp_forward(self.handle, T, _ptr(_bf16(x, "x")), _ptr(residual), _ptr(o.get("residual_out")),
                                     _ptr(o["mlp_out"]), _ptr(o.get("residual_stream")), _ptr(ws), ws.numel(),
                                     _stream(stream)))
+        return o
+
+    def mlp_forward_no_alloc(self, x: torch.Tensor, residual: Optional[torch.Tensor] = None,
+                             residual_stream: bool = True, out: Optional[dict] = None,
+                             status: Optional[torch.Tensor] = None, stream=None) -> dict:
+        """tp_mlp_forward_no_alloc: the decode-shaped block with the library's fixed scratch."""
+        T, H = x.shape
+        norm = bool(self.cfg.flags & TP_FLAG_HAS_NORM)
+        o = out if out is not None else {}
+        if "mlp_out" not in o:
+            o["mlp_out"] = torch.empty_like(x)
+        if norm and "residual_out" not in o:
+            o["residual_out"] = torch.empty_like(x)
+        if residual_stream and residual is not None and "residual_stream" not in o:
+            o["residual_stream"] = torch.empty_like(x)
+        _check(lib().tp_mlp_forward_no_alloc(self.handle, T, _ptr(_bf16(x, "x")), _ptr(residual),
+                                             _ptr(o.get("residual_out")), _ptr(o["mlp_out"]),
+                                             _ptr(o.get("residual_stream")), _ptr(status), _stream(stream)))
         return o
 
     def gate_up(self, x: torch.Tensor, h_out: Optional[torch.Tensor] = None, ws=None, stream=None) -> torch.Tensor:

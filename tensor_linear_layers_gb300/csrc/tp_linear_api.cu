@@ -702,6 +702,129 @@ int tp_attn_proj_forward(tp_linear_t* h, int64_t T, const void* x, void* qkv_out
   return ok();
 }
 
+// ---------------------------------------------------------------------------- no-allocation variant
+// Scratch of tp_mlp_forward_no_alloc: a file-scope device array, so callers that
+// must not allocate device memory still get the fused decode block. Every GPU
+// that loads this library holds these 16 MiB until the process exits.
+namespace {
+constexpr int64_t kNoAllocScratchBytes = int64_t(16) << 20;
+static __device__ __align__(256) unsigned char g_no_alloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_no_alloc_scratch per device ordinal, looked up once per
+// device with that device current (in host code the symbol itself is only a
+// host-side stand-in and must never be handed to a kernel).
+constexpr int kMaxDevices = 64;
+std::mutex g_no_alloc_mu;
+void* g_no_alloc_ptr[kMaxDevices] = {};
+
+// Scratch the fused decode kernel itself uses: the counters, x_norm, h and the
+// split-K partials of its own two plans.
+Layout no_alloc_layout(const tp_linear* h, int64_t T) {
+  Layout L{};
+  int64_t off = dyn_off(h);
+  if (h->cfg.flags & TP_FLAG_HAS_NORM) {
+    L.x_norm = off;
+    off = align256(off + T * h->H * 2);
+  }
+  L.h = off;
+  off = align256(off + (int64_t)h->cfg.t * T * h->Is * 2);
+  L.part_col = off;
+  off = align256(off + make_plan(h, 0, T, fused_gate_up_splits(h)).partial_bytes);
+  L.part_row = off;
+  off = align256(off + make_plan(h, 1, T).partial_bytes);
+  L.total = off;
+  return L;
+}
+
+int no_alloc_scratch(int device, void** out) {
+  if (device < 0 || device >= kMaxDevices) return fail(TP_ERR_UNSUPPORTED, "device ordinal %d", device);
+  std::lock_guard<std::mutex> lock(g_no_alloc_mu);
+  if (g_no_alloc_ptr[device] == nullptr) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_no_alloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    g_no_alloc_ptr[device] = ptr;
+  }
+  *out = g_no_alloc_ptr[device];
+  return TP_OK;
+}
+}  // namespace
+
+extern "C" int tp_mlp_forward_no_alloc(tp_linear_t* h, int64_t T, const void* x_in, const void* residual_in,
+                                       void* residual_out, void* mlp_out, void* residual_stream,
+                                       int32_t* status_dev, tp_stream_t stream) {
+  if (h == nullptr) return fail(TP_ERR_ARG, "handle is null");
+  if (h->cfg.kind != TP_BLOCK_MLP) return fail(TP_ERR_ARG, "not an MLP handle");
+  int rc = check_T(T);
+  if (rc) return rc;
+  if (T == 0) return ok();
+  if (T > kFusedMaxT)
+    return fail(TP_ERR_UNSUPPORTED, "tp_mlp_forward_no_alloc runs the decode-shaped block only: T=%lld > %lld",
+                (long long)T, (long long)kFusedMaxT);
+  const bool norm = (h->cfg.flags & TP_FLAG_HAS_NORM) != 0;
+  TP_CHECK_PTR(x_in, "x_in");
+  TP_CHECK_PTR(mlp_out, "mlp_out");
+  if (norm) {
+    TP_CHECK_PTR(residual_in, "residual_in");
+    TP_CHECK_PTR(residual_out, "residual_out");
+  }
+  if (residual_in != nullptr) TP_CHECK_PTR(residual_in, "residual_in");
+  if (residual_stream != nullptr) {
+    TP_CHECK_PTR(residual_stream, "residual_stream");
+    if (residual_in == nullptr) return fail(TP_ERR_ARG, "residual_stream needs a residual");
+  }
+  if (status_dev != nullptr && (reinterpret_cast<uintptr_t>(status_dev) & 3u) != 0)
+    return fail(TP_ERR_ARG, "status_dev is not 4-byte aligned");
+  if ((rc = check_device(h))) return rc;
+  const Layout L = no_alloc_layout(h, T);
+  if (L.total > kNoAllocScratchBytes)
+    return fail(TP_ERR_UNSUPPORTED,
+                "tp_mlp_forward_no_alloc: this shape needs %lld bytes of scratch, the fixed scratch holds %lld",
+                (long long)L.total, (long long)kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  if ((rc = no_alloc_scratch(h->device, &scratch))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(scratch);
+  // the phase counters and flags must start at zero; a call that gave up may have
+  // left them set, so clear them on every call (a memset, not an allocation)
+  cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)dyn_off(h), st);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the no-alloc scratch counters");
+  void* hbuf = ws + L.h;
+  const Plan p1 = make_plan(h, 0, T, fused_gate_up_splits(h)), p2 = make_plan(h, 1, T);
+  const void* xsrc = norm ? static_cast<const void*>(ws + L.x_norm) : x_in;
+  CUtensorMap map_x, map_h;
+  if ((rc = make_map(&map_x, xsrc, h->H, T, 1, 1, p1.bn))) return rc;
+  if ((rc = make_map(&map_h, hbuf, h->Ks, T, 1, h->cfg.t, p2.bn))) return rc;
+  MlpDecodeParams P{};
+  P.g1 = base_params(p1, T, scratch, L.part_col, kGbarColOff);
+  P.g1.out = static_cast<__nv_bfloat16*>(hbuf);
+  P.g1.Is = (int)h->Is;
+  P.g1.w_packed = static_cast<const uint8_t*>(h->w_col);
+  P.g2 = base_params(p2, T, scratch, L.part_row, kGbarRowOff);
+  P.g2.n_out = (int)h->H;
+  P.g2.ws_out = (int)h->H;
+  P.g2.out = static_cast<__nv_bfloat16*>(mlp_out);
+  P.g2.out2 = static_cast<__nv_bfloat16*>(residual_stream);
+  P.g2.resid = static_cast<const __nv_bfloat16*>(norm ? residual_out : residual_in);
+  P.g2.w_packed = static_cast<const uint8_t*>(h->w_row);
+  if (status_dev != nullptr) P.g1.status = P.g2.status = status_dev;
+  P.x_in = static_cast<const __nv_bfloat16*>(x_in);
+  P.res_in = static_cast<const __nv_bfloat16*>(residual_in);
+  P.gamma = static_cast<const __nv_bfloat16*>(h->gamma);
+  P.res_out = static_cast<__nv_bfloat16*>(residual_out);
+  P.x_norm = reinterpret_cast<__nv_bfloat16*>(ws + L.x_norm);
+  P.bars = reinterpret_cast<unsigned*>(ws + kDecodeBarsOff);
+  P.cnt1 = reinterpret_cast<unsigned*>(ws + kTileCountersOff);
+  P.hready = P.cnt1 + h->wt_col;
+  P.cnt2 = P.hready + h->wt_col;
+  P.eps = h->cfg.rms_eps;
+  P.H = (int)h->H;
+  P.has_norm = norm ? 1 : 0;
+  e = launch_mlp_decode(p1.bn, map_x, map_h, P, h->nsm, st);
+  if (e != cudaSuccess) return cuda_fail(e, "fused decode MLP launch (no-alloc)");
+  return ok();
+}
+
 // ---------------------------------------------------------------------------- capture
 namespace {
 constexpr int kSmemTableMaxLog2 = 13;  // 8192 slots = 64 KB of shared memory
