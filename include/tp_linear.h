@@ -50,7 +50,7 @@ extern "C" {
 #define TP_ERR_CAPACITY (-5)    /* device status: capture records exceeded capacity */
 #define TP_ERR_TIMEOUT (-6)     /* device status: a bounded on-chip wait gave up */
 
-typedef struct tp_linear tp_linear_t; /* opaque handle: metadata + prebuilt weight tensor maps */
+typedef struct tp_linear tp_linear_t; /* opaque handle: shapes, plans, packed-weight pointers */
 typedef void* tp_stream_t;            /* cudaStream_t */
 
 enum { TP_BLOCK_MLP = 0, TP_BLOCK_ATTN_PROJ = 1 };
@@ -71,13 +71,19 @@ typedef struct {
 
 /*
  * Sizes of the two packed weight buffers the caller allocates for a handle.
- *   MLP : col = gate_up  [t][2][I/t][H]   (shard r: its gate rows, then its up rows)
- *         row = down     [t][H][I/t]      (shard r: input columns r*I/t .. of W_down)
- *   ATTN: col = qkv      [t][w_s][H]      (shard r: its q heads | k heads | v heads,
- *                                          w_s = (nq/t + 2*kv_per_shard) * hd)
- *         row = o_proj   [t][H][nq*hd/t]
- * "MergedColumnParallelLinear" / "QkvParallelLinear" / "RowParallelLinear"
- * (weight_loader: narrow(dim, rank * shard, shard)).
+ * Logically each buffer holds the t shards the pages describe
+ * ("MergedColumnParallelLinear" / "QkvParallelLinear" / "RowParallelLinear",
+ * weight_loader: narrow(dim, rank * shard, shard)):
+ *   MLP : col = gate_up  shard r: its gate rows, then its up rows
+ *         row = down     shard r: input columns r*I/t .. (r+1)*I/t of W_down
+ *   ATTN: col = qkv      shard r: its q heads | k heads | v heads
+ *                        (w_s = (nq/t + 2*kv_per_shard) * hd rows)
+ *         row = o_proj   shard r: input columns of its heads
+ * Physically they are stored as 32 KB blocks of 256 rows x 64 input features
+ * in the 128-byte-swizzled image the tensor cores read (gate_up: 128 gate +
+ * the matching 128 up rows of one shard per block; row-parallel weights: K
+ * running over shard 0, then shard 1, ...). Rows or K past the end are zero,
+ * so the sizes are those of the padded block grid.
  */
 int tp_packed_weight_bytes(const tp_config_t* cfg, int64_t* col_bytes, int64_t* row_bytes);
 
