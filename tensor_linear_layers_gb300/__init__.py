@@ -154,6 +154,7 @@ class TPLinear:
                                   _ptr(self.gamma), _stream(stream), ctypes.byref(h)))
         self.handle = h
         self._ws = None
+        self._ws_sizes = {}
 
     def close(self):
         if getattr(self, "handle", None) is not None and self.handle.value:
@@ -168,9 +169,12 @@ class TPLinear:
 
     # ------------------------------------------------------------------ workspace
     def workspace_size(self, max_tokens: int) -> int:
-        b = ctypes.c_int64()
-        _check(lib().tp_workspace_size(self.handle, max_tokens, ctypes.byref(b)))
-        return b.value
+        got = self._ws_sizes.get(max_tokens)
+        if got is None:
+            b = ctypes.c_int64()
+            _check(lib().tp_workspace_size(self.handle, max_tokens, ctypes.byref(b)))
+            got = self._ws_sizes[max_tokens] = b.value
+        return got
 
     def workspace(self, max_tokens: int) -> torch.Tensor:
         """A zero-filled workspace for calls of up to max_tokens tokens (cached, grows on demand)."""

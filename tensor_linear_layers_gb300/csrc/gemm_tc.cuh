@@ -40,6 +40,7 @@
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <type_traits>
 #include "ptx.cuh"
 
 namespace tpl {
@@ -355,10 +356,16 @@ __device__ __forceinline__ bool grid_barrier(unsigned* gbar, unsigned nblocks, u
   return true;
 }
 
-template <bool SWAP, int KIND, int BN>
+// KIND2 >= 0 runs a second, independent problem (same operand shapes, split
+// count 1) in the same launch: the units of both problems form one list that
+// the persistent CTAs walk, so the two problems share the waves.
+template <bool SWAP, int KIND, int BN, int KIND2 = -1>
 __global__ void __launch_bounds__(192, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_act, const GemmParams p) {
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_act2,
+                   const GemmParams p, const GemmParams p2) {
   using S = GemmShape<SWAP, KIND, BN>;
+  constexpr bool kTwo = KIND2 >= 0;
+  const int units_all = p.units + (kTwo ? p2.units : 0);
   constexpr int STAGES = S::kStages;
   constexpr int NA = S::NA;
 
@@ -393,6 +400,7 @@ __global__ void __launch_bounds__(192, 1)
     *s_abort = 0;
     fence_barrier_init();
     prefetch_tensormap(&map_act);
+    if (kTwo) prefetch_tensormap(&map_act2);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(s_tmem)), S::kTmemCols);
@@ -403,22 +411,25 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
 
-  // unit -> (tile m, tile n, split)
-  auto decode_unit = [&](int u, int& tm, int& tn, int& sp) {
-    const int tile = u / p.splits;
-    sp = u - tile * p.splits;
-    if (!SWAP && p.group_m > 1) {
-      const int group_size = p.group_m * p.n_tiles;
+  // unit of the combined list -> (problem, tile m, tile n, split)
+  auto decode_unit = [&](int ug, bool& second, int& tm, int& tn, int& sp) {
+    second = kTwo && ug >= p.units;
+    const int u = second ? ug - p.units : ug;
+    const GemmParams& q = second ? p2 : p;
+    const int tile = u / q.splits;
+    sp = u - tile * q.splits;
+    if (!SWAP && q.group_m > 1) {
+      const int group_size = q.group_m * q.n_tiles;
       const int g = tile / group_size;
-      const int first_m = g * p.group_m;
-      const int rem = p.m_tiles - first_m;
-      const int gm = rem < p.group_m ? rem : p.group_m;
+      const int first_m = g * q.group_m;
+      const int rem = q.m_tiles - first_m;
+      const int gm = rem < q.group_m ? rem : q.group_m;
       const int in_g = tile - g * group_size;
       tm = first_m + in_g % gm;
       tn = in_g / gm;
     } else {
-      tm = tile / p.n_tiles;
-      tn = tile - tm * p.n_tiles;
+      tm = tile / q.n_tiles;
+      tn = tile - tm * q.n_tiles;
     }
   };
 
@@ -433,13 +444,17 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0, last_phase_bits = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+      for (int ug = blockIdx.x; ug < units_all && ok; ug += gridDim.x) {
         int tm, tn, sp;
-        decode_unit(u, tm, tn, sp);
-        const int kb0 = (int)((long long)sp * p.nkb / p.splits);
-        const int kb1 = (int)((long long)(sp + 1) * p.nkb / p.splits);
+        bool second;
+        decode_unit(ug, second, tm, tn, sp);
+        const GemmParams& q = second ? p2 : p;
+        const CUtensorMap* map = second ? &map_act2 : &map_act;
+        const bool row_kind = second ? (KIND2 == KIND_ROW) : (KIND == KIND_ROW);
+        const int kb0 = (int)((long long)sp * q.nkb / q.splits);
+        const int kb1 = (int)((long long)(sp + 1) * q.nkb / q.splits);
         const int wt = SWAP ? tm : tn;
-        const uint8_t* wsrc = p.w_packed + (size_t)wt * p.nkb * kWBlockBytes;
+        const uint8_t* wsrc = q.w_packed + (size_t)wt * q.nkb * kWBlockBytes;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, p.timeout_ns)) {
             if (!*s_abort) {
@@ -454,17 +469,17 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, S::kStageBytes);
           int kx = kb * 64, shard = 0;
-          if (KIND == KIND_ROW) {
-            shard = kb / p.kbs;
-            kx = (kb - shard * p.kbs) * 64;
+          if (row_kind) {
+            shard = kb / q.kbs;
+            kx = (kb - shard * q.kbs) * 64;
           }
           const uint8_t* wblk = wsrc + (size_t)kb * kWBlockBytes;
           if (!SWAP) {
-            tma_load_4d(sa, &map_act, fb, kx, tm * 128, 0, shard, pol_a);   // 128 tokens
+            tma_load_4d(sa, map, fb, kx, tm * 128, 0, shard, pol_a);        // 128 tokens
             bulk_load(sb, wblk, kWBlockBytes, fb, pol_w);                   // 256 weight rows
           } else {
             bulk_load(sa, wblk, kWBlockBytes, fb, pol_w);                   // 256 weight rows
-            tma_load_4d(sb, &map_act, fb, kx, tn * BN, 0, shard, pol_a);    // BN tokens
+            tma_load_4d(sb, map, fb, kx, tn * BN, 0, shard, pol_a);         // BN tokens
           }
           issued_mask |= 1u << stage;
           last_phase_bits = (last_phase_bits & ~(1u << stage)) | (phase << stage);
@@ -490,11 +505,13 @@ __global__ void __launch_bounds__(192, 1)
       int buf = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+      for (int ug = blockIdx.x; ug < units_all && ok; ug += gridDim.x) {
         int tm, tn, sp;
-        decode_unit(u, tm, tn, sp);
-        const int kb0 = (int)((long long)sp * p.nkb / p.splits);
-        const int kb1 = (int)((long long)(sp + 1) * p.nkb / p.splits);
+        bool second;
+        decode_unit(ug, second, tm, tn, sp);
+        const GemmParams& q = second ? p2 : p;
+        const int kb0 = (int)((long long)sp * q.nkb / q.splits);
+        const int kb1 = (int)((long long)(sp + 1) * q.nkb / q.splits);
         if (!mbar_wait_bounded(tempty_bar(buf), acc_phase ^ 1u, s_abort, p.timeout_ns)) {
           if (!*s_abort) {
             atomicExch(p.status, kStatusTimeout);
@@ -555,9 +572,10 @@ __global__ void __launch_bounds__(192, 1)
     constexpr int CH = S::kCh;
     constexpr int ACC = S::kAccCols;
 
-    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+    for (int ug = blockIdx.x; ug < units_all; ug += gridDim.x) {
       int tm, tn, sp;
-      decode_unit(u, tm, tn, sp);
+      bool second;
+      decode_unit(ug, second, tm, tn, sp);
       // one thread waits and the decision is shared, so all 128 epilogue
       // threads leave together and no named barrier is left half-joined
       if (et == 0) {
@@ -576,20 +594,31 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t acc = lane_addr + buf * ACC;
       const int tile = tm * p.n_tiles + tn;
       float g[CH], uu[CH];
-      if (p.splits == 1) {
+      // epilogue of one unit of problem kind K, straight from the accumulator
+      auto direct = [&](auto kind_c, const GemmParams& q) {
+        constexpr int K = decltype(kind_c)::value;
+        using SK = GemmShape<SWAP, K, BN>;
 #pragma unroll 1
-        for (int seg = 0; seg < S::kSeg; ++seg) {
+        for (int seg = 0; seg < SK::kSeg; ++seg) {
 #pragma unroll 1
-          for (int c0 = 0; c0 < S::kNG; c0 += CH) {
+          for (int c0 = 0; c0 < SK::kNG; c0 += CH) {
             const uint32_t col = seg * BN + c0;
             if (CH == 32) tmem_ld32(acc + col, g); else tmem_ld16(acc + col, g);
-            if (KIND == KIND_GATE_UP) {
-              if (CH == 32) tmem_ld32(acc + S::kUOff + col, uu); else tmem_ld16(acc + S::kUOff + col, uu);
+            if (K == KIND_GATE_UP) {
+              if (CH == 32) tmem_ld32(acc + SK::kUOff + col, uu); else tmem_ld16(acc + SK::kUOff + col, uu);
             }
             tc_wait_ld();
-            emit_vals<SWAP, KIND, BN, CH>(p, tm, tn, seg, row, c0, g, uu);
+            emit_vals<SWAP, K, BN, CH>(q, tm, tn, seg, row, c0, g, uu);
           }
         }
+      };
+      if (second) {
+        direct(std::integral_constant<int, (kTwo ? KIND2 : KIND)>{}, p2);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(buf));
+      } else if (p.splits == 1) {
+        direct(std::integral_constant<int, KIND>{}, p);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty_bar(buf));

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -24,6 +25,11 @@ cudaError_t launch_gemm_decode_col(int bn, const CUtensorMap& a, const GemmParam
 cudaError_t launch_gemm_decode_row(int bn, const CUtensorMap& a, const GemmParams& p, int grid,
                                    cudaStream_t st);
 int gemm_stages_prefill(int kind);
+cudaError_t launch_gemm_prefill_col_row(const CUtensorMap& a1, const GemmParams& p1, const CUtensorMap& a2,
+                                        const GemmParams& p2, int grid, cudaStream_t st);
+cudaError_t launch_gemm_pair(int kind, int kind2, const CUtensorMap& a1, const GemmParams& p1,
+                             const CUtensorMap& a2, const GemmParams& p2, int max_clusters, cudaStream_t st);
+int pair_max_clusters();
 int gemm_stages_decode_gate_up(int bn);
 int gemm_stages_decode_col(int bn);
 int gemm_stages_decode_row(int bn);
@@ -262,6 +268,37 @@ int check_device(const tp_linear* h) {
   return TP_OK;
 }
 
+// Prefill GEMMs may run on CTA pairs that share each weight block (multicast);
+// TPL_GEMM_PAIR=0 in the environment keeps them on single CTAs.
+bool pair_engine_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("TPL_GEMM_PAIR");
+    return v == nullptr || v[0] != '0';
+  }();
+  return on;
+}
+// Estimated cost (in k-block times of one CTA) of running prefill units of full K on
+// pairs vs. the single-CTA plan; a pair k-block is assumed to take 0.8 of a single one
+// because it pulls a third less from L2.
+bool prefer_pair(const tp_linear* h, const Plan* pls, int n, int ncl) {
+  if (!pair_engine_enabled() || ncl <= 0) return false;
+  long long pu = 0, units = 0;
+  double one = 0;
+  for (int i = 0; i < n; ++i) {
+    const Plan& pl = pls[i];
+    if (pl.swap) return false;
+    pu += (long long)((pl.m_tiles + 1) / 2) * pl.n_tiles;
+    units += pl.units;
+  }
+  // single-CTA cost of the same plans (as launched)
+  if (n == 1)
+    one = (double)ceil_div(pls[0].units, h->nsm) * ((double)pls[0].nkb / pls[0].splits + (pls[0].splits > 1 ? 16.0 : 0.0));
+  else
+    one = (double)ceil_div(units, h->nsm) * pls[0].nkb;
+  const double pair = (double)ceil_div(pu, ncl) * pls[0].nkb * 0.8;
+  return pair < one;
+}
+
 GemmParams base_params(const Plan& pl, int64_t T, void* ws, int64_t part_off, int64_t gbar_off) {
   GemmParams p{};
   p.T = (int)T;
@@ -297,6 +334,16 @@ int run_col(const tp_linear* h, int64_t T, const void* x, void* out, void* ws, c
     p.ws_out = (int)h->ws_qkv;
   }
   p.w_packed = static_cast<const uint8_t*>(h->w_col);
+  const int ncl = pl.swap ? 0 : pair_max_clusters();
+  if (!pl.swap && prefer_pair(h, &pl, 1, ncl)) {
+    const Plan p1 = make_plan(h, 0, T, 1);
+    GemmParams q = p;
+    q.splits = 1;
+    q.units = p1.units;
+    cudaError_t e = launch_gemm_pair(pl.kind, -1, map_x, q, map_x, q, ncl, st);
+    if (e != cudaSuccess) return cuda_fail(e, "column-parallel GEMM launch (pairs)");
+    return TP_OK;
+  }
   cudaError_t e = launch_gemm(pl.swap, pl.kind, pl.bn, map_x, p, pl.grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "column-parallel GEMM launch");
   return TP_OK;
@@ -316,8 +363,51 @@ int run_row(const tp_linear* h, int64_t T, const void* in_shards, const void* re
   p.out2 = static_cast<__nv_bfloat16*>(out2);
   p.resid = static_cast<const __nv_bfloat16*>(resid);
   p.w_packed = static_cast<const uint8_t*>(h->w_row);
+  const int ncl = pl.swap ? 0 : pair_max_clusters();
+  if (!pl.swap && prefer_pair(h, &pl, 1, ncl)) {
+    const Plan p1 = make_plan(h, 1, T, 1);
+    GemmParams q = p;
+    q.splits = 1;
+    q.units = p1.units;
+    cudaError_t e = launch_gemm_pair(pl.kind, -1, map_in, q, map_in, q, ncl, st);
+    if (e != cudaSuccess) return cuda_fail(e, "row-parallel GEMM launch (pairs)");
+    return TP_OK;
+  }
   cudaError_t e = launch_gemm(pl.swap, pl.kind, pl.bn, map_in, p, pl.grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "row-parallel GEMM launch");
+  return TP_OK;
+}
+
+// QKV and o_proj of one attention block at prefill size: the two GEMMs are
+// independent (o_proj reads the caller's attention output), so one launch walks
+// both problems' tiles and they share the waves.
+int run_col_row_together(const tp_linear* h, int64_t T, const void* x, void* qkv_out, const void* attn_in,
+                         void* o_out, void* ws, const Layout& L, cudaStream_t st) {
+  const Plan pc = make_plan(h, 0, T, 1), pr = make_plan(h, 1, T, 1);
+  CUtensorMap map_x, map_a;
+  int rc = make_map(&map_x, x, h->H, T, 1, 1, 128);
+  if (!rc) rc = make_map(&map_a, attn_in, h->Ks, T, 1, h->cfg.t, 128);
+  if (rc) return rc;
+  GemmParams p1 = base_params(pc, T, ws, L.part_col, kGbarColOff);
+  p1.out = static_cast<__nv_bfloat16*>(qkv_out);
+  p1.n_out = (int)h->n_col;
+  p1.ws_out = (int)h->ws_qkv;
+  p1.w_packed = static_cast<const uint8_t*>(h->w_col);
+  GemmParams p2 = base_params(pr, T, ws, L.part_row, kGbarRowOff);
+  p2.out = static_cast<__nv_bfloat16*>(o_out);
+  p2.n_out = (int)h->H;
+  p2.ws_out = (int)h->H;
+  p2.w_packed = static_cast<const uint8_t*>(h->w_row);
+  const int ncl = pair_max_clusters();
+  const Plan both[2] = {pc, pr};
+  cudaError_t e;
+  if (prefer_pair(h, both, 2, ncl)) {
+    e = launch_gemm_pair(KIND_COL, KIND_ROW, map_x, p1, map_a, p2, ncl, st);
+  } else {
+    const int grid = (int)std::min<int64_t>((int64_t)pc.units + pr.units, h->nsm);
+    e = launch_gemm_prefill_col_row(map_x, p1, map_a, p2, grid, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "attention projections launch");
   return TP_OK;
 }
 
@@ -512,8 +602,14 @@ int tp_workspace_size(const tp_linear_t* h, int64_t max_tokens, int64_t* bytes) 
   if (h == nullptr || bytes == nullptr) return fail(TP_ERR_ARG, "null argument");
   int rc = check_T(max_tokens);
   if (rc) return rc;
+  // Up to 128 tokens every T has its own plan; beyond, a plan depends on T only
+  // through the number of 128-token tiles, and the buffers grow with T, so the
+  // largest T of each tile count bounds that count.
   int64_t best = dyn_off(h);
-  for (int64_t T = 1; T <= max_tokens; ++T) best = std::max(best, make_layout(h, T).total);
+  for (int64_t T = 1; T <= std::min<int64_t>(max_tokens, kFusedMaxT); ++T)
+    best = std::max(best, make_layout(h, T).total);
+  for (int64_t m = 2; (m - 1) * 128 < max_tokens; ++m)
+    best = std::max(best, make_layout(h, std::min<int64_t>(max_tokens, m * 128)).total);
   *bytes = best;
   return ok();
 }
@@ -697,6 +793,10 @@ int tp_attn_proj_forward(tp_linear_t* h, int64_t T, const void* x, void* qkv_out
   if ((rc = check_device(h))) return rc;
   if (T == 0) return ok();
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (do_qkv && do_o && T > kFusedMaxT) {
+    if ((rc = run_col_row_together(h, T, x, qkv_out, attn_in, o_out, workspace, L, st))) return rc;
+    return ok();
+  }
   if (do_qkv && (rc = run_col(h, T, x, qkv_out, workspace, L, st))) return rc;
   if (do_o && (rc = run_row(h, T, attn_in, nullptr, o_out, nullptr, workspace, L, st))) return rc;
   return ok();

@@ -285,3 +285,13 @@ def test_fused_decode_block_matches_stage_calls(T):
     assert rel_err(fused["residual_stream"], ref["residual_stream"]) <= TOL
     assert rel_err(fused["mlp_out"], y.double().cpu().numpy()) <= 1e-2
     assert status_of(blk.workspace(T)) == 0
+
+
+def test_workspace_bound_covers_every_token_count():
+    # one workspace sized for max_tokens must serve every T <= max_tokens
+    blk, d = make_mlp(512, 1408, 2, norm=True)
+    ws = blk.workspace(300)
+    for T in list(range(1, 140)) + [200, 255, 256, 257, 299, 300]:
+        a = torch.zeros(T, 512, dtype=torch.bfloat16, device="cuda")
+        blk.mlp_forward(a, residual=a.clone(), ws=ws)
+    assert status_of(ws) == 0
