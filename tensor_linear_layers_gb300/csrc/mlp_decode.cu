@@ -290,27 +290,32 @@ __global__ void __launch_bounds__(192, 1)
       return r;
     };
     griddep_wait();
-    // ---- phase 0: residual add + RMSNorm, one row per CTA in turn. The loads of a
-    // chunk of up to 8 vectors per thread are issued together, and the rounded
-    // residual stays in registers for the second pass (H <= 8 * 8 * 128 = 8192
-    // in one chunk; longer rows loop).
+    // ---- phase 0: residual add + RMSNorm, one row per CTA in turn. The loads of
+    // a chunk (a, residual and gamma, up to 8 vectors per thread each) are issued
+    // together before anything waits on them, and the rounded residual stays in
+    // registers, so a row costs one memory round trip (H <= 8 * 8 * 128 = 8192 in
+    // one chunk; longer rows loop).
     if (P.has_norm) {
       const int H = P.H, nvec = H >> 3;
       constexpr int NV = 8;
+      const uint4* gv = reinterpret_cast<const uint4*>(P.gamma);
       for (int r = blockIdx.x; r < P.g1.T; r += grid) {
         const size_t roff = (size_t)r * H;
         const uint4* av = reinterpret_cast<const uint4*>(P.x_in + roff);
         const uint4* rv = reinterpret_cast<const uint4*>(P.res_in + roff);
         uint4* ro = reinterpret_cast<uint4*>(P.res_out + roff);
+        uint4* xo = reinterpret_cast<uint4*>(P.x_norm + roff);
+        const bool one_chunk = nvec <= NV * 128;
         float ss = 0.f;
+        uint4 a4[NV], r4[NV], g4[NV];
         for (int v0 = 0; v0 < nvec; v0 += NV * 128) {
-          uint4 a4[NV], r4[NV];
 #pragma unroll
           for (int k = 0; k < NV; ++k) {
             const int v = v0 + k * 128 + et;
             if (v < nvec) {
               a4[k] = __ldg(av + v);
               r4[k] = __ldg(rv + v);
+              g4[k] = __ldg(gv + v);
             }
           }
 #pragma unroll
@@ -319,8 +324,7 @@ __global__ void __launch_bounds__(192, 1)
             if (v < nvec) {
               const __nv_bfloat162* ab = reinterpret_cast<const __nv_bfloat162*>(&a4[k]);
               const __nv_bfloat162* rb = reinterpret_cast<const __nv_bfloat162*>(&r4[k]);
-              uint4 o;
-              __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+              __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&a4[k]);  // a4[k] becomes the residual
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const float2 fa = __bfloat1622float2(ab[i]), fr = __bfloat1622float2(rb[i]);
@@ -328,7 +332,7 @@ __global__ void __launch_bounds__(192, 1)
                 const float2 q2 = __bfloat1622float2(ob[i]);  // the stored residual is what is normalised
                 ss += q2.x * q2.x + q2.y * q2.y;
               }
-              ro[v] = o;
+              ro[v] = a4[k];
             }
           }
         }
@@ -338,23 +342,23 @@ __global__ void __launch_bounds__(192, 1)
         named_bar_sync(1, 128);
         const float inv = rsqrtf((s_red[0] + s_red[1] + s_red[2] + s_red[3]) / (float)H + P.eps);
         named_bar_sync(1, 128);
-        const uint4* gv = reinterpret_cast<const uint4*>(P.gamma);
-        uint4* xo = reinterpret_cast<uint4*>(P.x_norm + roff);
         for (int v0 = 0; v0 < nvec; v0 += NV * 128) {
-          uint4 r4[NV], g4[NV];
+          if (!one_chunk) {
+            // rows longer than one chunk: the registers hold the last chunk only
 #pragma unroll
-          for (int k = 0; k < NV; ++k) {
-            const int v = v0 + k * 128 + et;
-            if (v < nvec) {
-              r4[k] = ro[v];   // written by this thread above
-              g4[k] = __ldg(gv + v);
+            for (int k = 0; k < NV; ++k) {
+              const int v = v0 + k * 128 + et;
+              if (v < nvec) {
+                a4[k] = ro[v];   // written by this thread above
+                g4[k] = __ldg(gv + v);
+              }
             }
           }
 #pragma unroll
           for (int k = 0; k < NV; ++k) {
             const int v = v0 + k * 128 + et;
             if (v < nvec) {
-              const __nv_bfloat162* rb = reinterpret_cast<const __nv_bfloat162*>(&r4[k]);
+              const __nv_bfloat162* rb = reinterpret_cast<const __nv_bfloat162*>(&a4[k]);
               const __nv_bfloat162* gb = reinterpret_cast<const __nv_bfloat162*>(&g4[k]);
               uint4 o;
               __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
