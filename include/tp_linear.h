@@ -209,6 +209,17 @@ int tp_capture_rows(int64_t T, int64_t H, const int32_t* row_req, const int32_t*
                     int64_t* n_out_dev, void* workspace, int64_t workspace_bytes,
                     tp_stream_t stream);
 
+/*
+ * Wall-clock limit of every on-chip wait of the kernels launched after this
+ * call (process-wide; default 2 s). Every wait between pipeline roles and
+ * between CTAs is bounded: when one runs out, the kernel writes TP_ERR_TIMEOUT
+ * to the status word, lets its copies in flight land, frees tensor memory and
+ * returns, leaving the CUDA context usable (the workspace must then be zeroed
+ * again). A short limit makes waits run out on purpose, which is how the
+ * failure path is tested without faulting the GPU. ns <= 0 is TP_ERR_ARG.
+ */
+int tp_set_wait_timeout(int64_t ns);
+
 /* Thread-local message describing the last non-zero return on this thread. */
 const char* tp_last_error(void);
 

@@ -27,7 +27,7 @@ ABI_SYMBOLS = (
     "tp_packed_weight_bytes", "tp_linear_create", "tp_linear_destroy", "tp_workspace_size",
     "tp_mlp_forward", "tp_add_rms_norm", "tp_gate_up_forward", "tp_down_forward",
     "tp_attn_proj_forward", "tp_capture_workspace_size", "tp_capture_rows", "tp_last_error",
-    "tp_describe_plan", "tp_mlp_forward_no_alloc",
+    "tp_describe_plan", "tp_mlp_forward_no_alloc", "tp_set_wait_timeout",
 )
 
 
@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
                             I32, P, P, I64, P, P, I64, P],
         "tp_describe_plan": [P, I64, ctypes.POINTER(GemmPlan), I32],
         "tp_mlp_forward_no_alloc": [P, I64, P, P, P, P, P, P, P],
+        "tp_set_wait_timeout": [I64],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -122,6 +123,11 @@ def packed_weight_bytes(cfg: Config):
     a, b = ctypes.c_int64(), ctypes.c_int64()
     _check(lib().tp_packed_weight_bytes(ctypes.byref(cfg), ctypes.byref(a), ctypes.byref(b)))
     return a.value, b.value
+
+
+def set_wait_timeout(ns: int) -> None:
+    """Wall-clock limit (ns) of every on-chip wait in kernels launched afterwards (default 2 s)."""
+    _check(lib().tp_set_wait_timeout(int(ns)))
 
 
 def capture_workspace_size(T: int, n_sel: int) -> int:

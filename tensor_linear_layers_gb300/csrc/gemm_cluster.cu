@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(192, 1)
       if (!ok) {
         for (int s = 0; s < STAGES; ++s)
           if (issued_mask & (1u << s))
-            mbar_wait_bounded(full_bar(s), (last_phase_bits >> s) & 1u, nullptr, 20000000ull);
+            mbar_wait_bounded(full_bar(s), (last_phase_bits >> s) & 1u, nullptr, kTeardownNs);
       }
     }
     __syncwarp();
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       tc_commit(done_bar);
-      mbar_wait_bounded(done_bar, 0, nullptr, p.timeout_ns);
+      mbar_wait_bounded(done_bar, 0, nullptr, kTeardownNs);
     }
     __syncwarp();
   } else {

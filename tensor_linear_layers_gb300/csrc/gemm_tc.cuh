@@ -48,6 +48,10 @@ namespace tpl {
 enum GemmKind : int { KIND_GATE_UP = 0, KIND_COL = 1, KIND_ROW = 2 };
 
 constexpr int kStatusTimeout = -6;     // mirrors TP_ERR_TIMEOUT
+// Waits on the way out (copies in flight landing, the last MMAs completing
+// before tensor memory is freed) have their own limit, independent of the
+// configurable one, so a short configured limit never cuts them short.
+constexpr unsigned long long kTeardownNs = 20000000ull;
 constexpr int kWBlockRows = 256;       // rows of one packed weight block
 constexpr int kWBlockBytes = kWBlockRows * 128;  // 256 rows x 64 bf16
 
@@ -493,7 +497,7 @@ __global__ void __launch_bounds__(192, 1)
         // drain: let copies already in flight land before the CTA exits
         for (int s = 0; s < STAGES; ++s)
           if (issued_mask & (1u << s))
-            mbar_wait_bounded(full_bar(s), (last_phase_bits >> s) & 1u, nullptr, 20000000ull);
+            mbar_wait_bounded(full_bar(s), (last_phase_bits >> s) & 1u, nullptr, kTeardownNs);
       }
     }
     __syncwarp();
@@ -558,7 +562,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       // all issued MMAs complete before tensor memory is released
       tc_commit(done_bar);
-      mbar_wait_bounded(done_bar, 0, nullptr, p.timeout_ns);
+      mbar_wait_bounded(done_bar, 0, nullptr, kTeardownNs);
     }
     __syncwarp();
   } else {

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <cstdarg>
 #include <cstdio>
@@ -130,7 +131,8 @@ constexpr int64_t kDecodeBarsOff = 192;
 constexpr int64_t kTileCountersOff = 256;
 constexpr int64_t kFusedMaxT = 128;
 constexpr int64_t kCaptureOff = 256;
-constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per on-chip wait
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per on-chip wait
+std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
 
 }  // namespace
 
@@ -314,7 +316,7 @@ GemmParams base_params(const Plan& pl, int64_t T, void* ws, int64_t part_off, in
   p.partials = reinterpret_cast<float*>(w + part_off);
   p.gbar = reinterpret_cast<unsigned*>(w + gbar_off);
   p.status = reinterpret_cast<int*>(w);
-  p.timeout_ns = kTimeoutNs;
+  p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   return p;
 }
 
@@ -799,6 +801,12 @@ int tp_attn_proj_forward(tp_linear_t* h, int64_t T, const void* x, void* qkv_out
   }
   if (do_qkv && (rc = run_col(h, T, x, qkv_out, workspace, L, st))) return rc;
   if (do_o && (rc = run_row(h, T, attn_in, nullptr, o_out, nullptr, workspace, L, st))) return rc;
+  return ok();
+}
+
+int tp_set_wait_timeout(int64_t ns) {
+  if (ns <= 0) return fail(TP_ERR_ARG, "wait limit must be positive (got %lld ns)", (long long)ns);
+  g_timeout_ns.store((unsigned long long)ns, std::memory_order_relaxed);
   return ok();
 }
 

@@ -140,3 +140,9 @@ def test_capture_argument_checks(L):
     assert rc == tl.TP_ERR_ARG
     rc = L.tp_capture_rows(16, 512, p, p, p, 4, 1, arr, types, 0, p, p, 8, p, p, 16, None)
     assert rc == tl.TP_ERR_ARG and b"too small" in L.tp_last_error()
+
+
+def test_wait_limit_must_be_positive(L):
+    assert L.tp_set_wait_timeout(0) == tl.TP_ERR_ARG
+    assert L.tp_set_wait_timeout(-5) == tl.TP_ERR_ARG
+    assert L.tp_set_wait_timeout(2_000_000_000) == tl.TP_OK
