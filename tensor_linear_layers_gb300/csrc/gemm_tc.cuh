@@ -133,9 +133,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 
 // Epilogue of N (multiple of 8) accumulator columns c0 .. c0+N-1 of segment
 // `seg` in accumulator row `row`; g = values (gate for GATE_UP), u = up values.
+// Writes N accumulator values of one row. For the swapped row-parallel kind,
+// `rres` may hold the N residual values already loaded (else they are loaded
+// here, all before the first store, so that they travel together).
 template <bool SWAP, int KIND, int BN, int N>
 __device__ __forceinline__ void emit_vals(const GemmParams& p, int tm, int tn, int seg, int row, int c0,
-                                          const float* g, const float* u) {
+                                          const float* g, const float* u, const __nv_bfloat16* rres = nullptr) {
     if (!SWAP) {
       const int m = tm * 128 + row;
       if (m >= p.T) return;
@@ -220,14 +223,36 @@ __device__ __forceinline__ void emit_vals(const GemmParams& p, int tm, int tn, i
       } else {
         const int f = tm * 256 + seg * 128 + row;
         if (f >= p.n_out) return;
+        // residuals are loaded 8 tokens at a time, all before that group's stores
+        static_assert(N % 8 == 0, "token groups");
+        const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
 #pragma unroll
-        for (int j = 0; j < N; ++j) {
-          const int tok = tn * BN + c0 + j;
-          if (tok < p.T) {
-            const size_t off = (size_t)tok * p.n_out + f;
-            p.out[off] = __float2bfloat16_rn(g[j]);
-            if (p.out2 != nullptr)
-              p.out2[off] = __float2bfloat16_rn(g[j] + __bfloat162float(p.resid[off]));
+        for (int j0 = 0; j0 < N; j0 += 8) {
+          __nv_bfloat162 rv[4];  // packed pairs keep registers low
+          if (p.out2 != nullptr) {
+#pragma unroll
+            for (int j = j0; j < j0 + 8; j += 2) {
+              const int tok = tn * BN + c0 + j;
+              if (rres != nullptr) {
+                rv[(j - j0) / 2] = __halves2bfloat162(rres[j], rres[j + 1]);
+              } else {
+                const __nv_bfloat16 a = tok < p.T ? p.resid[(size_t)tok * p.n_out + f] : z;
+                const __nv_bfloat16 b = tok + 1 < p.T ? p.resid[(size_t)(tok + 1) * p.n_out + f] : z;
+                rv[(j - j0) / 2] = __halves2bfloat162(a, b);
+              }
+            }
+          }
+#pragma unroll
+          for (int j = j0; j < j0 + 8; ++j) {
+            const int tok = tn * BN + c0 + j;
+            if (tok < p.T) {
+              const size_t off = (size_t)tok * p.n_out + f;
+              p.out[off] = __float2bfloat16_rn(g[j]);
+              if (p.out2 != nullptr) {
+                const float r = ((j - j0) & 1) ? __high2float(rv[(j - j0) / 2]) : __low2float(rv[(j - j0) / 2]);
+                p.out2[off] = __float2bfloat16_rn(g[j] + r);
+              }
+            }
           }
         }
       }
@@ -246,12 +271,25 @@ __device__ __forceinline__ void reduce_tile_items(const GemmParams& p, int tile,
   constexpr int G = 8;
   constexpr int SC = (KIND == KIND_GATE_UP) ? 4 : 8;
   constexpr int ACC = S::kAccCols;
+  constexpr bool kRes = SWAP && KIND == KIND_ROW;
   const float* tile_part = p.partials + (size_t)tile * p.splits * ACC * 128;
   const int tm = tile / p.n_tiles, tn = tile - tm * p.n_tiles;
   for (int it = it_lo + tid; it < it_hi; it += nthreads) {
     const int row = it & 127;
     const int c0 = (it >> 7) * G;
     const float* base_part = tile_part + row;
+    // swapped row-parallel: the residual of the item's tokens is loaded along
+    // with the partials instead of after them
+    __nv_bfloat16 rres[G];
+    if (kRes && p.out2 != nullptr) {
+      const int seg = c0 / BN;
+      const int f = tm * 256 + seg * 128 + row;
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const int tok = tn * BN + c0 - seg * BN + j;
+        rres[j] = (f < p.n_out && tok < p.T) ? p.resid[(size_t)tok * p.n_out + f] : __float2bfloat16_rn(0.f);
+      }
+    }
     float g[G], u[G];
 #pragma unroll
     for (int j = 0; j < G; ++j) g[j] = u[j] = 0.f;
@@ -280,7 +318,8 @@ __device__ __forceinline__ void reduce_tile_items(const GemmParams& p, int tile,
       }
     }
     const int seg = (SWAP && KIND != KIND_GATE_UP) ? c0 / BN : 0;
-    emit_vals<SWAP, KIND, BN, G>(p, tm, tn, seg, row, c0 - seg * BN, g, u);
+    emit_vals<SWAP, KIND, BN, G>(p, tm, tn, seg, row, c0 - seg * BN, g, u,
+                                 (kRes && p.out2 != nullptr) ? rres : nullptr);
   }
 }
 // Items of one tile: 8-column groups of the columns that own an output, x 128 rows.

@@ -89,6 +89,13 @@ __device__ __forceinline__ void bulk_load_multicast(uint32_t dst, const void* sr
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "h"(cta_mask), "l"(policy)
       : "memory");
 }
+// Bulk prefetch of global memory into L2 (no destination, no completion);
+// bytes % 16 == 0, address 16-byte aligned.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes), "l"(policy)
+               : "memory");
+}
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
