@@ -54,6 +54,8 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 4);
   volatile int* s_ok = reinterpret_cast<volatile int*>(misc + 8);
   float* s_red = reinterpret_cast<float*>(misc + 16);  // 4 floats: norm reduction
+  // h tile of a gate_up unit, [token][128 columns] bf16, written out with 16-byte stores
+  __nv_bfloat16* s_h = reinterpret_cast<__nv_bfloat16*>(base_ptr + STAGES * S::kStageBytes + S::kBarBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -400,12 +402,28 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t acc = lane_addr + buf * ACC;
         if (p.splits == 1) {
           if (ph == 0) {
+            // silu(g) * u goes to shared memory as [token][column]; the tile is then
+            // written row by row with 16-byte stores (one warp store covers 512 bytes,
+            // where a column per thread would take a store per token)
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += CH) {
               if (CH == 32) { tmem_ld32(acc + c0, g); tmem_ld32(acc + BN + c0, uu); }
               else { tmem_ld16(acc + c0, g); tmem_ld16(acc + BN + c0, uu); }
               tc_wait_ld();
-              emit_vals<true, KIND_GATE_UP, BN, CH>(p, tm, 0, 0, row, c0, g, uu);
+#pragma unroll
+              for (int j = 0; j < CH; ++j) s_h[(c0 + j) * 128 + row] = __float2bfloat16_rn(silu_f(g[j]) * uu[j]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(buf));
+            named_bar_sync(1, 128);
+            const int r = tm / p.nb, i0 = (tm - r * p.nb) * 128;
+            __nv_bfloat16* dst = p.out + (size_t)r * p.T * p.Is + i0;
+            for (int idx = et; idx < p.T * 16; idx += 128) {
+              const int tok = idx >> 4, ch = idx & 15;
+              if (i0 + ch * 8 < p.Is)
+                *reinterpret_cast<uint4*>(dst + (size_t)tok * p.Is + ch * 8) =
+                    *reinterpret_cast<const uint4*>(s_h + tok * 128 + ch * 8);
             }
           } else {
 #pragma unroll 1
@@ -417,10 +435,10 @@ __global__ void __launch_bounds__(192, 1)
                 emit_vals<true, KIND_ROW, BN, CH>(p, tm, 0, seg, row, c0, g, uu);
               }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(buf));
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar(buf));
           if (ph == 0) {
             // this tile's h columns are complete
             fence_proxy_async_global();
@@ -556,20 +574,22 @@ cudaError_t launch_mlp_decode_bn(const CUtensorMap& mx, const CUtensorMap& mh, c
                                  int grid, cudaStream_t st) {
   using S = GemmShape<true, KIND_GATE_UP, BN>;
   auto kernel = mlp_decode_kernel<BN>;
+  constexpr int kSmem = S::kSmemBytes + BN * 128 * 2;  // ring, barriers, h tile
+  static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
   static std::atomic<uint64_t> attr_done{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(attr_done.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit, std::memory_order_acq_rel);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(192);
-  cfg.dynamicSmemBytes = S::kSmemBytes;
+  cfg.dynamicSmemBytes = kSmem;
   cfg.stream = st;
   // One CTA per SM (shared memory) and grid == SM count: every CTA is resident
   // while nothing else occupies the GPU. Programmatic serialisation lets the next
