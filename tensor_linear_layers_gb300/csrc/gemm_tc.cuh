@@ -272,7 +272,7 @@ __device__ __forceinline__ void reduce_tile_items(const GemmParams& p, int tile,
                                                   int tid, int nthreads) {
   using S = GemmShape<SWAP, KIND, BN>;
   constexpr int G = 8;
-  constexpr int SC = (KIND == KIND_GATE_UP) ? 4 : 8;
+  constexpr int SC = (KIND == KIND_GATE_UP) ? 4 : 10;  // up to 10 splits in one round trip
   constexpr int ACC = S::kAccCols;
   constexpr bool kRes = SWAP && KIND == KIND_ROW;
   const float* tile_part = p.partials + (size_t)tile * p.splits * ACC * 128;
