@@ -2,7 +2,7 @@
 // whole step for T <= 128 tokens.
 //
 //   norm     residual add + RMSNorm of the T rows by the epilogue warps (rows
-//            spread over CTAs); every CTA arrives on bars[0]
+//            spread over CTAs); the CTAs that own rows arrive on bars[0]
 //   gate_up  column-parallel units of 256 weight rows (128 gate + 128 up of
 //            one shard) x a K range; with split-K every split writes its fp32
 //            partial. After one grid-wide wait the CTAs add the partials tile
@@ -38,6 +38,8 @@ __global__ void __launch_bounds__(192, 1)
   constexpr int CH = S::kCh;
   constexpr int kItems1 = tile_items<true, KIND_GATE_UP, BN>();  // h of a gate_up tile is complete at this count
   const unsigned grid = gridDim.x;
+  // CTAs that own norm rows (row r goes to CTA r % grid); only they arrive on bars[0]
+  const unsigned norm_ctas = (unsigned)min((int)grid, P.g1.T);
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       auto dep_ready = [&](int dep) -> bool {
         if (dep < 0) {
-          if (!x_ready) x_ready = *reinterpret_cast<const volatile unsigned*>(P.bars) >= grid;
+          if (!x_ready) x_ready = *reinterpret_cast<const volatile unsigned*>(P.bars) >= norm_ctas;
           return x_ready;
         }
         return *reinterpret_cast<const volatile unsigned*>(P.hready + dep) >= (unsigned)kItems1;
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(192, 1)
           if (q_n <= keep) return true;
           const int dep = q_dep[q_head];
           const unsigned* c = dep < 0 ? P.bars : P.hready + dep;
-          if (!bar_wait(c, dep < 0 ? grid : (unsigned)kItems1, timeout, s_abort)) return false;
+          if (!bar_wait(c, dep < 0 ? norm_ctas : (unsigned)kItems1, timeout, s_abort)) return false;
           if (dep < 0) x_ready = true;
           issue_front();
         }
@@ -378,7 +380,7 @@ __global__ void __launch_bounds__(192, 1)
       fence_proxy_async_global();
       __threadfence();
       named_bar_sync(1, 128);
-      if (et == 0) bar_arrive(P.bars + 0);
+      if (et == 0 && blockIdx.x < norm_ctas) bar_arrive(P.bars + 0);
     }
 
     float g[CH], uu[CH];
