@@ -20,6 +20,11 @@ Sources, cited by page title and section throughout:
 * [MLX] mlxcel manual "Tensor Parallelism": Weight Sharding Strategies,
         GQA-Aware Attention Sharding.
 
+``attention.py`` holds the attention core between the QKV projection and
+o_proj (causal, GQA, sequences packed by offsets); the pages describe it
+only as attention over each rank's own heads, so it is the textbook
+scaled dot-product attention in their head layout.
+
 Every function computes in float64 from bf16 inputs converted exactly. Where
 the block has a plain definition (the unsharded Y = XW, SiLU, RMSNorm, row
 selection) the oracle is that definition; the sharded variants
@@ -37,3 +42,4 @@ from .tp_block import (  # noqa: F401
     qkv_parallel, o_proj_parallel, divide,
 )
 from .capture import capture_rows, pack_key  # noqa: F401
+from .attention import attention_core, attention_rows, kv_head_of  # noqa: F401

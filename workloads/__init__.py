@@ -43,7 +43,7 @@ TENSOR_TYPES = {"residual_stream": 0, "attn_out": 1, "mlp_out": 2, "final_norm":
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str                 # "mlp" or "attn"
+    kind: str                 # "mlp", "attn" (projections) or "attn_core" (attention core)
     T: int                    # tokens in the step
     H: int                    # hidden size
     t: int                    # logical tensor-parallel shards
@@ -60,13 +60,23 @@ class Workload:
     seed: int = 0
     desc: str = field(default="", compare=False)
 
+    def seq_lens(self) -> np.ndarray:
+        """Lengths of the packed sequences (attention core): one sequence, or the ragged batch."""
+        return ragged_batch(self)["lens"] if self.requests else np.array([self.T], dtype=np.int64)
+
     def flops(self) -> float:
+        if self.kind == "attn_core":
+            # q k^T and p v over the causal (query, key) pairs of every sequence and q head
+            L = self.seq_lens().astype(np.float64)
+            return 4.0 * self.hd * self.nq * float(np.sum(L * (L + 1) / 2))
         if self.kind == "mlp":
             return 2.0 * self.T * self.H * (2 * self.I) + 2.0 * self.T * self.I * self.H
         qkv_n = (self.nq + 2 * self.nkv) * self.hd
         return 2.0 * self.T * self.H * qkv_n + 2.0 * self.T * self.nq * self.hd * self.H
 
     def weight_bytes(self) -> int:
+        if self.kind == "attn_core":
+            return 0
         if self.kind == "mlp":
             return 2 * 3 * self.H * self.I
         return 2 * (self.H * (self.nq + 2 * self.nkv) * self.hd + self.nq * self.hd * self.H)
@@ -74,6 +84,8 @@ class Workload:
     def activation_bytes(self) -> int:
         """Bytes of activations read or written once by the whole block."""
         T, H = self.T, self.H
+        if self.kind == "attn_core":       # qkv in, attention output out
+            return 2 * T * (self.nq + 2 * self.nkv) * self.hd + 2 * T * self.nq * self.hd
         if self.kind == "mlp":
             b = 2 * T * H * 2                # x (or a) in, mlp_out
             if self.norm:
@@ -93,6 +105,13 @@ WORKLOADS = {
     "llama3_8b_attn_proj_prefill": Workload(
         "llama3_8b_attn_proj_prefill", "attn", T=4096, H=4096, nq=32, nkv=8, hd=128, t=4,
         w_std=0.02, desc="Llama-3-8B-shaped QKV + o_proj prefill, 4096 tokens, t=4"),
+    "llama3_8b_attn_core_prefill": Workload(
+        "llama3_8b_attn_core_prefill", "attn_core", T=4096, H=4096, nq=32, nkv=8, hd=128, t=4,
+        w_std=0.0, desc="Llama-3-8B-shaped causal GQA attention core, one 4096-token sequence, t=4"),
+    "qwen25_7b_ragged_attn_core": Workload(
+        "qwen25_7b_ragged_attn_core", "attn_core", T=2048, H=3584, nq=28, nkv=4, hd=128, t=4,
+        w_std=0.0, requests=64, mean_len=32,
+        desc="Ragged continuous batch, Qwen2.5-7B-shaped attention core, 2048 tokens / 64 requests, t=4"),
     "llama3_70b_mlp_prefill": Workload(
         "llama3_70b_mlp_prefill", "mlp", T=8192, H=8192, I=28672, t=8, w_std=0.015,
         desc="Llama-3-70B-shaped MLP prefill, 8192 tokens, t=8"),
@@ -171,6 +190,20 @@ def attn_inputs(w: Workload, T: int | None = None) -> dict:
     d["w_v"] = draw((w.nkv * hd, H), s, 4, b=w.w_std)
     d["w_o"] = draw((H, w.nq * hd), s, 5, b=w.w_std)
     return d
+
+
+def attn_core_inputs(w: Workload, lens=None) -> dict:
+    """Inputs of the attention core: qkv [t][T][w_s] ~ N(0, 1) in the QKV projection's
+    layout (shard r: its q heads, k heads, v heads) and the sequence offsets."""
+    lens = w.seq_lens() if lens is None else np.asarray(lens, dtype=np.int64)
+    T = int(lens.sum())
+    if w.t >= w.nkv:
+        kv_per = 1
+    else:
+        kv_per = w.nkv // w.t
+    ws = (w.nq // w.t + 2 * kv_per) * w.hd
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    return {"qkv": draw((w.t, T, ws), w.seed, 6), "cu_seqlens": cu, "T": T}
 
 
 def ragged_batch(w: Workload) -> dict:
