@@ -182,6 +182,30 @@ int tp_attn_proj_forward(tp_linear_t* h, int64_t T, const void* x, void* qkv_out
                          void* workspace, int64_t workspace_bytes, tp_stream_t stream);
 
 /*
+ * Attention core between the two projections ("vLLM Code Reading (Section 5)"
+ * §13: each rank runs attention on the heads it holds; "vLLM 源码完全拆解
+ * （十一）" QkvParallelLinear: which kv head a shard holds under GQA):
+ *   for every shard r and local q head i (global head h = r*nq/t + i):
+ *     attn_out[r][:, i*hd:(i+1)*hd] = softmax(q_h k_g^T / sqrt(hd) + causal) v_g,
+ *     g = the kv head of h's group (h / (nq/nkv)), held by shard r
+ *   sequence s is tokens [cu_seqlens[s], cu_seqlens[s+1]); a query sees the keys of
+ *   its own sequence at or before it. q and k are used as given (no positional
+ *   rotation is applied).
+ * qkv: [t][T][w_s] bf16, tp_attn_proj_forward's qkv_out. attn_out: [t][T][nq*hd/t]
+ * bf16, the layout of tp_attn_proj_forward's attn_in. cu_seqlens: DEVICE int32
+ * [n_seqs + 1], 0 = cu_seqlens[0] <= ... <= cu_seqlens[n_seqs] = T, 4-byte aligned.
+ * n_seqs in [1, T]; max_seqlen (host) >= every sequence length, <= T. head_dim 128
+ * (else TP_ERR_UNSUPPORTED). Scores and softmax in fp32, P rounded to bf16 for the
+ * P V product, output rounded to bf16. Offsets that do not rise from 0 to T, or a
+ * length above max_seqlen rounded up to 128, write TP_ERR_SHAPE to the workspace
+ * status word and leave attn_out unwritten. The workspace (tp_workspace_size of the
+ * handle covers up to max_tokens sequences) holds the per-call work table.
+ */
+int tp_attention_forward(tp_linear_t* h, int64_t T, const void* qkv, const int32_t* cu_seqlens,
+                         int32_t n_seqs, int32_t max_seqlen, void* attn_out, void* workspace,
+                         int64_t workspace_bytes, tp_stream_t stream);
+
+/*
  * Activation capture ("Tensor & pipeline parallelism": What the adapter hooks,
  * Duplicate records across TP ranks, Merging records): records every row i of
  * each tensor whose key (row_req[i] << 32) | (uint32)row_pos[i] is among the

@@ -27,7 +27,7 @@ ABI_SYMBOLS = (
     "tp_packed_weight_bytes", "tp_linear_create", "tp_linear_destroy", "tp_workspace_size",
     "tp_mlp_forward", "tp_add_rms_norm", "tp_gate_up_forward", "tp_down_forward",
     "tp_attn_proj_forward", "tp_capture_workspace_size", "tp_capture_rows", "tp_last_error",
-    "tp_describe_plan", "tp_mlp_forward_no_alloc", "tp_set_wait_timeout",
+    "tp_describe_plan", "tp_mlp_forward_no_alloc", "tp_set_wait_timeout", "tp_attention_forward",
 )
 
 
@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
         "tp_describe_plan": [P, I64, ctypes.POINTER(GemmPlan), I32],
         "tp_mlp_forward_no_alloc": [P, I64, P, P, P, P, P, P, P],
         "tp_set_wait_timeout": [I64],
+        "tp_attention_forward": [P, I64, P, P, I32, I32, P, P, I64, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -270,6 +271,24 @@ class TPLinear:
                                           _ptr(attn_in), _ptr(o_out if attn_in is not None else None),
                                           _ptr(ws), ws.numel(), _stream(stream)))
         return qkv_out, o_out
+
+    # ------------------------------------------------------------------ attention core
+    def attention_forward(self, qkv: torch.Tensor, cu_seqlens: torch.Tensor, max_seqlen: int,
+                          out=None, ws=None, stream=None) -> torch.Tensor:
+        """Causal GQA attention of every shard's local heads: qkv [t][T][w_s] (the
+        projection's output) -> attn [t][T][nq*hd/t] (o_proj's input). cu_seqlens:
+        int32 device tensor [n_seqs + 1] of sequence offsets."""
+        c = self.cfg
+        T = qkv.shape[1]
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+            raise TypeError("cu_seqlens must be an int32 CUDA tensor")
+        if out is None:
+            out = torch.empty(c.t, T, c.n_q_heads // c.t * c.head_dim, dtype=torch.bfloat16, device=qkv.device)
+        ws = self.workspace(T) if ws is None else ws
+        _check(lib().tp_attention_forward(self.handle, T, _ptr(_bf16(qkv, "qkv")), _ptr(cu_seqlens),
+                                          cu_seqlens.numel() - 1, int(max_seqlen), _ptr(out), _ptr(ws),
+                                          ws.numel(), _stream(stream)))
+        return out
 
 
 def add_rms_norm(a: torch.Tensor, residual: torch.Tensor, gamma: torch.Tensor, eps: float,

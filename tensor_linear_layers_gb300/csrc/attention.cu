@@ -1,0 +1,418 @@
+// Attention core between the column-parallel QKV projection and the
+// row-parallel o_proj: causal scaled-dot-product attention of every shard's
+// local q heads, each reading the kv head of its group, over sequences
+// packed along the token axis ("vLLM Code Reading (Section 5)" §13: each
+// rank runs attention on the heads it holds; "vLLM 源码完全拆解（十一）",
+// QkvParallelLinear: which kv heads a shard holds under GQA).
+//
+// Input is the projection's own output, qkv [t][T][w_s] (shard r: its q
+// heads | k heads | v heads, hd = 128 columns each); output is o_proj's
+// input, attn [t][T][q_per * hd]. Flash-style, one CTA per SM, persistent:
+//
+//   unit     (q head, sequence, 128-query tile); units run heaviest first
+//            (most key tiles), heads innermost so the q heads of one kv head
+//            run side by side and share its K/V tiles in L2
+//   warp 0   TMA: the Q tile (two 64-column boxes, 128-byte swizzle), then
+//            K and V tiles of 128 keys into a 2-stage ring
+//   warp 1   tcgen05.mma: S = Q K^T into one of two tensor-memory buffers,
+//            one key tile ahead of O += P V (P from shared memory, V read
+//            MN-major straight from its [key][hd] tile)
+//   warps 2-5 softmax, one query row per thread: the row of S from tensor
+//            memory, causal / sequence-end mask, running max and sum in the
+//            exp2 domain, P = 2^(s*c - m) as bf16 into shared memory. O is
+//            rescaled in tensor memory only when the row max grows by more
+//            than 2^8 (until then the stale max keeps every p <= 256); at the
+//            end O / l goes to global memory as bf16
+//
+// Every wait is bounded (status word TP_ERR_TIMEOUT on timeout).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "gemm_tc.cuh"
+#include "internal.h"
+
+namespace tpl {
+
+
+namespace {
+constexpr int kTileBytes = 128 * 128 * 2;    // 128 rows x 128 bf16: two 64-column boxes
+constexpr int kQOff = 0;
+constexpr int kKOff = kTileBytes;            // 2 stages
+constexpr int kVOff = 3 * kTileBytes;        // 2 stages
+constexpr int kPOff = 5 * kTileBytes;        // 2 buffers
+constexpr int kBarOff = 7 * kTileBytes;
+constexpr int kAttnSmem = 1024 + kBarOff + 256;
+constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128);
+constexpr uint32_t kIdescO = idesc_bf16_f32(128, 128) | kIdescBMnMajor;
+constexpr int kTmemCols = 512;               // S0 [0,128), S1 [128,256), O [256,384)
+constexpr float kRescaleLog2 = 8.0f;         // rescale O when the row max grows by more than this
+enum {
+  Q_FULL = 0, Q_EMPTY, K_FULL, K_FULL1, K_EMPTY, K_EMPTY1, V_FULL, V_FULL1, V_EMPTY, V_EMPTY1,
+  S_FULL, S_FULL1, S_EMPTY, S_EMPTY1, P_FULL, P_FULL1, P_EMPTY, P_EMPTY1, O_DONE, O_EMPTY, DONE, NBARS
+};
+static_assert(8 * NBARS + 16 <= 256, "barrier area");
+
+struct Unit {
+  int r, i, g, start, len, qt;
+};
+__device__ __forceinline__ Unit decode_unit(const AttnParams& p, int u) {
+  const int4 pr = p.pairs[u / p.heads];
+  const int hh = u - (u / p.heads) * p.heads;
+  Unit x;
+  x.r = hh / p.q_per;
+  x.i = hh - x.r * p.q_per;
+  const int first = p.rep > 1 ? x.r / p.rep : x.r * p.kv_per;  // first kv head the shard holds
+  x.g = (x.r * p.q_per + x.i) / p.group - first;
+  x.start = pr.x;
+  x.len = pr.y;
+  x.qt = pr.z;
+  return x;
+}
+}  // namespace
+
+// Work table: for every sequence s and q tile q < ceil(len_s / 128) one entry,
+// ordered by q descending (the number of key tiles), sequences ascending.
+// Checks the offsets (0 first, T last, none falling, no length above
+// max_tiles * 128); on a bad table it writes TP_ERR_SHAPE and no entries.
+__global__ void attn_prep_kernel(const int* cu, int n_seqs, int T, int max_tiles, int4* pairs, int* n_pairs,
+                                 int* status) {
+  extern __shared__ int off[];  // [max_tiles]
+  __shared__ int s_bad;
+  const int tid = threadIdx.x;
+  if (tid == 0) s_bad = (cu[0] != 0 || cu[n_seqs] != T) ? 1 : 0;
+  __syncthreads();
+  for (int s = tid; s < n_seqs; s += blockDim.x) {
+    const int len = cu[s + 1] - cu[s];
+    if (len < 0 || len > max_tiles * 128) atomicExch(&s_bad, 1);
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (tid == 0) {
+      *n_pairs = 0;
+      atomicExch(status, -2);  // TP_ERR_SHAPE
+    }
+    return;
+  }
+  for (int q = tid; q < max_tiles; q += blockDim.x) {
+    int c = 0;
+    for (int s = 0; s < n_seqs; ++s) c += (cu[s + 1] - cu[s]) > q * 128 ? 1 : 0;
+    off[q] = c;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int q = max_tiles - 1; q >= 0; --q) {
+      const int c = off[q];
+      off[q] = acc;
+      acc += c;
+    }
+    *n_pairs = acc;
+  }
+  __syncthreads();
+  for (int q = tid; q < max_tiles; q += blockDim.x) {
+    int pos = off[q];
+    for (int s = 0; s < n_seqs; ++s) {
+      const int len = cu[s + 1] - cu[s];
+      if (len > q * 128) pairs[pos++] = make_int4(cu[s], len, q, 0);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(192, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_addr);
+  const uint32_t bar0 = base + kBarOff;
+  auto bar = [&](int b) { return bar0 + 8u * b; };
+  uint8_t* misc = base_ptr + kBarOff + 8 * NBARS;
+  volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(misc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const unsigned grid = gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < NBARS; ++b) {
+      const bool four = (b == S_EMPTY || b == S_EMPTY1 || b == P_FULL || b == P_FULL1 || b == O_EMPTY);
+      mbar_init(bar(b), four ? 4 : 1);  // arrivals from the four softmax warps
+    }
+    *s_abort = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&map_qkv);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(s_tmem)), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int n_units = *p.n_pairs * p.heads;
+  const unsigned long long timeout = p.timeout_ns;
+  auto set_abort = [&]() {
+    if (!*s_abort) {
+      atomicExch(p.status, kStatusTimeout);
+      *s_abort = 1;
+    }
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_normal();
+      uint32_t full_mask = 0, full_phase = 0;  // bit b: barrier b has a copy in flight, its phase
+      auto issued = [&](int b, uint32_t ph) {
+        full_mask |= 1u << b;
+        full_phase = (full_phase & ~(1u << b)) | (ph << b);
+      };
+      auto load_tile = [&](uint32_t dst, int b, int col, int row, int r) {
+        mbar_arrive_expect_tx(bar(b), kTileBytes);
+        tma_load_4d(dst, &map_qkv, bar(b), col, row, r, 0, pol);
+        tma_load_4d(dst + kTileBytes / 2, &map_qkv, bar(b), col + 64, row, r, 0, pol);
+      };
+      bool ok = true;
+      int kv = 0;
+      for (int u = blockIdx.x, nu = 0; u < n_units && ok; u += grid, ++nu) {
+        const Unit x = decode_unit(p, u);
+        if (!mbar_wait_bounded(bar(Q_EMPTY), (nu & 1) ^ 1, s_abort, timeout)) {
+          ok = false;
+          break;
+        }
+        load_tile(base + kQOff, Q_FULL, x.i * 128, x.start + x.qt * 128, x.r);
+        issued(Q_FULL, nu & 1);
+        const int kcol = (p.q_per + x.g) * 128, vcol = (p.q_per + p.kv_per + x.g) * 128;
+        for (int kt = 0; kt <= x.qt; ++kt, ++kv) {
+          const int st = kv & 1;
+          const uint32_t ph = (kv >> 1) & 1;
+          if (!mbar_wait_bounded(bar(K_EMPTY + st), ph ^ 1, s_abort, timeout)) {
+            ok = false;
+            break;
+          }
+          load_tile(base + kKOff + st * kTileBytes, K_FULL + st, kcol, x.start + kt * 128, x.r);
+          issued(K_FULL + st, ph);
+          if (!mbar_wait_bounded(bar(V_EMPTY + st), ph ^ 1, s_abort, timeout)) {
+            ok = false;
+            break;
+          }
+          load_tile(base + kVOff + st * kTileBytes, V_FULL + st, vcol, x.start + kt * 128, x.r);
+          issued(V_FULL + st, ph);
+        }
+      }
+      if (!ok) {
+        set_abort();
+        // no copy into this CTA's shared memory may outlive it
+        for (int b = 0; b < NBARS; ++b)
+          if (full_mask & (1u << b)) mbar_wait_bounded(bar(b), (full_phase >> b) & 1u, nullptr, kTeardownNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      int kv = 0, sc = 0, pc = 0, vc = 0;
+      auto wait = [&](int b, uint32_t ph) -> bool {
+        if (mbar_wait_bounded(bar(b), ph, s_abort, timeout)) return true;
+        set_abort();
+        ok = false;
+        return false;
+      };
+      // O (+)= P V for the oldest key tile whose P is pending
+      auto issue_pv = [&](bool first, int nu) -> bool {
+        const int pb = pc & 1, vs = vc & 1;
+        if (!wait(P_FULL + pb, (pc >> 1) & 1) || !wait(V_FULL + vs, (vc >> 1) & 1)) return false;
+        if (first && !wait(O_EMPTY, (nu & 1) ^ 1)) return false;
+        tc_fence_after();
+        const uint32_t pa = base + kPOff + pb * kTileBytes, va = base + kVOff + vs * kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t ad = smem_desc_k128(pa + (ks >> 2) * (kTileBytes / 2) + (ks & 3) * 32);
+          const uint64_t bd = smem_desc_mn128(va + ks * 2048, kTileBytes / 2);  // 16 keys = two 8-row groups
+          tc_mma_bf16(tmem_base + 256, ad, bd, kIdescO, (first && ks == 0) ? 0u : 1u);
+        }
+        tc_commit(bar(V_EMPTY + vs));
+        tc_commit(bar(P_EMPTY + pb));
+        ++pc;
+        ++vc;
+        return true;
+      };
+      for (int u = blockIdx.x, nu = 0; u < n_units && ok; u += grid, ++nu) {
+        const Unit x = decode_unit(p, u);
+        if (!wait(Q_FULL, nu & 1)) break;
+        for (int kt = 0; kt <= x.qt && ok; ++kt, ++kv) {
+          const int st = kv & 1, b = sc & 1;
+          if (!wait(K_FULL + st, (kv >> 1) & 1) || !wait(S_EMPTY + b, ((sc >> 1) & 1) ^ 1)) break;
+          tc_fence_after();
+          const uint32_t qa = base + kQOff, ka = base + kKOff + st * kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t o = (ks >> 2) * (kTileBytes / 2) + (ks & 3) * 32;
+            tc_mma_bf16(tmem_base + b * 128, smem_desc_k128(qa + o), smem_desc_k128(ka + o), kIdescS,
+                        ks > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(K_EMPTY + st));
+          tc_commit(bar(S_FULL + b));
+          if (kt == x.qt) tc_commit(bar(Q_EMPTY));
+          ++sc;
+          if (kt > 0 && !issue_pv(kt == 1, nu)) break;
+        }
+        if (!ok || !issue_pv(x.qt == 0, nu)) break;
+        tc_commit(bar(O_DONE));
+      }
+      tc_commit(bar(DONE));
+      mbar_wait_bounded(bar(DONE), 0, nullptr, kTeardownNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;  // query row of the tile = tensor-memory lane
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16);
+    const float c = p.scale_log2;
+    int sc = 0, pc = 0;
+    bool ok = true;
+    auto wait_all = [&](int b, uint32_t ph) -> bool {
+      bool w = mbar_wait_bounded(bar(b), ph, s_abort, timeout);
+      w = __all_sync(0xffffffffu, w);
+      if (!w) {
+        if (lane == 0) set_abort();
+        ok = false;
+      }
+      return w;
+    };
+    float s[128];
+    for (int u = blockIdx.x, nu = 0; u < n_units && ok; u += grid, ++nu) {
+      const Unit x = decode_unit(p, u);
+      const int q_rel = x.qt * 128 + row;
+      float m = -INFINITY, l = 0.f;
+      for (int kt = 0; kt <= x.qt; ++kt) {
+        const int b = sc & 1;
+        if (!wait_all(S_FULL + b, (sc >> 1) & 1)) break;
+        tc_fence_after();
+        const uint32_t sa = lane_addr + b * 128;
+        tmem_ld32(sa, s);
+        tmem_ld32(sa + 32, s + 32);
+        tmem_ld32(sa + 64, s + 64);
+        tmem_ld32(sa + 96, s + 96);
+        tc_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(S_EMPTY + b));
+        ++sc;
+        if (kt == x.qt || (kt + 1) * 128 > x.len) {
+          // diagonal tile and the tile holding the sequence end
+#pragma unroll
+          for (int n = 0; n < 128; ++n) {
+            const int key = kt * 128 + n;
+            if (key > q_rel || key >= x.len) s[n] = -INFINITY;
+          }
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int n = 1; n < 128; ++n) mx = fmaxf(mx, s[n]);
+        mx *= c;
+        if (kt == 0) {
+          m = mx;  // the first P V overwrites O
+        } else if (mx > m + kRescaleLog2) {
+          const float f = fast_exp2(m - mx);
+          l *= f;
+          m = mx;
+          // O holds the products up to the previous key tile: let them land, then scale the row
+          const int pj = pc - 1;
+          if (!wait_all(P_EMPTY + (pj & 1), (pj >> 1) & 1)) break;
+          tc_fence_after();
+          float o[32];
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            tmem_ld32(lane_addr + 256 + c0, o);
+            tc_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] *= f;
+            tmem_st32(lane_addr + 256 + c0, o);
+          }
+          tc_wait_st();
+        }
+        const int pb = pc & 1;
+        if (!wait_all(P_EMPTY + pb, ((pc >> 1) & 1) ^ 1)) break;  // the P V two tiles back is done
+        uint8_t* prow = base_ptr + kPOff + pb * kTileBytes + row * 128;
+#pragma unroll
+        for (int ch = 0; ch < 16; ++ch) {
+          float e[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            e[j] = fast_exp2(fmaf(s[ch * 8 + j], c, -m));
+            l += e[j];
+          }
+          uint4 v;
+          v.x = pack_bf16x2(e[0], e[1]);
+          v.y = pack_bf16x2(e[2], e[3]);
+          v.z = pack_bf16x2(e[4], e[5]);
+          v.w = pack_bf16x2(e[6], e[7]);
+          *reinterpret_cast<uint4*>(prow + (ch >> 3) * (kTileBytes / 2) + (((ch & 7) ^ (row & 7)) << 4)) = v;
+        }
+        fence_proxy_async_shared();  // the tensor core reads P
+        tc_fence_before();           // and O as rescaled above
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(P_FULL + pb));
+        ++pc;
+      }
+      if (!ok || !wait_all(O_DONE, nu & 1)) break;
+      tc_fence_after();
+      const float inv = 1.0f / l;
+      __nv_bfloat16* dst = p.out + ((size_t)x.r * p.T + x.start + q_rel) * (size_t)(p.q_per * 128) + x.i * 128;
+      float o[32];
+#pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        tmem_ld32(lane_addr + 256 + c0, o);
+        tc_wait_ld();
+        if (q_rel < x.len) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(o[j] * inv, o[j + 1] * inv);
+            v.y = pack_bf16x2(o[j + 2] * inv, o[j + 3] * inv);
+            v.z = pack_bf16x2(o[j + 4] * inv, o[j + 5] * inv);
+            v.w = pack_bf16x2(o[j + 6] * inv, o[j + 7] * inv);
+            *reinterpret_cast<uint4*>(dst + c0 + j) = v;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(O_EMPTY));
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+cudaError_t launch_attention(const CUtensorMap& map_qkv, const AttnParams& p, const int* cu, int n_seqs,
+                             int max_tiles, int4* pairs, int* n_pairs, int grid, cudaStream_t st) {
+  attn_prep_kernel<<<1, 1024, max_tiles * (int)sizeof(int), st>>>(cu, n_seqs, p.T, max_tiles, pairs, n_pairs,
+                                                                    p.status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  static std::atomic<uint64_t> attr_done{0};
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  attn_fwd_kernel<<<grid, 192, kAttnSmem, st>>>(map_qkv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace tpl

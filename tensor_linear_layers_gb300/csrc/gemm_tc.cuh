@@ -378,6 +378,12 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy reads of them (tensor-core operands).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Grid-wide barrier for a cooperative launch, called by one thread per CTA.
 // gbar[0] counts arrivals and is reset by the last CTA to arrive, which then
 // bumps the generation gbar[1] that the others wait on. Bounded: returns

@@ -51,6 +51,22 @@ struct PackSpec {
 };
 cudaError_t launch_pack(const PackSpec& s, int64_t n_blocks, void* dst, cudaStream_t st);
 
+// ---------------------------------------------------------------- attention core
+struct AttnParams {
+  const int4* pairs;       // [n_pairs] {sequence start, length, q tile, 0}, heaviest first
+  const int* n_pairs;      // written by the preparation kernel
+  __nv_bfloat16* out;      // [t][T][q_per * 128]
+  int* status;
+  unsigned long long timeout_ns;
+  int T, q_per, kv_per, rep, group, heads;  // group = nq / nkv, heads = t * q_per
+  float scale_log2;        // log2(e) / sqrt(hd)
+};
+// Builds the (sequence, q tile) table from cu_seqlens (device) into `pairs` and
+// runs the attention kernel on `grid` CTAs; map_qkv covers qkv as
+// (w_s, T, t, 1) with 64 x 128 boxes.
+cudaError_t launch_attention(const CUtensorMap& map_qkv, const AttnParams& p, const int* cu, int n_seqs,
+                             int max_tiles, int4* pairs, int* n_pairs, int grid, cudaStream_t st);
+
 // ---------------------------------------------------------------- GEMM
 struct GemmParams;
 // Launch the GEMM instantiation for (swap, kind, bn); cudaErrorInvalidValue

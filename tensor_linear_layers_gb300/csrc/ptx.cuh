@@ -89,13 +89,6 @@ __device__ __forceinline__ void bulk_load_multicast(uint32_t dst, const void* sr
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "h"(cta_mask), "l"(policy)
       : "memory");
 }
-// Bulk prefetch of global memory into L2 (no destination, no completion);
-// bytes % 16 == 0, address 16-byte aligned.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes, uint64_t policy) {
-  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(reinterpret_cast<uint64_t>(src)),
-               "r"(bytes), "l"(policy)
-               : "memory");
-}
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -194,6 +187,29 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
       : "r"(taddr));
 }
 
+// 32 lanes x 32 bit, 32 consecutive columns per thread, register -> tensor memory.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  const uint32_t* r = reinterpret_cast<const uint32_t*>(v);
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tc_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// 2^x on the special-function unit (PTX ex2.approx, flush-to-zero); 2^-inf = 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Shared-memory matrix descriptor of a K-major bf16 tile stored as the TMA
 // unit writes it with 128-byte swizzling: rows of 64 elements (128 B), groups
 // of 8 rows 1024 B apart. Fields: start address >> 4 (bits 0-13), leading
@@ -209,6 +225,21 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
   return d;
 }
 
+// Descriptor of an MN-major bf16 operand (MN index contiguous) stored as the
+// TMA unit writes row-major [K][MN] boxes of 64 MN-elements with 128-byte
+// swizzling: an atom is 64 MN-elements x 8 K-rows (1 KB). Leading byte offset
+// = distance between atoms along MN (the next 64-column box), stride byte
+// offset = distance between 8-row groups along K (1024 B).
+__device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t saddr, uint32_t mn_atom_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((mn_atom_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 D, both
 // operands K-major: D format (bits 4-5) = 1, A format (7-9) = 1, B format
 // (10-12) = 1, N >> 3 (17-22), M >> 4 (24-28).
@@ -216,6 +247,8 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
+// Bit 16 of the instruction descriptor: B is MN-major (see smem_desc_mn128).
+constexpr uint32_t kIdescBMnMajor = 1u << 16;
 
 // ------------------------------------------------------------------ misc
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdlib>
 #include <cstdarg>
@@ -259,6 +260,12 @@ Layout make_layout(const tp_linear* h, int64_t T) {
   off = align256(off + make_plan(h, 1, T).partial_bytes);
   L.total = off;
   return L;
+}
+
+// Attention core workspace: after the handle's persistent counters and flags,
+// [256) the table size, [512) the (sequence, q tile) table, 16 B per entry.
+int64_t attn_ws_bytes(const tp_linear* h, int64_t T, int64_t n_seqs) {
+  return dyn_off(h) + 512 + 16 * (ceil_div(T, 128) + n_seqs + 1);
 }
 
 int check_device(const tp_linear* h) {
@@ -612,6 +619,8 @@ int tp_workspace_size(const tp_linear_t* h, int64_t max_tokens, int64_t* bytes) 
     best = std::max(best, make_layout(h, T).total);
   for (int64_t m = 2; (m - 1) * 128 < max_tokens; ++m)
     best = std::max(best, make_layout(h, std::min<int64_t>(max_tokens, m * 128)).total);
+  // the attention core's work table, for up to max_tokens sequences
+  if (h->cfg.kind == TP_BLOCK_ATTN_PROJ) best = std::max(best, attn_ws_bytes(h, max_tokens, max_tokens));
   *bytes = best;
   return ok();
 }
@@ -801,6 +810,54 @@ int tp_attn_proj_forward(tp_linear_t* h, int64_t T, const void* x, void* qkv_out
   }
   if (do_qkv && (rc = run_col(h, T, x, qkv_out, workspace, L, st))) return rc;
   if (do_o && (rc = run_row(h, T, attn_in, nullptr, o_out, nullptr, workspace, L, st))) return rc;
+  return ok();
+}
+
+int tp_attention_forward(tp_linear_t* h, int64_t T, const void* qkv, const int32_t* cu_seqlens,
+                         int32_t n_seqs, int32_t max_seqlen, void* attn_out, void* workspace,
+                         int64_t workspace_bytes, tp_stream_t stream) {
+  if (h == nullptr) return fail(TP_ERR_ARG, "handle is null");
+  if (h->cfg.kind != TP_BLOCK_ATTN_PROJ) return fail(TP_ERR_ARG, "not an attention handle");
+  int rc = check_T(T);
+  if (rc) return rc;
+  if (T == 0) return ok();
+  if (h->cfg.head_dim != 128) return fail(TP_ERR_UNSUPPORTED, "the attention core is built for head_dim 128");
+  TP_CHECK_PTR(qkv, "qkv");
+  TP_CHECK_PTR(attn_out, "attn_out");
+  if (cu_seqlens == nullptr || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)
+    return fail(TP_ERR_ARG, "cu_seqlens is null or not 4-byte aligned");
+  if (n_seqs < 1 || n_seqs > T) return fail(TP_ERR_SHAPE, "n_seqs must be in [1, T] (got %d)", n_seqs);
+  if (max_seqlen < 1 || max_seqlen > T)
+    return fail(TP_ERR_SHAPE, "max_seqlen must be in [1, T] (got %d)", max_seqlen);
+  const int max_tiles = (int)ceil_div(max_seqlen, 128);
+  if (max_tiles > 8192) return fail(TP_ERR_UNSUPPORTED, "max_seqlen > 1048576");
+  if (workspace == nullptr || !aligned16(workspace)) return fail(TP_ERR_ARG, "workspace is null or not 16-byte aligned");
+  if (workspace_bytes < attn_ws_bytes(h, T, n_seqs))
+    return fail(TP_ERR_ARG, "workspace too small: %lld bytes, %lld needed", (long long)workspace_bytes,
+                (long long)attn_ws_bytes(h, T, n_seqs));
+  if ((rc = check_device(h))) return rc;
+  CUtensorMap map_qkv;
+  if ((rc = make_map(&map_qkv, qkv, h->ws_qkv, T, h->cfg.t, 1, 128))) return rc;
+  char* ws = static_cast<char*>(workspace);
+  AttnParams p{};
+  p.pairs = reinterpret_cast<const int4*>(ws + dyn_off(h) + 512);
+  p.n_pairs = reinterpret_cast<const int*>(ws + dyn_off(h) + 256);
+  p.out = static_cast<__nv_bfloat16*>(attn_out);
+  p.status = reinterpret_cast<int*>(ws);
+  p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  p.T = (int)T;
+  p.q_per = h->q_per;
+  p.kv_per = h->kv_per;
+  p.rep = h->rep;
+  p.group = h->cfg.n_q_heads / h->cfg.n_kv_heads;
+  p.heads = h->cfg.t * h->q_per;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)h->cfg.head_dim));
+  const int64_t max_units = (ceil_div(T, 128) + n_seqs) * p.heads;
+  const int grid = (int)std::min<int64_t>(h->nsm, max_units);
+  const cudaError_t e =
+      launch_attention(map_qkv, p, cu_seqlens, n_seqs, max_tiles, const_cast<int4*>(p.pairs),
+                       const_cast<int*>(p.n_pairs), grid, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return ok();
 }
 
