@@ -13,14 +13,17 @@
 //            (most key tiles), heads innermost so the q heads of one kv head
 //            run side by side and share its K/V tiles in L2
 //   warp 0   TMA: the Q tile (two 64-column boxes, 128-byte swizzle), then
-//            K and V tiles of 128 keys into a 2-stage ring
-//   warp 1   tcgen05.mma: S = Q K^T into one of two tensor-memory buffers,
-//            one key tile ahead of O += P V (P from shared memory, V read
-//            MN-major straight from its [key][hd] tile)
+//            K and V tiles of 128 keys into a 3-stage ring
+//   warp 1   tcgen05.mma: S = Q K^T into one of three tensor-memory buffers,
+//            one key tile ahead of O += P V. P is written by the softmax into
+//            the buffer its S came from (bf16 pairs, the tensor-memory A
+//            operand), so P never passes through shared memory; V is read
+//            MN-major straight from its [key][hd] tile. A buffer is reused
+//            once the P V that read it has completed
 //   warps 2-5 softmax, one query row per thread: the row of S from tensor
 //            memory, causal / sequence-end mask, running max and sum in the
-//            exp2 domain, P = 2^(s*c - m) as bf16 into shared memory. O is
-//            rescaled in tensor memory only when the row max grows by more
+//            exp2 domain, P = 2^(s*c - m) as bf16 back into tensor memory. O
+//            is rescaled in tensor memory only when the row max grows by more
 //            than 2^8 (until then the stale max keeps every p <= 256); at the
 //            end O / l goes to global memory as bf16
 //
@@ -38,19 +41,25 @@ namespace tpl {
 
 namespace {
 constexpr int kTileBytes = 128 * 128 * 2;    // 128 rows x 128 bf16: two 64-column boxes
+constexpr int kStages = 3;                   // K/V ring
+constexpr int kSBufs = 3;                    // S/P buffers in tensor memory
 constexpr int kQOff = 0;
-constexpr int kKOff = kTileBytes;            // 2 stages
-constexpr int kVOff = 3 * kTileBytes;        // 2 stages
-constexpr int kPOff = 5 * kTileBytes;        // 2 buffers
-constexpr int kBarOff = 7 * kTileBytes;
+constexpr int kKOff = kTileBytes;
+constexpr int kVOff = kKOff + kStages * kTileBytes;
+constexpr int kBarOff = kVOff + kStages * kTileBytes;
 constexpr int kAttnSmem = 1024 + kBarOff + 256;
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128);
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 128) | kIdescBMnMajor;
-constexpr int kTmemCols = 512;               // S0 [0,128), S1 [128,256), O [256,384)
+constexpr int kTmemCols = 512;               // S/P buffers [0,128) [128,256) [256,384), O [384,512)
+constexpr int kOCol = kSBufs * 128;
 constexpr float kRescaleLog2 = 8.0f;         // rescale O when the row max grows by more than this
 enum {
-  Q_FULL = 0, Q_EMPTY, K_FULL, K_FULL1, K_EMPTY, K_EMPTY1, V_FULL, V_FULL1, V_EMPTY, V_EMPTY1,
-  S_FULL, S_FULL1, S_EMPTY, S_EMPTY1, P_FULL, P_FULL1, P_EMPTY, P_EMPTY1, O_DONE, O_EMPTY, DONE, NBARS
+  Q_FULL = 0, Q_EMPTY,
+  K_FULL, K_EMPTY = K_FULL + kStages, V_FULL = K_EMPTY + kStages, V_EMPTY = V_FULL + kStages,
+  S_FULL = V_EMPTY + kStages,      // S of a buffer computed
+  S_EMPTY = S_FULL + kSBufs,       // the P V that read a buffer's P completed
+  P_FULL = S_EMPTY + kSBufs,       // P written into a buffer (arrivals of the 4 softmax warps)
+  O_DONE = P_FULL + kSBufs, O_EMPTY, DONE, NBARS
 };
 static_assert(8 * NBARS + 16 <= 256, "barrier area");
 
@@ -137,7 +146,7 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < NBARS; ++b) {
-      const bool four = (b == S_EMPTY || b == S_EMPTY1 || b == P_FULL || b == P_FULL1 || b == O_EMPTY);
+      const bool four = (b >= P_FULL && b < P_FULL + kSBufs) || b == O_EMPTY;
       mbar_init(bar(b), four ? 4 : 1);  // arrivals from the four softmax warps
     }
     *s_abort = 0;
@@ -187,8 +196,8 @@ __global__ void __launch_bounds__(192, 1)
         issued(Q_FULL, nu & 1);
         const int kcol = (p.q_per + x.g) * 128, vcol = (p.q_per + p.kv_per + x.g) * 128;
         for (int kt = 0; kt <= x.qt; ++kt, ++kv) {
-          const int st = kv & 1;
-          const uint32_t ph = (kv >> 1) & 1;
+          const int st = kv % kStages;
+          const uint32_t ph = (kv / kStages) & 1;
           if (!mbar_wait_bounded(bar(K_EMPTY + st), ph ^ 1, s_abort, timeout)) {
             ok = false;
             break;
@@ -215,38 +224,38 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = true;
-      int kv = 0, sc = 0, pc = 0, vc = 0;
+      int kv = 0, sc = 0, pc = 0;  // K/V tiles, S tiles, P V products issued so far
       auto wait = [&](int b, uint32_t ph) -> bool {
         if (mbar_wait_bounded(bar(b), ph, s_abort, timeout)) return true;
         set_abort();
         ok = false;
         return false;
       };
-      // O (+)= P V for the oldest key tile whose P is pending
+      // O (+)= P V for the oldest key tile whose P is pending: P from the tile's
+      // tensor-memory buffer, V from its K/V stage (same index as the tile's K)
       auto issue_pv = [&](bool first, int nu) -> bool {
-        const int pb = pc & 1, vs = vc & 1;
-        if (!wait(P_FULL + pb, (pc >> 1) & 1) || !wait(V_FULL + vs, (vc >> 1) & 1)) return false;
+        const int pb = pc % kSBufs, vs = pc % kStages;
+        if (!wait(P_FULL + pb, (pc / kSBufs) & 1) || !wait(V_FULL + vs, (pc / kStages) & 1)) return false;
         if (first && !wait(O_EMPTY, (nu & 1) ^ 1)) return false;
         tc_fence_after();
-        const uint32_t pa = base + kPOff + pb * kTileBytes, va = base + kVOff + vs * kTileBytes;
+        const uint32_t va = base + kVOff + vs * kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t ad = smem_desc_k128(pa + (ks >> 2) * (kTileBytes / 2) + (ks & 3) * 32);
           const uint64_t bd = smem_desc_mn128(va + ks * 2048, kTileBytes / 2);  // 16 keys = two 8-row groups
-          tc_mma_bf16(tmem_base + 256, ad, bd, kIdescO, (first && ks == 0) ? 0u : 1u);
+          tc_mma_bf16_ta(tmem_base + kOCol, tmem_base + pb * 128 + ks * 8, bd, kIdescO,
+                         (first && ks == 0) ? 0u : 1u);
         }
         tc_commit(bar(V_EMPTY + vs));
-        tc_commit(bar(P_EMPTY + pb));
+        tc_commit(bar(S_EMPTY + pb));
         ++pc;
-        ++vc;
         return true;
       };
       for (int u = blockIdx.x, nu = 0; u < n_units && ok; u += grid, ++nu) {
         const Unit x = decode_unit(p, u);
         if (!wait(Q_FULL, nu & 1)) break;
         for (int kt = 0; kt <= x.qt && ok; ++kt, ++kv) {
-          const int st = kv & 1, b = sc & 1;
-          if (!wait(K_FULL + st, (kv >> 1) & 1) || !wait(S_EMPTY + b, ((sc >> 1) & 1) ^ 1)) break;
+          const int st = kv % kStages, b = sc % kSBufs;
+          if (!wait(K_FULL + st, (kv / kStages) & 1) || !wait(S_EMPTY + b, ((sc / kSBufs) & 1) ^ 1)) break;
           tc_fence_after();
           const uint32_t qa = base + kQOff, ka = base + kKOff + st * kTileBytes;
 #pragma unroll
@@ -274,7 +283,7 @@ __global__ void __launch_bounds__(192, 1)
     const int row = q4 * 32 + lane;  // query row of the tile = tensor-memory lane
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16);
     const float c = p.scale_log2;
-    int sc = 0, pc = 0;
+    int sc = 0;  // S tiles consumed (= P tiles produced)
     bool ok = true;
     auto wait_all = [&](int b, uint32_t ph) -> bool {
       bool w = mbar_wait_bounded(bar(b), ph, s_abort, timeout);
@@ -291,8 +300,8 @@ __global__ void __launch_bounds__(192, 1)
       const int q_rel = x.qt * 128 + row;
       float m = -INFINITY, l = 0.f;
       for (int kt = 0; kt <= x.qt; ++kt) {
-        const int b = sc & 1;
-        if (!wait_all(S_FULL + b, (sc >> 1) & 1)) break;
+        const int b = sc % kSBufs;
+        if (!wait_all(S_FULL + b, (sc / kSBufs) & 1)) break;
         tc_fence_after();
         const uint32_t sa = lane_addr + b * 128;
         tmem_ld32(sa, s);
@@ -300,10 +309,6 @@ __global__ void __launch_bounds__(192, 1)
         tmem_ld32(sa + 64, s + 64);
         tmem_ld32(sa + 96, s + 96);
         tc_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(S_EMPTY + b));
-        ++sc;
         if (kt == x.qt || (kt + 1) * 128 > x.len) {
           // diagonal tile and the tile holding the sequence end
 #pragma unroll
@@ -312,9 +317,16 @@ __global__ void __launch_bounds__(192, 1)
             if (key > q_rel || key >= x.len) s[n] = -INFINITY;
           }
         }
-        float mx = s[0];
+        // row max and (below) row sum as 8 independent chains: one dependent chain of
+        // 128 operations per tile would leave the warp waiting on its own latency
+        float mk[8];
 #pragma unroll
-        for (int n = 1; n < 128; ++n) mx = fmaxf(mx, s[n]);
+        for (int j = 0; j < 8; ++j) mk[j] = s[j];
+#pragma unroll
+        for (int n = 8; n < 128; n += 8)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) mk[j] = fmaxf(mk[j], s[n + j]);
+        float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])), fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
         mx *= c;
         if (kt == 0) {
           m = mx;  // the first P V overwrites O
@@ -323,43 +335,40 @@ __global__ void __launch_bounds__(192, 1)
           l *= f;
           m = mx;
           // O holds the products up to the previous key tile: let them land, then scale the row
-          const int pj = pc - 1;
-          if (!wait_all(P_EMPTY + (pj & 1), (pj >> 1) & 1)) break;
+          const int pj = sc - 1;
+          if (!wait_all(S_EMPTY + pj % kSBufs, (pj / kSBufs) & 1)) break;
           tc_fence_after();
           float o[32];
 #pragma unroll
           for (int c0 = 0; c0 < 128; c0 += 32) {
-            tmem_ld32(lane_addr + 256 + c0, o);
+            tmem_ld32(lane_addr + kOCol + c0, o);
             tc_wait_ld();
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] *= f;
-            tmem_st32(lane_addr + 256 + c0, o);
+            tmem_st32(lane_addr + kOCol + c0, o);
           }
-          tc_wait_st();
         }
-        const int pb = pc & 1;
-        if (!wait_all(P_EMPTY + pb, ((pc >> 1) & 1) ^ 1)) break;  // the P V two tiles back is done
-        uint8_t* prow = base_ptr + kPOff + pb * kTileBytes + row * 128;
+        // P = 2^(s c - m) as bf16 pairs into the first 64 columns of the buffer
+        float lk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-          float e[8];
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            e[j] = fast_exp2(fmaf(s[ch * 8 + j], c, -m));
-            l += e[j];
+          for (int j = 0; j < 32; ++j) {
+            const float e0 = fast_exp2(fmaf(s[h * 64 + 2 * j], c, -m));
+            const float e1 = fast_exp2(fmaf(s[h * 64 + 2 * j + 1], c, -m));
+            lk[(2 * j) & 7] += e0;
+            lk[(2 * j + 1) & 7] += e1;
+            pk[j] = pack_bf16x2(e0, e1);
           }
-          uint4 v;
-          v.x = pack_bf16x2(e[0], e[1]);
-          v.y = pack_bf16x2(e[2], e[3]);
-          v.z = pack_bf16x2(e[4], e[5]);
-          v.w = pack_bf16x2(e[6], e[7]);
-          *reinterpret_cast<uint4*>(prow + (ch >> 3) * (kTileBytes / 2) + (((ch & 7) ^ (row & 7)) << 4)) = v;
+          tmem_st32(sa + h * 32, reinterpret_cast<const float*>(pk));
         }
-        fence_proxy_async_shared();  // the tensor core reads P
-        tc_fence_before();           // and O as rescaled above
+        l += ((lk[0] + lk[1]) + (lk[2] + lk[3])) + ((lk[4] + lk[5]) + (lk[6] + lk[7]));
+        tc_wait_st();      // P, and O as rescaled above, are in tensor memory
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(P_FULL + pb));
-        ++pc;
+        if (lane == 0) mbar_arrive(bar(P_FULL + b));
+        ++sc;
       }
       if (!ok || !wait_all(O_DONE, nu & 1)) break;
       tc_fence_after();
@@ -368,7 +377,7 @@ __global__ void __launch_bounds__(192, 1)
       float o[32];
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 32) {
-        tmem_ld32(lane_addr + 256 + c0, o);
+        tmem_ld32(lane_addr + kOCol + c0, o);
         tc_wait_ld();
         if (q_rel < x.len) {
 #pragma unroll
