@@ -15,7 +15,7 @@
 //   warp 0   TMA: the Q tile (two 64-column boxes, 128-byte swizzle), then
 //            K and V tiles of 128 keys into a 3-stage ring
 //   warp 1   tcgen05.mma: S = Q K^T into one of three tensor-memory buffers,
-//            one key tile ahead of O += P V. P is written by the softmax into
+//            three key tiles ahead of O += P V. P is written by the softmax into
 //            the buffer its S came from (bf16 pairs, the tensor-memory A
 //            operand), so P never passes through shared memory; V is read
 //            MN-major straight from its [key][hd] tile. A buffer is reused
@@ -250,27 +250,38 @@ __global__ void __launch_bounds__(192, 1)
         ++pc;
         return true;
       };
+      // S = Q K^T of key tile kt of the current unit into buffer sc % kSBufs, once the
+      // P V that last read that buffer has completed
+      auto issue_s = [&](int kt, bool last) -> bool {
+        const int st = kv % kStages, b = sc % kSBufs;
+        if (!wait(S_EMPTY + b, ((sc / kSBufs) & 1) ^ 1) || !wait(K_FULL + st, (kv / kStages) & 1)) return false;
+        tc_fence_after();
+        const uint32_t qa = base + kQOff, ka = base + kKOff + st * kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t o = (ks >> 2) * (kTileBytes / 2) + (ks & 3) * 32;
+          tc_mma_bf16(tmem_base + b * 128, smem_desc_k128(qa + o), smem_desc_k128(ka + o), kIdescS, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(K_EMPTY + st));
+        tc_commit(bar(S_FULL + b));
+        if (last) tc_commit(bar(Q_EMPTY));
+        ++sc;
+        ++kv;
+        return true;
+      };
+      // S runs kSBufs key tiles ahead of P V: the softmax finds the next S computed
+      // while the tensor core works on the current P V
       for (int u = blockIdx.x, nu = 0; u < n_units && ok; u += grid, ++nu) {
         const Unit x = decode_unit(p, u);
+        const int n = x.qt + 1;
         if (!wait(Q_FULL, nu & 1)) break;
-        for (int kt = 0; kt <= x.qt && ok; ++kt, ++kv) {
-          const int st = kv % kStages, b = sc % kSBufs;
-          if (!wait(K_FULL + st, (kv / kStages) & 1) || !wait(S_EMPTY + b, ((sc / kSBufs) & 1) ^ 1)) break;
-          tc_fence_after();
-          const uint32_t qa = base + kQOff, ka = base + kKOff + st * kTileBytes;
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t o = (ks >> 2) * (kTileBytes / 2) + (ks & 3) * 32;
-            tc_mma_bf16(tmem_base + b * 128, smem_desc_k128(qa + o), smem_desc_k128(ka + o), kIdescS,
-                        ks > 0 ? 1u : 0u);
-          }
-          tc_commit(bar(K_EMPTY + st));
-          tc_commit(bar(S_FULL + b));
-          if (kt == x.qt) tc_commit(bar(Q_EMPTY));
-          ++sc;
-          if (kt > 0 && !issue_pv(kt == 1, nu)) break;
+        for (int kt = 0; kt < n && kt < kSBufs; ++kt)
+          if (!issue_s(kt, kt == n - 1)) break;
+        for (int j = 0; j < n && ok; ++j) {
+          if (!issue_pv(j == 0, nu)) break;
+          if (j + kSBufs < n && !issue_s(j + kSBufs, j + kSBufs == n - 1)) break;
         }
-        if (!ok || !issue_pv(x.qt == 0, nu)) break;
+        if (!ok) break;
         tc_commit(bar(O_DONE));
       }
       tc_commit(bar(DONE));
