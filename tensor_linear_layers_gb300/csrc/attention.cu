@@ -9,8 +9,9 @@
 // heads | k heads | v heads, hd = 128 columns each); output is o_proj's
 // input, attn [t][T][q_per * hd]. Flash-style, one CTA per SM, persistent:
 //
-//   unit     (q head, sequence, 128-query tile); units run heaviest first
-//            (most key tiles), heads innermost so the q heads of one kv head
+//   unit     (q head, sequence, 128-query tile); units are handed out heaviest
+//            first (most key tiles) from a counter, a CTA taking the next one
+//            as it frees up; heads are innermost so the q heads of one kv head
 //            run side by side and share its K/V tiles in L2
 //   warp 0   TMA: the Q tile (two 64-column boxes, 128-byte swizzle), then
 //            K and V tiles of 128 keys into a 3-stage ring
@@ -47,7 +48,9 @@ constexpr int kQOff = 0;
 constexpr int kKOff = kTileBytes;
 constexpr int kVOff = kKOff + kStages * kTileBytes;
 constexpr int kBarOff = kVOff + kStages * kTileBytes;
-constexpr int kAttnSmem = 1024 + kBarOff + 256;
+constexpr int kBarBytes = 512;
+constexpr int kAttnSmem = 1024 + kBarOff + kBarBytes;
+constexpr int kUnitSlots = 4;                // units the producer may hand out ahead of the consumers
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128);
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 128) | kIdescBMnMajor;
 constexpr int kTmemCols = 512;               // S/P buffers [0,128) [128,256) [256,384), O [384,512)
@@ -59,9 +62,13 @@ enum {
   S_FULL = V_EMPTY + kStages,      // S of a buffer computed
   S_EMPTY = S_FULL + kSBufs,       // the P V that read a buffer's P completed
   P_FULL = S_EMPTY + kSBufs,       // P written into a buffer (arrivals of the 4 softmax warps)
-  O_DONE = P_FULL + kSBufs, O_EMPTY, DONE, NBARS
+  O_DONE = P_FULL + kSBufs, O_EMPTY, DONE,
+  U_FULL,                          // a unit id published by the producer
+  U_EMPTY = U_FULL + kUnitSlots,   // read by the MMA thread and the four softmax warps
+  NBARS = U_EMPTY + kUnitSlots
 };
-static_assert(8 * NBARS + 16 <= 256, "barrier area");
+static_assert(8 * NBARS + 8 + 4 * kUnitSlots <= kBarBytes, "barrier area");
+static_assert(S_FULL <= 32, "copy barriers fit the producer's bit masks");
 
 struct Unit {
   int r, i, g, start, len, qt;
@@ -86,11 +93,14 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int u) {
 // Checks the offsets (0 first, T last, none falling, no length above
 // max_tiles * 128); on a bad table it writes TP_ERR_SHAPE and no entries.
 __global__ void attn_prep_kernel(const int* cu, int n_seqs, int T, int max_tiles, int4* pairs, int* n_pairs,
-                                 int* status) {
+                                 int* next_unit, int* status) {
   extern __shared__ int off[];  // [max_tiles]
   __shared__ int s_bad;
   const int tid = threadIdx.x;
-  if (tid == 0) s_bad = (cu[0] != 0 || cu[n_seqs] != T) ? 1 : 0;
+  if (tid == 0) {
+    s_bad = (cu[0] != 0 || cu[n_seqs] != T) ? 1 : 0;
+    *next_unit = 0;
+  }
   __syncthreads();
   for (int s = tid; s < n_seqs; s += blockDim.x) {
     const int len = cu[s + 1] - cu[s];
@@ -140,14 +150,15 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* misc = base_ptr + kBarOff + 8 * NBARS;
   volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(misc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 4);
+  volatile int* s_units = reinterpret_cast<volatile int*>(misc + 8);  // [kUnitSlots] unit ids, -1 = no more
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const unsigned grid = gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < NBARS; ++b) {
-      const bool four = (b >= P_FULL && b < P_FULL + kSBufs) || b == O_EMPTY;
-      mbar_init(bar(b), four ? 4 : 1);  // arrivals from the four softmax warps
+      const bool four = (b >= P_FULL && b < P_FULL + kSBufs) || b == O_EMPTY;  // the four softmax warps
+      const bool five = b >= U_EMPTY;                                            // and the MMA thread
+      mbar_init(bar(b), five ? 5 : (four ? 4 : 1));
     }
     *s_abort = 0;
     fence_barrier_init();
@@ -186,7 +197,17 @@ __global__ void __launch_bounds__(192, 1)
       };
       bool ok = true;
       int kv = 0;
-      for (int u = blockIdx.x, nu = 0; u < n_units && ok; u += grid, ++nu) {
+      for (int nu = 0; ok; ++nu) {
+        const int slot = nu % kUnitSlots;
+        if (!mbar_wait_bounded(bar(U_EMPTY + slot), ((nu / kUnitSlots) & 1) ^ 1, s_abort, timeout)) {
+          ok = false;
+          break;
+        }
+        int u = atomicAdd(p.next_unit, 1);
+        if (u >= n_units) u = -1;
+        s_units[slot] = u;
+        mbar_arrive(bar(U_FULL + slot));  // releases the id to the consumers
+        if (u < 0) break;
         const Unit x = decode_unit(p, u);
         if (!mbar_wait_bounded(bar(Q_EMPTY), (nu & 1) ^ 1, s_abort, timeout)) {
           ok = false;
@@ -215,7 +236,7 @@ __global__ void __launch_bounds__(192, 1)
       if (!ok) {
         set_abort();
         // no copy into this CTA's shared memory may outlive it
-        for (int b = 0; b < NBARS; ++b)
+        for (int b = 0; b < S_FULL; ++b)
           if (full_mask & (1u << b)) mbar_wait_bounded(bar(b), (full_phase >> b) & 1u, nullptr, kTeardownNs);
       }
     }
@@ -271,7 +292,12 @@ __global__ void __launch_bounds__(192, 1)
       };
       // S runs kSBufs key tiles ahead of P V: the softmax finds the next S computed
       // while the tensor core works on the current P V
-      for (int u = blockIdx.x, nu = 0; u < n_units && ok; u += grid, ++nu) {
+      for (int nu = 0; ok; ++nu) {
+        const int slot = nu % kUnitSlots;
+        if (!wait(U_FULL + slot, (nu / kUnitSlots) & 1)) break;
+        const int u = s_units[slot];
+        mbar_arrive(bar(U_EMPTY + slot));
+        if (u < 0) break;
         const Unit x = decode_unit(p, u);
         const int n = x.qt + 1;
         if (!wait(Q_FULL, nu & 1)) break;
@@ -306,7 +332,13 @@ __global__ void __launch_bounds__(192, 1)
       return w;
     };
     float s[128];
-    for (int u = blockIdx.x, nu = 0; u < n_units && ok; u += grid, ++nu) {
+    for (int nu = 0; ok; ++nu) {
+      const int slot = nu % kUnitSlots;
+      if (!wait_all(U_FULL + slot, (nu / kUnitSlots) & 1)) break;
+      const int u = s_units[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(U_EMPTY + slot));
+      if (u < 0) break;
       const Unit x = decode_unit(p, u);
       const int q_rel = x.qt * 128 + row;
       float m = -INFINITY, l = 0.f;
@@ -418,7 +450,7 @@ __global__ void __launch_bounds__(192, 1)
 cudaError_t launch_attention(const CUtensorMap& map_qkv, const AttnParams& p, const int* cu, int n_seqs,
                              int max_tiles, int4* pairs, int* n_pairs, int grid, cudaStream_t st) {
   attn_prep_kernel<<<1, 1024, max_tiles * (int)sizeof(int), st>>>(cu, n_seqs, p.T, max_tiles, pairs, n_pairs,
-                                                                    p.status);
+                                                                    p.next_unit, p.status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   static std::atomic<uint64_t> attr_done{0};

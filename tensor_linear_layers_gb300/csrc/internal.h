@@ -55,6 +55,7 @@ cudaError_t launch_pack(const PackSpec& s, int64_t n_blocks, void* dst, cudaStre
 struct AttnParams {
   const int4* pairs;       // [n_pairs] {sequence start, length, q tile, 0}, heaviest first
   const int* n_pairs;      // written by the preparation kernel
+  int* next_unit;          // units handed out so far (CTAs take the next one when free); zeroed by the preparation kernel
   __nv_bfloat16* out;      // [t][T][q_per * 128]
   int* status;
   unsigned long long timeout_ns;

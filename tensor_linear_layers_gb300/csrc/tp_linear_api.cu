@@ -263,7 +263,8 @@ Layout make_layout(const tp_linear* h, int64_t T) {
 }
 
 // Attention core workspace: after the handle's persistent counters and flags,
-// [256) the table size, [512) the (sequence, q tile) table, 16 B per entry.
+// [256) the table size, [260) the unit counter, [512) the (sequence, q tile)
+// table, 16 B per entry.
 int64_t attn_ws_bytes(const tp_linear* h, int64_t T, int64_t n_seqs) {
   return dyn_off(h) + 512 + 16 * (ceil_div(T, 128) + n_seqs + 1);
 }
@@ -842,6 +843,7 @@ int tp_attention_forward(tp_linear_t* h, int64_t T, const void* qkv, const int32
   AttnParams p{};
   p.pairs = reinterpret_cast<const int4*>(ws + dyn_off(h) + 512);
   p.n_pairs = reinterpret_cast<const int*>(ws + dyn_off(h) + 256);
+  p.next_unit = reinterpret_cast<int*>(ws + dyn_off(h) + 260);
   p.out = static_cast<__nv_bfloat16*>(attn_out);
   p.status = reinterpret_cast<int*>(ws);
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
