@@ -244,50 +244,67 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      // The issuing thread shares its sub-partition with a softmax warp, so every
+      // instruction it saves keeps the tensor pipe fed: descriptors are built once,
+      // a k-step is an add of a constant, and ring positions advance without division.
       bool ok = true;
-      int kv = 0, sc = 0, pc = 0;  // K/V tiles, S tiles, P V products issued so far
       auto wait = [&](int b, uint32_t ph) -> bool {
         if (mbar_wait_bounded(bar(b), ph, s_abort, timeout)) return true;
         set_abort();
         ok = false;
         return false;
       };
+      // stage i's descriptor is stage 0's plus i tiles in the address field (address >> 4,
+      // 14 bits; every shared address here is below 256 KB, so the field never carries)
+      const uint64_t q_desc = smem_desc_k128(base + kQOff);
+      const uint64_t k_desc0 = smem_desc_k128(base + kKOff);
+      const uint64_t v_desc0 = smem_desc_mn128(base + kVOff, kTileBytes / 2);
+      constexpr uint64_t kTileDesc = kTileBytes >> 4;
+      // ring positions and phase bits: K/V stage of the next S and of the next P V,
+      // S/P buffer of the next S and of the next P V
+      int ks_st = 0, pv_st = 0, s_buf = 0, p_buf = 0;
+      uint32_t ks_ph = 0, pv_ph = 0, s_ph = 0, p_ph = 0;
+      auto advance = [](int& i, uint32_t& ph, int n) {
+        if (++i == n) {
+          i = 0;
+          ph ^= 1u;
+        }
+      };
       // O (+)= P V for the oldest key tile whose P is pending: P from the tile's
-      // tensor-memory buffer, V from its K/V stage (same index as the tile's K)
+      // tensor-memory buffer, V from its K/V stage
       auto issue_pv = [&](bool first, int nu) -> bool {
-        const int pb = pc % kSBufs, vs = pc % kStages;
-        if (!wait(P_FULL + pb, (pc / kSBufs) & 1) || !wait(V_FULL + vs, (pc / kStages) & 1)) return false;
+        if (!wait(P_FULL + p_buf, p_ph) || !wait(V_FULL + pv_st, pv_ph)) return false;
         if (first && !wait(O_EMPTY, (nu & 1) ^ 1)) return false;
         tc_fence_after();
-        const uint32_t va = base + kVOff + vs * kTileBytes;
+        const uint64_t vd = v_desc0 + (uint64_t)pv_st * kTileDesc;
+        const uint32_t pa = tmem_base + p_buf * 128;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t bd = smem_desc_mn128(va + ks * 2048, kTileBytes / 2);  // 16 keys = two 8-row groups
-          tc_mma_bf16_ta(tmem_base + kOCol, tmem_base + pb * 128 + ks * 8, bd, kIdescO,
-                         (first && ks == 0) ? 0u : 1u);
-        }
-        tc_commit(bar(V_EMPTY + vs));
-        tc_commit(bar(S_EMPTY + pb));
-        ++pc;
+        for (int k = 0; k < 8; ++k)  // 16 keys = two 8-row groups of V = 2048 B; 8 columns of P
+          tc_mma_bf16_ta(tmem_base + kOCol, pa + k * 8, vd + (uint64_t)(k * (2048 >> 4)), kIdescO,
+                         (first && k == 0) ? 0u : 1u);
+        tc_commit(bar(V_EMPTY + pv_st));
+        tc_commit(bar(S_EMPTY + p_buf));
+        advance(pv_st, pv_ph, kStages);
+        advance(p_buf, p_ph, kSBufs);
         return true;
       };
-      // S = Q K^T of key tile kt of the current unit into buffer sc % kSBufs, once the
-      // P V that last read that buffer has completed
-      auto issue_s = [&](int kt, bool last) -> bool {
-        const int st = kv % kStages, b = sc % kSBufs;
-        if (!wait(S_EMPTY + b, ((sc / kSBufs) & 1) ^ 1) || !wait(K_FULL + st, (kv / kStages) & 1)) return false;
+      // S = Q K^T of the next key tile into the next buffer, once the P V that last
+      // read that buffer has completed
+      auto issue_s = [&](bool last) -> bool {
+        if (!wait(S_EMPTY + s_buf, s_ph ^ 1u) || !wait(K_FULL + ks_st, ks_ph)) return false;
         tc_fence_after();
-        const uint32_t qa = base + kQOff, ka = base + kKOff + st * kTileBytes;
+        const uint64_t kd = k_desc0 + (uint64_t)ks_st * kTileDesc;
+        const uint32_t d = tmem_base + s_buf * 128;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t o = (ks >> 2) * (kTileBytes / 2) + (ks & 3) * 32;
-          tc_mma_bf16(tmem_base + b * 128, smem_desc_k128(qa + o), smem_desc_k128(ka + o), kIdescS, ks > 0 ? 1u : 0u);
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t o = (uint64_t)(((k >> 2) * (kTileBytes / 2) + (k & 3) * 32) >> 4);
+          tc_mma_bf16(d, q_desc + o, kd + o, kIdescS, k > 0 ? 1u : 0u);
         }
-        tc_commit(bar(K_EMPTY + st));
-        tc_commit(bar(S_FULL + b));
+        tc_commit(bar(K_EMPTY + ks_st));
+        tc_commit(bar(S_FULL + s_buf));
         if (last) tc_commit(bar(Q_EMPTY));
-        ++sc;
-        ++kv;
+        advance(ks_st, ks_ph, kStages);
+        advance(s_buf, s_ph, kSBufs);
         return true;
       };
       // S runs kSBufs key tiles ahead of P V: the softmax finds the next S computed
@@ -302,10 +319,10 @@ __global__ void __launch_bounds__(192, 1)
         const int n = x.qt + 1;
         if (!wait(Q_FULL, nu & 1)) break;
         for (int kt = 0; kt < n && kt < kSBufs; ++kt)
-          if (!issue_s(kt, kt == n - 1)) break;
+          if (!issue_s(kt == n - 1)) break;
         for (int j = 0; j < n && ok; ++j) {
           if (!issue_pv(j == 0, nu)) break;
-          if (j + kSBufs < n && !issue_s(j + kSBufs, j + kSBufs == n - 1)) break;
+          if (j + kSBufs < n && !issue_s(j + kSBufs == n - 1)) break;
         }
         if (!ok) break;
         tc_commit(bar(O_DONE));
