@@ -15,8 +15,9 @@
 //            run side by side and share its K/V tiles in L2
 //   warp 0   TMA: the Q tile (two 64-column boxes, 128-byte swizzle), then
 //            K and V tiles of 128 keys into a 3-stage ring
-//   warp 1   tcgen05.mma: S = Q K^T into one of three tensor-memory buffers,
-//            three key tiles ahead of O += P V. P is written by the softmax into
+//   warp 6   tcgen05.mma: S = Q K^T into one of three tensor-memory buffers,
+//            up to three key tiles ahead of O += P V
+//   warp 1   tcgen05.mma: O += P V, once the softmax has written P. P is written by the softmax into
 //            the buffer its S came from (bf16 pairs, the tensor-memory A
 //            operand), so P never passes through shared memory; V is read
 //            MN-major straight from its [key][hd] tile. A buffer is reused
@@ -51,6 +52,8 @@ constexpr int kBarOff = kVOff + kStages * kTileBytes;
 constexpr int kBarBytes = 512;
 constexpr int kAttnSmem = 1024 + kBarOff + kBarBytes;
 constexpr int kUnitSlots = 4;                // units the producer may hand out ahead of the consumers
+constexpr int kSWarp = 6;                    // issues the S = Q K^T MMAs (warp 1 issues P V)
+constexpr int kThreads = 32 * (kSWarp + 1);
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128);
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 128) | kIdescBMnMajor;
 constexpr int kTmemCols = 512;               // S/P buffers [0,128) [128,256) [256,384), O [384,512)
@@ -62,9 +65,9 @@ enum {
   S_FULL = V_EMPTY + kStages,      // S of a buffer computed
   S_EMPTY = S_FULL + kSBufs,       // the P V that read a buffer's P completed
   P_FULL = S_EMPTY + kSBufs,       // P written into a buffer (arrivals of the 4 softmax warps)
-  O_DONE = P_FULL + kSBufs, O_EMPTY, DONE,
+  O_DONE = P_FULL + kSBufs, O_EMPTY, DONE, DONE_S,
   U_FULL,                          // a unit id published by the producer
-  U_EMPTY = U_FULL + kUnitSlots,   // read by the MMA thread and the four softmax warps
+  U_EMPTY = U_FULL + kUnitSlots,   // read by the two MMA threads and the four softmax warps
   NBARS = U_EMPTY + kUnitSlots
 };
 static_assert(8 * NBARS + 8 + 4 * kUnitSlots <= kBarBytes, "barrier area");
@@ -139,7 +142,7 @@ __global__ void attn_prep_kernel(const int* cu, int n_seqs, int T, int max_tiles
   }
 }
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -157,8 +160,8 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     for (int b = 0; b < NBARS; ++b) {
       const bool four = (b >= P_FULL && b < P_FULL + kSBufs) || b == O_EMPTY;  // the four softmax warps
-      const bool five = b >= U_EMPTY;                                            // and the MMA thread
-      mbar_init(bar(b), five ? 5 : (four ? 4 : 1));
+      const bool six = b >= U_EMPTY;                                             // and the two MMA threads
+      mbar_init(bar(b), six ? 6 : (four ? 4 : 1));
     }
     *s_abort = 0;
     fence_barrier_init();
@@ -241,12 +244,15 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kSWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 6 issues S = Q K^T, warp 1 O += P V. Each shares its sub-partition with a
+    // softmax warp, so every instruction saved keeps the tensor pipe fed: descriptors
+    // are built once, a k-step adds a constant, ring positions advance without division.
+    // Ordering between the two goes through mbarriers: S_FULL (S done) -> softmax ->
+    // P_FULL -> P V -> S_EMPTY (buffer free for the S three tiles later).
     if (lane == 0) {
-      // The issuing thread shares its sub-partition with a softmax warp, so every
-      // instruction it saves keeps the tensor pipe fed: descriptors are built once,
-      // a k-step is an add of a constant, and ring positions advance without division.
+      const bool s_role = warp == kSWarp;
       bool ok = true;
       auto wait = [&](int b, uint32_t ph) -> bool {
         if (mbar_wait_bounded(bar(b), ph, s_abort, timeout)) return true;
@@ -254,61 +260,20 @@ __global__ void __launch_bounds__(192, 1)
         ok = false;
         return false;
       };
-      // stage i's descriptor is stage 0's plus i tiles in the address field (address >> 4,
-      // 14 bits; every shared address here is below 256 KB, so the field never carries)
-      const uint64_t q_desc = smem_desc_k128(base + kQOff);
-      const uint64_t k_desc0 = smem_desc_k128(base + kKOff);
-      const uint64_t v_desc0 = smem_desc_mn128(base + kVOff, kTileBytes / 2);
-      constexpr uint64_t kTileDesc = kTileBytes >> 4;
-      // ring positions and phase bits: K/V stage of the next S and of the next P V,
-      // S/P buffer of the next S and of the next P V
-      int ks_st = 0, pv_st = 0, s_buf = 0, p_buf = 0;
-      uint32_t ks_ph = 0, pv_ph = 0, s_ph = 0, p_ph = 0;
       auto advance = [](int& i, uint32_t& ph, int n) {
         if (++i == n) {
           i = 0;
           ph ^= 1u;
         }
       };
-      // O (+)= P V for the oldest key tile whose P is pending: P from the tile's
-      // tensor-memory buffer, V from its K/V stage
-      auto issue_pv = [&](bool first, int nu) -> bool {
-        if (!wait(P_FULL + p_buf, p_ph) || !wait(V_FULL + pv_st, pv_ph)) return false;
-        if (first && !wait(O_EMPTY, (nu & 1) ^ 1)) return false;
-        tc_fence_after();
-        const uint64_t vd = v_desc0 + (uint64_t)pv_st * kTileDesc;
-        const uint32_t pa = tmem_base + p_buf * 128;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)  // 16 keys = two 8-row groups of V = 2048 B; 8 columns of P
-          tc_mma_bf16_ta(tmem_base + kOCol, pa + k * 8, vd + (uint64_t)(k * (2048 >> 4)), kIdescO,
-                         (first && k == 0) ? 0u : 1u);
-        tc_commit(bar(V_EMPTY + pv_st));
-        tc_commit(bar(S_EMPTY + p_buf));
-        advance(pv_st, pv_ph, kStages);
-        advance(p_buf, p_ph, kSBufs);
-        return true;
-      };
-      // S = Q K^T of the next key tile into the next buffer, once the P V that last
-      // read that buffer has completed
-      auto issue_s = [&](bool last) -> bool {
-        if (!wait(S_EMPTY + s_buf, s_ph ^ 1u) || !wait(K_FULL + ks_st, ks_ph)) return false;
-        tc_fence_after();
-        const uint64_t kd = k_desc0 + (uint64_t)ks_st * kTileDesc;
-        const uint32_t d = tmem_base + s_buf * 128;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t o = (uint64_t)(((k >> 2) * (kTileBytes / 2) + (k & 3) * 32) >> 4);
-          tc_mma_bf16(d, q_desc + o, kd + o, kIdescS, k > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(K_EMPTY + ks_st));
-        tc_commit(bar(S_FULL + s_buf));
-        if (last) tc_commit(bar(Q_EMPTY));
-        advance(ks_st, ks_ph, kStages);
-        advance(s_buf, s_ph, kSBufs);
-        return true;
-      };
-      // S runs kSBufs key tiles ahead of P V: the softmax finds the next S computed
-      // while the tensor core works on the current P V
+      // stage i's descriptor is stage 0's plus i tiles in the address field (address >> 4,
+      // 14 bits; every shared address here is below 256 KB, so the field never carries)
+      constexpr uint64_t kTileDesc = kTileBytes >> 4;
+      const uint64_t q_desc = smem_desc_k128(base + kQOff);
+      const uint64_t k_desc0 = smem_desc_k128(base + kKOff);
+      const uint64_t v_desc0 = smem_desc_mn128(base + kVOff, kTileBytes / 2);
+      int st = 0, buf = 0;        // K/V stage and S/P buffer of the next MMA group
+      uint32_t st_ph = 0, buf_ph = 0;
       for (int nu = 0; ok; ++nu) {
         const int slot = nu % kUnitSlots;
         if (!wait(U_FULL + slot, (nu / kUnitSlots) & 1)) break;
@@ -317,18 +282,54 @@ __global__ void __launch_bounds__(192, 1)
         if (u < 0) break;
         const Unit x = decode_unit(p, u);
         const int n = x.qt + 1;
-        if (!wait(Q_FULL, nu & 1)) break;
-        for (int kt = 0; kt < n && kt < kSBufs; ++kt)
-          if (!issue_s(kt == n - 1)) break;
-        for (int j = 0; j < n && ok; ++j) {
-          if (!issue_pv(j == 0, nu)) break;
-          if (j + kSBufs < n && !issue_s(j + kSBufs == n - 1)) break;
+        if (s_role) {
+          if (!wait(Q_FULL, nu & 1)) break;
+          for (int j = 0; j < n; ++j) {
+            // the P V that last read this buffer has completed, and K is in
+            if (!wait(S_EMPTY + buf, buf_ph ^ 1u) || !wait(K_FULL + st, st_ph)) break;
+            tc_fence_after();
+            const uint64_t kd = k_desc0 + (uint64_t)st * kTileDesc;
+            const uint32_t d = tmem_base + buf * 128;
+            tc_mma_bf16_c<false>(d, q_desc, kd, kIdescS);
+#pragma unroll
+            for (int k = 1; k < 8; ++k) {
+              const uint64_t o = (uint64_t)(((k >> 2) * (kTileBytes / 2) + (k & 3) * 32) >> 4);
+              tc_mma_bf16_c<true>(d, q_desc + o, kd + o, kIdescS);
+            }
+            tc_commit(bar(K_EMPTY + st));
+            tc_commit(bar(S_FULL + buf));
+            if (j == n - 1) tc_commit(bar(Q_EMPTY));
+            advance(st, st_ph, kStages);
+            advance(buf, buf_ph, kSBufs);
+          }
+        } else {
+          for (int j = 0; j < n; ++j) {
+            if (!wait(P_FULL + buf, buf_ph) || !wait(V_FULL + st, st_ph)) break;
+            if (j == 0 && !wait(O_EMPTY, (nu & 1) ^ 1)) break;
+            tc_fence_after();
+            const uint64_t vd = v_desc0 + (uint64_t)st * kTileDesc;
+            const uint32_t pa = tmem_base + buf * 128;
+            // 16 keys = two 8-row groups of V (2048 B) and 8 columns of P
+            if (j == 0)
+              tc_mma_bf16_ta_c<false>(tmem_base + kOCol, pa, vd, kIdescO);
+            else
+              tc_mma_bf16_ta_c<true>(tmem_base + kOCol, pa, vd, kIdescO);
+#pragma unroll
+            for (int k = 1; k < 8; ++k)
+              tc_mma_bf16_ta_c<true>(tmem_base + kOCol, pa + k * 8, vd + (uint64_t)(k * (2048 >> 4)), kIdescO);
+            tc_commit(bar(V_EMPTY + st));
+            tc_commit(bar(S_EMPTY + buf));
+            advance(st, st_ph, kStages);
+            advance(buf, buf_ph, kSBufs);
+          }
+          if (!ok) break;
+          tc_commit(bar(O_DONE));
         }
-        if (!ok) break;
-        tc_commit(bar(O_DONE));
       }
-      tc_commit(bar(DONE));
-      mbar_wait_bounded(bar(DONE), 0, nullptr, kTeardownNs);
+      // this thread's MMAs complete before tensor memory is released
+      const int done = s_role ? DONE_S : DONE;
+      tc_commit(bar(done));
+      mbar_wait_bounded(bar(done), 0, nullptr, kTeardownNs);
     }
     __syncwarp();
   } else {
@@ -480,7 +481,7 @@ cudaError_t launch_attention(const CUtensorMap& map_qkv, const AttnParams& p, co
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit, std::memory_order_acq_rel);
   }
-  attn_fwd_kernel<<<grid, 192, kAttnSmem, st>>>(map_qkv, p);
+  attn_fwd_kernel<<<grid, kThreads, kAttnSmem, st>>>(map_qkv, p);
   return cudaGetLastError();
 }
 
