@@ -59,13 +59,18 @@ constexpr uint32_t kIdescO = idesc_bf16_f32(128, 128) | kIdescBMnMajor;
 constexpr int kTmemCols = 512;               // S/P buffers [0,128) [128,256) [256,384), O [384,512)
 constexpr int kOCol = kSBufs * 128;
 constexpr float kRescaleLog2 = 8.0f;         // rescale O when the row max grows by more than this
+// Key tile j uses slot j % 3 of everything: K/V stage, S/P buffer and the barriers
+// below. A wait costs an MMA issuer a few hundred cycles even when the barrier has
+// already completed, so each issuer's inputs meet on one barrier per slot:
+//   S_READY[i]  K landed (producer arrival + bytes) and the buffer is free (commit of
+//               the P V three tiles back; armed once at start for the first three)
+//   PV_READY[i] V landed (producer arrival + bytes) and P written (4 softmax warps)
+static_assert(kStages == kSBufs, "K/V stages and S/P buffers advance together");
 enum {
   Q_FULL = 0, Q_EMPTY,
-  K_FULL, K_EMPTY = K_FULL + kStages, V_FULL = K_EMPTY + kStages, V_EMPTY = V_FULL + kStages,
+  S_READY, K_EMPTY = S_READY + kStages, PV_READY = K_EMPTY + kStages, V_EMPTY = PV_READY + kStages,
   S_FULL = V_EMPTY + kStages,      // S of a buffer computed
-  S_EMPTY = S_FULL + kSBufs,       // the P V that read a buffer's P completed
-  P_FULL = S_EMPTY + kSBufs,       // P written into a buffer (arrivals of the 4 softmax warps)
-  O_DONE = P_FULL + kSBufs, O_EMPTY, DONE, DONE_S,
+  O_DONE = S_FULL + kSBufs, O_EMPTY, DONE, DONE_S,
   U_FULL,                          // a unit id published by the producer
   U_EMPTY = U_FULL + kUnitSlots,   // read by the two MMA threads and the four softmax warps
   NBARS = U_EMPTY + kUnitSlots
@@ -159,10 +164,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < NBARS; ++b) {
-      const bool four = (b >= P_FULL && b < P_FULL + kSBufs) || b == O_EMPTY;  // the four softmax warps
-      const bool six = b >= U_EMPTY;                                             // and the two MMA threads
-      mbar_init(bar(b), six ? 6 : (four ? 4 : 1));
+      int count = 1;
+      if (b == O_EMPTY) count = 4;                          // the four softmax warps
+      if (b >= U_EMPTY) count = 6;                          // and the two MMA threads
+      if (b >= S_READY && b < S_READY + kStages) count = 2;  // producer + P V commit
+      if (b >= PV_READY && b < PV_READY + kStages) count = 5;  // producer + four softmax warps
+      mbar_init(bar(b), count);
     }
+    // the buffers start free: arm the first use of every S_READY
+    for (int i = 0; i < kStages; ++i) mbar_arrive(bar(S_READY + i));
     *s_abort = 0;
     fence_barrier_init();
     prefetch_tensormap(&map_qkv);
@@ -226,14 +236,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          load_tile(base + kKOff + st * kTileBytes, K_FULL + st, kcol, x.start + kt * 128, x.r);
-          issued(K_FULL + st, ph);
+          load_tile(base + kKOff + st * kTileBytes, S_READY + st, kcol, x.start + kt * 128, x.r);
+          issued(S_READY + st, ph);
           if (!mbar_wait_bounded(bar(V_EMPTY + st), ph ^ 1, s_abort, timeout)) {
             ok = false;
             break;
           }
-          load_tile(base + kVOff + st * kTileBytes, V_FULL + st, vcol, x.start + kt * 128, x.r);
-          issued(V_FULL + st, ph);
+          load_tile(base + kVOff + st * kTileBytes, PV_READY + st, vcol, x.start + kt * 128, x.r);
+          issued(PV_READY + st, ph);
         }
       }
       if (!ok) {
@@ -250,7 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // softmax warp, so every instruction saved keeps the tensor pipe fed: descriptors
     // are built once, a k-step adds a constant, ring positions advance without division.
     // Ordering between the two goes through mbarriers: S_FULL (S done) -> softmax ->
-    // P_FULL -> P V -> S_EMPTY (buffer free for the S three tiles later).
+    // PV_READY (P written, V in) -> P V -> S_READY (buffer free for the S three tiles
+    // later, with its K).
     if (lane == 0) {
       const bool s_role = warp == kSWarp;
       bool ok = true;
@@ -285,8 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (s_role) {
           if (!wait(Q_FULL, nu & 1)) break;
           for (int j = 0; j < n; ++j) {
-            // the P V that last read this buffer has completed, and K is in
-            if (!wait(S_EMPTY + buf, buf_ph ^ 1u) || !wait(K_FULL + st, st_ph)) break;
+            // K is in and the P V that last read this buffer has completed
+            if (!wait(S_READY + st, st_ph)) break;
             tc_fence_after();
             const uint64_t kd = k_desc0 + (uint64_t)st * kTileDesc;
             const uint32_t d = tmem_base + buf * 128;
@@ -304,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
           for (int j = 0; j < n; ++j) {
-            if (!wait(P_FULL + buf, buf_ph) || !wait(V_FULL + st, st_ph)) break;
+            if (!wait(PV_READY + st, st_ph)) break;  // V is in and P written
             if (j == 0 && !wait(O_EMPTY, (nu & 1) ^ 1)) break;
             tc_fence_after();
             const uint64_t vd = v_desc0 + (uint64_t)st * kTileDesc;
@@ -317,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 1; k < 8; ++k)
               tc_mma_bf16_ta_c<true>(tmem_base + kOCol, pa + k * 8, vd + (uint64_t)(k * (2048 >> 4)), kIdescO);
-            tc_commit(bar(V_EMPTY + st));
-            tc_commit(bar(S_EMPTY + buf));
+            tc_commit(bar(V_EMPTY + st));   // V consumed; O holds this tile (softmax rescale)
+            tc_commit(bar(S_READY + st));   // the buffer's P is consumed
             advance(st, st_ph, kStages);
             advance(buf, buf_ph, kSBufs);
           }
@@ -397,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mx;
           // O holds the products up to the previous key tile: let them land, then scale the row
           const int pj = sc - 1;
-          if (!wait_all(S_EMPTY + pj % kSBufs, (pj / kSBufs) & 1)) break;
+          if (!wait_all(V_EMPTY + pj % kSBufs, (pj / kSBufs) & 1)) break;
           tc_fence_after();
           float o[32];
 #pragma unroll
@@ -428,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_wait_st();      // P, and O as rescaled above, are in tensor memory
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(P_FULL + b));
+        if (lane == 0) mbar_arrive(bar(PV_READY + b));
         ++sc;
       }
       if (!ok || !wait_all(O_DONE, nu & 1)) break;
