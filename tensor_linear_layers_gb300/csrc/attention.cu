@@ -389,16 +389,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (key > q_rel || key >= x.len) s[n] = -INFINITY;
           }
         }
-        // row max and (below) row sum as 8 independent chains: one dependent chain of
-        // 128 operations per tile would leave the warp waiting on its own latency
+        // row max (three-input max) and, below, the exponent and row sum on fp32 pairs:
+        // the softmax issues every instruction of the tile from one warp per
+        // sub-partition, so it is bound by their count. Independent chains (8 for the
+        // max, 4 pairs for the sum) keep it from waiting on its own latency.
         float mk[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) mk[j] = s[j];
+        for (int j = 0; j < 8; ++j) mk[j] = fmaxf(s[j], s[8 + j]);
 #pragma unroll
-        for (int n = 8; n < 128; n += 8)
+        for (int n = 16; n < 128; n += 16)
 #pragma unroll
-          for (int j = 0; j < 8; ++j) mk[j] = fmaxf(mk[j], s[n + j]);
-        float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])), fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
+          for (int j = 0; j < 8; ++j) mk[j] = fmax3(mk[j], s[n + j], s[n + 8 + j]);
+        float mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7]));
         mx *= c;
         if (kt == 0) {
           m = mx;  // the first P V overwrites O
@@ -421,21 +423,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // P = 2^(s c - m) as bf16 pairs into the first 64 columns of the buffer
-        float lk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const uint64_t c2 = f32x2_pack(c, c), nm2 = f32x2_pack(-m, -m);
+        uint64_t lk[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t pk[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float e0 = fast_exp2(fmaf(s[h * 64 + 2 * j], c, -m));
-            const float e1 = fast_exp2(fmaf(s[h * 64 + 2 * j + 1], c, -m));
-            lk[(2 * j) & 7] += e0;
-            lk[(2 * j + 1) & 7] += e1;
+            float x0, x1;
+            f32x2_unpack(f32x2_fma(f32x2_pack(s[h * 64 + 2 * j], s[h * 64 + 2 * j + 1]), c2, nm2), x0, x1);
+            const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+            lk[j & 3] = f32x2_add(lk[j & 3], f32x2_pack(e0, e1));
             pk[j] = pack_bf16x2(e0, e1);
           }
           tmem_st32(sa + h * 32, reinterpret_cast<const float*>(pk));
         }
-        l += ((lk[0] + lk[1]) + (lk[2] + lk[3])) + ((lk[4] + lk[5]) + (lk[6] + lk[7]));
+        float la[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) f32x2_unpack(lk[j], la[2 * j], la[2 * j + 1]);
+        l += ((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7]));
         tc_wait_st();      // P, and O as rescaled above, are in tensor memory
         tc_fence_before();
         __syncwarp();
