@@ -189,6 +189,8 @@ def dominant_kernel_bytes(w: workloads.Workload) -> float:
 
 
 def dominant_kernel_flops(w: workloads.Workload) -> float:
+    if w.kind == "attn_core":
+        return w.flops()
     if w.kind == "mlp":
         return 2.0 * w.T * w.H * 2 * w.I
     return 2.0 * w.T * w.H * (w.nq + 2 * w.nkv) * w.hd
@@ -212,6 +214,19 @@ class OracleSample:
         rng = np.random.default_rng(seed)
         self.rows = min(w.T, rows)
         small = workloads.Workload(**{**w.__dict__, "T": self.rows})
+        if w.kind == "attn_core":
+            # sampled query rows of the packed sequences; a row i of its sequence costs
+            # 4 hd (i + 1) flops per q head
+            self.feat = 0
+            d = workloads.attn_core_inputs(w)
+            self.qkv = d["qkv"]
+            self.cu = d["cu_seqlens"]
+            self.rows = min(d["T"], rows)
+            self.row_ids = np.linspace(0, d["T"] - 1, self.rows).astype(np.int64)
+            starts = self.cu[np.searchsorted(self.cu, self.row_ids, side="right") - 1]
+            self.flops = 4.0 * w.hd * w.nq * float(np.sum(self.row_ids - starts + 1))
+            self.wbytes = 0.0
+            return
         if w.kind == "mlp":
             self.feat = max(8, min(w.I, feat))
             d = workloads.mlp_inputs(small, T=self.rows)
@@ -230,6 +245,9 @@ class OracleSample:
 
     def run(self):
         w, o = self.w, self.oracle
+        if w.kind == "attn_core":
+            o.attention_rows(self.qkv, w.nq, w.nkv, w.hd, w.t, self.cu, self.row_ids)
+            return
         if w.kind == "mlp":
             o.mlp_layer(*self.args, **self.kw)
         else:
@@ -239,7 +257,9 @@ class OracleSample:
 
     def describe(self, n, el):
         w = self.w
-        if w.kind == "mlp":
+        if w.kind == "attn_core":
+            what = f"{self.rows} of {w.T} query rows (evenly spaced) through the causal attention of all {w.nq} q heads"
+        elif w.kind == "mlp":
             what = f"{self.rows} of {w.T} tokens x {self.feat} of {w.I} intermediate features (hidden {w.H})"
         else:
             what = f"{self.rows} of {w.T} tokens through QKV and o_proj"
@@ -275,7 +295,13 @@ def config_obj(w: workloads.Workload, n: int, rotate: int, decode: bool):
         c["fused_add_rmsnorm"] = w.norm
     else:
         c.update({"n_q_heads": w.nq, "n_kv_heads": w.nkv, "head_dim": w.hd})
-    c["l2"] = f"{rotate} rotating weight copies ({rotate * w.weight_bytes() / 1e9:.2f} GB) > 129 MB L2"
+    if w.kind == "attn_core":
+        c["sequences"] = int(len(w.seq_lens()))
+        c["causal"] = True
+        qkv_b = 2 * w.T * (w.nq + 2 * (w.nkv if w.t < w.nkv else w.t)) * w.hd
+        c["l2"] = f"{rotate} rotating qkv inputs ({rotate * qkv_b / 1e9:.2f} GB) > 129 MB L2"
+    else:
+        c["l2"] = f"{rotate} rotating weight copies ({rotate * w.weight_bytes() / 1e9:.2f} GB) > 129 MB L2"
     c["parallelism"] = f"replicas x{n}" if n > 1 else "single GPU (t shards on one GPU)"
     return c
 
@@ -362,6 +388,22 @@ def run_ours(args, ws, rank, local):
             j = i % R
             blocks[j].gate_up(xs[j], h_out=hbufs[j], ws=wss[j])
         hbufs = [torch.empty(w.t, w.T, w.I // w.t, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    elif w.kind == "attn_core":
+        dw = workloads.attn_inputs(w, T=1)
+        cfg = tl.make_config(tl.TP_BLOCK_ATTN_PROJ, w.t, w.H, n_q_heads=w.nq, n_kv_heads=w.nkv, head_dim=w.hd)
+        blocks = [tl.TPLinear(cfg, [dw[k].to(dev) for k in ("w_q", "w_k", "w_v", "w_o")])]
+        dc = workloads.attn_core_inputs(w)
+        cu = torch.from_numpy(dc["cu_seqlens"]).to(dev)
+        max_len = int(np.max(np.diff(dc["cu_seqlens"])))
+        qkvs = [workloads.draw(tuple(dc["qkv"].shape), 1000 + rank * R + r, 6).to(dev) for r in range(R)]
+        aos = [torch.empty(w.t, w.T, w.nq // w.t * w.hd, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        wss = [blocks[0].workspace(w.T)]
+        launches_per_step = 2          # work-table preparation + the attention kernel
+
+        def step(i):
+            j = i % R
+            blocks[0].attention_forward(qkvs[j], cu, max_len, out=aos[j], ws=wss[0])
+        dominant = step
     else:
         d = workloads.attn_inputs(w)
         cfg = tl.make_config(tl.TP_BLOCK_ATTN_PROJ, w.t, w.H, n_q_heads=w.nq, n_kv_heads=w.nkv, head_dim=w.hd)
@@ -417,8 +459,8 @@ def run_ours(args, ws, rank, local):
     # ---- dominant kernel: in decode the step is a single fused kernel, so its
     # average launch duration is the timed region's per-step time; otherwise the
     # column-parallel GEMM alone, same stream, events around K2 launches
-    if launches_per_step == 1:
-        dom_s = sec
+    if launches_per_step == 1 or w.kind == "attn_core":
+        dom_s = sec                    # attention core: both launches of a step (conservative)
     else:
         K2 = min(K, 2000 if decode else 20)
         for i in range(3):
@@ -449,6 +491,17 @@ def run_ours(args, ws, rank, local):
             blocks[j].mlp_forward(xs[j], residual=rs[j], out=outs[j], ws=wss[j])
             for k, v in outs[j].items():
                 ho[j][k].copy_(v, non_blocking=True)
+    elif w.kind == "attn_core":
+        hq = [qkvs[j].cpu().pin_memory() for j in range(R)]
+        ho = [torch.empty(aos[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
+        h2d = hq[0].numel() * 2
+        d2h = ho[0].numel() * 2
+
+        def e2e_step(i):
+            j = i % R
+            qkvs[j].copy_(hq[j], non_blocking=True)
+            blocks[0].attention_forward(qkvs[j], cu, max_len, out=aos[j], ws=wss[0])
+            ho[j].copy_(aos[j], non_blocking=True)
     else:
         hx = [xs[j].cpu().pin_memory() for j in range(R)]
         hA = [As[j].cpu().pin_memory() for j in range(R)]
@@ -500,14 +553,19 @@ def run_ours(args, ws, rank, local):
         unit = "TFLOP/s"
         value = ws * flops / sec / 1e12
         e2e_value = ws * flops / e2e_s / 1e12
-        whole = launches_per_step == 1
+        whole = launches_per_step == 1 or w.kind == "attn_core"
         dom_alg = flops if whole else dominant_kernel_flops(w)
         achieved = dom_alg / dom_s / 1e12
+        if w.kind == "attn_core":
+            key, kname = "attn_core@", "causal GQA attention (attn_fwd_kernel, with its work-table preparation)"
+        elif whole:
+            key, kname = "attn_proj@", "QKV + o_proj in one launch (tc_gemm_pair_kernel<COL, ROW>)"
+        else:
+            key, kname = "gate_up@", "gate_up column-parallel GEMM (tc_gemm_pair_kernel<GATE_UP>)"
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / pk["bf16_tflops"],
-                "traffic": ncu_traffic(("attn_proj@" if whole else "gate_up@") + w.name),
-                "kernel": ("QKV + o_proj in one launch (tc_gemm_pair_kernel<COL, ROW>)" if whole
-                           else "gate_up column-parallel GEMM (tc_gemm_pair_kernel<GATE_UP>)"),
+                "traffic": ncu_traffic(key + w.name),
+                "kernel": kname,
                 "algorithmic_flops_per_launch": dom_alg, "avg_launch_us": dom_s * 1e6,
                 "peak_source": pk["source"] + " bf16_tflops (cuBLAS burst)"}
 
