@@ -23,7 +23,9 @@ Sources, cited by page title and section throughout:
 ``attention.py`` holds the attention core between the QKV projection and
 o_proj (causal, GQA, sequences packed by offsets); the pages describe it
 only as attention over each rank's own heads, so it is the textbook
-scaled dot-product attention in their head layout.
+scaled dot-product attention in their head layout. ``decoder_layer.py``
+chains the steps into one decoder layer (input norm, QKV, attention, o_proj,
+add + norm, MLP) in the order the pages give.
 
 Every function computes in float64 from bf16 inputs converted exactly. Where
 the block has a plain definition (the unsharded Y = XW, SiLU, RMSNorm, row
@@ -43,3 +45,4 @@ from .tp_block import (  # noqa: F401
 )
 from .capture import capture_rows, pack_key  # noqa: F401
 from .attention import attention_core, attention_rows, kv_head_of  # noqa: F401
+from .decoder_layer import decoder_layer  # noqa: F401
