@@ -191,7 +191,7 @@ def dominant_kernel_bytes(w: workloads.Workload) -> float:
 def dominant_kernel_flops(w: workloads.Workload) -> float:
     if w.kind == "attn_core":
         return w.flops()
-    if w.kind == "mlp":
+    if w.kind in ("mlp", "layer"):
         return 2.0 * w.T * w.H * 2 * w.I
     return 2.0 * w.T * w.H * (w.nq + 2 * w.nkv) * w.hd
 
@@ -227,6 +227,19 @@ class OracleSample:
             self.flops = 4.0 * w.hd * w.nq * float(np.sum(self.row_ids - starts + 1))
             self.wbytes = 0.0
             return
+        if w.kind == "layer":
+            # the first `rows` tokens: under causal attention they depend on no later
+            # token, so the sample is an exact prefix of the whole step's work
+            self.feat = 0
+            d = workloads.layer_inputs(w, T=self.rows)
+            cu_full = np.concatenate([[0], np.cumsum(w.seq_lens())])
+            self.cu = np.array([c for c in cu_full if c < self.rows] + [self.rows], np.int64)
+            self.args = d
+            L = np.diff(self.cu).astype(np.float64)
+            self.flops = (small.proj_flops() + small.mlp_flops()
+                          + 4.0 * w.hd * w.nq * float(np.sum(L * (L + 1) / 2)))
+            self.wbytes = float(w.weight_bytes())
+            return
         if w.kind == "mlp":
             self.feat = max(8, min(w.I, feat))
             d = workloads.mlp_inputs(small, T=self.rows)
@@ -248,6 +261,12 @@ class OracleSample:
         if w.kind == "attn_core":
             o.attention_rows(self.qkv, w.nq, w.nkv, w.hd, w.t, self.cu, self.row_ids)
             return
+        if w.kind == "layer":
+            d = self.args
+            o.decoder_layer(d["hidden"], d["residual"], d["gamma_attn"], d["w_q"], d["w_k"], d["w_v"], d["w_o"],
+                            d["gamma_mlp"], d["w_gate"], d["w_up"], d["w_down"], w.nq, w.nkv, w.hd, w.t,
+                            self.cu, w.eps)
+            return
         if w.kind == "mlp":
             o.mlp_layer(*self.args, **self.kw)
         else:
@@ -259,6 +278,9 @@ class OracleSample:
         w = self.w
         if w.kind == "attn_core":
             what = f"{self.rows} of {w.T} query rows (evenly spaced) through the causal attention of all {w.nq} q heads"
+        elif w.kind == "layer":
+            what = (f"the first {self.rows} of {w.T} tokens ({len(self.cu) - 1} sequence(s)) through the whole "
+                    f"layer: norm, QKV, causal attention, o_proj, add + norm, MLP")
         elif w.kind == "mlp":
             what = f"{self.rows} of {w.T} tokens x {self.feat} of {w.I} intermediate features (hidden {w.H})"
         else:
@@ -295,11 +317,18 @@ def config_obj(w: workloads.Workload, n: int, rotate: int, decode: bool):
         c["fused_add_rmsnorm"] = w.norm
     else:
         c.update({"n_q_heads": w.nq, "n_kv_heads": w.nkv, "head_dim": w.hd})
+    if w.kind == "layer":
+        c["intermediate"] = w.I
+        c["sequences"] = int(len(w.seq_lens()))
+        c["causal"] = True
     if w.kind == "attn_core":
         c["sequences"] = int(len(w.seq_lens()))
         c["causal"] = True
         qkv_b = 2 * w.T * (w.nq + 2 * (w.nkv if w.t < w.nkv else w.t)) * w.hd
         c["l2"] = f"{rotate} rotating qkv inputs ({rotate * qkv_b / 1e9:.2f} GB) > 129 MB L2"
+    elif w.kind == "layer":
+        c["l2"] = (f"weights {w.weight_bytes() / 1e9:.2f} GB and the step's intermediates "
+                   f"(h alone {2 * w.T * w.I / 1e9:.2f} GB) > 129 MB L2; {rotate} rotating inputs")
     else:
         c["l2"] = f"{rotate} rotating weight copies ({rotate * w.weight_bytes() / 1e9:.2f} GB) > 129 MB L2"
     c["parallelism"] = f"replicas x{n}" if n > 1 else "single GPU (t shards on one GPU)"
@@ -388,6 +417,38 @@ def run_ours(args, ws, rank, local):
             j = i % R
             blocks[j].gate_up(xs[j], h_out=hbufs[j], ws=wss[j])
         hbufs = [torch.empty(w.t, w.T, w.I // w.t, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    elif w.kind == "layer":
+        d = workloads.layer_inputs(w, T=1)
+        ca = tl.make_config(tl.TP_BLOCK_ATTN_PROJ, w.t, w.H, n_q_heads=w.nq, n_kv_heads=w.nkv, head_dim=w.hd,
+                            rms_eps=w.eps, flags=tl.TP_FLAG_HAS_NORM)
+        cm = tl.make_config(tl.TP_BLOCK_MLP, w.t, w.H, w.I, rms_eps=w.eps, flags=tl.TP_FLAG_HAS_NORM)
+        attn_b = tl.TPLinear(ca, [d[k].to(dev) for k in ("w_q", "w_k", "w_v", "w_o")],
+                             gamma=d["gamma_attn"].to(dev))
+        mlp_b = tl.TPLinear(cm, [d[k].to(dev) for k in ("w_gate", "w_up", "w_down")],
+                            gamma=d["gamma_mlp"].to(dev))
+        del d
+        layer = tl.TPLayer(attn_b, mlp_b, w.T)
+        blocks = [attn_b, mlp_b]
+        lens = w.seq_lens()
+        cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).to(dev)
+        max_len = int(np.max(lens))
+        xs = [workloads.draw((w.T, w.H), 1000 + rank * R + r, 0).to(dev) for r in range(R)]
+        rs = [workloads.draw((w.T, w.H), 1000 + rank * R + r, 1).to(dev) for r in range(R)]
+        outs = [{k: torch.empty_like(xs[0]) for k in ("residual_attn", "attn_out", "residual_mlp", "mlp_out",
+                                                     "residual_stream")} for _ in range(R)]
+        wss = [layer.workspace()]
+        # norm, QKV, attention (2), o_proj, then the MLP: norm + gate_up + down, or one fused kernel
+        launches_per_step = 5 + (1 if w.T <= 128 else 3)
+        hbufs = [torch.empty(w.t, w.T, w.I // w.t, dtype=torch.bfloat16, device=dev)]
+        gws = mlp_b.workspace(w.T)
+
+        def step(i):
+            j = i % R
+            layer.forward(xs[j], rs[j], cu, max_len, out=outs[j], ws=wss[0])
+
+        def dominant(i):
+            j = i % R
+            mlp_b.gate_up(xs[j], h_out=hbufs[0], ws=gws)
     elif w.kind == "attn_core":
         dw = workloads.attn_inputs(w, T=1)
         cfg = tl.make_config(tl.TP_BLOCK_ATTN_PROJ, w.t, w.H, n_q_heads=w.nq, n_kv_heads=w.nkv, head_dim=w.hd)
@@ -434,7 +495,7 @@ def run_ours(args, ws, rank, local):
     for i in range(W):
         step(i)
     torch.cuda.synchronize()
-    for b, wsb in zip(blocks, wss):
+    for wsb in wss:
         st = int(wsb[:4].view(torch.int32).item())
         if st != 0:
             raise RuntimeError(f"device status {st} after warm-up")
@@ -491,6 +552,22 @@ def run_ours(args, ws, rank, local):
             blocks[j].mlp_forward(xs[j], residual=rs[j], out=outs[j], ws=wss[j])
             for k, v in outs[j].items():
                 ho[j][k].copy_(v, non_blocking=True)
+    elif w.kind == "layer":
+        hx = [xs[j].cpu().pin_memory() for j in range(R)]
+        hr = [rs[j].cpu().pin_memory() for j in range(R)]
+        # the layer's result as the next layer takes it: (hidden = mlp_out, residual = r2)
+        hm = [torch.empty(xs[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
+        hres = [torch.empty(xs[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
+        h2d = 2 * hx[0].numel() * 2
+        d2h = 2 * hm[0].numel() * 2
+
+        def e2e_step(i):
+            j = i % R
+            xs[j].copy_(hx[j], non_blocking=True)
+            rs[j].copy_(hr[j], non_blocking=True)
+            layer.forward(xs[j], rs[j], cu, max_len, out=outs[j], ws=wss[0])
+            hm[j].copy_(outs[j]["mlp_out"], non_blocking=True)
+            hres[j].copy_(outs[j]["residual_mlp"], non_blocking=True)
     elif w.kind == "attn_core":
         hq = [qkvs[j].cpu().pin_memory() for j in range(R)]
         ho = [torch.empty(aos[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
@@ -529,7 +606,7 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(f0.elapsed_time(f1) / K3, ws) / 1e3
 
-    for b, wsb in zip(blocks, wss):
+    for wsb in wss:
         st = int(wsb[:4].view(torch.int32).item())
         if st != 0:
             raise RuntimeError(f"device status {st} after the timed region")
@@ -558,6 +635,8 @@ def run_ours(args, ws, rank, local):
         achieved = dom_alg / dom_s / 1e12
         if w.kind == "attn_core":
             key, kname = "attn_core@", "causal GQA attention (attn_fwd_kernel, with its work-table preparation)"
+        elif w.kind == "layer":
+            key, kname = "gate_up@", "the layer's gate_up column-parallel GEMM (tc_gemm_pair_kernel<GATE_UP>)"
         elif whole:
             key, kname = "attn_proj@", "QKV + o_proj in one launch (tc_gemm_pair_kernel<COL, ROW>)"
         else:

@@ -54,7 +54,8 @@ typedef struct tp_linear tp_linear_t; /* opaque handle: shapes, plans, packed-we
 typedef void* tp_stream_t;            /* cudaStream_t */
 
 enum { TP_BLOCK_MLP = 0, TP_BLOCK_ATTN_PROJ = 1 };
-enum { TP_FLAG_HAS_NORM = 1 };        /* MLP: fused residual add + RMSNorm in front of gate_up */
+enum { TP_FLAG_HAS_NORM = 1 };        /* MLP: fused residual add + RMSNorm in front of gate_up;
+                                         ATTN: the handle carries the layer's input RMSNorm */
 
 typedef struct {
   int32_t kind;          /* TP_BLOCK_MLP or TP_BLOCK_ATTN_PROJ */
@@ -64,7 +65,7 @@ typedef struct {
   int32_t n_q_heads;     /* ATTN: nq % t == 0 */
   int32_t n_kv_heads;    /* ATTN: nkv % t == 0, or t % nkv == 0 (kv heads replicated) */
   int32_t head_dim;      /* ATTN: hd % 8 == 0 */
-  float rms_eps;         /* MLP with TP_FLAG_HAS_NORM */
+  float rms_eps;         /* with TP_FLAG_HAS_NORM */
   int32_t flags;         /* TP_FLAG_* */
   int32_t reserved;      /* must be 0 */
 } tp_config_t;
@@ -92,7 +93,8 @@ int tp_packed_weight_bytes(const tp_config_t* cfg, int64_t* col_bytes, int64_t* 
  * `stream`) and return a handle. w_full: MLP {W_gate [I,H], W_up [I,H],
  * W_down [H,I]}, n_w = 3; ATTN {W_q [nq*hd,H], W_k [nkv*hd,H], W_v [nkv*hd,H],
  * W_o [H,nq*hd]}, n_w = 4. gamma: RMSNorm weight [H] bf16 (MLP with
- * TP_FLAG_HAS_NORM), else NULL. The handle borrows w_col_packed, w_row_packed
+ * TP_FLAG_HAS_NORM; ATTN with TP_FLAG_HAS_NORM: the layer's input_layernorm,
+ * used by tp_decoder_layer_forward), else NULL. The handle borrows w_col_packed, w_row_packed
  * and gamma for its lifetime; w_full may be freed once `stream` has passed the
  * packing. The shard count follows divide(): a remainder is TP_ERR_SHAPE.
  */
@@ -156,7 +158,7 @@ int tp_mlp_forward_no_alloc(tp_linear_t* h, int64_t T, const void* x_in, const v
 
 /*
  * The steps of tp_mlp_forward, one call each (same semantics, same kernels):
- *   tp_add_rms_norm : residual_out = a + residual_in; x_out = RMSNorm(residual_out) * gamma.
+ *   tp_add_rms_norm : residual_out = a + residual_in (NULL: a); x_out = RMSNorm(residual_out) * gamma.
  *                     a, residual_in, residual_out, x_out [T, H]; gamma [H]. Any H % 8 == 0.
  *   tp_gate_up_forward: h_out [t][T][I/t] = silu(x W_gate,r^T) * (x W_up,r^T) per shard r.
  *   tp_down_forward : mlp_out = sum_r h_in[r] W_down,r^T; residual_stream = mlp_out + residual.
@@ -204,6 +206,52 @@ int tp_attn_proj_forward(tp_linear_t* h, int64_t T, const void* x, void* qkv_out
 int tp_attention_forward(tp_linear_t* h, int64_t T, const void* qkv, const int32_t* cu_seqlens,
                          int32_t n_seqs, int32_t max_seqlen, void* attn_out, void* workspace,
                          int64_t workspace_bytes, tp_stream_t stream);
+
+/*
+ * One whole decoder layer, in the order "vLLM Code Reading (Section 5)" §13-§14
+ * gives (QKV split by head, attention on each shard's heads, o_proj reduced, then
+ * the MLP) with the fused add + norm of "Tensor & pipeline parallelism"
+ * (residual_stream; the attn_out and mlp_out hook points):
+ *   r1 = hidden_in + residual_in          (residual_in NULL: r1 = hidden_in, a first layer)
+ *   x1 = RMSNorm(r1) * gamma_attn         (input_layernorm: the attention handle's gamma and eps)
+ *   qkv = x1 [Wq_r; Wk_r; Wv_r]^T          (per shard, as tp_attn_proj_forward)
+ *   A   = attention core                  (as tp_attention_forward, over cu_seqlens)
+ *   attn_out = sum_r A_r Wo_r^T            (o_proj, reduced on chip)
+ *   r2 = attn_out + r1; x2 = RMSNorm(r2) * gamma_mlp   (the MLP handle's norm)
+ *   mlp_out = sum_r h_r Wdown_r^T, h_r = silu(x2 Wg_r^T) * (x2 Wu_r^T)
+ *   residual_stream = mlp_out + r2        (if residual_stream != NULL)
+ * Every intermediate is rounded to bf16, as between separate calls.
+ *
+ * tp_layer_create binds an attention handle and an MLP handle, both created with
+ * TP_FLAG_HAS_NORM, of the same hidden size, on the current device, head_dim 128;
+ * it borrows both for its lifetime (destroy the layer first). max_tokens fixes the
+ * workspace layout: every call takes T <= max_tokens. The workspace
+ * (tp_layer_workspace_size bytes, caller-owned, ZERO-FILLED before first use)
+ * holds both halves' working storage and the intermediates x1, qkv and A; bytes
+ * [0, 4) are the status word of every kernel of the layer (TP_ERR_SHAPE for bad
+ * offsets, TP_ERR_TIMEOUT for a wait that gave up). Pointers in io: [T, H] bf16
+ * device tensors, 16-byte aligned; cu_seqlens as for tp_attention_forward. All
+ * host-side checks run before anything is enqueued.
+ */
+typedef struct tp_layer tp_layer_t;
+typedef struct {
+  const void* hidden_in;      /* [T, H] hidden states entering the layer */
+  const void* residual_in;    /* [T, H] or NULL */
+  const int32_t* cu_seqlens;  /* device int32 [n_seqs + 1] */
+  int32_t n_seqs;
+  int32_t max_seqlen;         /* host: >= every sequence length, <= T */
+  void* residual_attn;        /* out r1 [T, H] */
+  void* attn_out;             /* out [T, H] */
+  void* residual_mlp;         /* out r2 [T, H] */
+  void* mlp_out;              /* out [T, H] */
+  void* residual_stream;      /* out [T, H] or NULL */
+} tp_layer_io_t;
+
+int tp_layer_create(tp_linear_t* attn, tp_linear_t* mlp, int64_t max_tokens, tp_layer_t** out);
+int tp_layer_destroy(tp_layer_t* layer);
+int tp_layer_workspace_size(const tp_layer_t* layer, int64_t* bytes);
+int tp_decoder_layer_forward(tp_layer_t* layer, int64_t T, const tp_layer_io_t* io, void* workspace,
+                             int64_t workspace_bytes, tp_stream_t stream);
 
 /*
  * Activation capture ("Tensor & pipeline parallelism": What the adapter hooks,

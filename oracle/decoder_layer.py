@@ -29,12 +29,12 @@ from __future__ import annotations
 
 import numpy as np
 
-from .attention import _as_f64, attention_core
+from .attention import _as_f64, attention_core, attention_rows
 from .tp_block import add_rms_norm, mlp_block, o_proj_parallel, qkv_parallel, rms_norm
 
 
 def decoder_layer(hidden, residual, gamma_attn, w_q, w_k, w_v, w_o, gamma_mlp, w_gate, w_up, w_down,
-                  nq: int, nkv: int, hd: int, t: int, cu_seqlens, eps: float = 1e-5) -> dict:
+                  nq: int, nkv: int, hd: int, t: int, cu_seqlens, eps: float = 1e-5, rows=None) -> dict:
     """The tensors of one decoder layer: residual_attn (r1), attn_out, residual_mlp (r2),
     mlp_out, residual_stream, plus the shard-major intermediates qkv and attn (A).
 
@@ -42,6 +42,11 @@ def decoder_layer(hidden, residual, gamma_attn, w_q, w_k, w_v, w_o, gamma_mlp, w
     hidden, residual [T, H]; gamma_attn, gamma_mlp [H]; w_q [nq*hd, H], w_k, w_v [nkv*hd, H],
     w_o [H, nq*hd], w_gate, w_up [I, H], w_down [H, I] (stored [out, in]); cu_seqlens
     [n_seqs + 1] token offsets of the packed sequences.
+
+    ``rows``: compute the outputs of those token rows only. Keys and values need
+    every earlier token of a row's sequence, so r1, x1 and qkv are computed for all
+    tokens; everything after the attention is per row. ``qkv`` is then still
+    [t, T, w_s] and every other tensor has len(rows) rows.
     """
     f = _as_f64
     hid = f(hidden)
@@ -51,7 +56,13 @@ def decoder_layer(hidden, residual, gamma_attn, w_q, w_k, w_v, w_o, gamma_mlp, w
     else:
         x1, r1 = add_rms_norm(hid, f(residual), f(gamma_attn), eps)
     qkv = qkv_parallel(x1, f(w_q), f(w_k), f(w_v), nq, nkv, hd, t)
-    attn = attention_core(qkv, nq, nkv, hd, t, np.asarray(cu_seqlens, np.int64))
+    cu = np.asarray(cu_seqlens, np.int64)
+    if rows is None:
+        attn = attention_core(qkv, nq, nkv, hd, t, cu)
+    else:
+        rows = np.asarray(rows, np.int64)
+        attn = attention_rows(qkv, nq, nkv, hd, t, cu, rows)
+        r1 = r1[rows]
     attn_out = o_proj_parallel(attn, f(w_o), t)
     x2, r2 = add_rms_norm(attn_out, r1, f(gamma_mlp), eps)
     mlp_out = mlp_block(x2, f(w_gate), f(w_up), f(w_down))

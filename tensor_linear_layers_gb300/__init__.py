@@ -28,6 +28,7 @@ ABI_SYMBOLS = (
     "tp_mlp_forward", "tp_add_rms_norm", "tp_gate_up_forward", "tp_down_forward",
     "tp_attn_proj_forward", "tp_capture_workspace_size", "tp_capture_rows", "tp_last_error",
     "tp_describe_plan", "tp_mlp_forward_no_alloc", "tp_set_wait_timeout", "tp_attention_forward",
+    "tp_layer_create", "tp_layer_destroy", "tp_layer_workspace_size", "tp_decoder_layer_forward",
 )
 
 
@@ -42,6 +43,14 @@ class Config(ctypes.Structure):
                 ("intermediate", ctypes.c_int64), ("n_q_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("rms_eps", ctypes.c_float), ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class LayerIO(ctypes.Structure):
+    _fields_ = [("hidden_in", ctypes.c_void_p), ("residual_in", ctypes.c_void_p),
+                ("cu_seqlens", ctypes.c_void_p), ("n_seqs", ctypes.c_int32), ("max_seqlen", ctypes.c_int32),
+                ("residual_attn", ctypes.c_void_p), ("attn_out", ctypes.c_void_p),
+                ("residual_mlp", ctypes.c_void_p), ("mlp_out", ctypes.c_void_p),
+                ("residual_stream", ctypes.c_void_p)]
 
 
 class GemmPlan(ctypes.Structure):
@@ -81,6 +90,10 @@ def lib() -> ctypes.CDLL:
         "tp_mlp_forward_no_alloc": [P, I64, P, P, P, P, P, P, P],
         "tp_set_wait_timeout": [I64],
         "tp_attention_forward": [P, I64, P, P, I32, I32, P, P, I64, P],
+        "tp_layer_create": [P, P, I64, ctypes.POINTER(P)],
+        "tp_layer_destroy": [P],
+        "tp_layer_workspace_size": [P, PI64],
+        "tp_decoder_layer_forward": [P, I64, ctypes.POINTER(LayerIO), P, I64, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -291,12 +304,66 @@ class TPLinear:
         return out
 
 
-def add_rms_norm(a: torch.Tensor, residual: torch.Tensor, gamma: torch.Tensor, eps: float,
+class TPLayer:
+    """One decoder layer (tp_decoder_layer_forward) over an attention handle and an
+    MLP handle, both created with TP_FLAG_HAS_NORM (the input and post-attention
+    norms). The handles must outlive this object."""
+
+    def __init__(self, attn: TPLinear, mlp: TPLinear, max_tokens: int):
+        self.attn, self.mlp, self.max_tokens = attn, mlp, max_tokens
+        h = ctypes.c_void_p()
+        _check(lib().tp_layer_create(attn.handle, mlp.handle, max_tokens, ctypes.byref(h)))
+        self.handle = h
+        b = ctypes.c_int64()
+        _check(lib().tp_layer_workspace_size(h, ctypes.byref(b)))
+        self.workspace_bytes = b.value
+        self._ws = None
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            lib().tp_layer_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def workspace(self) -> torch.Tensor:
+        if self._ws is None:
+            self._ws = torch.zeros(self.workspace_bytes, dtype=torch.uint8, device=self.attn.w_col.device)
+        return self._ws
+
+    def forward(self, hidden: torch.Tensor, residual: Optional[torch.Tensor], cu_seqlens: torch.Tensor,
+                max_seqlen: int, out: Optional[dict] = None, residual_stream: bool = True, ws=None,
+                stream=None) -> dict:
+        """Returns {residual_attn, attn_out, residual_mlp, mlp_out[, residual_stream]}, each [T, H]."""
+        T = hidden.shape[0]
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+            raise TypeError("cu_seqlens must be an int32 CUDA tensor")
+        o = out if out is not None else {}
+        for k in ("residual_attn", "attn_out", "residual_mlp", "mlp_out") + (
+                ("residual_stream",) if residual_stream else ()):
+            if k not in o:
+                o[k] = torch.empty_like(hidden)
+        io = LayerIO(_bf16(hidden, "hidden").data_ptr(),
+                     None if residual is None else _bf16(residual, "residual").data_ptr(),
+                     cu_seqlens.data_ptr(), cu_seqlens.numel() - 1, int(max_seqlen),
+                     o["residual_attn"].data_ptr(), o["attn_out"].data_ptr(), o["residual_mlp"].data_ptr(),
+                     o["mlp_out"].data_ptr(), o["residual_stream"].data_ptr() if "residual_stream" in o else None)
+        ws = self.workspace() if ws is None else ws
+        _check(lib().tp_decoder_layer_forward(self.handle, T, ctypes.byref(io), _ptr(ws), ws.numel(),
+                                              _stream(stream)))
+        return o
+
+
+def add_rms_norm(a: torch.Tensor, residual: Optional[torch.Tensor], gamma: torch.Tensor, eps: float,
                  residual_out=None, x_out=None, stream=None):
     T, H = a.shape
     residual_out = torch.empty_like(a) if residual_out is None else residual_out
     x_out = torch.empty_like(a) if x_out is None else x_out
-    _check(lib().tp_add_rms_norm(T, H, _ptr(_bf16(a, "a")), _ptr(_bf16(residual, "residual")),
+    _check(lib().tp_add_rms_norm(T, H, _ptr(_bf16(a, "a")), None if residual is None else _ptr(_bf16(residual, "residual")),
                                  _ptr(_bf16(gamma, "gamma")), eps, _ptr(residual_out), _ptr(x_out),
                                  _stream(stream)))
     return x_out, residual_out

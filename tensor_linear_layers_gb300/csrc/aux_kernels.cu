@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(kNormThreads)
   const int nvec = H >> 3;
   const size_t roff = (size_t)row * H;
   const uint4* av = reinterpret_cast<const uint4*>(a + roff);
-  const uint4* rv = reinterpret_cast<const uint4*>(res + roff);
+  const uint4* rv = res != nullptr ? reinterpret_cast<const uint4*>(res + roff) : nullptr;
   uint4* ro = reinterpret_cast<uint4*>(res_out + roff);
   float r[kNormMaxVec][8];
   float ss = 0.f;
@@ -53,9 +53,11 @@ __global__ void __launch_bounds__(kNormThreads)
     if (v < nvec) {
       float fa[8], fr[8];
       bf16x8_to_f32(__ldg(av + v), fa);
-      bf16x8_to_f32(__ldg(rv + v), fr);
+      if (res != nullptr) {  // no residual (a model's first layer): r = a
+        bf16x8_to_f32(__ldg(rv + v), fr);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) fa[i] += fr[i];
+        for (int i = 0; i < 8; ++i) fa[i] += fr[i];
+      }
       const uint4 packed = f32_to_bf16x8(fa);
       ro[v] = packed;
       bf16x8_to_f32(packed, r[k]);  // the stored (bf16) residual is what gets normalised

@@ -135,6 +135,15 @@ constexpr int64_t kCaptureOff = 256;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per on-chip wait
 std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
 
+// A decoder-layer call runs the MLP half in its own part of the layer's
+// workspace; while it enqueues, every kernel it launches writes device errors
+// to the layer's status word instead of that part's own first word.
+thread_local int* t_status = nullptr;
+struct StatusRedirect {
+  explicit StatusRedirect(int* s) { t_status = s; }
+  ~StatusRedirect() { t_status = nullptr; }
+};
+
 }  // namespace
 
 // ============================================================================ handle
@@ -323,7 +332,7 @@ GemmParams base_params(const Plan& pl, int64_t T, void* ws, int64_t part_off, in
   char* w = static_cast<char*>(ws);
   p.partials = reinterpret_cast<float*>(w + part_off);
   p.gbar = reinterpret_cast<unsigned*>(w + gbar_off);
-  p.status = reinterpret_cast<int*>(w);
+  p.status = t_status != nullptr ? t_status : reinterpret_cast<int*>(w);
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   return p;
 }
@@ -460,11 +469,6 @@ int validate_cfg(const tp_config_t* c) {
                   (long long)c->intermediate, c->t);
     if ((c->intermediate / c->t) % 8 != 0)
       return fail(TP_ERR_UNSUPPORTED, "intermediate / t must be a multiple of 8");
-    if (c->flags & ~TP_FLAG_HAS_NORM) return fail(TP_ERR_ARG, "unknown flags 0x%x", c->flags);
-    if ((c->flags & TP_FLAG_HAS_NORM) && !(c->rms_eps >= 0.0f))
-      return fail(TP_ERR_ARG, "rms_eps must be >= 0");
-    if ((c->flags & TP_FLAG_HAS_NORM) && c->hidden > max_norm_hidden())
-      return fail(TP_ERR_UNSUPPORTED, "hidden > %d with the fused norm", max_norm_hidden());
   } else {
     if (c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0)
       return fail(TP_ERR_SHAPE, "head counts must be positive");
@@ -475,8 +479,12 @@ int validate_cfg(const tp_config_t* c) {
     if (c->n_q_heads % c->n_kv_heads != 0)
       return fail(TP_ERR_SHAPE, "n_q_heads must be a multiple of n_kv_heads");
     if (c->head_dim % 8 != 0) return fail(TP_ERR_UNSUPPORTED, "head_dim must be a multiple of 8");
-    if (c->flags != 0) return fail(TP_ERR_ARG, "flags must be 0 for the attention projections");
   }
+  if (c->flags & ~TP_FLAG_HAS_NORM) return fail(TP_ERR_ARG, "unknown flags 0x%x", c->flags);
+  if ((c->flags & TP_FLAG_HAS_NORM) && !(c->rms_eps >= 0.0f))
+    return fail(TP_ERR_ARG, "rms_eps must be >= 0");
+  if ((c->flags & TP_FLAG_HAS_NORM) && c->hidden > max_norm_hidden())
+    return fail(TP_ERR_UNSUPPORTED, "hidden > %d with the fused norm", max_norm_hidden());
   return TP_OK;
 }
 
@@ -548,7 +556,7 @@ int tp_linear_create(const tp_config_t* cfg, const void* const* w_full, int32_t 
   for (int i = 0; i < need; ++i) TP_CHECK_PTR(w_full[i], "w_full[i]");
   TP_CHECK_PTR(w_col_packed, "w_col_packed");
   TP_CHECK_PTR(w_row_packed, "w_row_packed");
-  if (mlp && (cfg->flags & TP_FLAG_HAS_NORM)) TP_CHECK_PTR(gamma, "gamma");
+  if (cfg->flags & TP_FLAG_HAS_NORM) TP_CHECK_PTR(gamma, "gamma");
 
   tp_linear* h = new (std::nothrow) tp_linear();
   if (h == nullptr) return fail(TP_ERR_ARG, "out of host memory");
@@ -556,7 +564,7 @@ int tp_linear_create(const tp_config_t* cfg, const void* const* w_full, int32_t 
   derive(h);
   h->w_col = w_col_packed;
   h->w_row = w_row_packed;
-  h->gamma = (mlp && (cfg->flags & TP_FLAG_HAS_NORM)) ? gamma : nullptr;
+  h->gamma = (cfg->flags & TP_FLAG_HAS_NORM) ? gamma : nullptr;
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->nsm, cudaDevAttrMultiProcessorCount, h->device);
   if (e != cudaSuccess) {
@@ -652,7 +660,7 @@ int tp_add_rms_norm(int64_t T, int64_t H, const void* a, const void* residual_in
   if (!(eps >= 0.0f)) return fail(TP_ERR_ARG, "eps must be >= 0");
   if (T == 0) return ok();
   TP_CHECK_PTR(a, "a");
-  TP_CHECK_PTR(residual_in, "residual_in");
+  if (residual_in != nullptr) TP_CHECK_PTR(residual_in, "residual_in");
   TP_CHECK_PTR(gamma, "gamma");
   TP_CHECK_PTR(residual_out, "residual_out");
   TP_CHECK_PTR(x_out, "x_out");
@@ -845,7 +853,7 @@ int tp_attention_forward(tp_linear_t* h, int64_t T, const void* qkv, const int32
   p.n_pairs = reinterpret_cast<const int*>(ws + dyn_off(h) + 256);
   p.next_unit = reinterpret_cast<int*>(ws + dyn_off(h) + 260);
   p.out = static_cast<__nv_bfloat16*>(attn_out);
-  p.status = reinterpret_cast<int*>(ws);
+  p.status = t_status != nullptr ? t_status : reinterpret_cast<int*>(ws);
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   p.T = (int)T;
   p.q_per = h->q_per;
@@ -1074,6 +1082,116 @@ int tp_capture_rows(int64_t T, int64_t H, const int32_t* row_req, const int32_t*
       reinterpret_cast<int32_t*>(ws + c.rows), reinterpret_cast<int32_t*>(ws + c.n_match),
       reinterpret_cast<int*>(ws), copy_grid, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "capture launch");
+  return ok();
+}
+
+}  // extern "C"
+
+// ============================================================================ decoder layer
+// One layer = the attention handle's half, then the MLP handle's half, on one
+// stream. The workspace layout is fixed by max_tokens: the attention half's
+// workspace from byte 0 (its status word is the layer's), the MLP half's, then
+// x1 [T][H], qkv [t][T][w_s] and the attention output A [t][T][nq*hd/t].
+struct tp_layer {
+  tp_linear* attn;
+  tp_linear* mlp;
+  int64_t max_tokens;
+  int64_t attn_ws, mlp_off, mlp_ws, x1_off, qkv_off, a_off, total;
+};
+
+extern "C" {
+
+int tp_layer_create(tp_linear_t* attn, tp_linear_t* mlp, int64_t max_tokens, tp_layer_t** out) {
+  if (out == nullptr) return fail(TP_ERR_ARG, "out is null");
+  *out = nullptr;
+  if (attn == nullptr || mlp == nullptr) return fail(TP_ERR_ARG, "handle is null");
+  if (attn->cfg.kind != TP_BLOCK_ATTN_PROJ) return fail(TP_ERR_ARG, "first handle is not an attention handle");
+  if (mlp->cfg.kind != TP_BLOCK_MLP) return fail(TP_ERR_ARG, "second handle is not an MLP handle");
+  if (!(attn->cfg.flags & TP_FLAG_HAS_NORM) || !(mlp->cfg.flags & TP_FLAG_HAS_NORM))
+    return fail(TP_ERR_ARG, "both handles need TP_FLAG_HAS_NORM (input and post-attention norms)");
+  if (attn->H != mlp->H)
+    return fail(TP_ERR_SHAPE, "hidden sizes differ (%lld vs %lld)", (long long)attn->H, (long long)mlp->H);
+  if (attn->device != mlp->device) return fail(TP_ERR_ARG, "handles are on different devices");
+  if (attn->cfg.head_dim != 128) return fail(TP_ERR_UNSUPPORTED, "the attention core is built for head_dim 128");
+  if (max_tokens < 1) return fail(TP_ERR_SHAPE, "max_tokens must be >= 1");
+  int rc = check_T(max_tokens);
+  if (rc) return rc;
+  tp_layer* L = new (std::nothrow) tp_layer();
+  if (L == nullptr) return fail(TP_ERR_ARG, "out of host memory");
+  L->attn = attn;
+  L->mlp = mlp;
+  L->max_tokens = max_tokens;
+  if ((rc = tp_workspace_size(attn, max_tokens, &L->attn_ws)) ||
+      (rc = tp_workspace_size(mlp, max_tokens, &L->mlp_ws))) {
+    delete L;
+    return rc;
+  }
+  L->mlp_off = align256(L->attn_ws);
+  L->x1_off = align256(L->mlp_off + L->mlp_ws);
+  L->qkv_off = align256(L->x1_off + max_tokens * attn->H * 2);
+  L->a_off = align256(L->qkv_off + (int64_t)attn->cfg.t * max_tokens * attn->ws_qkv * 2);
+  L->total = align256(L->a_off + (int64_t)attn->cfg.t * max_tokens * attn->Ks * 2);
+  *out = L;
+  return ok();
+}
+
+int tp_layer_destroy(tp_layer_t* layer) {
+  delete layer;
+  return ok();
+}
+
+int tp_layer_workspace_size(const tp_layer_t* layer, int64_t* bytes) {
+  if (layer == nullptr || bytes == nullptr) return fail(TP_ERR_ARG, "null argument");
+  *bytes = layer->total;
+  return ok();
+}
+
+int tp_decoder_layer_forward(tp_layer_t* layer, int64_t T, const tp_layer_io_t* io, void* workspace,
+                             int64_t workspace_bytes, tp_stream_t stream) {
+  if (layer == nullptr || io == nullptr) return fail(TP_ERR_ARG, "null argument");
+  int rc = check_T(T);
+  if (rc) return rc;
+  if (T > layer->max_tokens)
+    return fail(TP_ERR_SHAPE, "T=%lld exceeds the layer's max_tokens=%lld", (long long)T,
+                (long long)layer->max_tokens);
+  if (T == 0) return ok();
+  tp_linear* at = layer->attn;
+  TP_CHECK_PTR(io->hidden_in, "hidden_in");
+  if (io->residual_in != nullptr) TP_CHECK_PTR(io->residual_in, "residual_in");
+  TP_CHECK_PTR(io->residual_attn, "residual_attn");
+  TP_CHECK_PTR(io->attn_out, "attn_out");
+  TP_CHECK_PTR(io->residual_mlp, "residual_mlp");
+  TP_CHECK_PTR(io->mlp_out, "mlp_out");
+  if (io->residual_stream != nullptr) TP_CHECK_PTR(io->residual_stream, "residual_stream");
+  if (io->cu_seqlens == nullptr || (reinterpret_cast<uintptr_t>(io->cu_seqlens) & 3u) != 0)
+    return fail(TP_ERR_ARG, "cu_seqlens is null or not 4-byte aligned");
+  if (io->n_seqs < 1 || io->n_seqs > T) return fail(TP_ERR_SHAPE, "n_seqs must be in [1, T] (got %d)", io->n_seqs);
+  if (io->max_seqlen < 1 || io->max_seqlen > T)
+    return fail(TP_ERR_SHAPE, "max_seqlen must be in [1, T] (got %d)", io->max_seqlen);
+  if (ceil_div(io->max_seqlen, 128) > 8192) return fail(TP_ERR_UNSUPPORTED, "max_seqlen > 1048576");
+  if (workspace == nullptr || !aligned16(workspace))
+    return fail(TP_ERR_ARG, "workspace is null or not 16-byte aligned");
+  if (workspace_bytes < layer->total)
+    return fail(TP_ERR_ARG, "workspace too small: %lld bytes, %lld needed", (long long)workspace_bytes,
+                (long long)layer->total);
+  if ((rc = check_device(at))) return rc;
+  char* ws = static_cast<char*>(workspace);
+  void* x1 = ws + layer->x1_off;
+  void* qkv = ws + layer->qkv_off;
+  void* A = ws + layer->a_off;
+  StatusRedirect redirect(reinterpret_cast<int*>(ws));
+  if ((rc = tp_add_rms_norm(T, at->H, io->hidden_in, io->residual_in, at->gamma, at->cfg.rms_eps,
+                            io->residual_attn, x1, stream)))
+    return rc;
+  if ((rc = tp_attn_proj_forward(at, T, x1, qkv, nullptr, nullptr, ws, layer->attn_ws, stream))) return rc;
+  if ((rc = tp_attention_forward(at, T, qkv, io->cu_seqlens, io->n_seqs, io->max_seqlen, A, ws,
+                                 layer->attn_ws, stream)))
+    return rc;
+  if ((rc = tp_attn_proj_forward(at, T, nullptr, nullptr, A, io->attn_out, ws, layer->attn_ws, stream)))
+    return rc;
+  if ((rc = tp_mlp_forward(layer->mlp, T, io->attn_out, io->residual_attn, io->residual_mlp, io->mlp_out,
+                           io->residual_stream, ws + layer->mlp_off, layer->mlp_ws, stream)))
+    return rc;
   return ok();
 }
 

@@ -146,3 +146,35 @@ def test_wait_limit_must_be_positive(L):
     assert L.tp_set_wait_timeout(0) == tl.TP_ERR_ARG
     assert L.tp_set_wait_timeout(-5) == tl.TP_ERR_ARG
     assert L.tp_set_wait_timeout(2_000_000_000) == tl.TP_OK
+
+
+def test_layer_calls_reject_null_arguments(L):
+    h = ctypes.c_void_p()
+    assert L.tp_layer_create(None, None, 128, ctypes.byref(h)) == tl.TP_ERR_ARG and not h.value
+    assert L.tp_layer_create(None, None, 128, None) == tl.TP_ERR_ARG
+    b = ctypes.c_int64()
+    assert L.tp_layer_workspace_size(None, ctypes.byref(b)) == tl.TP_ERR_ARG
+    io = tl.LayerIO()
+    assert L.tp_decoder_layer_forward(None, 16, ctypes.byref(io), None, 0, None) == tl.TP_ERR_ARG
+    assert L.tp_layer_destroy(None) == tl.TP_OK
+
+
+def test_attention_handle_accepts_the_input_norm_flag(L):
+    # the attention handle may carry the layer's input RMSNorm; unknown flags stay errors
+    cfg = tl.make_config(tl.TP_BLOCK_ATTN_PROJ, 4, 4096, n_q_heads=32, n_kv_heads=8, head_dim=128,
+                         flags=tl.TP_FLAG_HAS_NORM)
+    assert tl.packed_weight_bytes(cfg)[1] == 4096 * 4096 * 2
+    cfg.flags = 2
+    with pytest.raises(tl.TPError) as e:
+        tl.packed_weight_bytes(cfg)
+    assert e.value.code == tl.TP_ERR_ARG
+    cfg.flags, cfg.rms_eps = tl.TP_FLAG_HAS_NORM, -1.0
+    with pytest.raises(tl.TPError) as e:
+        tl.packed_weight_bytes(cfg)
+    assert e.value.code == tl.TP_ERR_ARG
+
+
+def test_norm_without_residual_passes_host_checks(L):
+    # a first layer has no incoming residual: residual_in may be NULL (T = 0: nothing launched)
+    p = ctypes.c_void_p(0x10000)
+    assert L.tp_add_rms_norm(0, 512, p, None, p, 1e-5, p, p, None) == tl.TP_OK

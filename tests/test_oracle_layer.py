@@ -177,3 +177,15 @@ _orig = {k: getattr(dl, k) for k in ("add_rms_norm", "attention_core", "mlp_bloc
 def test_planted_mistake_is_caught(monkeypatch, name, bad):
     monkeypatch.setattr(dl, name, bad)
     assert not _pin_passes()
+
+
+def test_rows_subset_matches_the_full_layer():
+    nq, nkv, hd, H_, I_ = 8, 4, 8, 32, 64
+    cu = [0, 20, 21, 40]
+    p = _params(H_, I_, nq, nkv, hd, cu[-1], 12)
+    full = _oracle(p, nq, nkv, hd, 2, cu)
+    rows = [39, 0, 20, 21, 5]
+    sub = oracle.decoder_layer(p["hidden"], p["residual"], p["ga"], p["wq"], p["wk"], p["wv"], p["wo"], p["gm"],
+                               p["wg"], p["wu"], p["wd"], nq, nkv, hd, 2, cu, EPS, rows=rows)
+    for k in KEYS:
+        np.testing.assert_allclose(sub[k], full[k][rows], rtol=1e-12, atol=1e-12, err_msg=k)

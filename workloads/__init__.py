@@ -43,7 +43,7 @@ TENSOR_TYPES = {"residual_stream": 0, "attn_out": 1, "mlp_out": 2, "final_norm":
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str                 # "mlp", "attn" (projections) or "attn_core" (attention core)
+    kind: str                 # "mlp", "attn" (projections), "attn_core" (attention core) or "layer"
     T: int                    # tokens in the step
     H: int                    # hidden size
     t: int                    # logical tensor-parallel shards
@@ -64,28 +64,44 @@ class Workload:
         """Lengths of the packed sequences (attention core): one sequence, or the ragged batch."""
         return ragged_batch(self)["lens"] if self.requests else np.array([self.T], dtype=np.int64)
 
-    def flops(self) -> float:
-        if self.kind == "attn_core":
-            # q k^T and p v over the causal (query, key) pairs of every sequence and q head
-            L = self.seq_lens().astype(np.float64)
-            return 4.0 * self.hd * self.nq * float(np.sum(L * (L + 1) / 2))
-        if self.kind == "mlp":
-            return 2.0 * self.T * self.H * (2 * self.I) + 2.0 * self.T * self.I * self.H
+    def attn_core_flops(self) -> float:
+        """q k^T and p v over the causal (query, key) pairs of every sequence and q head."""
+        L = self.seq_lens().astype(np.float64)
+        return 4.0 * self.hd * self.nq * float(np.sum(L * (L + 1) / 2))
+
+    def mlp_flops(self) -> float:
+        return 2.0 * self.T * self.H * (2 * self.I) + 2.0 * self.T * self.I * self.H
+
+    def proj_flops(self) -> float:
         qkv_n = (self.nq + 2 * self.nkv) * self.hd
         return 2.0 * self.T * self.H * qkv_n + 2.0 * self.T * self.nq * self.hd * self.H
 
+    def flops(self) -> float:
+        if self.kind == "attn_core":
+            return self.attn_core_flops()
+        if self.kind == "mlp":
+            return self.mlp_flops()
+        if self.kind == "layer":
+            return self.proj_flops() + self.attn_core_flops() + self.mlp_flops()
+        return self.proj_flops()
+
     def weight_bytes(self) -> int:
+        proj = 2 * (self.H * (self.nq + 2 * self.nkv) * self.hd + self.nq * self.hd * self.H)
         if self.kind == "attn_core":
             return 0
         if self.kind == "mlp":
             return 2 * 3 * self.H * self.I
-        return 2 * (self.H * (self.nq + 2 * self.nkv) * self.hd + self.nq * self.hd * self.H)
+        if self.kind == "layer":
+            return proj + 2 * 3 * self.H * self.I
+        return proj
 
     def activation_bytes(self) -> int:
         """Bytes of activations read or written once by the whole block."""
         T, H = self.T, self.H
         if self.kind == "attn_core":       # qkv in, attention output out
             return 2 * T * (self.nq + 2 * self.nkv) * self.hd + 2 * T * self.nq * self.hd
+        if self.kind == "layer":             # hidden, residual in; r1, attn_out, r2, mlp_out, stream out
+            return 2 * T * H * 7
         if self.kind == "mlp":
             b = 2 * T * H * 2                # x (or a) in, mlp_out
             if self.norm:
@@ -112,6 +128,16 @@ WORKLOADS = {
         "qwen25_7b_ragged_attn_core", "attn_core", T=2048, H=3584, nq=28, nkv=4, hd=128, t=4,
         w_std=0.0, requests=64, mean_len=32,
         desc="Ragged continuous batch, Qwen2.5-7B-shaped attention core, 2048 tokens / 64 requests, t=4"),
+    "llama3_8b_layer_prefill": Workload(
+        "llama3_8b_layer_prefill", "layer", T=4096, H=4096, I=14336, nq=32, nkv=8, hd=128, t=4,
+        w_std=0.02, norm=True,
+        desc="Llama-3-8B-shaped decoder layer prefill (norm, QKV, attention, o_proj, add + norm, MLP), "
+             "one 4096-token sequence, t=4"),
+    "qwen25_7b_ragged_layer": Workload(
+        "qwen25_7b_ragged_layer", "layer", T=2048, H=3584, I=18944, nq=28, nkv=4, hd=128, t=4,
+        w_std=0.02, norm=True, requests=64, mean_len=32, capture_frac=0.1,
+        desc="Ragged continuous batch, Qwen2.5-7B-shaped decoder layer with attn_out / mlp_out / "
+             "residual_stream capture, 2048 tokens / 64 requests, t=4"),
     "llama3_70b_mlp_prefill": Workload(
         "llama3_70b_mlp_prefill", "mlp", T=8192, H=8192, I=28672, t=8, w_std=0.015,
         desc="Llama-3-70B-shaped MLP prefill, 8192 tokens, t=8"),
@@ -204,6 +230,23 @@ def attn_core_inputs(w: Workload, lens=None) -> dict:
     ws = (w.nq // w.t + 2 * kv_per) * w.hd
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     return {"qkv": draw((w.t, T, ws), w.seed, 6), "cu_seqlens": cu, "T": T}
+
+
+def layer_inputs(w: Workload, T: int | None = None) -> dict:
+    """Inputs of one decoder layer: hidden states and residual entering it, the
+    attention weights (q, k, v, o), the input norm's gamma, the MLP weights
+    (gate, up, down) and the post-attention norm's gamma."""
+    T = w.T if T is None else T
+    H, I, s, hd = w.H, w.I, w.seed, w.hd
+    return {
+        "hidden": draw((T, H), s, 0), "residual": draw((T, H), s, 1),
+        "w_q": draw((w.nq * hd, H), s, 2, b=w.w_std), "w_k": draw((w.nkv * hd, H), s, 3, b=w.w_std),
+        "w_v": draw((w.nkv * hd, H), s, 4, b=w.w_std), "w_o": draw((H, w.nq * hd), s, 5, b=w.w_std),
+        "gamma_attn": draw((H,), s, 6, kind="uniform", a=0.9, b=1.1),
+        "w_gate": draw((I, H), s, 7, b=w.w_std), "w_up": draw((I, H), s, 8, b=w.w_std),
+        "w_down": draw((H, I), s, 9, b=w.w_std),
+        "gamma_mlp": draw((H,), s, 10, kind="uniform", a=0.9, b=1.1),
+    }
 
 
 def ragged_batch(w: Workload) -> dict:
