@@ -54,8 +54,18 @@ typedef struct tp_linear tp_linear_t; /* opaque handle: shapes, plans, packed-we
 typedef void* tp_stream_t;            /* cudaStream_t */
 
 enum { TP_BLOCK_MLP = 0, TP_BLOCK_ATTN_PROJ = 1 };
-enum { TP_FLAG_HAS_NORM = 1 };        /* MLP: fused residual add + RMSNorm in front of gate_up;
-                                         ATTN: the handle carries the layer's input RMSNorm */
+enum {
+  TP_FLAG_HAS_NORM = 1, /* MLP: fused residual add + RMSNorm in front of gate_up;
+                           ATTN: the handle carries the layer's input RMSNorm */
+  /* Gathered activations ("vLLM 源码完全拆解（十一）" ColumnParallelLinear gather_output=True,
+   * RowParallelLinear input_is_parallel=False): the column-parallel output and the
+   * row-parallel input are [T][t * w] (the t shards' columns side by side in each row,
+   * i.e. the unsharded tensor) instead of shard-major [t][T][w]. Applies to h_out /
+   * h_in of the stage calls, qkv_out / attn_in of tp_attn_proj_forward and qkv /
+   * attn_out of tp_attention_forward. Results are bit-identical to the shard-major
+   * layout: only the addresses change. */
+  TP_FLAG_GATHERED = 2
+};
 
 typedef struct {
   int32_t kind;          /* TP_BLOCK_MLP or TP_BLOCK_ATTN_PROJ */

@@ -22,6 +22,7 @@ TP_ERR_ARG, TP_ERR_SHAPE, TP_ERR_UNSUPPORTED, TP_ERR_CUDA, TP_ERR_CAPACITY, TP_E
     -1, -2, -3, -4, -5, -6)
 TP_BLOCK_MLP, TP_BLOCK_ATTN_PROJ = 0, 1
 TP_FLAG_HAS_NORM = 1
+TP_FLAG_GATHERED = 2
 
 ABI_SYMBOLS = (
     "tp_packed_weight_bytes", "tp_linear_create", "tp_linear_destroy", "tp_workspace_size",
@@ -245,10 +246,17 @@ class TPLinear:
                                              _ptr(o.get("residual_stream")), _ptr(status), _stream(stream)))
         return o
 
+    @property
+    def gathered(self) -> bool:
+        return bool(self.cfg.flags & TP_FLAG_GATHERED)
+
     def gate_up(self, x: torch.Tensor, h_out: Optional[torch.Tensor] = None, ws=None, stream=None) -> torch.Tensor:
+        """h [t][T][I/t] (shard-major), or [T][I] with TP_FLAG_GATHERED."""
         T = x.shape[0]
         t, Is = self.cfg.t, self.cfg.intermediate // self.cfg.t
-        h_out = torch.empty(t, T, Is, dtype=torch.bfloat16, device=x.device) if h_out is None else h_out
+        if h_out is None:
+            shape = (T, t * Is) if self.gathered else (t, T, Is)
+            h_out = torch.empty(shape, dtype=torch.bfloat16, device=x.device)
         ws = self.workspace(T) if ws is None else ws
         _check(lib().tp_gate_up_forward(self.handle, T, _ptr(_bf16(x, "x")), _ptr(h_out), _ptr(ws), ws.numel(),
                                         _stream(stream)))
@@ -256,7 +264,7 @@ class TPLinear:
 
     def down(self, h_in: torch.Tensor, residual: Optional[torch.Tensor] = None, out=None, stream_out=None,
              ws=None, stream=None):
-        T = h_in.shape[1]
+        T = h_in.shape[0] if self.gathered else h_in.shape[1]
         H = self.cfg.hidden
         out = torch.empty(T, H, dtype=torch.bfloat16, device=h_in.device) if out is None else out
         if residual is not None and stream_out is None:
@@ -270,13 +278,14 @@ class TPLinear:
     def attn_proj_forward(self, x: Optional[torch.Tensor], attn_in: Optional[torch.Tensor],
                           qkv_out=None, o_out=None, ws=None, stream=None):
         c = self.cfg
-        T = (x if x is not None else attn_in[0]).shape[0]
+        T = x.shape[0] if x is not None else (attn_in.shape[0] if self.gathered else attn_in.shape[1])
         q_per = c.n_q_heads // c.t
         kv_per = 1 if c.t >= c.n_kv_heads else c.n_kv_heads // c.t
         w_s = (q_per + 2 * kv_per) * c.head_dim
         dev = self.w_col.device
         if x is not None and qkv_out is None:
-            qkv_out = torch.empty(c.t, T, w_s, dtype=torch.bfloat16, device=dev)
+            shape = (T, c.t * w_s) if self.gathered else (c.t, T, w_s)
+            qkv_out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
         if attn_in is not None and o_out is None:
             o_out = torch.empty(T, c.hidden, dtype=torch.bfloat16, device=dev)
         ws = self.workspace(T) if ws is None else ws
@@ -292,11 +301,12 @@ class TPLinear:
         projection's output) -> attn [t][T][nq*hd/t] (o_proj's input). cu_seqlens:
         int32 device tensor [n_seqs + 1] of sequence offsets."""
         c = self.cfg
-        T = qkv.shape[1]
+        T = qkv.shape[0] if self.gathered else qkv.shape[1]
         if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
             raise TypeError("cu_seqlens must be an int32 CUDA tensor")
         if out is None:
-            out = torch.empty(c.t, T, c.n_q_heads // c.t * c.head_dim, dtype=torch.bfloat16, device=qkv.device)
+            shape = (T, c.n_q_heads * c.head_dim) if self.gathered else (c.t, T, c.n_q_heads // c.t * c.head_dim)
+            out = torch.empty(shape, dtype=torch.bfloat16, device=qkv.device)
         ws = self.workspace(T) if ws is None else ws
         _check(lib().tp_attention_forward(self.handle, T, _ptr(_bf16(qkv, "qkv")), _ptr(cu_seqlens),
                                           cu_seqlens.numel() - 1, int(max_seqlen), _ptr(out), _ptr(ws),

@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok || !wait_all(O_DONE, nu & 1)) break;
       tc_fence_after();
       const float inv = 1.0f / l;
-      __nv_bfloat16* dst = p.out + ((size_t)x.r * p.T + x.start + q_rel) * (size_t)(p.q_per * 128) + x.i * 128;
+      __nv_bfloat16* dst = p.out + (size_t)x.r * p.out_sstride + (size_t)(x.start + q_rel) * p.out_rstride + x.i * 128;
       float o[32];
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 32) {

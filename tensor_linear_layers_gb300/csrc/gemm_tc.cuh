@@ -68,6 +68,11 @@ struct GemmParams {
   int Is;            // KIND_GATE_UP: I / t
   int n_out;         // KIND_COL / KIND_ROW: output features
   int ws_out;        // KIND_COL: features per output shard (== n_out if unsplit)
+  // KIND_GATE_UP / KIND_COL output of shard r, token m, feature c (within the shard):
+  // out[r * out_sstride + m * out_rstride + c]. Shard-major [t][T][w]: (T * w, w);
+  // gathered [T][t * w]: (w, t * w)
+  long long out_sstride;
+  int out_rstride;
   const uint8_t* w_packed;     // packed weight blocks
   __nv_bfloat16* out;
   __nv_bfloat16* out2;         // KIND_ROW: y + resid (nullable)
@@ -148,7 +153,7 @@ __device__ __forceinline__ void emit_vals(const GemmParams& p, int tm, int tn, i
       if (KIND == KIND_GATE_UP) {
         const int r = tn / p.nb, blk = tn - r * p.nb;
         const int i0 = blk * 128 + c0;
-        __nv_bfloat16* dst = p.out + ((size_t)r * p.T + m) * p.Is + i0;
+        __nv_bfloat16* dst = p.out + (size_t)r * p.out_sstride + (size_t)m * p.out_rstride + i0;
 #pragma unroll
         for (int j = 0; j < N; j += 8) {
           if (i0 + j < p.Is) {
@@ -171,7 +176,7 @@ __device__ __forceinline__ void emit_vals(const GemmParams& p, int tm, int tn, i
             v.y = pack_bf16x2(g[j + 2], g[j + 3]);
             v.z = pack_bf16x2(g[j + 4], g[j + 5]);
             v.w = pack_bf16x2(g[j + 6], g[j + 7]);
-            *reinterpret_cast<uint4*>(p.out + ((size_t)ro * p.T + m) * p.ws_out + c) = v;
+            *reinterpret_cast<uint4*>(p.out + (size_t)ro * p.out_sstride + (size_t)m * p.out_rstride + c) = v;
           }
         }
       } else {
@@ -207,21 +212,21 @@ __device__ __forceinline__ void emit_vals(const GemmParams& p, int tm, int tn, i
         const int r = tm / p.nb, blk = tm - r * p.nb;
         const int i = blk * 128 + row;
         if (i >= p.Is) return;
-        __nv_bfloat16* dst = p.out + (size_t)r * p.T * p.Is + i;
+        __nv_bfloat16* dst = p.out + (size_t)r * p.out_sstride + i;
 #pragma unroll
         for (int j = 0; j < N; ++j) {
           const int tok = tn * BN + c0 + j;
-          if (tok < p.T) dst[(size_t)tok * p.Is] = __float2bfloat16_rn(silu_f(g[j]) * u[j]);
+          if (tok < p.T) dst[(size_t)tok * p.out_rstride] = __float2bfloat16_rn(silu_f(g[j]) * u[j]);
         }
       } else if (KIND == KIND_COL) {
         const int f = tm * 256 + seg * 128 + row;
         if (f >= p.n_out) return;
         const int ro = f / p.ws_out, c = f - ro * p.ws_out;
-        __nv_bfloat16* dst = p.out + (size_t)ro * p.T * p.ws_out + c;
+        __nv_bfloat16* dst = p.out + (size_t)ro * p.out_sstride + c;
 #pragma unroll
         for (int j = 0; j < N; ++j) {
           const int tok = tn * BN + c0 + j;
-          if (tok < p.T) dst[(size_t)tok * p.ws_out] = __float2bfloat16_rn(g[j]);
+          if (tok < p.T) dst[(size_t)tok * p.out_rstride] = __float2bfloat16_rn(g[j]);
         }
       } else {
         const int f = tm * 256 + seg * 128 + row;

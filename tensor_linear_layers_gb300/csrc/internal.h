@@ -56,7 +56,9 @@ struct AttnParams {
   const int4* pairs;       // [n_pairs] {sequence start, length, q tile, 0}, heaviest first
   const int* n_pairs;      // written by the preparation kernel
   int* next_unit;          // units handed out so far (CTAs take the next one when free); zeroed by the preparation kernel
-  __nv_bfloat16* out;      // [t][T][q_per * 128]
+  __nv_bfloat16* out;      // shard r, token m at out + r * out_sstride + m * out_rstride
+  long long out_sstride;   // [t][T][q_per * 128]: T * q_per * 128; gathered [T][t * q_per * 128]: q_per * 128
+  int out_rstride;         // q_per * 128, or t * q_per * 128 gathered
   int* status;
   unsigned long long timeout_ns;
   int T, q_per, kv_per, rep, group, heads;  // group = nq / nkv, heads = t * q_per

@@ -121,6 +121,43 @@ int make_map(CUtensorMap* m, const void* ptr, int64_t d0, int64_t d1, int64_t d2
   return TP_OK;
 }
 
+// Tensor map of a t-shard activation with per-shard width w and T rows:
+// shard-major [t][T][w] (each shard's rows contiguous, as a rank holds them) or
+// gathered [T][t * w] (the shards' columns side by side in every row). The shard
+// index is dimension 2 (shard_dim == 2) or 3 (shard_dim == 3) of the map.
+int make_shard_map(CUtensorMap* m, const void* ptr, int64_t w, int64_t T, int64_t t, int shard_dim,
+                   bool gathered, int box_rows) {
+  if (!gathered) return shard_dim == 2 ? make_map(m, ptr, w, T, t, 1, box_rows) : make_map(m, ptr, w, T, 1, t, box_rows);
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t row = (cuuint64_t)(t * w * 2), shard = (cuuint64_t)(w * 2);
+  cuuint64_t dims[4], strides[3];
+  dims[0] = (cuuint64_t)w;
+  dims[1] = (cuuint64_t)T;
+  strides[0] = row;
+  if (shard_dim == 2) {
+    dims[2] = (cuuint64_t)t;
+    dims[3] = 1;
+    strides[1] = shard;
+    strides[2] = row * (cuuint64_t)T;
+  } else {
+    dims[2] = 1;
+    dims[3] = (cuuint64_t)t;
+    strides[1] = row * (cuuint64_t)T;
+    strides[2] = shard;
+  }
+  const cuuint32_t box[4] = {64u, (cuuint32_t)box_rows, 1u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a gathered %lld x %lld x %lld map",
+                (int)r, (long long)w, (long long)T, (long long)t);
+  return TP_OK;
+}
+
 // ============================================================================ workspace layout
 // header: [0] status word; [64] grid barrier of the column-parallel GEMM;
 // [128] grid barrier of the row-parallel GEMM; [192] counters of the fused
@@ -337,6 +374,14 @@ GemmParams base_params(const Plan& pl, int64_t T, void* ws, int64_t part_off, in
   return p;
 }
 
+bool gathered(const tp_linear* h) { return (h->cfg.flags & TP_FLAG_GATHERED) != 0; }
+
+// where the column-parallel GEMM writes shard r, token m: per-shard width w
+void set_col_out(GemmParams& p, const tp_linear* h, int64_t T, int64_t w, bool gath) {
+  p.out_sstride = gath ? w : T * w;
+  p.out_rstride = (int)(gath ? h->cfg.t * w : w);
+}
+
 // column-parallel GEMM: gate_up (MLP) or QKV (ATTN)
 int run_col(const tp_linear* h, int64_t T, const void* x, void* out, void* ws, const Layout& L,
             cudaStream_t st) {
@@ -352,6 +397,7 @@ int run_col(const tp_linear* h, int64_t T, const void* x, void* out, void* ws, c
     p.n_out = (int)h->n_col;
     p.ws_out = (int)h->ws_qkv;
   }
+  set_col_out(p, h, T, h->cfg.kind == TP_BLOCK_MLP ? h->Is : h->ws_qkv, gathered(h));
   p.w_packed = static_cast<const uint8_t*>(h->w_col);
   const int ncl = pl.swap ? 0 : pair_max_clusters();
   if (!pl.swap && prefer_pair(h, &pl, 1, ncl)) {
@@ -373,7 +419,7 @@ int run_row(const tp_linear* h, int64_t T, const void* in_shards, const void* re
             void* out2, void* ws, const Layout& L, cudaStream_t st) {
   const Plan pl = make_plan(h, 1, T);
   CUtensorMap map_in;
-  int rc = make_map(&map_in, in_shards, h->Ks, T, 1, h->cfg.t, pl.swap ? pl.bn : 128);
+  int rc = make_shard_map(&map_in, in_shards, h->Ks, T, h->cfg.t, 3, gathered(h), pl.swap ? pl.bn : 128);
   if (rc) return rc;
   GemmParams p = base_params(pl, T, ws, L.part_row, kGbarRowOff);
   p.n_out = (int)h->H;
@@ -405,12 +451,13 @@ int run_col_row_together(const tp_linear* h, int64_t T, const void* x, void* qkv
   const Plan pc = make_plan(h, 0, T, 1), pr = make_plan(h, 1, T, 1);
   CUtensorMap map_x, map_a;
   int rc = make_map(&map_x, x, h->H, T, 1, 1, 128);
-  if (!rc) rc = make_map(&map_a, attn_in, h->Ks, T, 1, h->cfg.t, 128);
+  if (!rc) rc = make_shard_map(&map_a, attn_in, h->Ks, T, h->cfg.t, 3, gathered(h), 128);
   if (rc) return rc;
   GemmParams p1 = base_params(pc, T, ws, L.part_col, kGbarColOff);
   p1.out = static_cast<__nv_bfloat16*>(qkv_out);
   p1.n_out = (int)h->n_col;
   p1.ws_out = (int)h->ws_qkv;
+  set_col_out(p1, h, T, h->ws_qkv, gathered(h));
   p1.w_packed = static_cast<const uint8_t*>(h->w_col);
   GemmParams p2 = base_params(pr, T, ws, L.part_row, kGbarRowOff);
   p2.out = static_cast<__nv_bfloat16*>(o_out);
@@ -480,7 +527,7 @@ int validate_cfg(const tp_config_t* c) {
       return fail(TP_ERR_SHAPE, "n_q_heads must be a multiple of n_kv_heads");
     if (c->head_dim % 8 != 0) return fail(TP_ERR_UNSUPPORTED, "head_dim must be a multiple of 8");
   }
-  if (c->flags & ~TP_FLAG_HAS_NORM) return fail(TP_ERR_ARG, "unknown flags 0x%x", c->flags);
+  if (c->flags & ~(TP_FLAG_HAS_NORM | TP_FLAG_GATHERED)) return fail(TP_ERR_ARG, "unknown flags 0x%x", c->flags);
   if ((c->flags & TP_FLAG_HAS_NORM) && !(c->rms_eps >= 0.0f))
     return fail(TP_ERR_ARG, "rms_eps must be >= 0");
   if ((c->flags & TP_FLAG_HAS_NORM) && c->hidden > max_norm_hidden())
@@ -756,6 +803,7 @@ int tp_mlp_forward(tp_linear_t* h, int64_t T, const void* x_in, const void* resi
     P.g1 = base_params(p1, T, workspace, L.part_col, kGbarColOff);
     P.g1.out = static_cast<__nv_bfloat16*>(hbuf);
     P.g1.Is = (int)h->Is;
+    set_col_out(P.g1, h, T, h->Is, false);   // h stays inside the launch: shard-major
     P.g1.w_packed = static_cast<const uint8_t*>(h->w_col);
     P.g2 = base_params(p2, T, workspace, L.part_row, kGbarRowOff);
     P.g2.n_out = (int)h->H;
@@ -846,13 +894,15 @@ int tp_attention_forward(tp_linear_t* h, int64_t T, const void* qkv, const int32
                 (long long)attn_ws_bytes(h, T, n_seqs));
   if ((rc = check_device(h))) return rc;
   CUtensorMap map_qkv;
-  if ((rc = make_map(&map_qkv, qkv, h->ws_qkv, T, h->cfg.t, 1, 128))) return rc;
+  if ((rc = make_shard_map(&map_qkv, qkv, h->ws_qkv, T, h->cfg.t, 2, gathered(h), 128))) return rc;
   char* ws = static_cast<char*>(workspace);
   AttnParams p{};
   p.pairs = reinterpret_cast<const int4*>(ws + dyn_off(h) + 512);
   p.n_pairs = reinterpret_cast<const int*>(ws + dyn_off(h) + 256);
   p.next_unit = reinterpret_cast<int*>(ws + dyn_off(h) + 260);
   p.out = static_cast<__nv_bfloat16*>(attn_out);
+  p.out_sstride = gathered(h) ? h->Ks : T * h->Ks;
+  p.out_rstride = (int)(gathered(h) ? h->cfg.t * h->Ks : h->Ks);
   p.status = t_status != nullptr ? t_status : reinterpret_cast<int*>(ws);
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   p.T = (int)T;
@@ -974,6 +1024,7 @@ extern "C" int tp_mlp_forward_no_alloc(tp_linear_t* h, int64_t T, const void* x_
   P.g1 = base_params(p1, T, scratch, L.part_col, kGbarColOff);
   P.g1.out = static_cast<__nv_bfloat16*>(hbuf);
   P.g1.Is = (int)h->Is;
+  set_col_out(P.g1, h, T, h->Is, false);
   P.g1.w_packed = static_cast<const uint8_t*>(h->w_col);
   P.g2 = base_params(p2, T, scratch, L.part_row, kGbarRowOff);
   P.g2.n_out = (int)h->H;

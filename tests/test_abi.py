@@ -164,7 +164,9 @@ def test_attention_handle_accepts_the_input_norm_flag(L):
     cfg = tl.make_config(tl.TP_BLOCK_ATTN_PROJ, 4, 4096, n_q_heads=32, n_kv_heads=8, head_dim=128,
                          flags=tl.TP_FLAG_HAS_NORM)
     assert tl.packed_weight_bytes(cfg)[1] == 4096 * 4096 * 2
-    cfg.flags = 2
+    cfg.flags = tl.TP_FLAG_HAS_NORM | tl.TP_FLAG_GATHERED    # gathered layout: accepted
+    assert tl.packed_weight_bytes(cfg)[1] == 4096 * 4096 * 2
+    cfg.flags = 4
     with pytest.raises(tl.TPError) as e:
         tl.packed_weight_bytes(cfg)
     assert e.value.code == tl.TP_ERR_ARG
