@@ -175,6 +175,15 @@ int tp_mlp_forward_no_alloc(tp_linear_t* h, int64_t T, const void* x_in, const v
  */
 int tp_add_rms_norm(int64_t T, int64_t H, const void* a, const void* residual_in, const void* gamma,
                     float eps, void* residual_out, void* x_out, tp_stream_t stream);
+/*
+ * Sequence parallelism ("Tensor Parallelism", collectives: reduce-scatter;
+ * "Tensor & pipeline parallelism", residual_stream: the residual split across
+ * the TP ranks by token): the reduce-scatter that ends a row-parallel layer
+ * keeps rank r's rows [r*Tp/t, (r+1)*Tp/t) of the reduced output, Tp = T padded
+ * up to a multiple of t. Here the reduction happens on chip and the scatter is
+ * a view: give mlp_out / o_out a buffer of Tp rows whose last Tp - T rows are
+ * zero and read it as [t][Tp/t][H]; rank r's slice is slice r.
+ */
 int tp_gate_up_forward(tp_linear_t* h, int64_t T, const void* x, void* h_out,
                        void* workspace, int64_t workspace_bytes, tp_stream_t stream);
 int tp_down_forward(tp_linear_t* h, int64_t T, const void* h_in, const void* residual,

@@ -41,7 +41,7 @@ page-printed head counts in ``tests/golden/``). None is "parity unpinned".
 from .tp_block import (  # noqa: F401
     bf16_to_f64, linear, column_parallel, row_parallel, silu, silu_mul, rms_norm,
     add_rms_norm, mlp_block, mlp_block_tp, mlp_layer, gqa_partition, qkv_shard_rows,
-    qkv_parallel, o_proj_parallel, divide,
+    qkv_parallel, o_proj_parallel, divide, reduce_scatter,
 )
 from .capture import capture_rows, pack_key  # noqa: F401
 from .attention import attention_core, attention_rows, kv_head_of  # noqa: F401

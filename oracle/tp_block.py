@@ -75,6 +75,27 @@ def row_parallel(X: np.ndarray, W: np.ndarray, t: int) -> list[np.ndarray]:
     return [linear(X[:, r * s:(r + 1) * s], W[:, r * s:(r + 1) * s]) for r in range(t)]
 
 
+def reduce_scatter(partials, t: int) -> list[np.ndarray]:
+    """Sequence-parallel end of a row-parallel layer: the t partial sums are added and
+    the sum is split by token, rank r keeping rows [r*T/t, (r+1)*T/t).
+
+    [MLX] "Tensor Parallelism", collectives: a reduce-scatter replaces the
+    all-reduce when the next layer needs only a shard of the output; [UC]
+    "residual_stream" and [VCR] section 4 (PP + SP): with sequence parallelism
+    the residual is split across the TP ranks by token, after padding the token
+    count. Rows are padded with zeros up to a multiple of t (the padded count is
+    t * ceil(T/t)); slice r of the result is what rank r holds.
+    """
+    y = np.zeros_like(np.asarray(partials[0], np.float64))
+    for p in partials:
+        y = y + np.asarray(p, np.float64)
+    T = y.shape[0]
+    per = -(-T // t)
+    pad = np.zeros((per * t - T,) + y.shape[1:])
+    y = np.concatenate([y, pad], axis=0)
+    return [y[r * per:(r + 1) * per] for r in range(t)]
+
+
 # --------------------------------------------------------------------------- elementwise
 
 def silu(z: np.ndarray) -> np.ndarray:

@@ -71,6 +71,22 @@ def test_row_partials_sum_to_unsharded(t):
         assert not np.allclose(parts[0], X @ W.T)
 
 
+@pytest.mark.parametrize("T,t", [(8, 4), (10, 4), (3, 8), (5, 1)])
+def test_reduce_scatter_slices_the_reduced_rows(T, t):
+    # each rank keeps its own token rows of the sum; together (padding removed) they
+    # are the all-reduce result, written here as explicit loops over tokens and shards
+    X, W = rand(T, 16), rand(6, 16)
+    parts = oracle.row_parallel(X, W, 2)
+    sl = oracle.reduce_scatter(parts, t)
+    per = -(-T // t)
+    assert len(sl) == t and all(s.shape == (per, 6) for s in sl)
+    for r in range(t):
+        for i in range(per):
+            tok = r * per + i
+            want = [0.0] * 6 if tok >= T else [sum(X[tok, c] * W[o, c] for c in range(16)) for o in range(6)]
+            np.testing.assert_allclose(sl[r][i], want, rtol=1e-12, atol=1e-12)
+
+
 def test_divide_rejects_remainder():
     assert oracle.divide(1408, 2) == 704
     with pytest.raises(ValueError):
