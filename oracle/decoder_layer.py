@@ -43,26 +43,40 @@ def decoder_layer(hidden, residual, gamma_attn, w_q, w_k, w_v, w_o, gamma_mlp, w
     w_o [H, nq*hd], w_gate, w_up [I, H], w_down [H, I] (stored [out, in]); cu_seqlens
     [n_seqs + 1] token offsets of the packed sequences.
 
-    ``rows``: compute the outputs of those token rows only. Keys and values need
-    every earlier token of a row's sequence, so r1, x1 and qkv are computed for all
-    tokens; everything after the attention is per row. ``qkv`` is then still
-    [t, T, w_s] and every other tensor has len(rows) rows.
+    ``rows``: compute the outputs of those token rows only. A row's attention reads
+    the keys and values of its own sequence up to itself, so r1, x1 and qkv are
+    computed for exactly those tokens (rows are independent through the norm and
+    the projections); everything after the attention is per row. ``qkv`` is then
+    still [t, T, w_s], zero at the tokens no row needs, and every other tensor has
+    len(rows) rows.
     """
     f = _as_f64
-    hid = f(hidden)
-    if residual is None:
-        r1 = hid
-        x1 = rms_norm(r1, f(gamma_attn), eps)
-    else:
-        x1, r1 = add_rms_norm(hid, f(residual), f(gamma_attn), eps)
-    qkv = qkv_parallel(x1, f(w_q), f(w_k), f(w_v), nq, nkv, hd, t)
     cu = np.asarray(cu_seqlens, np.int64)
+    hid = f(hidden)
+    res = None if residual is None else f(residual)
+    T = hid.shape[0]
     if rows is None:
-        attn = attention_core(qkv, nq, nkv, hd, t, cu)
+        tok = np.arange(T)
     else:
         rows = np.asarray(rows, np.int64)
+        need = np.zeros(T, dtype=bool)
+        for row in rows:
+            need[cu[np.searchsorted(cu, row, side="right") - 1]:row + 1] = True
+        tok = np.nonzero(need)[0]
+    if res is None:
+        r1 = hid[tok]
+        x1 = rms_norm(r1, f(gamma_attn), eps)
+    else:
+        x1, r1 = add_rms_norm(hid[tok], res[tok], f(gamma_attn), eps)
+    qkv_tok = qkv_parallel(x1, f(w_q), f(w_k), f(w_v), nq, nkv, hd, t)
+    if rows is None:
+        qkv = qkv_tok
+        attn = attention_core(qkv, nq, nkv, hd, t, cu)
+    else:
+        qkv = np.zeros((t, T, qkv_tok.shape[2]))
+        qkv[:, tok] = qkv_tok
         attn = attention_rows(qkv, nq, nkv, hd, t, cu, rows)
-        r1 = r1[rows]
+        r1 = r1[np.searchsorted(tok, rows)]
     attn_out = o_proj_parallel(attn, f(w_o), t)
     x2, r2 = add_rms_norm(attn_out, r1, f(gamma_mlp), eps)
     mlp_out = mlp_block(x2, f(w_gate), f(w_up), f(w_down))

@@ -19,9 +19,9 @@ def bf16_to_f64(x) -> np.ndarray:
     A bf16 value is the top half of an IEEE float32, so widening the bits and
     viewing them as float32 is exact, and so is float32 -> float64.
     """
-    if not isinstance(x, np.ndarray):            # torch tensor
+    if not isinstance(x, np.ndarray):            # torch tensor: widening bf16 -> float64 is exact
         import torch
-        x = x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+        return x.detach().cpu().to(torch.float64).numpy()
     bits = np.asarray(x, dtype=np.uint16).astype(np.uint32) << 16
     return bits.view(np.float32).astype(np.float64)
 

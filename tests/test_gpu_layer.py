@@ -165,13 +165,16 @@ def test_qwen_ragged_layer_full_size_with_capture():
 
 
 def test_llama3_8b_layer_full_size_sampled_rows():
+    # rows of the first three query tiles: under causal attention they need only the
+    # first 384 tokens, which keeps the float64 oracle cheap; rows near the end of the
+    # 4096-token sequence are checked for the attention core alone (test_gpu_attention)
     w = workloads.WORKLOADS["llama3_8b_layer_prefill"]
     d = workloads.layer_inputs(w)
     attn, mlp, layer = make_layer(w, d, w.T)
     out, cu = run(layer, d, [w.T])
-    rows = [0, 1, 127, 128, 2047, 4095] + list(np.random.default_rng(1).integers(0, w.T, 10))
-    ref = ref_layer(w, d, cu, rows=sorted(set(int(r) for r in rows)))
+    rows = [0, 1, 127, 128, 255, 256, 383] + list(np.random.default_rng(1).integers(0, 384, 9))
     rows = sorted(set(int(r) for r in rows))
+    ref = ref_layer(w, d, cu, rows=rows)
     for k in KEYS:
         assert rel_err(out[k][rows], ref[k]) <= TOL, k
     assert status_of(layer.workspace()) == 0

@@ -32,8 +32,12 @@ def test_bf16_to_f64_known_bits():
     want = [1.0, -2.0, 1.0 + 2.0 ** -7, 0.0, -0.0, (2 - 2 ** -7) * 2.0 ** 127, 2.0 ** -133]
     got = oracle.bf16_to_f64(bits)
     assert list(got) == want
+    # the torch-tensor path (a library widening) gives the same values, subnormals included
+    tb = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16)
+    assert list(oracle.bf16_to_f64(tb)) == want
     t = torch.randn(1000).to(torch.bfloat16)
-    assert np.array_equal(oracle.bf16_to_f64(t), t.double().numpy())
+    t_bits = t.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.bf16_to_f64(t), oracle.bf16_to_f64(t_bits))
 
 
 # --------------------------------------------------------------------------- linear and the split algebra
