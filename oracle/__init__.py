@@ -25,7 +25,9 @@ o_proj (causal, GQA, sequences packed by offsets); the pages describe it
 only as attention over each rank's own heads, so it is the textbook
 scaled dot-product attention in their head layout. ``decoder_layer.py``
 chains the steps into one decoder layer (input norm, QKV, attention, o_proj,
-add + norm, MLP) in the order the pages give.
+add + norm, MLP) in the order the pages give. ``moe.py`` is the top-k
+mixture-of-experts block whose experts are split by the same column/row
+pattern (within-expert tensor parallelism); its routing is an input.
 
 Every function computes in float64 from bf16 inputs converted exactly. Where
 the block has a plain definition (the unsharded Y = XW, SiLU, RMSNorm, row
@@ -46,3 +48,4 @@ from .tp_block import (  # noqa: F401
 from .capture import capture_rows, pack_key  # noqa: F401
 from .attention import attention_core, attention_rows, kv_head_of  # noqa: F401
 from .decoder_layer import decoder_layer  # noqa: F401
+from .moe import moe_block, moe_block_tp  # noqa: F401
