@@ -176,7 +176,7 @@ def max_over_ranks(v: float, ws: int) -> float:
 
 # ---------------------------------------------------------------------------- work model
 def work_model(w: workloads.Workload):
-    decode = w.kind == "mlp" and w.T <= 128
+    decode = w.kind in ("mlp", "moe") and w.T <= 128
     flops = w.flops()
     wbytes = w.weight_bytes()
     abytes = w.activation_bytes()
@@ -227,6 +227,15 @@ class OracleSample:
             self.flops = 4.0 * w.hd * w.nq * float(np.sum(self.row_ids - starts + 1))
             self.wbytes = 0.0
             return
+        if w.kind == "moe":
+            # the first `rows` tokens, every routed entry through its expert
+            self.feat = 0
+            d = workloads.moe_inputs(w, T=self.rows)
+            self.args = d
+            self.flops = w.top_k * small.mlp_flops()
+            hit = np.unique(d["expert_ids"])
+            self.wbytes = float(len(hit) * 2 * 3 * w.H * w.I)
+            return
         if w.kind == "layer":
             # the first `rows` tokens: under causal attention they depend on no later
             # token, so the sample is an exact prefix of the whole step's work
@@ -261,6 +270,10 @@ class OracleSample:
         if w.kind == "attn_core":
             o.attention_rows(self.qkv, w.nq, w.nkv, w.hd, w.t, self.cu, self.row_ids)
             return
+        if w.kind == "moe":
+            d = self.args
+            o.moe_block(d["x"], d["expert_ids"], d["gates"], d["w_gate"], d["w_up"], d["w_down"])
+            return
         if w.kind == "layer":
             d = self.args
             o.decoder_layer(d["hidden"], d["residual"], d["gamma_attn"], d["w_q"], d["w_k"], d["w_v"], d["w_o"],
@@ -278,6 +291,9 @@ class OracleSample:
         w = self.w
         if w.kind == "attn_core":
             what = f"{self.rows} of {w.T} query rows (evenly spaced) through the causal attention of all {w.nq} q heads"
+        elif w.kind == "moe":
+            what = (f"the first {self.rows} of {w.T} tokens, top-{w.top_k} of {w.experts} experts "
+                    f"(intermediate {w.I}, hidden {w.H})")
         elif w.kind == "layer":
             what = (f"the first {self.rows} of {w.T} tokens ({len(self.cu) - 1} sequence(s)) through the whole "
                     f"layer: norm, QKV, causal attention, o_proj, add + norm, MLP")
@@ -321,11 +337,17 @@ def config_obj(w: workloads.Workload, n: int, rotate: int, decode: bool):
         c["intermediate"] = w.I
         c["sequences"] = int(len(w.seq_lens()))
         c["causal"] = True
+    if w.kind == "moe":
+        for k in ("n_q_heads", "n_kv_heads", "head_dim"):
+            c.pop(k, None)
+        c.update({"intermediate": w.I, "experts": w.experts, "top_k": w.top_k})
     if w.kind == "attn_core":
         c["sequences"] = int(len(w.seq_lens()))
         c["causal"] = True
         qkv_b = 2 * w.T * (w.nq + 2 * (w.nkv if w.t < w.nkv else w.t)) * w.hd
         c["l2"] = f"{rotate} rotating qkv inputs ({rotate * qkv_b / 1e9:.2f} GB) > 129 MB L2"
+    elif w.kind == "moe":
+        c["l2"] = f"expert weights {w.weight_bytes() / 1e9:.2f} GB > 129 MB L2; {rotate} rotating inputs"
     elif w.kind == "layer":
         c["l2"] = (f"weights {w.weight_bytes() / 1e9:.2f} GB and the step's intermediates "
                    f"(h alone {2 * w.T * w.I / 1e9:.2f} GB) > 129 MB L2; {rotate} rotating inputs")
@@ -417,6 +439,25 @@ def run_ours(args, ws, rank, local):
             j = i % R
             blocks[j].gate_up(xs[j], h_out=hbufs[j], ws=wss[j])
         hbufs = [torch.empty(w.t, w.T, w.I // w.t, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    elif w.kind == "moe":
+        d = workloads.moe_inputs(w)
+        cfg = tl.make_config(tl.TP_BLOCK_MOE, w.t, w.H, w.I, n_experts=w.experts)
+        wl = []
+        for e in range(w.experts):
+            wl += [d["w_gate"][e].to(dev), d["w_up"][e].to(dev), d["w_down"][e].to(dev)]
+        blocks = [tl.TPLinear(cfg, wl)]
+        del wl
+        ids = torch.from_numpy(d["expert_ids"]).to(dev)
+        gts = torch.from_numpy(d["gates"]).to(dev)
+        xs = [workloads.draw((w.T, w.H), 1000 + rank * R + r, 0).to(dev) for r in range(R)]
+        outs = [torch.empty_like(xs[0]) for _ in range(R)]
+        wss = [blocks[0].workspace(w.T * w.top_k)]
+        launches_per_step = 5           # routing sort, row gather, grouped gate_up, grouped down, combine
+
+        def step(i):
+            j = i % R
+            blocks[0].moe_forward(xs[j], ids, gts, out=outs[j], ws=wss[0])
+        dominant = step
     elif w.kind == "layer":
         d = workloads.layer_inputs(w, T=1)
         ca = tl.make_config(tl.TP_BLOCK_ATTN_PROJ, w.t, w.H, n_q_heads=w.nq, n_kv_heads=w.nkv, head_dim=w.hd,
@@ -520,8 +561,8 @@ def run_ours(args, ws, rank, local):
     # ---- dominant kernel: in decode the step is a single fused kernel, so its
     # average launch duration is the timed region's per-step time; otherwise the
     # column-parallel GEMM alone, same stream, events around K2 launches
-    if launches_per_step == 1 or w.kind == "attn_core":
-        dom_s = sec                    # attention core: both launches of a step (conservative)
+    if launches_per_step == 1 or w.kind in ("attn_core", "moe"):
+        dom_s = sec                    # attention core, MoE: every launch of a step (conservative)
     else:
         K2 = min(K, 2000 if decode else 20)
         for i in range(3):
@@ -552,6 +593,21 @@ def run_ours(args, ws, rank, local):
             blocks[j].mlp_forward(xs[j], residual=rs[j], out=outs[j], ws=wss[j])
             for k, v in outs[j].items():
                 ho[j][k].copy_(v, non_blocking=True)
+    elif w.kind == "moe":
+        hx = [xs[j].cpu().pin_memory() for j in range(R)]
+        hid = ids.cpu().pin_memory()
+        hg = gts.cpu().pin_memory()
+        ho = [torch.empty(xs[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
+        h2d = hx[0].numel() * 2 + hid.numel() * 4 + hg.numel() * 4
+        d2h = ho[0].numel() * 2
+
+        def e2e_step(i):
+            j = i % R
+            xs[j].copy_(hx[j], non_blocking=True)
+            ids.copy_(hid, non_blocking=True)
+            gts.copy_(hg, non_blocking=True)
+            blocks[0].moe_forward(xs[j], ids, gts, out=outs[j], ws=wss[0])
+            ho[j].copy_(outs[j], non_blocking=True)
     elif w.kind == "layer":
         hx = [xs[j].cpu().pin_memory() for j in range(R)]
         hr = [rs[j].cpu().pin_memory() for j in range(R)]
@@ -616,27 +672,34 @@ def run_ours(args, ws, rank, local):
         unit = "GB/s"
         value = ws * wbytes / sec / 1e9
         e2e_value = ws * wbytes / e2e_s / 1e9
-        fused = launches_per_step == 1
+        fused = launches_per_step == 1 or w.kind == "moe"
         dom_alg = float(wbytes + abytes) if fused else dominant_kernel_bytes(w)
         achieved = dom_alg / dom_s / 1e9
+        if w.kind == "moe":
+            key, kname = "moe@", "the MoE step: routing, gather, grouped expert GEMMs (tc_gemm_kernel), combine"
+        elif fused:
+            key, kname = "mlp_decode@", "fused decode MLP block (mlp_decode_kernel)"
+        else:
+            key, kname = "gate_up@", "gate_up column-parallel GEMM (tc_gemm_kernel<swap, GATE_UP>)"
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"],
-                "traffic": ncu_traffic(("mlp_decode@" if fused else "gate_up@") + w.name),
-                "kernel": ("fused decode MLP block (mlp_decode_kernel)" if fused
-                           else "gate_up column-parallel GEMM (tc_gemm_kernel<swap, GATE_UP>)"),
+                "traffic": ncu_traffic(key + w.name),
+                "kernel": kname,
                 "algorithmic_bytes_per_launch": dom_alg, "avg_launch_us": dom_s * 1e6,
                 "peak_source": pk["source"] + " hbm_gbs (copy, burst)"}
     else:
         unit = "TFLOP/s"
         value = ws * flops / sec / 1e12
         e2e_value = ws * flops / e2e_s / 1e12
-        whole = launches_per_step == 1 or w.kind == "attn_core"
+        whole = launches_per_step == 1 or w.kind in ("attn_core", "moe")
         dom_alg = flops if whole else dominant_kernel_flops(w)
         achieved = dom_alg / dom_s / 1e12
         if w.kind == "attn_core":
             key, kname = "attn_core@", "causal GQA attention (attn_fwd_kernel, with its work-table preparation)"
         elif w.kind == "layer":
             key, kname = "gate_up@", "the layer's gate_up column-parallel GEMM (tc_gemm_pair_kernel<GATE_UP>)"
+        elif w.kind == "moe":
+            key, kname = "moe@", "the MoE step: routing, gather, grouped expert GEMMs (tc_gemm_kernel), combine"
         elif whole:
             key, kname = "attn_proj@", "QKV + o_proj in one launch (tc_gemm_pair_kernel<COL, ROW>)"
         else:

@@ -53,7 +53,7 @@ extern "C" {
 typedef struct tp_linear tp_linear_t; /* opaque handle: shapes, plans, packed-weight pointers */
 typedef void* tp_stream_t;            /* cudaStream_t */
 
-enum { TP_BLOCK_MLP = 0, TP_BLOCK_ATTN_PROJ = 1 };
+enum { TP_BLOCK_MLP = 0, TP_BLOCK_ATTN_PROJ = 1, TP_BLOCK_MOE = 2 };
 enum {
   TP_FLAG_HAS_NORM = 1, /* MLP: fused residual add + RMSNorm in front of gate_up;
                            ATTN: the handle carries the layer's input RMSNorm */
@@ -68,16 +68,16 @@ enum {
 };
 
 typedef struct {
-  int32_t kind;          /* TP_BLOCK_MLP or TP_BLOCK_ATTN_PROJ */
+  int32_t kind;          /* TP_BLOCK_MLP, TP_BLOCK_ATTN_PROJ or TP_BLOCK_MOE */
   int32_t t;             /* logical tensor-parallel size: 1, 2, 4 or 8 */
   int64_t hidden;        /* H */
-  int64_t intermediate;  /* MLP: I, I % t == 0, (I / t) % 8 == 0 */
+  int64_t intermediate;  /* MLP, MOE (per expert): I, I % t == 0, (I / t) % 8 == 0 */
   int32_t n_q_heads;     /* ATTN: nq % t == 0 */
   int32_t n_kv_heads;    /* ATTN: nkv % t == 0, or t % nkv == 0 (kv heads replicated) */
   int32_t head_dim;      /* ATTN: hd % 8 == 0 */
   float rms_eps;         /* with TP_FLAG_HAS_NORM */
   int32_t flags;         /* TP_FLAG_* */
-  int32_t reserved;      /* must be 0 */
+  int32_t n_experts;     /* MOE: experts, 1..256; 0 for the other kinds */
 } tp_config_t;
 
 /*
@@ -225,6 +225,27 @@ int tp_attn_proj_forward(tp_linear_t* h, int64_t T, const void* x, void* qkv_out
 int tp_attention_forward(tp_linear_t* h, int64_t T, const void* qkv, const int32_t* cu_seqlens,
                          int32_t n_seqs, int32_t max_seqlen, void* attn_out, void* workspace,
                          int64_t workspace_bytes, tp_stream_t stream);
+
+/*
+ * Mixture-of-experts block with within-expert tensor parallelism ("Tensor
+ * Parallelism", MoE Expert Parallelism, Within-Expert Parallel: every expert's
+ * FFN is split with the dense column-parallel gate/up and row-parallel down
+ * pattern). A TP_BLOCK_MOE handle holds n_experts experts, created from
+ * w_full = {W_gate_0, W_up_0, W_down_0, W_gate_1, ...} (n_w = 3 * n_experts,
+ * shapes as for the MLP, I per expert); the packed buffers hold the experts one
+ * after another. The routing is the caller's:
+ *   y[i] = sum_{j < top_k} gates[i][j] * FFN_{expert_ids[i][j]}(x[i]),
+ *   FFN_e(x) = sum_r h_r Wdown_e,r^T,  h_r = silu(x Wg_e,r^T) * (x Wu_e,r^T)
+ * x, y: [T, H] bf16; expert_ids: int32 [T][top_k] in [0, n_experts); gates: fp32
+ * [T][top_k] (both device, 4-byte aligned). The slots of a token are added in
+ * order, in fp32, and y is rounded once. Rows go to experts by a stable sort, each
+ * expert's rows padded to 128; every expert's h and output are rounded to bf16.
+ * For an MoE handle, tp_workspace_size's max_tokens counts routed entries
+ * (T * top_k). An id out of range writes TP_ERR_SHAPE to the status word and
+ * y = 0. top_k in [1, n_experts] (else TP_ERR_SHAPE).
+ */
+int tp_moe_forward(tp_linear_t* h, int64_t T, int32_t top_k, const void* x, const int32_t* expert_ids,
+                   const float* gates, void* y, void* workspace, int64_t workspace_bytes, tp_stream_t stream);
 
 /*
  * One whole decoder layer, in the order "vLLM Code Reading (Section 5)" §13-§14

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libtplinear.so")
 TP_OK = 0
 TP_ERR_ARG, TP_ERR_SHAPE, TP_ERR_UNSUPPORTED, TP_ERR_CUDA, TP_ERR_CAPACITY, TP_ERR_TIMEOUT = (
     -1, -2, -3, -4, -5, -6)
-TP_BLOCK_MLP, TP_BLOCK_ATTN_PROJ = 0, 1
+TP_BLOCK_MLP, TP_BLOCK_ATTN_PROJ, TP_BLOCK_MOE = 0, 1, 2
 TP_FLAG_HAS_NORM = 1
 TP_FLAG_GATHERED = 2
 
@@ -30,6 +30,7 @@ ABI_SYMBOLS = (
     "tp_attn_proj_forward", "tp_capture_workspace_size", "tp_capture_rows", "tp_last_error",
     "tp_describe_plan", "tp_mlp_forward_no_alloc", "tp_set_wait_timeout", "tp_attention_forward",
     "tp_layer_create", "tp_layer_destroy", "tp_layer_workspace_size", "tp_decoder_layer_forward",
+    "tp_moe_forward",
 )
 
 
@@ -43,7 +44,7 @@ class Config(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("t", ctypes.c_int32), ("hidden", ctypes.c_int64),
                 ("intermediate", ctypes.c_int64), ("n_q_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("rms_eps", ctypes.c_float), ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("rms_eps", ctypes.c_float), ("flags", ctypes.c_int32), ("n_experts", ctypes.c_int32)]
 
 
 class LayerIO(ctypes.Structure):
@@ -95,6 +96,7 @@ def lib() -> ctypes.CDLL:
         "tp_layer_destroy": [P],
         "tp_layer_workspace_size": [P, PI64],
         "tp_decoder_layer_forward": [P, I64, ctypes.POINTER(LayerIO), P, I64, P],
+        "tp_moe_forward": [P, I64, I32, P, P, P, P, P, I64, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -130,8 +132,9 @@ def _bf16(t: torch.Tensor, name: str) -> torch.Tensor:
 
 
 def make_config(kind: int, t: int, hidden: int, intermediate: int = 0, n_q_heads: int = 0,
-                n_kv_heads: int = 0, head_dim: int = 0, rms_eps: float = 1e-5, flags: int = 0) -> Config:
-    return Config(kind, t, hidden, intermediate, n_q_heads, n_kv_heads, head_dim, rms_eps, flags, 0)
+                n_kv_heads: int = 0, head_dim: int = 0, rms_eps: float = 1e-5, flags: int = 0,
+                n_experts: int = 0) -> Config:
+    return Config(kind, t, hidden, intermediate, n_q_heads, n_kv_heads, head_dim, rms_eps, flags, n_experts)
 
 
 def packed_weight_bytes(cfg: Config):
@@ -273,6 +276,19 @@ class TPLinear:
         _check(lib().tp_down_forward(self.handle, T, _ptr(_bf16(h_in, "h_in")), _ptr(residual), _ptr(out),
                                      _ptr(stream_out), _ptr(ws), ws.numel(), _stream(stream)))
         return out, stream_out
+
+    # ------------------------------------------------------------------ mixture of experts
+    def moe_forward(self, x: torch.Tensor, expert_ids: torch.Tensor, gates: torch.Tensor, out=None, ws=None,
+                    stream=None) -> torch.Tensor:
+        """y [T, H] = sum_j gates[:, j] * expert_{ids[:, j]}(x); ids int32 [T, k], gates fp32 [T, k]."""
+        T, k = expert_ids.shape
+        if expert_ids.dtype != torch.int32 or gates.dtype != torch.float32 or not expert_ids.is_cuda:
+            raise TypeError("expert_ids must be int32 and gates float32 CUDA tensors")
+        out = torch.empty_like(x) if out is None else out
+        ws = self.workspace(T * k) if ws is None else ws
+        _check(lib().tp_moe_forward(self.handle, T, k, _ptr(_bf16(x, "x")), _ptr(expert_ids.contiguous()),
+                                    _ptr(gates.contiguous()), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+        return out
 
     # ------------------------------------------------------------------ attention projections
     def attn_proj_forward(self, x: Optional[torch.Tensor], attn_in: Optional[torch.Tensor],

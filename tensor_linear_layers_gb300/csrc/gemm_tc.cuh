@@ -77,6 +77,13 @@ struct GemmParams {
   __nv_bfloat16* out;
   __nv_bfloat16* out2;         // KIND_ROW: y + resid (nullable)
   const __nv_bfloat16* resid;  // KIND_ROW: residual [T][n_out]
+  // Grouped problems (mixture of experts): token tile tm multiplies the weights of
+  // expert tile_expert[tm] (expert_wbytes apart in w_packed), and only tiles
+  // tm < *m_valid exist (both written on the device before the launch). Null for
+  // one weight matrix. Only the unswapped, unsplit prefill engine takes them.
+  const int* tile_expert;
+  const int* m_valid;
+  long long expert_wbytes;
   float* partials;             // split-K fp32 partials [tile][split][col][128 rows]
   unsigned* gbar;              // grid barrier {arrivals, generation}
   int* status;                 // device status word
@@ -506,12 +513,14 @@ __global__ void __launch_bounds__(192, 1)
         bool second;
         decode_unit(ug, second, tm, tn, sp);
         const GemmParams& q = second ? p2 : p;
+        if (!SWAP && q.tile_expert != nullptr && tm >= *q.m_valid) continue;
         const CUtensorMap* map = second ? &map_act2 : &map_act;
         const bool row_kind = second ? (KIND2 == KIND_ROW) : (KIND == KIND_ROW);
         const int kb0 = (int)((long long)sp * q.nkb / q.splits);
         const int kb1 = (int)((long long)(sp + 1) * q.nkb / q.splits);
         const int wt = SWAP ? tm : tn;
         const uint8_t* wsrc = q.w_packed + (size_t)wt * q.nkb * kWBlockBytes;
+        if (!SWAP && q.tile_expert != nullptr) wsrc += (size_t)q.tile_expert[tm] * (size_t)q.expert_wbytes;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, p.timeout_ns)) {
             if (!*s_abort) {
@@ -567,6 +576,7 @@ __global__ void __launch_bounds__(192, 1)
         bool second;
         decode_unit(ug, second, tm, tn, sp);
         const GemmParams& q = second ? p2 : p;
+        if (!SWAP && q.tile_expert != nullptr && tm >= *q.m_valid) continue;
         const int kb0 = (int)((long long)sp * q.nkb / q.splits);
         const int kb1 = (int)((long long)(sp + 1) * q.nkb / q.splits);
         if (!mbar_wait_bounded(tempty_bar(buf), acc_phase ^ 1u, s_abort, p.timeout_ns)) {
@@ -633,6 +643,7 @@ __global__ void __launch_bounds__(192, 1)
       int tm, tn, sp;
       bool second;
       decode_unit(ug, second, tm, tn, sp);
+      if (!SWAP && (second ? p2 : p).tile_expert != nullptr && tm >= *(second ? p2 : p).m_valid) continue;
       // one thread waits and the decision is shared, so all 128 epilogue
       // threads leave together and no named barrier is left half-joined
       if (et == 0) {

@@ -61,7 +61,11 @@ struct AttnParams {
   int out_rstride;         // q_per * 128, or t * q_per * 128 gathered
   int* status;
   unsigned long long timeout_ns;
-  int T, q_per, kv_per, rep, group, heads;  // group = nq / nkv, heads = t * q_per
+  int T, t, q_per, kv_per, rep, group;
+  // units pair two local q heads that read the same kv head: the shard's heads
+  // form runs of `run` heads per kv head, each run gives `half` = ceil(run / 2)
+  // units (the last single when run is odd), pairs_per_shard in all
+  int run, half, pairs_per_shard;
   float scale_log2;        // log2(e) / sqrt(hd)
 };
 // Builds the (sequence, q tile) table from cu_seqlens (device) into `pairs` and
@@ -81,5 +85,13 @@ struct MlpDecodeParams;
 // The fused decode-shaped MLP block (T <= 128): one cooperative launch.
 cudaError_t launch_mlp_decode(int bn, const CUtensorMap& map_x, const CUtensorMap& map_h,
                               const MlpDecodeParams& P, int grid, cudaStream_t st);
+
+// Mixture of experts (moe.cu): routing sort, row gather, weighted combine.
+cudaError_t launch_moe_route(const int* ids, int n_entries, int k, int E, int max_rows, int* rank, int* perm_row,
+                             int* row_src, int* tile_expert, int* m_valid, int* status, cudaStream_t st);
+cudaError_t launch_moe_gather(const void* x, int H, const int* row_src, const int* m_valid, int max_rows,
+                              void* x_perm, int nsm, cudaStream_t st);
+cudaError_t launch_moe_combine(const void* y_perm, int H, int T, int k, const int* perm_row, const float* gates,
+                               void* y, int nsm, cudaStream_t st);
 
 }  // namespace tpl

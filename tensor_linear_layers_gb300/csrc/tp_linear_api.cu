@@ -225,7 +225,7 @@ struct Plan {
 // force_splits > 0 overrides the split count.
 Plan make_plan(const tp_linear* h, int which, int64_t T, int force_splits = 0) {
   Plan pl{};
-  const bool mlp = h->cfg.kind == TP_BLOCK_MLP;
+  const bool mlp = h->cfg.kind != TP_BLOCK_ATTN_PROJ;
   pl.kind = which == 0 ? (mlp ? KIND_GATE_UP : KIND_COL) : KIND_ROW;
   pl.swap = T <= 128;
   pl.bn = pl.swap ? (T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128) : 256;
@@ -313,6 +313,37 @@ Layout make_layout(const tp_linear* h, int64_t T) {
 // table, 16 B per entry.
 int64_t attn_ws_bytes(const tp_linear* h, int64_t T, int64_t n_seqs) {
   return dyn_off(h) + 512 + 16 * (ceil_div(T, 128) + n_seqs + 1);
+}
+
+// Mixture-of-experts workspace for n_entries routed (token, expert) entries:
+// after the header, the valid tile count, per-entry ranks and rows, the token of
+// every row, the expert of every 128-row tile, then x, h and y in row order.
+// Each expert's rows start on a 128-row boundary: at most n_entries + 127 E rows.
+struct MoeLayout {
+  int64_t max_rows, m_valid, rank, perm_row, row_src, tile_expert, x_perm, h_perm, y_perm, total;
+};
+MoeLayout moe_layout(const tp_linear* h, int64_t n_entries) {
+  MoeLayout L{};
+  L.max_rows = ceil_div(n_entries + (int64_t)h->cfg.n_experts * 127, 128) * 128;
+  int64_t off = dyn_off(h);
+  L.m_valid = off;
+  off = align256(off + 4);
+  L.rank = off;
+  off = align256(off + 4 * n_entries);
+  L.perm_row = off;
+  off = align256(off + 4 * n_entries);
+  L.row_src = off;
+  off = align256(off + 4 * L.max_rows);
+  L.tile_expert = off;
+  off = align256(off + 4 * (L.max_rows / 128));
+  L.x_perm = off;
+  off = align256(off + 2 * L.max_rows * h->H);
+  L.h_perm = off;
+  off = align256(off + 2 * (int64_t)h->cfg.t * L.max_rows * h->Is);
+  L.y_perm = off;
+  off = align256(off + 2 * L.max_rows * h->H);
+  L.total = off;
+  return L;
 }
 
 int check_device(const tp_linear* h) {
@@ -500,15 +531,21 @@ int check_T(int64_t T) {
 
 int validate_cfg(const tp_config_t* c) {
   if (c == nullptr) return fail(TP_ERR_ARG, "config is null");
-  if (c->kind != TP_BLOCK_MLP && c->kind != TP_BLOCK_ATTN_PROJ)
+  if (c->kind != TP_BLOCK_MLP && c->kind != TP_BLOCK_ATTN_PROJ && c->kind != TP_BLOCK_MOE)
     return fail(TP_ERR_ARG, "unknown block kind %d", c->kind);
-  if (c->reserved != 0) return fail(TP_ERR_ARG, "reserved field must be 0");
+  if (c->kind == TP_BLOCK_MOE) {
+    if (c->n_experts < 1 || c->n_experts > 256)
+      return fail(TP_ERR_UNSUPPORTED, "n_experts must be in [1, 256] (got %d)", c->n_experts);
+    if (c->flags != 0) return fail(TP_ERR_ARG, "flags must be 0 for the MoE block");
+  } else if (c->n_experts != 0) {
+    return fail(TP_ERR_ARG, "n_experts must be 0 unless kind is TP_BLOCK_MOE");
+  }
   if (c->t <= 0) return fail(TP_ERR_SHAPE, "t must be positive (got %d)", c->t);
   if ((c->t & (c->t - 1)) != 0 || c->t > 8)
     return fail(TP_ERR_UNSUPPORTED, "t must be a power of 2 in [1, 8] (got %d)", c->t);
   if (c->hidden <= 0 || c->hidden > (1 << 20)) return fail(TP_ERR_SHAPE, "hidden out of range");
   if (c->hidden % 8 != 0) return fail(TP_ERR_UNSUPPORTED, "hidden must be a multiple of 8");
-  if (c->kind == TP_BLOCK_MLP) {
+  if (c->kind != TP_BLOCK_ATTN_PROJ) {
     if (c->intermediate <= 0 || c->intermediate > (1 << 22))
       return fail(TP_ERR_SHAPE, "intermediate out of range");
     if (c->intermediate % c->t != 0)
@@ -539,7 +576,7 @@ void derive(tp_linear* h) {
   const tp_config_t& c = h->cfg;
   h->H = c.hidden;
   const int t = c.t;
-  if (c.kind == TP_BLOCK_MLP) {
+  if (c.kind != TP_BLOCK_ATTN_PROJ) {
     h->I = c.intermediate;
     h->Is = c.intermediate / t;
     h->Ks = h->Is;
@@ -558,7 +595,7 @@ void derive(tp_linear* h) {
     h->Ks = (int64_t)c.n_q_heads * c.head_dim / t;
   }
   h->nkb_col = (int)ceil_div(h->H, 64);
-  if (c.kind == TP_BLOCK_MLP) {
+  if (c.kind != TP_BLOCK_ATTN_PROJ) {
     h->nb = (int)ceil_div(h->Is, 128);
     h->wt_col = t * h->nb;
   } else {
@@ -584,8 +621,9 @@ int tp_packed_weight_bytes(const tp_config_t* cfg, int64_t* col_bytes, int64_t* 
   tp_linear tmp{};
   tmp.cfg = *cfg;
   derive(&tmp);
-  *col_bytes = (int64_t)tmp.wt_col * tmp.nkb_col * kWBlockBytes;
-  *row_bytes = (int64_t)tmp.wt_row * tmp.nkb_row * kWBlockBytes;
+  const int64_t E = cfg->kind == TP_BLOCK_MOE ? cfg->n_experts : 1;
+  *col_bytes = E * tmp.wt_col * tmp.nkb_col * kWBlockBytes;
+  *row_bytes = E * tmp.wt_row * tmp.nkb_row * kWBlockBytes;
   return ok();
 }
 
@@ -596,8 +634,9 @@ int tp_linear_create(const tp_config_t* cfg, const void* const* w_full, int32_t 
   *out = nullptr;
   int rc = validate_cfg(cfg);
   if (rc) return rc;
-  const bool mlp = cfg->kind == TP_BLOCK_MLP;
-  const int need = mlp ? 3 : 4;
+  const bool mlp = cfg->kind != TP_BLOCK_ATTN_PROJ;
+  const int n_exp = cfg->kind == TP_BLOCK_MOE ? cfg->n_experts : 1;
+  const int need = mlp ? 3 * n_exp : 4;
   if (w_full == nullptr || n_w != need)
     return fail(TP_ERR_ARG, "expected %d full weight pointers, got %d", need, n_w);
   for (int i = 0; i < need; ++i) TP_CHECK_PTR(w_full[i], "w_full[i]");
@@ -648,8 +687,19 @@ int tp_linear_create(const tp_config_t* cfg, const void* const* w_full, int32_t 
   pr.Is = h->Ks;
   pr.kbs = h->kbs_row;
   pr.nkb = h->nkb_row;
-  e = launch_pack(pc, (int64_t)h->wt_col * h->nkb_col, w_col_packed, st);
-  if (e == cudaSuccess) e = launch_pack(pr, (int64_t)h->wt_row * h->nkb_row, w_row_packed, st);
+  // experts one after another, each in the dense layout
+  const int64_t col_blocks = (int64_t)h->wt_col * h->nkb_col, row_blocks = (int64_t)h->wt_row * h->nkb_row;
+  e = cudaSuccess;
+  for (int x = 0; x < n_exp && e == cudaSuccess; ++x) {
+    if (mlp) {
+      pc.src[0] = static_cast<const __nv_bfloat16*>(w_full[3 * x]);
+      pc.src[1] = static_cast<const __nv_bfloat16*>(w_full[3 * x + 1]);
+      pr.src[0] = static_cast<const __nv_bfloat16*>(w_full[3 * x + 2]);
+    }
+    e = launch_pack(pc, col_blocks, static_cast<uint8_t*>(w_col_packed) + x * col_blocks * kWBlockBytes, st);
+    if (e == cudaSuccess)
+      e = launch_pack(pr, row_blocks, static_cast<uint8_t*>(w_row_packed) + x * row_blocks * kWBlockBytes, st);
+  }
   if (e != cudaSuccess) {
     delete h;
     return cuda_fail(e, "weight packing");
@@ -670,6 +720,10 @@ int tp_workspace_size(const tp_linear_t* h, int64_t max_tokens, int64_t* bytes) 
   // Up to 128 tokens every T has its own plan; beyond, a plan depends on T only
   // through the number of 128-token tiles, and the buffers grow with T, so the
   // largest T of each tile count bounds that count.
+  if (h->cfg.kind == TP_BLOCK_MOE) {   // max_tokens counts routed entries (tokens x top_k)
+    *bytes = moe_layout(h, max_tokens).total;
+    return ok();
+  }
   int64_t best = dyn_off(h);
   for (int64_t T = 1; T <= std::min<int64_t>(max_tokens, kFusedMaxT); ++T)
     best = std::max(best, make_layout(h, T).total);
@@ -909,15 +963,95 @@ int tp_attention_forward(tp_linear_t* h, int64_t T, const void* qkv, const int32
   p.q_per = h->q_per;
   p.kv_per = h->kv_per;
   p.rep = h->rep;
+  p.t = h->cfg.t;
   p.group = h->cfg.n_q_heads / h->cfg.n_kv_heads;
-  p.heads = h->cfg.t * h->q_per;
+  p.run = std::min(p.group, p.q_per);
+  p.half = (p.run + 1) / 2;
+  p.pairs_per_shard = p.q_per / p.run * p.half;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)h->cfg.head_dim));
-  const int64_t max_units = (ceil_div(T, 128) + n_seqs) * p.heads;
+  const int64_t max_units = (ceil_div(T, 128) + n_seqs) * p.t * p.pairs_per_shard;
   const int grid = (int)std::min<int64_t>(h->nsm, max_units);
   const cudaError_t e =
       launch_attention(map_qkv, p, cu_seqlens, n_seqs, max_tiles, const_cast<int4*>(p.pairs),
                        const_cast<int*>(p.n_pairs), grid, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return ok();
+}
+
+int tp_moe_forward(tp_linear_t* h, int64_t T, int32_t top_k, const void* x, const int32_t* expert_ids,
+                   const float* gates, void* y, void* workspace, int64_t workspace_bytes, tp_stream_t stream) {
+  if (h == nullptr) return fail(TP_ERR_ARG, "handle is null");
+  if (h->cfg.kind != TP_BLOCK_MOE) return fail(TP_ERR_ARG, "not an MoE handle");
+  int rc = check_T(T);
+  if (rc) return rc;
+  const int E = h->cfg.n_experts;
+  if (top_k < 1 || top_k > E) return fail(TP_ERR_SHAPE, "top_k must be in [1, n_experts] (got %d)", top_k);
+  if (T == 0) return ok();
+  const int64_t N = T * top_k;
+  if (N > (1 << 24)) return fail(TP_ERR_UNSUPPORTED, "more than 16777216 routed entries");
+  TP_CHECK_PTR(x, "x");
+  TP_CHECK_PTR(y, "y");
+  if (expert_ids == nullptr || (reinterpret_cast<uintptr_t>(expert_ids) & 3u) != 0)
+    return fail(TP_ERR_ARG, "expert_ids is null or not 4-byte aligned");
+  if (gates == nullptr || (reinterpret_cast<uintptr_t>(gates) & 3u) != 0)
+    return fail(TP_ERR_ARG, "gates is null or not 4-byte aligned");
+  if (workspace == nullptr || !aligned16(workspace)) return fail(TP_ERR_ARG, "workspace is null or not 16-byte aligned");
+  const MoeLayout L = moe_layout(h, N);
+  if (workspace_bytes < L.total)
+    return fail(TP_ERR_ARG, "workspace too small: %lld bytes, %lld needed for %lld routed entries",
+                (long long)workspace_bytes, (long long)L.total, (long long)N);
+  if ((rc = check_device(h))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* m_valid = reinterpret_cast<int*>(ws + L.m_valid);
+  int* tile_expert = reinterpret_cast<int*>(ws + L.tile_expert);
+  int* perm_row = reinterpret_cast<int*>(ws + L.perm_row);
+  const int64_t R = L.max_rows;
+  cudaError_t e = launch_moe_route(expert_ids, (int)N, top_k, E, (int)R, reinterpret_cast<int*>(ws + L.rank), perm_row,
+                                   reinterpret_cast<int*>(ws + L.row_src), tile_expert, m_valid,
+                                   reinterpret_cast<int*>(ws), st);
+  if (e == cudaSuccess)
+    e = launch_moe_gather(x, (int)h->H, reinterpret_cast<int*>(ws + L.row_src), m_valid, (int)R, ws + L.x_perm,
+                          h->nsm, st);
+  if (e != cudaSuccess) return cuda_fail(e, "MoE routing launch");
+  // grouped GEMMs: every 128-row tile belongs to one expert; tiles past *m_valid are skipped
+  for (int which = 0; which < 2; ++which) {
+    Plan pl{};
+    pl.swap = false;
+    pl.kind = which == 0 ? KIND_GATE_UP : KIND_ROW;
+    pl.bn = 256;
+    pl.splits = 1;
+    pl.m_tiles = (int)(R / 128);
+    pl.n_tiles = which == 0 ? h->wt_col : h->wt_row;
+    pl.nkb = which == 0 ? h->nkb_col : h->nkb_row;
+    pl.kbs = which == 0 ? 0 : h->kbs_row;
+    pl.nb = which == 0 ? h->nb : 0;
+    pl.units = pl.m_tiles * pl.n_tiles;
+    pl.grid = std::min(pl.units, h->nsm);
+    CUtensorMap map_a;
+    rc = which == 0 ? make_map(&map_a, ws + L.x_perm, h->H, R, 1, 1, 128)
+                    : make_shard_map(&map_a, ws + L.h_perm, h->Is, R, h->cfg.t, 3, false, 128);
+    if (rc) return rc;
+    GemmParams p = base_params(pl, R, workspace, 0, which == 0 ? kGbarColOff : kGbarRowOff);
+    p.tile_expert = tile_expert;
+    p.m_valid = m_valid;
+    p.expert_wbytes = (long long)pl.n_tiles * pl.nkb * kWBlockBytes;
+    if (which == 0) {
+      p.out = reinterpret_cast<__nv_bfloat16*>(ws + L.h_perm);
+      p.Is = (int)h->Is;
+      set_col_out(p, h, R, h->Is, false);
+      p.w_packed = static_cast<const uint8_t*>(h->w_col);
+    } else {
+      p.n_out = (int)h->H;
+      p.ws_out = (int)h->H;
+      p.out = reinterpret_cast<__nv_bfloat16*>(ws + L.y_perm);
+      p.w_packed = static_cast<const uint8_t*>(h->w_row);
+    }
+    e = launch_gemm(false, pl.kind, pl.bn, map_a, p, pl.grid, st);
+    if (e != cudaSuccess) return cuda_fail(e, "grouped expert GEMM launch");
+  }
+  e = launch_moe_combine(ws + L.y_perm, (int)h->H, (int)T, top_k, perm_row, gates, y, h->nsm, st);
+  if (e != cudaSuccess) return cuda_fail(e, "MoE combine launch");
   return ok();
 }
 

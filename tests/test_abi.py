@@ -180,3 +180,24 @@ def test_norm_without_residual_passes_host_checks(L):
     # a first layer has no incoming residual: residual_in may be NULL (T = 0: nothing launched)
     p = ctypes.c_void_p(0x10000)
     assert L.tp_add_rms_norm(0, 512, p, None, p, 1e-5, p, p, None) == tl.TP_OK
+
+
+def test_moe_config_and_packing(L):
+    # each expert is packed in the dense MLP layout, experts one after another
+    dense = tl.packed_weight_bytes(cfg_mlp(t=4, H=512, I=1024))
+    moe = tl.packed_weight_bytes(tl.make_config(tl.TP_BLOCK_MOE, 4, 512, 1024, n_experts=8))
+    assert moe == (8 * dense[0], 8 * dense[1])
+    for cfg, code in [
+        (tl.make_config(tl.TP_BLOCK_MOE, 4, 512, 1024, n_experts=0), tl.TP_ERR_UNSUPPORTED),
+        (tl.make_config(tl.TP_BLOCK_MOE, 4, 512, 1024, n_experts=257), tl.TP_ERR_UNSUPPORTED),
+        (tl.make_config(tl.TP_BLOCK_MOE, 4, 512, 1026, n_experts=8), tl.TP_ERR_SHAPE),
+        (tl.make_config(tl.TP_BLOCK_MOE, 4, 512, 1024, n_experts=8, flags=tl.TP_FLAG_HAS_NORM), tl.TP_ERR_ARG),
+        (tl.make_config(tl.TP_BLOCK_MLP, 4, 512, 1024, n_experts=2), tl.TP_ERR_ARG),
+    ]:
+        with pytest.raises(tl.TPError) as e:
+            tl.packed_weight_bytes(cfg)
+        assert e.value.code == code
+
+
+def test_moe_forward_rejects_null_handle(L):
+    assert L.tp_moe_forward(None, 4, 2, None, None, None, None, None, 0, None) == tl.TP_ERR_ARG

@@ -43,7 +43,7 @@ TENSOR_TYPES = {"residual_stream": 0, "attn_out": 1, "mlp_out": 2, "final_norm":
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str                 # "mlp", "attn" (projections), "attn_core" (attention core) or "layer"
+    kind: str                 # "mlp", "attn" (projections), "attn_core" (attention core), "layer" or "moe"
     T: int                    # tokens in the step
     H: int                    # hidden size
     t: int                    # logical tensor-parallel shards
@@ -57,6 +57,8 @@ class Workload:
     requests: int = 0         # ragged batch: number of requests (0 = not ragged)
     mean_len: int = 0
     capture_frac: float = 0.0
+    experts: int = 0          # moe: experts (each an MLP of intermediate size I)
+    top_k: int = 0            # moe: experts per token
     seed: int = 0
     desc: str = field(default="", compare=False)
 
@@ -77,6 +79,8 @@ class Workload:
         return 2.0 * self.T * self.H * qkv_n + 2.0 * self.T * self.nq * self.hd * self.H
 
     def flops(self) -> float:
+        if self.kind == "moe":                # every routed (token, expert) entry through one expert MLP
+            return self.top_k * self.mlp_flops()
         if self.kind == "attn_core":
             return self.attn_core_flops()
         if self.kind == "mlp":
@@ -89,6 +93,8 @@ class Workload:
         proj = 2 * (self.H * (self.nq + 2 * self.nkv) * self.hd + self.nq * self.hd * self.H)
         if self.kind == "attn_core":
             return 0
+        if self.kind == "moe":
+            return self.experts * 2 * 3 * self.H * self.I
         if self.kind == "mlp":
             return 2 * 3 * self.H * self.I
         if self.kind == "layer":
@@ -102,6 +108,8 @@ class Workload:
             return 2 * T * (self.nq + 2 * self.nkv) * self.hd + 2 * T * self.nq * self.hd
         if self.kind == "layer":             # hidden, residual in; r1, attn_out, r2, mlp_out, stream out
             return 2 * T * H * 7
+        if self.kind == "moe":               # x in, y out
+            return 2 * T * H * 2
         if self.kind == "mlp":
             b = 2 * T * H * 2                # x (or a) in, mlp_out
             if self.norm:
@@ -138,6 +146,12 @@ WORKLOADS = {
         w_std=0.02, norm=True, requests=64, mean_len=32, capture_frac=0.1,
         desc="Ragged continuous batch, Qwen2.5-7B-shaped decoder layer with attn_out / mlp_out / "
              "residual_stream capture, 2048 tokens / 64 requests, t=4"),
+    "mixtral_8x7b_moe_prefill": Workload(
+        "mixtral_8x7b_moe_prefill", "moe", T=4096, H=4096, I=14336, t=4, w_std=0.02, experts=8, top_k=2,
+        desc="Mixtral-8x7B-shaped MoE block prefill, 4096 tokens, top-2 of 8 experts, each expert split t=4"),
+    "mixtral_8x7b_moe_decode": Workload(
+        "mixtral_8x7b_moe_decode", "moe", T=32, H=4096, I=14336, t=4, w_std=0.02, experts=8, top_k=2,
+        desc="Mixtral-8x7B-shaped MoE block decode, 32 tokens, top-2 of 8 experts, each expert split t=4"),
     "llama3_70b_mlp_prefill": Workload(
         "llama3_70b_mlp_prefill", "mlp", T=8192, H=8192, I=28672, t=8, w_std=0.015,
         desc="Llama-3-70B-shaped MLP prefill, 8192 tokens, t=8"),
@@ -247,6 +261,32 @@ def layer_inputs(w: Workload, T: int | None = None) -> dict:
         "w_down": draw((H, I), s, 9, b=w.w_std),
         "gamma_mlp": draw((H,), s, 10, kind="uniform", a=0.9, b=1.1),
     }
+
+
+def moe_inputs(w: Workload, T: int | None = None) -> dict:
+    """Inputs of an MoE block: x ~ N(0, 1), per-expert gate/up/down weights, and the
+    routing. Routing recipe: numpy default_rng(seed + 7); expert popularity
+    p_e proportional to (e + 1)^-0.5 (a skewed load); each token takes top_k
+    distinct experts drawn with those probabilities; its gates are U(0.1, 1)
+    draws scaled to sum to one (the shape of a softmax over the chosen logits)."""
+    T = w.T if T is None else T
+    H, I, s = w.H, w.I, w.seed
+    d = {"x": draw((T, H), s, 0)}
+    d["w_gate"] = [draw((I, H), s, 2 + 3 * e, b=w.w_std) for e in range(w.experts)]
+    d["w_up"] = [draw((I, H), s, 3 + 3 * e, b=w.w_std) for e in range(w.experts)]
+    d["w_down"] = [draw((H, I), s, 4 + 3 * e, b=w.w_std) for e in range(w.experts)]
+    d.update(moe_routing(w, T))
+    return d
+
+
+def moe_routing(w: Workload, T: int) -> dict:
+    rng = np.random.default_rng(w.seed + 7)
+    pop = 1.0 / np.sqrt(np.arange(1, w.experts + 1))
+    pop = pop / pop.sum()
+    ids = np.stack([rng.choice(w.experts, w.top_k, replace=False, p=pop) for _ in range(T)]).astype(np.int32)
+    u = rng.uniform(0.1, 1.0, (T, w.top_k))
+    gates = (u / u.sum(axis=1, keepdims=True)).astype(np.float32)
+    return {"expert_ids": ids.reshape(T, w.top_k), "gates": gates}
 
 
 def ragged_batch(w: Workload) -> dict:
