@@ -61,11 +61,7 @@ struct AttnParams {
   int out_rstride;         // q_per * 128, or t * q_per * 128 gathered
   int* status;
   unsigned long long timeout_ns;
-  int T, t, q_per, kv_per, rep, group;
-  // units pair two local q heads that read the same kv head: the shard's heads
-  // form runs of `run` heads per kv head, each run gives `half` = ceil(run / 2)
-  // units (the last single when run is odd), pairs_per_shard in all
-  int run, half, pairs_per_shard;
+  int T, q_per, kv_per, rep, group, heads;  // group = nq / nkv, heads = t * q_per
   float scale_log2;        // log2(e) / sqrt(hd)
 };
 // Builds the (sequence, q tile) table from cu_seqlens (device) into `pairs` and

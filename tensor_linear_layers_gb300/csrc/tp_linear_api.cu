@@ -963,13 +963,10 @@ int tp_attention_forward(tp_linear_t* h, int64_t T, const void* qkv, const int32
   p.q_per = h->q_per;
   p.kv_per = h->kv_per;
   p.rep = h->rep;
-  p.t = h->cfg.t;
   p.group = h->cfg.n_q_heads / h->cfg.n_kv_heads;
-  p.run = std::min(p.group, p.q_per);
-  p.half = (p.run + 1) / 2;
-  p.pairs_per_shard = p.q_per / p.run * p.half;
+  p.heads = h->cfg.t * h->q_per;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)h->cfg.head_dim));
-  const int64_t max_units = (ceil_div(T, 128) + n_seqs) * p.t * p.pairs_per_shard;
+  const int64_t max_units = (ceil_div(T, 128) + n_seqs) * p.heads;
   const int grid = (int)std::min<int64_t>(h->nsm, max_units);
   const cudaError_t e =
       launch_attention(map_qkv, p, cu_seqlens, n_seqs, max_tiles, const_cast<int4*>(p.pairs),

@@ -152,3 +152,24 @@ def test_projection_attention_projection_chain():
     g = o.double().cpu().numpy()
     assert float(np.max(np.abs(g - ref_o)) / np.max(np.abs(ref_o))) <= TOL
     assert status_of(blk.workspace(T)) == 0
+
+
+@pytest.mark.parametrize("how", ["one_row", "whole_tile"])
+def test_running_max_jump_rescales_o(how):
+    # the running max grows by more than the lazy threshold at a later key tile: for a
+    # single query row (one lane of a warp) or for every row (a whole scaled key tile)
+    nq, nkv, t, lens = 8, 2, 2, [500]
+    blk, _ = make_attn(256, nq, nkv, t)
+    q_per, kv_per = nq // t, nkv // t
+    qkv = workloads.draw((t, 500, qkv_width(nq, nkv, t)), 14, 0).float()
+    kc = slice(q_per * 128, (q_per + kv_per) * 128)             # every k head of a shard
+    if how == "one_row":
+        # key 300 = 8 x query 350 (head 0's kv head): only row 350 sees a score jump
+        qkv[:, 300, q_per * 128:q_per * 128 + 128] = 8.0 * qkv[:, 350, 0:128]
+    else:
+        qkv[:, 256:384, kc] *= 6.0                               # key tile 2 of every sequence row
+    qkv = qkv.to(torch.bfloat16)
+    out, cu = run(blk, qkv, lens)
+    ref = oracle.attention_core(qkv, nq, nkv, 128, t, cu.cpu().numpy())
+    assert rel_err_shards(out, ref) <= TOL
+    assert status_of(blk.workspace(500)) == 0
