@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(192, 1)
   const int pu1 = ((p.m_tiles + 1) >> 1) * p.n_tiles;
   const int pu_all = pu1 + (kTwo ? ((p2.m_tiles + 1) >> 1) * p2.n_tiles : 0);
   // pair unit -> (problem, token tile of this CTA, weight tile); grouped along M
-  auto decode = [&](int pu, bool& second, int& tm, int& tn) {
+  // pm: the pair of token tiles; grouped problems look the tiles up (false: pair skipped)
+  auto decode = [&](int pu, bool& second, int& tm, int& tn, int& pm) -> bool {
     second = kTwo && pu >= pu1;
     const GemmParams& q = second ? p2 : p;
     const int u = second ? pu - pu1 : pu;
@@ -88,9 +89,16 @@ __global__ void __launch_bounds__(192, 1)
     const int rem = m_pairs - first;
     const int gm = rem < gm_pairs ? rem : gm_pairs;
     const int in_g = u - g * group_size;
-    const int pm = first + in_g % gm;
+    pm = first + in_g % gm;
     tn = in_g / gm;
+    if (q.pair_tiles != nullptr) {
+      if (pm >= *q.pair_count) return false;
+      tm = q.pair_tiles[2 * pm + rank];
+      if (tm < 0) tm = q.m_tiles;   // no second tile: rows past the buffer read as zero, none stored
+      return true;
+    }
     tm = 2 * pm + rank;     // may be a tile past T: its rows read as zero and are not stored
+    return true;
   };
   auto fail = [&](const GemmParams& q) {
     if (!*s_abort) {
@@ -109,13 +117,15 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t issued_mask = 0, last_phase_bits = 0;
       bool ok = true;
       for (int pu = cluster; pu < pu_all && ok; pu += nclusters) {
-        int tm, tn;
+        int tm, tn, pm;
         bool second;
-        decode(pu, second, tm, tn);
+        if (!decode(pu, second, tm, tn, pm)) continue;
         const GemmParams& q = second ? p2 : p;
         const CUtensorMap* map = second ? &map_act2 : &map_act;
         const bool row_kind = second ? (KIND2 == KIND_ROW) : (KIND == KIND_ROW);
         const uint8_t* wsrc = q.w_packed + (size_t)tn * q.nkb * kWBlockBytes + rank * kHalfB;
+        if (q.pair_tiles != nullptr)   // both tiles of a pair belong to the expert of its first
+          wsrc += (size_t)q.tile_expert[q.pair_tiles[2 * pm]] * (size_t)q.expert_wbytes;
         for (int kb = 0; kb < q.nkb; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, q.timeout_ns)) {
             fail(q);
@@ -158,9 +168,9 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int pu = cluster; pu < pu_all && ok; pu += nclusters) {
-        int tm, tn;
+        int tm, tn, pm;
         bool second;
-        decode(pu, second, tm, tn);
+        if (!decode(pu, second, tm, tn, pm)) continue;
         const GemmParams& q = second ? p2 : p;
         if (!mbar_wait_bounded(tempty_bar(buf), acc_phase ^ 1u, s_abort, q.timeout_ns)) {
           fail(q);
@@ -210,9 +220,9 @@ __global__ void __launch_bounds__(192, 1)
     constexpr int CH = 32;
     float g[CH], uu[CH];
     for (int pu = cluster; pu < pu_all; pu += nclusters) {
-      int tm, tn;
+      int tm, tn, pm;
       bool second;
-      decode(pu, second, tm, tn);
+      if (!decode(pu, second, tm, tn, pm)) continue;
       if (et == 0) {
         const bool ok = mbar_wait_bounded(tfull_bar(buf), acc_phase, s_abort, p.timeout_ns);
         if (!ok) fail(p);

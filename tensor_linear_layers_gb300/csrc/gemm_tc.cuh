@@ -84,6 +84,11 @@ struct GemmParams {
   const int* tile_expert;
   const int* m_valid;
   long long expert_wbytes;
+  // CTA-pair engine on grouped problems: pair pm runs token tiles pair_tiles[2 pm]
+  // and pair_tiles[2 pm + 1] (-1: no second tile), both of one expert; only pairs
+  // pm < *pair_count exist
+  const int* pair_tiles;
+  const int* pair_count;
   float* partials;             // split-K fp32 partials [tile][split][col][128 rows]
   unsigned* gbar;              // grid barrier {arrivals, generation}
   int* status;                 // device status word

@@ -84,7 +84,8 @@ cudaError_t launch_mlp_decode(int bn, const CUtensorMap& map_x, const CUtensorMa
 
 // Mixture of experts (moe.cu): routing sort, row gather, weighted combine.
 cudaError_t launch_moe_route(const int* ids, int n_entries, int k, int E, int max_rows, int* rank, int* perm_row,
-                             int* row_src, int* tile_expert, int* m_valid, int* status, cudaStream_t st);
+                             int* row_src, int* tile_expert, int* m_valid, int* pair_tiles, int* pair_count,
+                             int* status, cudaStream_t st);
 cudaError_t launch_moe_gather(const void* x, int H, const int* row_src, const int* m_valid, int max_rows,
                               void* x_perm, int nsm, cudaStream_t st);
 cudaError_t launch_moe_combine(const void* y_perm, int H, int T, int k, const int* perm_row, const float* gates,

@@ -7,7 +7,9 @@
 //                       a 128-row boundary, so no token tile mixes experts:
 //                       tile m belongs to tile_expert[m], m < *m_valid.
 //                       perm_row[entry] = its row; row_src[row] = its token
-//                       (-1 for padding rows)
+//                       (-1 for padding rows). For the CTA-pair engine it
+//                       also lists each expert's tiles two by two
+//                       (pair_tiles, -1 when an expert's last tile is alone)
 //   moe_gather_kernel   x_perm[row] = x[row_src[row]] (zero for padding)
 //   (grouped gate_up and down GEMMs on x_perm, per-tile expert weights)
 //   moe_combine_kernel  y[i] = sum_j gate[i][j] * y_perm[perm_row[i*k + j]],
@@ -31,7 +33,8 @@ constexpr int kRouteWarps = kRouteThreads / 32;
 __global__ void __launch_bounds__(kRouteThreads, 1)
     moe_route_kernel(const int* __restrict__ ids, int n_entries, int k, int E, int max_rows,
                      int* __restrict__ rank, int* __restrict__ perm_row, int* __restrict__ row_src,
-                     int* __restrict__ tile_expert, int* __restrict__ m_valid, int* __restrict__ status) {
+                     int* __restrict__ tile_expert, int* __restrict__ m_valid, int* __restrict__ pair_tiles,
+                     int* __restrict__ pair_count, int* __restrict__ status) {
   extern __shared__ int sm[];
   int* cnt = sm;
   int* off = cnt + E;
@@ -77,6 +80,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     for (int i = tid; i < n_entries; i += kRouteThreads) perm_row[i] = -1;
     if (tid == 0) {
       *m_valid = 0;
+      *pair_count = 0;
       atomicExch(status, -2);  // TP_ERR_SHAPE
     }
     return;
@@ -97,6 +101,19 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     int x = 0;
     while (off[x + 1] <= m * 128) ++x;
     tile_expert[m] = x;
+  }
+  if (tid == 0) {
+    // pairs of tiles of one expert, experts in order (the CTA-pair engine)
+    int np = 0;
+    for (int x = 0; x < E; ++x) {
+      const int t0 = off[x] / 128, nt = (off[x + 1] - off[x]) / 128;
+      for (int i = 0; i < nt; i += 2) {
+        pair_tiles[2 * np] = t0 + i;
+        pair_tiles[2 * np + 1] = i + 1 < nt ? t0 + i + 1 : -1;
+        ++np;
+      }
+    }
+    *pair_count = np;
   }
   __syncthreads();
   for (int i = tid; i < n_entries; i += kRouteThreads) {
@@ -152,14 +169,15 @@ __global__ void moe_combine_kernel(const __nv_bfloat16* __restrict__ y_perm, int
 }
 
 cudaError_t launch_moe_route(const int* ids, int n_entries, int k, int E, int max_rows, int* rank, int* perm_row,
-                             int* row_src, int* tile_expert, int* m_valid, int* status, cudaStream_t st) {
+                             int* row_src, int* tile_expert, int* m_valid, int* pair_tiles, int* pair_count,
+                             int* status, cudaStream_t st) {
   const size_t smem = sizeof(int) * ((size_t)E + E + 1 + (size_t)kRouteWarps * E);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   moe_route_kernel<<<1, kRouteThreads, smem, st>>>(ids, n_entries, k, E, max_rows, rank, perm_row, row_src,
-                                                   tile_expert, m_valid, status);
+                                                   tile_expert, m_valid, pair_tiles, pair_count, status);
   return cudaGetLastError();
 }
 

@@ -320,14 +320,17 @@ int64_t attn_ws_bytes(const tp_linear* h, int64_t T, int64_t n_seqs) {
 // every row, the expert of every 128-row tile, then x, h and y in row order.
 // Each expert's rows start on a 128-row boundary: at most n_entries + 127 E rows.
 struct MoeLayout {
-  int64_t max_rows, m_valid, rank, perm_row, row_src, tile_expert, x_perm, h_perm, y_perm, total;
+  int64_t max_rows, max_pairs, m_valid, pair_count, rank, perm_row, row_src, tile_expert, pair_tiles, x_perm, h_perm,
+      y_perm, total;
 };
 MoeLayout moe_layout(const tp_linear* h, int64_t n_entries) {
   MoeLayout L{};
   L.max_rows = ceil_div(n_entries + (int64_t)h->cfg.n_experts * 127, 128) * 128;
+  L.max_pairs = L.max_rows / 256 + h->cfg.n_experts;   // each expert leaves at most one lone tile
   int64_t off = dyn_off(h);
   L.m_valid = off;
-  off = align256(off + 4);
+  L.pair_count = off + 4;
+  off = align256(off + 8);
   L.rank = off;
   off = align256(off + 4 * n_entries);
   L.perm_row = off;
@@ -336,6 +339,8 @@ MoeLayout moe_layout(const tp_linear* h, int64_t n_entries) {
   off = align256(off + 4 * L.max_rows);
   L.tile_expert = off;
   off = align256(off + 4 * (L.max_rows / 128));
+  L.pair_tiles = off;
+  off = align256(off + 8 * L.max_pairs);
   L.x_perm = off;
   off = align256(off + 2 * L.max_rows * h->H);
   L.h_perm = off;
@@ -1004,14 +1009,20 @@ int tp_moe_forward(tp_linear_t* h, int64_t T, int32_t top_k, const void* x, cons
   int* tile_expert = reinterpret_cast<int*>(ws + L.tile_expert);
   int* perm_row = reinterpret_cast<int*>(ws + L.perm_row);
   const int64_t R = L.max_rows;
+  int* pair_tiles = reinterpret_cast<int*>(ws + L.pair_tiles);
+  int* pair_count = reinterpret_cast<int*>(ws + L.pair_count);
   cudaError_t e = launch_moe_route(expert_ids, (int)N, top_k, E, (int)R, reinterpret_cast<int*>(ws + L.rank), perm_row,
-                                   reinterpret_cast<int*>(ws + L.row_src), tile_expert, m_valid,
-                                   reinterpret_cast<int*>(ws), st);
+                                   reinterpret_cast<int*>(ws + L.row_src), tile_expert, m_valid, pair_tiles,
+                                   pair_count, reinterpret_cast<int*>(ws), st);
   if (e == cudaSuccess)
     e = launch_moe_gather(x, (int)h->H, reinterpret_cast<int*>(ws + L.row_src), m_valid, (int)R, ws + L.x_perm,
                           h->nsm, st);
   if (e != cudaSuccess) return cuda_fail(e, "MoE routing launch");
-  // grouped GEMMs: every 128-row tile belongs to one expert; tiles past *m_valid are skipped
+  // grouped GEMMs: every 128-row tile belongs to one expert; tiles past *m_valid are skipped.
+  // With about a tile or more per expert the CTA-pair engine takes them, two tiles of one
+  // expert sharing each weight block.
+  const int ncl = pair_max_clusters();
+  const bool pairs = pair_engine_enabled() && ncl > 0 && N >= 128LL * E;
   for (int which = 0; which < 2; ++which) {
     Plan pl{};
     pl.swap = false;
@@ -1044,7 +1055,14 @@ int tp_moe_forward(tp_linear_t* h, int64_t T, int32_t top_k, const void* x, cons
       p.out = reinterpret_cast<__nv_bfloat16*>(ws + L.y_perm);
       p.w_packed = static_cast<const uint8_t*>(h->w_row);
     }
-    e = launch_gemm(false, pl.kind, pl.bn, map_a, p, pl.grid, st);
+    if (pairs) {
+      p.m_tiles = (int)(2 * L.max_pairs);
+      p.pair_tiles = pair_tiles;
+      p.pair_count = pair_count;
+      e = launch_gemm_pair(pl.kind, -1, map_a, p, map_a, p, ncl, st);
+    } else {
+      e = launch_gemm(false, pl.kind, pl.bn, map_a, p, pl.grid, st);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "grouped expert GEMM launch");
   }
   e = launch_moe_combine(ws + L.y_perm, (int)h->H, (int)T, top_k, perm_row, gates, y, h->nsm, st);
