@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
 
-    // Barrier among the 128 epilogue threads that shares one thread's verdict.
+    // Barrier among the 128 epilogue threads that shares one thread's decision.
     auto agree = [&](bool mine_ok) -> bool {
       if (et == 0) *s_ok = mine_ok ? 1 : 0;
       named_bar_sync(1, 128);
