@@ -28,6 +28,9 @@ chains the steps into one decoder layer (input norm, QKV, attention, o_proj,
 add + norm, MLP) in the order the pages give. ``moe.py`` is the top-k
 mixture-of-experts block whose experts are split by the same column/row
 pattern (within-expert tensor parallelism); its routing is an input.
+``kv_cache.py`` is the paged KV cache: the write of each new token's keys and
+values to its slot, and attention of new tokens over their requests' cached
+keys through the block tables.
 
 Every function computes in float64 from bf16 inputs converted exactly. Where
 the block has a plain definition (the unsharded Y = XW, SiLU, RMSNorm, row
@@ -49,3 +52,4 @@ from .capture import capture_rows, pack_key  # noqa: F401
 from .attention import attention_core, attention_rows, kv_head_of  # noqa: F401
 from .decoder_layer import decoder_layer  # noqa: F401
 from .moe import moe_block, moe_block_tp  # noqa: F401
+from .kv_cache import kv_cache_write, paged_attention, slot_of  # noqa: F401
