@@ -176,7 +176,7 @@ def max_over_ranks(v: float, ws: int) -> float:
 
 # ---------------------------------------------------------------------------- work model
 def work_model(w: workloads.Workload):
-    decode = w.kind in ("mlp", "moe") and w.T <= 128
+    decode = (w.kind in ("mlp", "moe") and w.T <= 128) or w.kind == "paged"
     flops = w.flops()
     wbytes = w.weight_bytes()
     abytes = w.activation_bytes()
@@ -227,6 +227,17 @@ class OracleSample:
             self.flops = 4.0 * w.hd * w.nq * float(np.sum(self.row_ids - starts + 1))
             self.wbytes = 0.0
             return
+        if w.kind == "paged":
+            # the first `rows` requests' new tokens over their cached keys
+            self.feat = 0
+            self.rows = min(w.T, rows)
+            self.lens = [int(x) for x in w.seq_lens()[:self.rows]]
+            q_per, kv_per = w.nq // w.t, (1 if w.t >= w.nkv else w.nkv // w.t)
+            width = (q_per + 2 * kv_per) * w.hd
+            self.full = workloads.draw((w.t, int(sum(self.lens)), width), seed + 5, 0)
+            self.wbytes = float(sum(self.lens) * 2 * w.nkv * w.hd * 2)
+            self.flops = 4.0 * w.hd * w.nq * float(sum(self.lens))
+            return
         if w.kind == "moe":
             # the first `rows` tokens, every routed entry through its expert
             self.feat = 0
@@ -270,6 +281,26 @@ class OracleSample:
         if w.kind == "attn_core":
             o.attention_rows(self.qkv, w.nq, w.nkv, w.hd, w.t, self.cu, self.row_ids)
             return
+        if w.kind == "paged":
+            # fill a cache through slots and attend: the oracle's write and read paths
+            q_per, kv_per = w.nq // w.t, (1 if w.t >= w.nkv else w.nkv // w.t)
+            bs = 16
+            nb = sum(-(-L // bs) for L in self.lens)
+            ck = np.zeros((w.t, nb, bs, kv_per, w.hd))
+            cv = np.zeros_like(ck)
+            tables = np.zeros((len(self.lens), max(-(-L // bs) for L in self.lens)), dtype=np.int64)
+            used = 0
+            for b, L in enumerate(self.lens):
+                n = -(-L // bs)
+                tables[b, :n] = np.arange(used, used + n)
+                used += n
+            slots = np.concatenate([[tables[b, p // bs] * bs + p % bs for p in range(L)]
+                                    for b, L in enumerate(self.lens)])
+            o.kv_cache_write(self.full, slots, ck, cv, w.nq, w.nkv, w.hd, w.t, bs)
+            ends = np.cumsum(self.lens) - 1
+            o.paged_attention(self.full[:, ends], np.arange(len(self.lens) + 1), self.lens, tables, ck, cv,
+                              w.nq, w.nkv, w.hd, w.t, bs)
+            return
         if w.kind == "moe":
             d = self.args
             o.moe_block(d["x"], d["expert_ids"], d["gates"], d["w_gate"], d["w_up"], d["w_down"])
@@ -291,6 +322,9 @@ class OracleSample:
         w = self.w
         if w.kind == "attn_core":
             what = f"{self.rows} of {w.T} query rows (evenly spaced) through the causal attention of all {w.nq} q heads"
+        elif w.kind == "paged":
+            what = (f"the first {self.rows} of {w.T} requests ({sum(self.lens)} cached tokens): cache write "
+                    f"of every token and decode attention of each request's last token")
         elif w.kind == "moe":
             what = (f"the first {self.rows} of {w.T} tokens, top-{w.top_k} of {w.experts} experts "
                     f"(intermediate {w.I}, hidden {w.H})")
@@ -337,6 +371,10 @@ def config_obj(w: workloads.Workload, n: int, rotate: int, decode: bool):
         c["intermediate"] = w.I
         c["sequences"] = int(len(w.seq_lens()))
         c["causal"] = True
+    if w.kind == "paged":
+        lens = w.seq_lens()
+        c.update({"requests": w.T, "cached_tokens": int(lens.sum()), "seq_len_range": [int(lens.min()), int(lens.max())],
+                  "block_size": 16, "new_tokens_per_request": 1})
     if w.kind == "moe":
         for k in ("n_q_heads", "n_kv_heads", "head_dim"):
             c.pop(k, None)
@@ -346,6 +384,8 @@ def config_obj(w: workloads.Workload, n: int, rotate: int, decode: bool):
         c["causal"] = True
         qkv_b = 2 * w.T * (w.nq + 2 * (w.nkv if w.t < w.nkv else w.t)) * w.hd
         c["l2"] = f"{rotate} rotating qkv inputs ({rotate * qkv_b / 1e9:.2f} GB) > 129 MB L2"
+    elif w.kind == "paged":
+        c["l2"] = f"KV cache read per step {w.kv_cache_bytes() / 1e9:.2f} GB > 129 MB L2; {rotate} rotating caches"
     elif w.kind == "moe":
         c["l2"] = f"expert weights {w.weight_bytes() / 1e9:.2f} GB > 129 MB L2; {rotate} rotating inputs"
     elif w.kind == "layer":
@@ -439,6 +479,51 @@ def run_ours(args, ws, rank, local):
             j = i % R
             blocks[j].gate_up(xs[j], h_out=hbufs[j], ws=wss[j])
         hbufs = [torch.empty(w.t, w.T, w.I // w.t, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    elif w.kind == "paged":
+        dw = workloads.attn_inputs(w, T=1)
+        cfg = tl.make_config(tl.TP_BLOCK_ATTN_PROJ, w.t, w.H, n_q_heads=w.nq, n_kv_heads=w.nkv, head_dim=w.hd)
+        blocks = [tl.TPLinear(cfg, [dw[k].to(dev) for k in ("w_q", "w_k", "w_v", "w_o")])]
+        lens = [int(x) for x in w.seq_lens()]
+        bs = 16
+        q_per, kv_per = w.nq // w.t, (1 if w.t >= w.nkv else w.nkv // w.t)
+        width = (q_per + 2 * kv_per) * w.hd
+        nb_req = [-(-L // bs) for L in lens]
+        n_blocks = sum(nb_req)
+        tables = np.zeros((len(lens), max(nb_req)), dtype=np.int32)
+        perm = np.random.default_rng(rank).permutation(n_blocks)   # scattered blocks
+        used = 0
+        for b, n in enumerate(nb_req):
+            tables[b, :n] = perm[used:used + n]
+            used += n
+        tables_d = torch.from_numpy(tables).to(dev)
+        caches = []
+        for r_ in range(R):
+            ck = torch.empty(blocks[0].kv_cache_shape(n_blocks, bs), dtype=torch.bfloat16, device=dev)
+            cv = torch.empty_like(ck)
+            for b, L in enumerate(lens):     # the cached context, one request at a time
+                full = workloads.draw((w.t, L, width), 1000 + rank * R + r_, b).to(dev)
+                slots = torch.from_numpy(np.array([tables[b, p // bs] * bs + p % bs for p in range(L)],
+                                                  dtype=np.int32)).to(dev)
+                blocks[0].kv_cache_write(full, slots, ck, cv)
+            caches.append((ck, cv))
+        new_slots = torch.from_numpy(np.array([tables[b, (L - 1) // bs] * bs + (L - 1) % bs
+                                               for b, L in enumerate(lens)], dtype=np.int32)).to(dev)
+        qkvs = [workloads.draw((w.t, len(lens), width), 2000 + rank * R + r_, 0).to(dev) for r_ in range(R)]
+        qsl = torch.arange(len(lens) + 1, dtype=torch.int32, device=dev)
+        lens_d = torch.tensor(lens, dtype=torch.int32, device=dev)
+        aos = [torch.empty(w.t, len(lens), q_per * w.hd, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        pws = torch.zeros(blocks[0].paged_attention_workspace_size(len(lens), 1, max(lens)), dtype=torch.uint8,
+                          device=dev)
+        kws = torch.zeros(16, dtype=torch.uint8, device=dev)
+        wss = [pws, kws]
+        launches_per_step = 3           # cache write, split attention, split merge
+
+        def step(i):
+            j = i % R
+            ck, cv = caches[j]
+            blocks[0].kv_cache_write(qkvs[j], new_slots, ck, cv, ws=kws)
+            blocks[0].paged_attention(qkvs[j], qsl, lens_d, tables_d, ck, cv, 1, max(lens), out=aos[j], ws=pws)
+        dominant = step
     elif w.kind == "moe":
         d = workloads.moe_inputs(w)
         cfg = tl.make_config(tl.TP_BLOCK_MOE, w.t, w.H, w.I, n_experts=w.experts)
@@ -561,8 +646,8 @@ def run_ours(args, ws, rank, local):
     # ---- dominant kernel: in decode the step is a single fused kernel, so its
     # average launch duration is the timed region's per-step time; otherwise the
     # column-parallel GEMM alone, same stream, events around K2 launches
-    if launches_per_step == 1 or w.kind in ("attn_core", "moe"):
-        dom_s = sec                    # attention core, MoE: every launch of a step (conservative)
+    if launches_per_step == 1 or w.kind in ("attn_core", "moe", "paged"):
+        dom_s = sec                    # attention core, MoE, paged decode: every launch of a step (conservative)
     else:
         K2 = min(K, 2000 if decode else 20)
         for i in range(3):
@@ -593,6 +678,19 @@ def run_ours(args, ws, rank, local):
             blocks[j].mlp_forward(xs[j], residual=rs[j], out=outs[j], ws=wss[j])
             for k, v in outs[j].items():
                 ho[j][k].copy_(v, non_blocking=True)
+    elif w.kind == "paged":
+        hq = [qkvs[j].cpu().pin_memory() for j in range(R)]
+        ho = [torch.empty(aos[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
+        h2d = hq[0].numel() * 2
+        d2h = ho[0].numel() * 2
+
+        def e2e_step(i):
+            j = i % R
+            ck, cv = caches[j]
+            qkvs[j].copy_(hq[j], non_blocking=True)
+            blocks[0].kv_cache_write(qkvs[j], new_slots, ck, cv, ws=kws)
+            blocks[0].paged_attention(qkvs[j], qsl, lens_d, tables_d, ck, cv, 1, max(lens), out=aos[j], ws=pws)
+            ho[j].copy_(aos[j], non_blocking=True)
     elif w.kind == "moe":
         hx = [xs[j].cpu().pin_memory() for j in range(R)]
         hid = ids.cpu().pin_memory()
@@ -672,10 +770,12 @@ def run_ours(args, ws, rank, local):
         unit = "GB/s"
         value = ws * wbytes / sec / 1e9
         e2e_value = ws * wbytes / e2e_s / 1e9
-        fused = launches_per_step == 1 or w.kind == "moe"
+        fused = launches_per_step == 1 or w.kind in ("moe", "paged")
         dom_alg = float(wbytes + abytes) if fused else dominant_kernel_bytes(w)
         achieved = dom_alg / dom_s / 1e9
-        if w.kind == "moe":
+        if w.kind == "paged":
+            key, kname = "paged@", "paged decode step: cache write, split attention (paged_attn_kernel), split merge"
+        elif w.kind == "moe":
             key, kname = "moe@", "the MoE step: routing, gather, grouped expert GEMMs (tc_gemm_kernel), combine"
         elif fused:
             key, kname = "mlp_decode@", "fused decode MLP block (mlp_decode_kernel)"

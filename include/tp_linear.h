@@ -227,6 +227,42 @@ int tp_attention_forward(tp_linear_t* h, int64_t T, const void* qkv, const int32
                          int64_t workspace_bytes, tp_stream_t stream);
 
 /*
+ * Paged KV cache ("vLLM Code Reading (Section 5)" §13: each rank's attention kernel
+ * writes the KV cache of the heads it holds; the model runner's slot mapping comes
+ * from the block table). Layout, per shard r: cache_k[r], cache_v[r] are
+ * [num_blocks][block_size][kv_per][128] bf16 (kv_per = the shard's kv heads), so a
+ * cache is t * num_blocks * block_size * kv_per * 128 elements; slot s is block
+ * s / block_size, offset s % block_size.
+ *
+ * tp_kv_cache_write: for every token i of qkv ([t][T][w_s], or gathered) with
+ *   slot_mapping[i] >= 0, copies the k and v heads of every shard into that slot.
+ *   A slot past the cache writes TP_ERR_SHAPE to the status word (workspace bytes
+ *   [0, 4); the workspace needs 16 bytes here) and is skipped; negative = padding.
+ * tp_paged_attention: the new tokens of request b are rows [query_start_loc[b],
+ *   query_start_loc[b+1]) of qkv and the last positions of its seq_lens[b] tokens;
+ *   the token at position p attends (causally) to positions 0..p of its request,
+ *   read from the cache through block_tables[b][p / block_size] (int32, row length
+ *   max_blocks_per_req). Write the new tokens to the cache first. attn_out has the
+ *   attention core's layout. Scores, softmax and the split merge in fp32, output
+ *   rounded to bf16. Device arrays: query_start_loc [n_reqs + 1], seq_lens [n_reqs],
+ *   block_tables [n_reqs][max_blocks_per_req], all int32. Host bounds: every request
+ *   has at most max_query_len new tokens and max_seq_len tokens (else TP_ERR_SHAPE in
+ *   the status word); block ids outside [0, num_blocks) likewise. The workspace
+ *   (tp_paged_attention_workspace_size) holds the status word and the per-split
+ *   partial results. head_dim 128.
+ */
+int tp_kv_cache_write(tp_linear_t* h, int64_t T, const void* qkv, const int32_t* slot_mapping, void* cache_k,
+                      void* cache_v, int64_t num_blocks, int32_t block_size, void* workspace,
+                      int64_t workspace_bytes, tp_stream_t stream);
+int tp_paged_attention_workspace_size(const tp_linear_t* h, int32_t n_reqs, int32_t max_query_len,
+                                      int32_t max_seq_len, int64_t* bytes);
+int tp_paged_attention(tp_linear_t* h, int64_t T, const void* qkv, const int32_t* query_start_loc,
+                       const int32_t* seq_lens, int32_t n_reqs, int32_t max_query_len, int32_t max_seq_len,
+                       const int32_t* block_tables, int32_t max_blocks_per_req, const void* cache_k,
+                       const void* cache_v, int64_t num_blocks, int32_t block_size, void* attn_out,
+                       void* workspace, int64_t workspace_bytes, tp_stream_t stream);
+
+/*
  * Mixture-of-experts block with within-expert tensor parallelism ("Tensor
  * Parallelism", MoE Expert Parallelism, Within-Expert Parallel: every expert's
  * FFN is split with the dense column-parallel gate/up and row-parallel down

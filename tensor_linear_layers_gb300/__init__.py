@@ -30,7 +30,7 @@ ABI_SYMBOLS = (
     "tp_attn_proj_forward", "tp_capture_workspace_size", "tp_capture_rows", "tp_last_error",
     "tp_describe_plan", "tp_mlp_forward_no_alloc", "tp_set_wait_timeout", "tp_attention_forward",
     "tp_layer_create", "tp_layer_destroy", "tp_layer_workspace_size", "tp_decoder_layer_forward",
-    "tp_moe_forward",
+    "tp_moe_forward", "tp_kv_cache_write", "tp_paged_attention_workspace_size", "tp_paged_attention",
 )
 
 
@@ -97,6 +97,9 @@ def lib() -> ctypes.CDLL:
         "tp_layer_workspace_size": [P, PI64],
         "tp_decoder_layer_forward": [P, I64, ctypes.POINTER(LayerIO), P, I64, P],
         "tp_moe_forward": [P, I64, I32, P, P, P, P, P, I64, P],
+        "tp_kv_cache_write": [P, I64, P, P, P, P, I64, I32, P, I64, P],
+        "tp_paged_attention_workspace_size": [P, I32, I32, I32, PI64],
+        "tp_paged_attention": [P, I64, P, P, P, I32, I32, I32, P, I32, P, P, I64, I32, P, P, I64, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -276,6 +279,56 @@ class TPLinear:
         _check(lib().tp_down_forward(self.handle, T, _ptr(_bf16(h_in, "h_in")), _ptr(residual), _ptr(out),
                                      _ptr(stream_out), _ptr(ws), ws.numel(), _stream(stream)))
         return out, stream_out
+
+    # ------------------------------------------------------------------ paged KV cache
+    def kv_cache_shape(self, num_blocks: int, block_size: int):
+        """Shape of one of the two caches: [t][num_blocks][block_size][kv heads per shard][head_dim]."""
+        c = self.cfg
+        kv_per = 1 if c.t >= c.n_kv_heads else c.n_kv_heads // c.t
+        return (c.t, num_blocks, block_size, kv_per, c.head_dim)
+
+    def kv_cache_write(self, qkv: torch.Tensor, slot_mapping: torch.Tensor, cache_k: torch.Tensor,
+                       cache_v: torch.Tensor, ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """Copy every token's k and v heads into its slot (slot_mapping int32 [T], -1 = skip).
+        Returns the 16-byte workspace whose first word is the status."""
+        T = qkv.shape[0] if self.gathered else qkv.shape[1]
+        _, nb, bs, _, _ = cache_k.shape
+        ws = torch.zeros(16, dtype=torch.uint8, device=qkv.device) if ws is None else ws
+        _check(lib().tp_kv_cache_write(self.handle, T, _ptr(_bf16(qkv, "qkv")), _ptr(slot_mapping),
+                                       _ptr(_bf16(cache_k, "cache_k")), _ptr(_bf16(cache_v, "cache_v")), nb, bs,
+                                       _ptr(ws), ws.numel(), _stream(stream)))
+        return ws
+
+    def paged_attention_workspace_size(self, n_reqs: int, max_query_len: int, max_seq_len: int) -> int:
+        b = ctypes.c_int64()
+        _check(lib().tp_paged_attention_workspace_size(self.handle, n_reqs, max_query_len, max_seq_len,
+                                                       ctypes.byref(b)))
+        return b.value
+
+    def paged_attention(self, qkv: torch.Tensor, query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
+                        block_tables: torch.Tensor, cache_k: torch.Tensor, cache_v: torch.Tensor,
+                        max_query_len: int, max_seq_len: int, out=None, ws=None, stream=None):
+        """Attention of the new tokens (rows of qkv) over their requests' cached keys.
+        Returns (attn in the attention core's output layout, workspace)."""
+        c = self.cfg
+        T = qkv.shape[0] if self.gathered else qkv.shape[1]
+        n_reqs = query_start_loc.numel() - 1
+        _, nb, bs, _, _ = cache_k.shape
+        if out is None:
+            shape = (T, c.n_q_heads * c.head_dim) if self.gathered else (c.t, T, c.n_q_heads // c.t * c.head_dim)
+            out = torch.empty(shape, dtype=torch.bfloat16, device=qkv.device)
+        if ws is None:
+            ws = torch.zeros(self.paged_attention_workspace_size(n_reqs, max_query_len, max_seq_len),
+                             dtype=torch.uint8, device=qkv.device)
+        for name, a in (("query_start_loc", query_start_loc), ("seq_lens", seq_lens), ("block_tables", block_tables)):
+            if a.dtype != torch.int32 or not a.is_cuda or not a.is_contiguous():
+                raise TypeError(f"{name} must be a contiguous int32 CUDA tensor")
+        _check(lib().tp_paged_attention(self.handle, T, _ptr(_bf16(qkv, "qkv")), _ptr(query_start_loc),
+                                        _ptr(seq_lens), n_reqs, int(max_query_len), int(max_seq_len),
+                                        _ptr(block_tables), block_tables.shape[1], _ptr(_bf16(cache_k, "cache_k")),
+                                        _ptr(_bf16(cache_v, "cache_v")), nb, bs, _ptr(out), _ptr(ws), ws.numel(),
+                                        _stream(stream)))
+        return out, ws
 
     # ------------------------------------------------------------------ mixture of experts
     def moe_forward(self, x: torch.Tensor, expert_ids: torch.Tensor, gates: torch.Tensor, out=None, ws=None,

@@ -82,6 +82,33 @@ struct MlpDecodeParams;
 cudaError_t launch_mlp_decode(int bn, const CUtensorMap& map_x, const CUtensorMap& map_h,
                               const MlpDecodeParams& P, int grid, cudaStream_t st);
 
+// Paged KV cache (kv_cache.cu).
+struct PagedAttnParams {
+  const __nv_bfloat16* qkv;          // new tokens: shard r, token i at qkv + r * sstride_in + i * rstride_in
+  long long sstride_in;
+  int rstride_in;
+  const int* qsl;                    // [n_reqs + 1] new-token offsets
+  const int* seq_lens;               // [n_reqs] tokens of each request, new ones included
+  const int* block_tables;           // [n_reqs][max_blocks]
+  const __nv_bfloat16* cache_k;      // [t][num_blocks][block_size][kv_per][128]
+  const __nv_bfloat16* cache_v;
+  __nv_bfloat16* out;                // shard r, token i at out + r * sstride_out + i * rstride_out
+  long long sstride_out;
+  int rstride_out;
+  float* partials;                   // [item][q_stride][128 + 2]: o, max, sum of each split
+  int* status;
+  int t, q_per, kv_per, rep, max_blocks, num_blocks, block_size, max_query_len, max_seq_len;
+  int split_len, n_splits;           // keys per split, splits per (request, shard, kv head)
+  int q_stride;                      // query slots of one item: max_query_len * (q heads per kv head)
+  int c_stride;                      // (token, q head) slots of one request and shard: max_query_len * q_per
+  float scale_log2;
+  unsigned long long timeout_ns;     // bound of every wait on a copy
+};
+cudaError_t launch_kv_write(const void* qkv, int T, int t, long long sstride, int rstride, int q_per, int kv_per,
+                            const int* slots, long long n_slots, void* ck, void* cv, int* status, int nsm,
+                            cudaStream_t st);
+cudaError_t launch_paged_attention(const PagedAttnParams& p, int n_reqs, cudaStream_t st);
+
 // Mixture of experts (moe.cu): routing sort, row gather, weighted combine.
 cudaError_t launch_moe_route(const int* ids, int n_entries, int k, int E, int max_rows, int* rank, int* perm_row,
                              int* row_src, int* tile_expert, int* m_valid, int* pair_tiles, int* pair_count,

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <atomic>
 #include <cstdlib>
@@ -977,6 +978,129 @@ int tp_attention_forward(tp_linear_t* h, int64_t T, const void* qkv, const int32
       launch_attention(map_qkv, p, cu_seqlens, n_seqs, max_tiles, const_cast<int4*>(p.pairs),
                        const_cast<int*>(p.n_pairs), grid, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return ok();
+}
+
+// Paged attention: splits along each request's keys so that about six CTAs per SM are launched.
+struct PagedPlan {
+  int split_len, n_splits, q_stride, c_stride;
+  int64_t ws_bytes;
+};
+PagedPlan paged_plan(const tp_linear* h, int n_reqs, int max_query_len, int max_seq_len) {
+  PagedPlan pl{};
+  const int gq = h->q_per / (h->rep > 1 ? 1 : h->kv_per);
+  const int64_t per_split = (int64_t)n_reqs * h->cfg.t * h->kv_per;
+  const int max_chunks = (int)ceil_div(std::max(max_seq_len, 1), 128);
+  const int want = (int)std::max<int64_t>(1, std::min<int64_t>(max_chunks, ceil_div(6LL * h->nsm, std::max<int64_t>(per_split, 1))));
+  pl.split_len = (int)ceil_div(ceil_div(std::max(max_seq_len, 1), want), 128) * 128;
+  pl.n_splits = (int)ceil_div(std::max(max_seq_len, 1), pl.split_len);
+  pl.q_stride = max_query_len * gq;
+  pl.c_stride = max_query_len * h->q_per;
+  pl.ws_bytes = 256 + per_split * pl.n_splits * pl.q_stride * (128 + 2) * 4;
+  return pl;
+}
+
+int tp_kv_cache_write(tp_linear_t* h, int64_t T, const void* qkv, const int32_t* slot_mapping, void* cache_k,
+                      void* cache_v, int64_t num_blocks, int32_t block_size, void* workspace, int64_t workspace_bytes,
+                      tp_stream_t stream) {
+  if (h == nullptr) return fail(TP_ERR_ARG, "handle is null");
+  if (h->cfg.kind != TP_BLOCK_ATTN_PROJ) return fail(TP_ERR_ARG, "not an attention handle");
+  int rc = check_T(T);
+  if (rc) return rc;
+  if (h->cfg.head_dim != 128) return fail(TP_ERR_UNSUPPORTED, "the KV cache is built for head_dim 128");
+  if (num_blocks < 1 || block_size < 1) return fail(TP_ERR_SHAPE, "num_blocks and block_size must be >= 1");
+  if (T == 0) return ok();
+  TP_CHECK_PTR(qkv, "qkv");
+  TP_CHECK_PTR(cache_k, "cache_k");
+  TP_CHECK_PTR(cache_v, "cache_v");
+  if (slot_mapping == nullptr || (reinterpret_cast<uintptr_t>(slot_mapping) & 3u) != 0)
+    return fail(TP_ERR_ARG, "slot_mapping is null or not 4-byte aligned");
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < 16)
+    return fail(TP_ERR_ARG, "workspace is null, not 16-byte aligned or under 16 bytes");
+  if ((rc = check_device(h))) return rc;
+  const bool gath = gathered(h);
+  const cudaError_t e = launch_kv_write(qkv, (int)T, h->cfg.t, gath ? h->ws_qkv : T * h->ws_qkv,
+                                        (int)(gath ? h->cfg.t * h->ws_qkv : h->ws_qkv), h->q_per, h->kv_per,
+                                        slot_mapping, num_blocks * (long long)block_size, cache_k, cache_v,
+                                        reinterpret_cast<int*>(workspace), h->nsm, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "KV cache write launch");
+  return ok();
+}
+
+int tp_paged_attention_workspace_size(const tp_linear_t* h, int32_t n_reqs, int32_t max_query_len,
+                                      int32_t max_seq_len, int64_t* bytes) {
+  if (h == nullptr || bytes == nullptr) return fail(TP_ERR_ARG, "null argument");
+  if (h->cfg.kind != TP_BLOCK_ATTN_PROJ) return fail(TP_ERR_ARG, "not an attention handle");
+  if (n_reqs < 1 || max_query_len < 1 || max_seq_len < max_query_len)
+    return fail(TP_ERR_SHAPE, "need n_reqs >= 1 and 1 <= max_query_len <= max_seq_len");
+  *bytes = paged_plan(h, n_reqs, max_query_len, max_seq_len).ws_bytes;
+  return ok();
+}
+
+int tp_paged_attention(tp_linear_t* h, int64_t T, const void* qkv, const int32_t* query_start_loc,
+                       const int32_t* seq_lens, int32_t n_reqs, int32_t max_query_len, int32_t max_seq_len,
+                       const int32_t* block_tables, int32_t max_blocks_per_req, const void* cache_k,
+                       const void* cache_v, int64_t num_blocks, int32_t block_size, void* attn_out,
+                       void* workspace, int64_t workspace_bytes, tp_stream_t stream) {
+  if (h == nullptr) return fail(TP_ERR_ARG, "handle is null");
+  if (h->cfg.kind != TP_BLOCK_ATTN_PROJ) return fail(TP_ERR_ARG, "not an attention handle");
+  int rc = check_T(T);
+  if (rc) return rc;
+  if (h->cfg.head_dim != 128) return fail(TP_ERR_UNSUPPORTED, "the KV cache is built for head_dim 128");
+  if (T == 0) return ok();
+  if (n_reqs < 1 || max_query_len < 1 || max_seq_len < max_query_len || max_query_len > T)
+    return fail(TP_ERR_SHAPE, "need n_reqs >= 1 and 1 <= max_query_len <= min(T, max_seq_len)");
+  if (num_blocks < 1 || block_size < 1 || max_blocks_per_req < 1 ||
+      (int64_t)max_blocks_per_req * block_size < max_seq_len)
+    return fail(TP_ERR_SHAPE, "the block tables cannot hold max_seq_len tokens");
+  if (num_blocks > INT32_MAX) return fail(TP_ERR_UNSUPPORTED, "more than 2^31 - 1 cache blocks");
+  if (num_blocks * (int64_t)block_size * h->kv_per * 128 > (int64_t(1) << 40))
+    return fail(TP_ERR_UNSUPPORTED, "cache larger than 2^40 elements per shard");
+  TP_CHECK_PTR(qkv, "qkv");
+  TP_CHECK_PTR(cache_k, "cache_k");
+  TP_CHECK_PTR(cache_v, "cache_v");
+  TP_CHECK_PTR(attn_out, "attn_out");
+  for (const int32_t* q : {query_start_loc, seq_lens, block_tables})
+    if (q == nullptr || (reinterpret_cast<uintptr_t>(q) & 3u) != 0)
+      return fail(TP_ERR_ARG, "query_start_loc, seq_lens and block_tables must be 4-byte aligned device arrays");
+  const PagedPlan pl = paged_plan(h, n_reqs, max_query_len, max_seq_len);
+  if (workspace == nullptr || !aligned16(workspace)) return fail(TP_ERR_ARG, "workspace is null or not 16-byte aligned");
+  if (workspace_bytes < pl.ws_bytes)
+    return fail(TP_ERR_ARG, "workspace too small: %lld bytes, %lld needed", (long long)workspace_bytes,
+                (long long)pl.ws_bytes);
+  if ((rc = check_device(h))) return rc;
+  const bool gath = gathered(h);
+  PagedAttnParams p{};
+  p.qkv = static_cast<const __nv_bfloat16*>(qkv);
+  p.sstride_in = gath ? h->ws_qkv : T * h->ws_qkv;
+  p.rstride_in = (int)(gath ? h->cfg.t * h->ws_qkv : h->ws_qkv);
+  p.qsl = query_start_loc;
+  p.seq_lens = seq_lens;
+  p.block_tables = block_tables;
+  p.cache_k = static_cast<const __nv_bfloat16*>(cache_k);
+  p.cache_v = static_cast<const __nv_bfloat16*>(cache_v);
+  p.out = static_cast<__nv_bfloat16*>(attn_out);
+  p.sstride_out = gath ? h->Ks : T * h->Ks;
+  p.rstride_out = (int)(gath ? h->cfg.t * h->Ks : h->Ks);
+  p.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + 256);
+  p.status = reinterpret_cast<int*>(workspace);
+  p.t = h->cfg.t;
+  p.q_per = h->q_per;
+  p.kv_per = h->kv_per;
+  p.rep = h->rep;
+  p.max_blocks = max_blocks_per_req;
+  p.num_blocks = (int)num_blocks;
+  p.block_size = block_size;
+  p.max_query_len = max_query_len;
+  p.max_seq_len = max_seq_len;
+  p.split_len = pl.split_len;
+  p.n_splits = pl.n_splits;
+  p.q_stride = pl.q_stride;
+  p.c_stride = pl.c_stride;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt(128.0));
+  p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  const cudaError_t e = launch_paged_attention(p, n_reqs, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "paged attention launch");
   return ok();
 }
 

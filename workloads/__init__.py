@@ -43,7 +43,7 @@ TENSOR_TYPES = {"residual_stream": 0, "attn_out": 1, "mlp_out": 2, "final_norm":
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str                 # "mlp", "attn" (projections), "attn_core" (attention core), "layer" or "moe"
+    kind: str                 # "mlp", "attn", "attn_core", "layer", "moe" or "paged" (KV-cache decode attention)
     T: int                    # tokens in the step
     H: int                    # hidden size
     t: int                    # logical tensor-parallel shards
@@ -63,8 +63,15 @@ class Workload:
     desc: str = field(default="", compare=False)
 
     def seq_lens(self) -> np.ndarray:
-        """Lengths of the packed sequences (attention core): one sequence, or the ragged batch."""
+        """Lengths of the packed sequences (attention core): one sequence, or the ragged batch.
+        Paged decode: each request's tokens (cached context + its new one), U[256, 4096]."""
+        if self.kind == "paged":
+            return np.random.default_rng(self.seed + 11).integers(256, 4097, self.T).astype(np.int64)
         return ragged_batch(self)["lens"] if self.requests else np.array([self.T], dtype=np.int64)
+
+    def kv_cache_bytes(self) -> int:
+        """Keys and values the paged decode step reads: every request's tokens, all kv heads."""
+        return int(self.seq_lens().sum()) * 2 * self.nkv * self.hd * 2
 
     def attn_core_flops(self) -> float:
         """q k^T and p v over the causal (query, key) pairs of every sequence and q head."""
@@ -79,6 +86,8 @@ class Workload:
         return 2.0 * self.T * self.H * qkv_n + 2.0 * self.T * self.nq * self.hd * self.H
 
     def flops(self) -> float:
+        if self.kind == "paged":              # q.k and p.v of each request's new token over its tokens
+            return 4.0 * self.hd * self.nq * float(self.seq_lens().sum())
         if self.kind == "moe":                # every routed (token, expert) entry through one expert MLP
             return self.top_k * self.mlp_flops()
         if self.kind == "attn_core":
@@ -93,6 +102,8 @@ class Workload:
         proj = 2 * (self.H * (self.nq + 2 * self.nkv) * self.hd + self.nq * self.hd * self.H)
         if self.kind == "attn_core":
             return 0
+        if self.kind == "paged":              # the KV cache streamed per step stands in for weights
+            return self.kv_cache_bytes()
         if self.kind == "moe":
             return self.experts * 2 * 3 * self.H * self.I
         if self.kind == "mlp":
@@ -110,6 +121,8 @@ class Workload:
             return 2 * T * H * 7
         if self.kind == "moe":               # x in, y out
             return 2 * T * H * 2
+        if self.kind == "paged":             # each request's new qkv row in, attention row out
+            return 2 * T * ((self.nq + 2 * self.nkv) * self.hd + self.nq * self.hd)
         if self.kind == "mlp":
             b = 2 * T * H * 2                # x (or a) in, mlp_out
             if self.norm:
@@ -146,6 +159,10 @@ WORKLOADS = {
         w_std=0.02, norm=True, requests=64, mean_len=32, capture_frac=0.1,
         desc="Ragged continuous batch, Qwen2.5-7B-shaped decoder layer with attn_out / mlp_out / "
              "residual_stream capture, 2048 tokens / 64 requests, t=4"),
+    "llama3_8b_paged_decode": Workload(
+        "llama3_8b_paged_decode", "paged", T=32, H=4096, nq=32, nkv=8, hd=128, t=4, w_std=0.0,
+        desc="Llama-3-8B-shaped decode attention over a paged KV cache, 32 requests of 256-4096 tokens "
+             "(block size 16), one new token each, t=4"),
     "mixtral_8x7b_moe_prefill": Workload(
         "mixtral_8x7b_moe_prefill", "moe", T=4096, H=4096, I=14336, t=4, w_std=0.02, experts=8, top_k=2,
         desc="Mixtral-8x7B-shaped MoE block prefill, 4096 tokens, top-2 of 8 experts, each expert split t=4"),
