@@ -249,7 +249,8 @@ int tp_attention_forward(tp_linear_t* h, int64_t T, const void* qkv, const int32
  *   has at most max_query_len new tokens and max_seq_len tokens (else TP_ERR_SHAPE in
  *   the status word); block ids outside [0, num_blocks) likewise. The workspace
  *   (tp_paged_attention_workspace_size) holds the status word and the per-split
- *   partial results. head_dim 128.
+ *   partial results. head_dim 128; t * num_blocks * block_size < 2^31
+ *   (TP_ERR_UNSUPPORTED otherwise). qkv, the caches and attn_out 16-byte aligned.
  */
 int tp_kv_cache_write(tp_linear_t* h, int64_t T, const void* qkv, const int32_t* slot_mapping, void* cache_k,
                       void* cache_v, int64_t num_blocks, int32_t block_size, void* workspace,

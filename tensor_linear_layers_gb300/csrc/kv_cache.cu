@@ -91,10 +91,17 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t* r, const void* p) {
 }
 
 namespace {
-constexpr int kRow = kHd + 8;                      // bf16 row stride in shared memory: ldmatrix rows hit distinct banks
-constexpr int kMRows = 16;                         // query rows of one pass (the m16 tile)
-constexpr int kPagedSmem = 2 * kChunk * kRow * 2 + 2 * kMRows * kRow * 2 + kMRows * kChunk * 4;
+constexpr int kMRows = 16;                               // query rows of one pass (the m16 tile)
+constexpr int kWarps = kAttnThreads / 32;
+constexpr int kPagedSmem = (2 * kChunk + 2 * kMRows) * kHd * 2;   // K, V, Q, P tiles (bf16, 256-byte rows)
 }  // namespace
+
+// Byte offset of element (row, col) of a bf16 tile with 256-byte rows: the 16-byte
+// pieces of a row are permuted by the row's low three bits, so eight consecutive
+// rows read at the same column (an ldmatrix) fall in eight distinct bank groups.
+__device__ __forceinline__ uint32_t swz(int row, int col) {
+  return row * 256 + ((((col >> 3) ^ row) & 7) | ((col >> 3) & 8)) * 16 + (col & 7) * 2;
+}
 
 // One CTA (8 warps) per (request, shard, kv head, split). The split's keys go in
 // chunks of 128, staged in shared memory with 16-byte copies: the next chunk's
@@ -103,19 +110,19 @@ constexpr int kPagedSmem = 2 * kChunk * kRow * 2 + 2 * kMRows * kRow * 2 + kMRow
 // of every chunk). Up to 16 queries per pass (the q heads of the kv group times
 // the request's new tokens) form the rows of m16n8k16 tensor-core products:
 // S = Q K^T with warp w taking keys [16 w, 16 w + 16), O += P V with warp w
-// taking head dimensions [16 w, 16 w + 16); the running max and sum are kept per
-// query in fp32, P is rounded to bf16.
+// taking head dimensions [16 w, 16 w + 16). The softmax stays in the S
+// fragments: the chunk's row maxima are exchanged through a small table, every
+// lane keeps the running max of its two rows, each warp its partial row sums
+// (merged at the end of the pass); P is rounded to bf16 for the second product.
 __global__ void __launch_bounds__(kAttnThreads)
     paged_attn_kernel(const PagedAttnParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  __nv_bfloat16* ks = reinterpret_cast<__nv_bfloat16*>(smem);                     // [128 keys][kRow]
-  __nv_bfloat16* vs = ks + kChunk * kRow;                                          // [128 keys][kRow]
-  __nv_bfloat16* qsb = vs + kChunk * kRow;                                         // [16 queries][kRow]
-  __nv_bfloat16* psb = qsb + kMRows * kRow;                                        // [16 queries][kRow] (keys)
-  float (*sc)[kChunk] = reinterpret_cast<float (*)[kChunk]>(psb + kMRows * kRow);   // [16][128]
-  __shared__ long long rowoff[2][kChunk];   // element offset of each key's row in the cache (-1: none), per chunk parity
-  __shared__ float s_m[kMRows], s_l[kMRows], s_f[kMRows];
-  __shared__ int s_pos[kMRows];
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ks = smem;                                      // [128 keys][128] bf16, swizzled
+  uint8_t* vs = ks + kChunk * 256;                         // [128 keys][128]
+  uint8_t* qsb = vs + kChunk * 256;                        // [16 queries][128]
+  uint8_t* psb = qsb + kMRows * 256;                       // [16 queries][128 keys]
+  __shared__ int rowrow[2][kChunk];   // cache row (shard, block, offset) of each key of a chunk (-1: none), per parity
+  __shared__ float xch[kWarps][kMRows];                    // per-warp row maxima, then row sums
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gr = lane >> 2, tq = lane & 3;   // fragment row group and column pair of this lane
   // item -> (request, shard, local kv head, split)
@@ -137,53 +144,60 @@ __global__ void __launch_bounds__(kAttnThreads)
   const int gq = p.q_per / (p.rep > 1 ? 1 : p.kv_per);
   const int h0 = g * gq;
   const int nq = n_new * gq;                       // queries of this item
+  const long long row_elems = (long long)p.kv_per * kHd;
   float* part = p.partials + (size_t)blockIdx.x * p.q_stride * (kHd + 2);
   auto lookup = [&](int c0, int par) {             // its row through the block table, one key per thread
     if (tid < kChunk) {
       const int key = c0 + tid;
-      long long off = -1;
+      int row = -1;
       if (key < k1) {
         const int blk = p.block_tables[(size_t)b * p.max_blocks + key / p.block_size];
         if (blk >= 0 && blk < p.num_blocks)
-          off = (((long long)r * p.num_blocks + blk) * p.block_size + key % p.block_size) * p.kv_per * kHd + g * kHd;
+          row = (r * p.num_blocks + blk) * p.block_size + key % p.block_size;
         else
           atomicExch(p.status, kStatusShape);
       }
-      rowoff[par][tid] = off;
+      rowrow[par][tid] = row;
     }
   };
   // 16-byte copies, 16 per row; missing rows read as zero (a committed group per call)
-  auto load_rows = [&](__nv_bfloat16* dst, const __nv_bfloat16* cache, int par) {
+  auto load_rows = [&](uint8_t* dst, const __nv_bfloat16* cache, int par) {
 #pragma unroll 4
     for (int e = tid; e < kChunk * 16; e += kAttnThreads) {
       const int row = e >> 4, c = e & 15;
-      const long long ro = rowoff[par][row];
-      const bool have = ro >= 0;
-      cp_async16(dst + row * kRow + c * 8, cache + (have ? ro : 0) + c * 8, have ? 16 : 0);
+      const int cr = rowrow[par][row];
+      const __nv_bfloat16* src = cache + (cr >= 0 ? cr * row_elems + g * kHd : 0) + c * 8;
+      cp_async16(dst + swz(row, c * 8), src, cr >= 0 ? 16 : 0);
     }
     cp_async_commit();
   };
-  int ci = 0;   // chunks of this CTA so far: chunk ci uses rowoff[ci & 1]
+  // ldmatrix lane addresses: A tiles (rows 16, k 16) and the two B n-tiles of one k-step
+  const int a_row = (lane & 7) + 8 * ((lane >> 3) & 1), a_col = 8 * (lane >> 4);
+  const int bk_row = (lane & 7) + 8 * (lane >> 4), bk_col = 8 * ((lane >> 3) & 1);
+  const int bv_row = (lane & 7) + 8 * ((lane >> 3) & 1), bv_col = 8 * (lane >> 4);
+  int ci = 0;   // chunks of this CTA so far: chunk ci uses rowrow[ci & 1]
   for (int qa = 0; qa < nq; qa += kMRows) {
     const int qc = min(kMRows, nq - qa);
     // the pass's queries as bf16 rows (rows past qc zero); query j: token q0 + (qa + j) / gq,
     // head h0 + (qa + j) % gq
-    for (int e = tid; e < kMRows * kHd; e += kAttnThreads) {
-      const int j = e / kHd, d = e - j * kHd;
-      __nv_bfloat16 v = __float2bfloat16_rn(0.f);
+    for (int e = tid; e < kMRows * kHd / 8; e += kAttnThreads) {
+      const int j = e >> 4, c = e & 15;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (j < qc) {
         const int tok = q0 + (qa + j) / gq, h = h0 + (qa + j) % gq;
-        v = p.qkv[(size_t)r * p.sstride_in + (size_t)tok * p.rstride_in + h * kHd + d];
+        v = *reinterpret_cast<const uint4*>(p.qkv + (size_t)r * p.sstride_in + (size_t)tok * p.rstride_in + h * kHd +
+                                            c * 8);
       }
-      qsb[j * kRow + d] = v;
-      psb[j * kRow + d] = __float2bfloat16_rn(0.f);
+      *reinterpret_cast<uint4*>(qsb + swz(j, c * 8)) = v;
     }
-    if (tid < kMRows) {
-      s_m[tid] = -INFINITY;
-      s_l[tid] = 0.f;
-      s_f[tid] = 0.f;
-      s_pos[tid] = tid < qc ? L - n_new + (qa + tid) / gq : -1;
+    // causal limit of this lane's rows gr and gr + 8 (-1: no query)
+    int pos[2];
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int row = gr + 8 * h2;
+      pos[h2] = row < qc ? L - n_new + (qa + row) / gq : -1;
     }
+    float m_run[2] = {-INFINITY, -INFINITY}, l_w[2] = {0.f, 0.f};
     float oacc[2][4];                                // O rows gr, gr + 8; head dims 16 warp + 8 nt + 2 tq, +1
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -201,80 +215,83 @@ __global__ void __launch_bounds__(kAttnThreads)
       if (more) lookup(c0 + kChunk, par ^ 1);
       cp_async_wait_but_one();             // this chunk's K (its V may still be in flight)
       __syncthreads();
-      {
-        // S = Q K^T for keys [16 warp, +16): 8 k-steps of 16 head dimensions, 2 n-tiles of 8 keys
-        float cs[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      // S = Q K^T for keys [16 warp, +16): 8 k-steps of 16 head dimensions, 2 n-tiles of 8 keys
+      float cs[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-        for (int kk = 0; kk < kHd / 16; ++kk) {
-          uint32_t a[4], bk[4];
-          ldsm_x4(a, qsb + ((lane & 7) + 8 * ((lane >> 3) & 1)) * kRow + 16 * kk + 8 * (lane >> 4));
-          ldsm_x4(bk, ks + (16 * warp + (lane & 7) + 8 * (lane >> 4)) * kRow + 16 * kk + 8 * ((lane >> 3) & 1));
-          mma_bf16_16816(cs[0], a, bk);
-          mma_bf16_16816(cs[1], a, bk + 2);
+      for (int kk = 0; kk < kHd / 16; ++kk) {
+        uint32_t a[4], bk[4];
+        ldsm_x4(a, qsb + swz(a_row, 16 * kk + a_col));
+        ldsm_x4(bk, ks + swz(16 * warp + bk_row, 16 * kk + bk_col));
+        mma_bf16_16816(cs[0], a, bk);
+        mma_bf16_16816(cs[1], a, bk + 2);
+      }
+      // scaled scores with the mask (missing key or after the query), and this warp's row maxima
+      float mloc[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int kl = 16 * warp + 8 * nt + 2 * tq + (i & 1);
+          const bool ok = rowrow[par][kl] >= 0 && c0 + kl <= pos[i >> 1];
+          cs[nt][i] = ok ? cs[nt][i] * p.scale_log2 : -INFINITY;
+          mloc[i >> 1] = fmaxf(mloc[i >> 1], cs[nt][i]);
         }
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int row = gr + 8 * (i >> 1), kl = 16 * warp + 8 * nt + 2 * tq + (i & 1);
-            const int key = c0 + kl;
-            if (row < qc)
-              sc[row][kl] = (rowoff[par][kl] >= 0 && key <= s_pos[row]) ? cs[nt][i] * p.scale_log2 : -INFINITY;
-          }
+      for (int h2 = 0; h2 < 2; ++h2) {
+        mloc[h2] = fmaxf(mloc[h2], __shfl_xor_sync(0xffffffffu, mloc[h2], 1));
+        mloc[h2] = fmaxf(mloc[h2], __shfl_xor_sync(0xffffffffu, mloc[h2], 2));
+        if (tq == 0) xch[warp][gr + 8 * h2] = mloc[h2];
       }
       __syncthreads();
       // the keys are read: the next chunk's keys start loading
       if (more) load_rows(ks, p.cache_k, par ^ 1);
       else cp_async_commit();              // an empty group keeps the count uniform
-      // running max and sum, a warp per query; P as bf16 rows for the product with V
-      for (int j = warp; j < qc; j += kAttnThreads / 32) {
-        float mx = -INFINITY;
-        for (int e = lane; e < kChunk; e += 32) mx = fmaxf(mx, sc[j][e]);
+      // new running max of this lane's rows, P = 2^(s - m) as bf16, rescale factors
+      float f[2];
 #pragma unroll
-        for (int o2 = 16; o2 > 0; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
-        const float m_old = s_m[j];
-        const float m_new = fmaxf(m_old, mx);
-        float sum = 0.f;
-        for (int e = lane; e < kChunk; e += 32) {
-          const float pe = m_new == -INFINITY ? 0.f : exp2f(sc[j][e] - m_new);
-          psb[j * kRow + e] = __float2bfloat16_rn(pe);
-          sum += pe;
-        }
+      for (int h2 = 0; h2 < 2; ++h2) {
+        float mx = m_run[h2];
 #pragma unroll
-        for (int o2 = 16; o2 > 0; o2 >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o2);
-        if (lane == 0) {
-          const float f = (m_old == -INFINITY) ? 0.f : exp2f(m_old - m_new);
-          s_f[j] = f;
-          s_l[j] = s_l[j] * f + sum;
-          s_m[j] = m_new;
-        }
+        for (int w2 = 0; w2 < kWarps; ++w2) mx = fmaxf(mx, xch[w2][gr + 8 * h2]);
+        f[h2] = m_run[h2] == -INFINITY ? 0.f : exp2f(m_run[h2] - mx);
+        l_w[h2] *= f[h2];
+        m_run[h2] = mx;
       }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const float mx = m_run[h2];
+          const float p0 = mx == -INFINITY ? 0.f : exp2f(cs[nt][2 * h2] - mx);
+          const float p1 = mx == -INFINITY ? 0.f : exp2f(cs[nt][2 * h2 + 1] - mx);
+          l_w[h2] += p0 + p1;
+          *reinterpret_cast<__nv_bfloat162*>(psb + swz(gr + 8 * h2, 16 * warp + 8 * nt + 2 * tq)) =
+              __floats2bfloat162_rn(p0, p1);
+        }
       cp_async_wait_but_one();             // this chunk's V (the next chunk's K may still be in flight)
       __syncthreads();
-      {
-        // O = O * f + P V for head dimensions [16 warp, +16): 8 k-steps of 16 keys, 2 n-tiles of 8
-        const float f0 = s_f[gr], f1 = s_f[gr + 8];
+      // O = O * f + P V for head dimensions [16 warp, +16): 8 k-steps of 16 keys, 2 n-tiles of 8
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          oacc[nt][0] *= f0;
-          oacc[nt][1] *= f0;
-          oacc[nt][2] *= f1;
-          oacc[nt][3] *= f1;
-        }
+      for (int nt = 0; nt < 2; ++nt) {
+        oacc[nt][0] *= f[0];
+        oacc[nt][1] *= f[0];
+        oacc[nt][2] *= f[1];
+        oacc[nt][3] *= f[1];
+      }
 #pragma unroll
-        for (int kk = 0; kk < kChunk / 16; ++kk) {
-          uint32_t a[4], bv[4];
-          ldsm_x4(a, psb + ((lane & 7) + 8 * ((lane >> 3) & 1)) * kRow + 16 * kk + 8 * (lane >> 4));
-          ldsm_x4_t(bv, vs + (16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1)) * kRow + 16 * warp + 8 * (lane >> 4));
-          mma_bf16_16816(oacc[0], a, bv);
-          mma_bf16_16816(oacc[1], a, bv + 2);
-        }
+      for (int kk = 0; kk < kChunk / 16; ++kk) {
+        uint32_t a[4], bv[4];
+        ldsm_x4(a, psb + swz(a_row, 16 * kk + a_col));
+        ldsm_x4_t(bv, vs + swz(16 * kk + bv_row, 16 * warp + bv_col));
+        mma_bf16_16816(oacc[0], a, bv);
+        mma_bf16_16816(oacc[1], a, bv + 2);
       }
       __syncthreads();
       // the values are read: the next chunk's values start loading
       if (more) load_rows(vs, p.cache_v, par ^ 1);
     }
-    // this split's partial result of every query of the pass
+    // this split's partial result of every query of the pass: o per warp's head dimensions,
+    // the running max (the same in every lane of a row), the row sums merged over lanes and warps
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -282,9 +299,21 @@ __global__ void __launch_bounds__(kAttnThreads)
         const int row = gr + 8 * (i >> 1);
         if (row < qc) part[(size_t)(qa + row) * (kHd + 2) + 16 * warp + 8 * nt + 2 * tq + (i & 1)] = oacc[nt][i];
       }
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      float l = l_w[h2];
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      const int row = gr + 8 * h2;
+      if (tq == 0) xch[warp][row] = l;
+      if (warp == 0 && tq == 0 && row < qc) part[(size_t)(qa + row) * (kHd + 2) + kHd] = m_run[h2];
+    }
+    __syncthreads();
     if (tid < qc) {
-      part[(size_t)(qa + tid) * (kHd + 2) + kHd] = s_m[tid];
-      part[(size_t)(qa + tid) * (kHd + 2) + kHd + 1] = s_l[tid];
+      float l = 0.f;
+#pragma unroll
+      for (int w2 = 0; w2 < kWarps; ++w2) l += xch[w2][tid];
+      part[(size_t)(qa + tid) * (kHd + 2) + kHd + 1] = l;
     }
     __syncthreads();
   }
@@ -340,6 +369,9 @@ cudaError_t launch_paged_attention(const PagedAttnParams& p, int n_reqs, cudaStr
   static bool attr_done = false;   // the same attribute on every device
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(paged_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPagedSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(paged_attn_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }

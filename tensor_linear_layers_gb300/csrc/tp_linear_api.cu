@@ -1056,6 +1056,8 @@ int tp_paged_attention(tp_linear_t* h, int64_t T, const void* qkv, const int32_t
   if (num_blocks > INT32_MAX) return fail(TP_ERR_UNSUPPORTED, "more than 2^31 - 1 cache blocks");
   if (num_blocks * (int64_t)block_size * h->kv_per * 128 > (int64_t(1) << 40))
     return fail(TP_ERR_UNSUPPORTED, "cache larger than 2^40 elements per shard");
+  if (num_blocks * (int64_t)block_size * h->cfg.t > INT32_MAX)
+    return fail(TP_ERR_UNSUPPORTED, "more than 2^31 - 1 cache slots over all shards");
   TP_CHECK_PTR(qkv, "qkv");
   TP_CHECK_PTR(cache_k, "cache_k");
   TP_CHECK_PTR(cache_v, "cache_v");
