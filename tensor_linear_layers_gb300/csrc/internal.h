@@ -100,9 +100,7 @@ struct PagedAttnParams {
   int t, q_per, kv_per, rep, max_blocks, num_blocks, block_size, max_query_len, max_seq_len;
   int split_len, n_splits;           // keys per split, splits per (request, shard, kv head)
   int q_stride;                      // query slots of one item: max_query_len * (q heads per kv head)
-  int c_stride;                      // (token, q head) slots of one request and shard: max_query_len * q_per
   float scale_log2;
-  unsigned long long timeout_ns;     // bound of every wait on a copy
 };
 cudaError_t launch_kv_write(const void* qkv, int T, int t, long long sstride, int rstride, int q_per, int kv_per,
                             const int* slots, long long n_slots, void* ck, void* cv, int* status, int nsm,

@@ -5,19 +5,19 @@
 // Cache layout, per shard r: cache[r][block][offset][kv_per][hd] bf16, slot s =
 // block * block_size + offset. Attention of new tokens over their requests'
 // cached keys is HBM-bound at decode (every cached key and value is read once
-// per step for a handful of queries), so it runs on the CUDA cores, split
-// along the sequence (flash-decoding):
+// per step for a handful of queries), so it is split along the sequence
+// (flash-decoding) to fill the GPU, and its two small products per chunk of
+// keys run as warp-level m16n8k16 tensor-core tiles:
 //
 //   kv_write_kernel     each token's k and v heads of every shard to its slot
 //   paged_attn_kernel   one CTA per (request, shard, kv head, sequence split):
 //                       the queries of every q head that reads this kv head and
-//                       every new token of the request, over the split's keys
-//                       in chunks of 128: thread = key for q.k (key row read
-//                       from its block), a warp per query for the running max
-//                       and sum, thread = head dimension for p.v. Writes the
-//                       split's (max, sum, unnormalised o) per query.
-//   paged_combine_kernel the splits of every query merged (log-sum-exp), o / l
-//                       rounded to bf16 into the attention output layout
+//                       every new token of the request (16 per pass), over the
+//                       split's keys in chunks of 128 staged in shared memory.
+//                       Writes the split's (max, sum, unnormalised o) per query.
+//   paged_merge_kernel  one CTA per (request, shard, kv head, query): the splits
+//                       merged (log-sum-exp), o / l as bf16 in the attention
+//                       output layout
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -62,10 +62,13 @@ __global__ void kv_write_kernel(const __nv_bfloat16* __restrict__ qkv, int T, in
   }
 }
 
-// 16-byte global -> shared copy without a register round trip; src_bytes 0 fills zeros
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+// 16-byte global -> shared copy without a register round trip; src_bytes 0 fills zeros;
+// pol: L2 eviction policy of the line read
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes, uint64_t pol) {
   const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(src_bytes) : "memory");
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(s), "l"(gmem), "r"(src_bytes),
+               "l"(pol)
+               : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // wait until at most one committed group of this thread is still in flight
@@ -125,6 +128,7 @@ __global__ void __launch_bounds__(kAttnThreads)
   __shared__ float xch[kWarps][kMRows];                    // per-warp row maxima, then row sums
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gr = lane >> 2, tq = lane & 3;   // fragment row group and column pair of this lane
+  griddep_launch_dependents();               // the merge grid may be scheduled once every split has started
   // item -> (request, shard, local kv head, split)
   int item = blockIdx.x;
   const int sp = item % p.n_splits;
@@ -160,14 +164,16 @@ __global__ void __launch_bounds__(kAttnThreads)
       rowrow[par][tid] = row;
     }
   };
-  // 16-byte copies, 16 per row; missing rows read as zero (a committed group per call)
+  // 16-byte copies, 16 per row; missing rows read as zero (a committed group per call). The
+  // cache is read once per step: its lines go first from L2, the splits' partials stay.
+  const uint64_t pol = policy_evict_first();
   auto load_rows = [&](uint8_t* dst, const __nv_bfloat16* cache, int par) {
 #pragma unroll 4
     for (int e = tid; e < kChunk * 16; e += kAttnThreads) {
       const int row = e >> 4, c = e & 15;
       const int cr = rowrow[par][row];
       const __nv_bfloat16* src = cache + (cr >= 0 ? cr * row_elems + g * kHd : 0) + c * 8;
-      cp_async16(dst + swz(row, c * 8), src, cr >= 0 ? 16 : 0);
+      cp_async16(dst + swz(row, c * 8), src, cr >= 0 ? 16 : 0, pol);
     }
     cp_async_commit();
   };
@@ -319,38 +325,59 @@ __global__ void __launch_bounds__(kAttnThreads)
   }
 }
 
+// One CTA per (request, shard, kv head, query slot), a thread per head dimension: the
+// splits' partial results of the query merged (log-sum-exp, running over batches of
+// eight splits whose max, sum and o are loaded together) and o / l written as bf16
+// in the attention output layout. Launched behind the attention grid with
+// programmatic serialisation: it is scheduled while the attention grid's last CTAs
+// run and waits for its completion (griddepcontrol.wait) before reading a partial.
 __global__ void __launch_bounds__(kHd)
-    paged_combine_kernel(const PagedAttnParams p) {
-  // block -> (request, shard, (token, local q head) of the request)
+    paged_merge_kernel(const PagedAttnParams p) {
   int idx = blockIdx.x;
-  const int qi = idx % p.c_stride;
-  idx /= p.c_stride;
+  const int j = idx % p.q_stride;                          // query of the group
+  idx /= p.q_stride;
+  const int g = idx % p.kv_per;
+  idx /= p.kv_per;
   const int r = idx % p.t;
   const int b = idx / p.t;
   const int q0 = p.qsl[b], n_new = p.qsl[b + 1] - q0;
-  const int gq = p.q_per / (p.rep > 1 ? 1 : p.kv_per);
-  if (n_new < 0 || n_new > p.max_query_len) return;
-  const int n_items_q = n_new * p.q_per;          // (token, local q head) pairs of the request and shard
-  if (qi >= n_items_q) return;
-  const int tok = qi / p.q_per, h = qi % p.q_per;  // local q head h reads local kv head h / gq
-  const int g = h / gq;
-  const int jq = tok * gq + (h - g * gq);          // its query index within item (b, r, g)
   const int L = p.seq_lens[b];
-  const int ns = L > 0 ? min(p.n_splits, (L + p.split_len - 1) / p.split_len) : 0;
-  const size_t item0 = (((size_t)b * p.t + r) * p.kv_per + g) * p.n_splits;
-  float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, p.partials[((item0 + s) * p.q_stride + jq) * (kHd + 2) + kHd]);
-  float o = 0.f, l = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float* pj = p.partials + ((item0 + s) * p.q_stride + jq) * (kHd + 2);
-    const float ms = pj[kHd];
-    if (ms == -INFINITY) continue;
-    const float f = exp2f(ms - M);
-    o += pj[threadIdx.x] * f;
-    l += pj[kHd + 1] * f;
+  griddep_wait();
+  if (n_new < 0 || n_new > p.max_query_len || L < n_new || L > p.max_seq_len) return;   // reported by the splits
+  const int gq = p.q_per / (p.rep > 1 ? 1 : p.kv_per);
+  if (j >= n_new * gq) return;
+  const int d = threadIdx.x;
+  const int ns = min(p.n_splits, (L + p.split_len - 1) / p.split_len);   // splits that hold keys
+  const size_t split_stride = (size_t)p.q_stride * (kHd + 2);
+  const float* pj = p.partials + (size_t)(blockIdx.x / p.q_stride) * p.n_splits * split_stride + (size_t)j * (kHd + 2);
+  float M = -INFINITY, o = 0.f, l = 0.f;
+  for (int s0 = 0; s0 < ns; s0 += 8) {
+    float mb[8], lb[8], ob[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const bool have = s0 + i < ns;
+      const float* ps = pj + (size_t)(s0 + i) * split_stride;
+      mb[i] = have ? __ldcg(ps + kHd) : -INFINITY;
+      lb[i] = have ? __ldcg(ps + kHd + 1) : 0.f;
+      ob[i] = have ? __ldcg(ps + d) : 0.f;
+    }
+    float mn = M;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mn = fmaxf(mn, mb[i]);
+    if (mn == -INFINITY) continue;
+    const float f = M == -INFINITY ? 0.f : exp2f(M - mn);
+    o *= f;
+    l *= f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float w = mb[i] == -INFINITY ? 0.f : exp2f(mb[i] - mn);
+      o += w * ob[i];
+      l += w * lb[i];
+    }
+    M = mn;
   }
-  const float val = l > 0.f ? o / l : 0.f;
-  p.out[(size_t)r * p.sstride_out + (size_t)(q0 + tok) * p.rstride_out + h * kHd + threadIdx.x] = __float2bfloat16_rn(val);
+  const int tok = q0 + j / gq, h = g * gq + j % gq;
+  p.out[(size_t)r * p.sstride_out + (size_t)tok * p.rstride_out + h * kHd + d] = __float2bfloat16_rn(l > 0.f ? o / l : 0.f);
 }
 
 cudaError_t launch_kv_write(const void* qkv, int T, int t, long long sstride, int rstride, int q_per, int kv_per,
@@ -378,8 +405,17 @@ cudaError_t launch_paged_attention(const PagedAttnParams& p, int n_reqs, cudaStr
   paged_attn_kernel<<<(unsigned)items, kAttnThreads, kPagedSmem, st>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  paged_combine_kernel<<<(unsigned)((long long)n_reqs * p.t * p.c_stride), kHd, 0, st>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)((long long)n_reqs * p.t * p.kv_per * p.q_stride));
+  cfg.blockDim = dim3(kHd);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, paged_merge_kernel, p);
 }
 
 }  // namespace tpl

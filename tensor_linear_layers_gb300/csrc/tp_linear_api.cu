@@ -981,22 +981,24 @@ int tp_attention_forward(tp_linear_t* h, int64_t T, const void* qkv, const int32
   return ok();
 }
 
-// Paged attention: splits along each request's keys so that about six CTAs per SM are launched.
+// Paged attention: splits along each request's keys so that about twelve CTAs per SM are
+// launched, at most 512 splits. Workspace: the status word, then the splits' partial results.
 struct PagedPlan {
-  int split_len, n_splits, q_stride, c_stride;
-  int64_t ws_bytes;
+  int split_len, n_splits, q_stride;
+  int64_t partials_off, ws_bytes;
 };
 PagedPlan paged_plan(const tp_linear* h, int n_reqs, int max_query_len, int max_seq_len) {
   PagedPlan pl{};
   const int gq = h->q_per / (h->rep > 1 ? 1 : h->kv_per);
   const int64_t per_split = (int64_t)n_reqs * h->cfg.t * h->kv_per;
   const int max_chunks = (int)ceil_div(std::max(max_seq_len, 1), 128);
-  const int want = (int)std::max<int64_t>(1, std::min<int64_t>(max_chunks, ceil_div(6LL * h->nsm, std::max<int64_t>(per_split, 1))));
+  const int want = (int)std::max<int64_t>(
+      1, std::min<int64_t>({max_chunks, 512, ceil_div(12LL * h->nsm, std::max<int64_t>(per_split, 1))}));
   pl.split_len = (int)ceil_div(ceil_div(std::max(max_seq_len, 1), want), 128) * 128;
   pl.n_splits = (int)ceil_div(std::max(max_seq_len, 1), pl.split_len);
   pl.q_stride = max_query_len * gq;
-  pl.c_stride = max_query_len * h->q_per;
-  pl.ws_bytes = 256 + per_split * pl.n_splits * pl.q_stride * (128 + 2) * 4;
+  pl.partials_off = 256;
+  pl.ws_bytes = pl.partials_off + per_split * pl.n_splits * pl.q_stride * (128 + 2) * 4;
   return pl;
 }
 
@@ -1084,7 +1086,7 @@ int tp_paged_attention(tp_linear_t* h, int64_t T, const void* qkv, const int32_t
   p.out = static_cast<__nv_bfloat16*>(attn_out);
   p.sstride_out = gath ? h->Ks : T * h->Ks;
   p.rstride_out = (int)(gath ? h->cfg.t * h->Ks : h->Ks);
-  p.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + 256);
+  p.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.partials_off);
   p.status = reinterpret_cast<int*>(workspace);
   p.t = h->cfg.t;
   p.q_per = h->q_per;
@@ -1098,9 +1100,7 @@ int tp_paged_attention(tp_linear_t* h, int64_t T, const void* qkv, const int32_t
   p.split_len = pl.split_len;
   p.n_splits = pl.n_splits;
   p.q_stride = pl.q_stride;
-  p.c_stride = pl.c_stride;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt(128.0));
-  p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   const cudaError_t e = launch_paged_attention(p, n_reqs, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged attention launch");
   return ok();
