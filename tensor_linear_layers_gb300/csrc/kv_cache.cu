@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kAttnThreads)
   uint8_t* vs = ks + kChunk * 256;                         // [128 keys][128]
   uint8_t* qsb = vs + kChunk * 256;                        // [16 queries][128]
   uint8_t* psb = qsb + kMRows * 256;                       // [16 queries][128 keys]
-  __shared__ int rowrow[2][kChunk];   // cache row (shard, block, offset) of each key of a chunk (-1: none), per parity
+  __shared__ long long rowoff[2][kChunk];   // element offset of each key's k (or v) head in a cache (-1: none), per parity
   __shared__ float xch[kWarps][kMRows];                    // per-warp row maxima, then row sums
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gr = lane >> 2, tq = lane & 3;   // fragment row group and column pair of this lane
@@ -137,9 +137,15 @@ __global__ void __launch_bounds__(kAttnThreads)
   item /= p.kv_per;
   const int r = item % p.t;
   const int b = item / p.t;
+  const int k0 = sp * p.split_len;
+  // the block-table entries of the first chunk's keys load together with the request's
+  // offsets and length (they do not depend on them)
+  int blk_first = -1;
+  if (tid < kChunk && (k0 + tid) / p.block_size < p.max_blocks)
+    blk_first = p.block_tables[(size_t)b * p.max_blocks + (k0 + tid) / p.block_size];
   const int q0 = p.qsl[b], n_new = p.qsl[b + 1] - q0;
   const int L = p.seq_lens[b];
-  const int k0 = sp * p.split_len, k1 = min(L, k0 + p.split_len);
+  const int k1 = min(L, k0 + p.split_len);
   if (n_new < 0 || n_new > p.max_query_len || L < n_new || L > p.max_seq_len) {
     if (tid == 0 && sp == 0 && r == 0 && g == 0) atomicExch(p.status, kStatusShape);
     return;
@@ -150,30 +156,37 @@ __global__ void __launch_bounds__(kAttnThreads)
   const int nq = n_new * gq;                       // queries of this item
   const long long row_elems = (long long)p.kv_per * kHd;
   float* part = p.partials + (size_t)blockIdx.x * p.q_stride * (kHd + 2);
-  auto lookup = [&](int c0, int par) {             // its row through the block table, one key per thread
+  // each key's cache row through the block table, one key per thread (blk: its entry, if loaded)
+  auto lookup = [&](int c0, int par, bool have_blk, int blk) {
     if (tid < kChunk) {
       const int key = c0 + tid;
-      int row = -1;
+      long long off = -1;
       if (key < k1) {
-        const int blk = p.block_tables[(size_t)b * p.max_blocks + key / p.block_size];
+        if (!have_blk) blk = p.block_tables[(size_t)b * p.max_blocks + key / p.block_size];
         if (blk >= 0 && blk < p.num_blocks)
-          row = (r * p.num_blocks + blk) * p.block_size + key % p.block_size;
+          off = (long long)((r * p.num_blocks + blk) * p.block_size + key % p.block_size) * row_elems + g * kHd;
         else
           atomicExch(p.status, kStatusShape);
       }
-      rowrow[par][tid] = row;
+      rowoff[par][tid] = off;
     }
   };
   // 16-byte copies, 16 per row; missing rows read as zero (a committed group per call). The
   // cache is read once per step: its lines go first from L2, the splits' partials stay.
   const uint64_t pol = policy_evict_first();
+  // thread = 16-byte piece lc of rows lr, lr + 16, ..., lr + 112: its shared-memory
+  // offsets differ by 16 rows, the same swizzle
+  const int lr = tid >> 4, lc = tid & 15;
+  const uint32_t ldst = swz(lr, lc * 8);
   auto load_rows = [&](uint8_t* dst, const __nv_bfloat16* cache, int par) {
-#pragma unroll 4
-    for (int e = tid; e < kChunk * 16; e += kAttnThreads) {
-      const int row = e >> 4, c = e & 15;
-      const int cr = rowrow[par][row];
-      const __nv_bfloat16* src = cache + (cr >= 0 ? cr * row_elems + g * kHd : 0) + c * 8;
-      cp_async16(dst + swz(row, c * 8), src, cr >= 0 ? 16 : 0, pol);
+#pragma unroll
+    for (int k0 = 0; k0 < kChunk / 16; k0 += 4) {
+      long long o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[k] = rowoff[par][lr + 16 * (k0 + k)];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        cp_async16(dst + ldst + (k0 + k) * 16 * 256, cache + (o[k] >= 0 ? o[k] : 0) + lc * 8, o[k] >= 0 ? 16 : 0, pol);
     }
     cp_async_commit();
   };
@@ -181,9 +194,16 @@ __global__ void __launch_bounds__(kAttnThreads)
   const int a_row = (lane & 7) + 8 * ((lane >> 3) & 1), a_col = 8 * (lane >> 4);
   const int bk_row = (lane & 7) + 8 * (lane >> 4), bk_col = 8 * ((lane >> 3) & 1);
   const int bv_row = (lane & 7) + 8 * ((lane >> 3) & 1), bv_col = 8 * (lane >> 4);
-  int ci = 0;   // chunks of this CTA so far: chunk ci uses rowrow[ci & 1]
+  int ci = 0;   // chunks of this CTA so far: chunk ci uses rowoff[ci & 1]
   for (int qa = 0; qa < nq; qa += kMRows) {
     const int qc = min(kMRows, nq - qa);
+    // the first chunk's keys and values start loading
+    if (k0 < k1) {
+      lookup(k0, ci & 1, qa == 0, blk_first);
+      __syncthreads();
+      load_rows(ks, p.cache_k, ci & 1);
+      load_rows(vs, p.cache_v, ci & 1);
+    }
     // the pass's queries as bf16 rows (rows past qc zero); query j: token q0 + (qa + j) / gq,
     // head h0 + (qa + j) % gq
     for (int e = tid; e < kMRows * kHd / 8; e += kAttnThreads) {
@@ -209,16 +229,10 @@ __global__ void __launch_bounds__(kAttnThreads)
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) oacc[nt][i] = 0.f;
-    if (k0 < k1) {
-      lookup(k0, ci & 1);
-      __syncthreads();
-      load_rows(ks, p.cache_k, ci & 1);
-      load_rows(vs, p.cache_v, ci & 1);
-    }
     for (int c0 = k0; c0 < k1; c0 += kChunk, ++ci) {
       const int par = ci & 1;
       const bool more = c0 + kChunk < k1;
-      if (more) lookup(c0 + kChunk, par ^ 1);
+      if (more) lookup(c0 + kChunk, par ^ 1, false, 0);
       cp_async_wait_but_one();             // this chunk's K (its V may still be in flight)
       __syncthreads();
       // S = Q K^T for keys [16 warp, +16): 8 k-steps of 16 head dimensions, 2 n-tiles of 8 keys
@@ -238,7 +252,7 @@ __global__ void __launch_bounds__(kAttnThreads)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int kl = 16 * warp + 8 * nt + 2 * tq + (i & 1);
-          const bool ok = rowrow[par][kl] >= 0 && c0 + kl <= pos[i >> 1];
+          const bool ok = rowoff[par][kl] >= 0 && c0 + kl <= pos[i >> 1];
           cs[nt][i] = ok ? cs[nt][i] * p.scale_log2 : -INFINITY;
           mloc[i >> 1] = fmaxf(mloc[i >> 1], cs[nt][i]);
         }
