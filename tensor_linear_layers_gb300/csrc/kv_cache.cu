@@ -216,7 +216,8 @@ __global__ void __launch_bounds__(kAttnThreads)
       }
       *reinterpret_cast<uint4*>(qsb + swz(j, c * 8)) = v;
     }
-    // causal limit of this lane's rows gr and gr + 8 (-1: no query)
+    // causal limit of this lane's rows gr and gr + 8 (-1: no query), and of the pass's first query
+    const int pos_min = L - n_new + qa / gq;
     int pos[2];
 #pragma unroll
     for (int h2 = 0; h2 < 2; ++h2) {
@@ -245,17 +246,30 @@ __global__ void __launch_bounds__(kAttnThreads)
         mma_bf16_16816(cs[0], a, bk);
         mma_bf16_16816(cs[1], a, bk + 2);
       }
-      // scaled scores with the mask (missing key or after the query), and this warp's row maxima
+      // scaled scores with the mask (missing key or after the query), and this warp's row maxima;
+      // a chunk whose keys all exist and precede every query of the pass needs no mask (rows
+      // without a query then score 0 and are never stored; a key of a block id out of range
+      // reads zeros and has raised the status)
       float mloc[2] = {-INFINITY, -INFINITY};
+      if (c0 + kChunk <= k1 && c0 + kChunk - 1 <= pos_min) {
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int kl = 16 * warp + 8 * nt + 2 * tq + (i & 1);
-          const bool ok = rowoff[par][kl] >= 0 && c0 + kl <= pos[i >> 1];
-          cs[nt][i] = ok ? cs[nt][i] * p.scale_log2 : -INFINITY;
-          mloc[i >> 1] = fmaxf(mloc[i >> 1], cs[nt][i]);
-        }
+          for (int i = 0; i < 4; ++i) {
+            cs[nt][i] *= p.scale_log2;
+            mloc[i >> 1] = fmaxf(mloc[i >> 1], cs[nt][i]);
+          }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int kl = 16 * warp + 8 * nt + 2 * tq + (i & 1);
+            const bool ok = rowoff[par][kl] >= 0 && c0 + kl <= pos[i >> 1];
+            cs[nt][i] = ok ? cs[nt][i] * p.scale_log2 : -INFINITY;
+            mloc[i >> 1] = fmaxf(mloc[i >> 1], cs[nt][i]);
+          }
+      }
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         mloc[h2] = fmaxf(mloc[h2], __shfl_xor_sync(0xffffffffu, mloc[h2], 1));
