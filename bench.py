@@ -514,15 +514,14 @@ def run_ours(args, ws, rank, local):
         aos = [torch.empty(w.t, len(lens), q_per * w.hd, dtype=torch.bfloat16, device=dev) for _ in range(R)]
         pws = torch.zeros(blocks[0].paged_attention_workspace_size(len(lens), 1, max(lens)), dtype=torch.uint8,
                           device=dev)
-        kws = torch.zeros(16, dtype=torch.uint8, device=dev)
-        wss = [pws, kws]
-        launches_per_step = 3           # cache write, split attention, split merge
+        wss = [pws]
+        launches_per_step = 2           # split attention (it writes the new tokens' k and v first), split merge
 
         def step(i):
             j = i % R
             ck, cv = caches[j]
-            blocks[0].kv_cache_write(qkvs[j], new_slots, ck, cv, ws=kws)
-            blocks[0].paged_attention(qkvs[j], qsl, lens_d, tables_d, ck, cv, 1, max(lens), out=aos[j], ws=pws)
+            blocks[0].paged_attention(qkvs[j], qsl, lens_d, tables_d, ck, cv, 1, max(lens), out=aos[j], ws=pws,
+                                      slot_mapping=new_slots)
         dominant = step
     elif w.kind == "moe":
         d = workloads.moe_inputs(w)
@@ -688,8 +687,8 @@ def run_ours(args, ws, rank, local):
             j = i % R
             ck, cv = caches[j]
             qkvs[j].copy_(hq[j], non_blocking=True)
-            blocks[0].kv_cache_write(qkvs[j], new_slots, ck, cv, ws=kws)
-            blocks[0].paged_attention(qkvs[j], qsl, lens_d, tables_d, ck, cv, 1, max(lens), out=aos[j], ws=pws)
+            blocks[0].paged_attention(qkvs[j], qsl, lens_d, tables_d, ck, cv, 1, max(lens), out=aos[j], ws=pws,
+                                      slot_mapping=new_slots)
             ho[j].copy_(aos[j], non_blocking=True)
     elif w.kind == "moe":
         hx = [xs[j].cpu().pin_memory() for j in range(R)]
@@ -774,7 +773,7 @@ def run_ours(args, ws, rank, local):
         dom_alg = float(wbytes + abytes) if fused else dominant_kernel_bytes(w)
         achieved = dom_alg / dom_s / 1e9
         if w.kind == "paged":
-            key, kname = "paged@", "paged decode step: cache write, split attention (paged_attn_kernel), split merge"
+            key, kname = "paged@", "paged decode step: split attention with the new tokens' cache write (paged_attn_kernel), split merge"
         elif w.kind == "moe":
             key, kname = "moe@", "the MoE step: routing, gather, grouped expert GEMMs (tc_gemm_kernel), combine"
         elif fused:

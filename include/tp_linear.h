@@ -242,7 +242,13 @@ int tp_attention_forward(tp_linear_t* h, int64_t T, const void* qkv, const int32
  *   query_start_loc[b+1]) of qkv and the last positions of its seq_lens[b] tokens;
  *   the token at position p attends (causally) to positions 0..p of its request,
  *   read from the cache through block_tables[b][p / block_size] (int32, row length
- *   max_blocks_per_req). Write the new tokens to the cache first. attn_out has the
+ *   max_blocks_per_req). The new tokens' k and v must be in the cache: either
+ *   written before (tp_kv_cache_write), or written by this call when slot_mapping
+ *   (int32 [T], device, may be null) is given: token i goes to slot_mapping[i] as
+ *   tp_kv_cache_write would put it (negative = padding, past the cache =
+ *   TP_ERR_SHAPE), by the attention kernel itself, before it reads that position.
+ *   The slot of a new token must be the one its request's block table names for its
+ *   position, and no other request of the call may read it. attn_out has the
  *   attention core's layout. Scores, softmax and the split merge in fp32, output
  *   rounded to bf16. Device arrays: query_start_loc [n_reqs + 1], seq_lens [n_reqs],
  *   block_tables [n_reqs][max_blocks_per_req], all int32. Host bounds: every request
@@ -259,8 +265,8 @@ int tp_paged_attention_workspace_size(const tp_linear_t* h, int32_t n_reqs, int3
                                       int32_t max_seq_len, int64_t* bytes);
 int tp_paged_attention(tp_linear_t* h, int64_t T, const void* qkv, const int32_t* query_start_loc,
                        const int32_t* seq_lens, int32_t n_reqs, int32_t max_query_len, int32_t max_seq_len,
-                       const int32_t* block_tables, int32_t max_blocks_per_req, const void* cache_k,
-                       const void* cache_v, int64_t num_blocks, int32_t block_size, void* attn_out,
+                       const int32_t* block_tables, int32_t max_blocks_per_req, const int32_t* slot_mapping,
+                       void* cache_k, void* cache_v, int64_t num_blocks, int32_t block_size, void* attn_out,
                        void* workspace, int64_t workspace_bytes, tp_stream_t stream);
 
 /*

@@ -99,7 +99,7 @@ def lib() -> ctypes.CDLL:
         "tp_moe_forward": [P, I64, I32, P, P, P, P, P, I64, P],
         "tp_kv_cache_write": [P, I64, P, P, P, P, I64, I32, P, I64, P],
         "tp_paged_attention_workspace_size": [P, I32, I32, I32, PI64],
-        "tp_paged_attention": [P, I64, P, P, P, I32, I32, I32, P, I32, P, P, I64, I32, P, P, I64, P],
+        "tp_paged_attention": [P, I64, P, P, P, I32, I32, I32, P, I32, P, P, P, I64, I32, P, P, I64, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -307,8 +307,9 @@ class TPLinear:
 
     def paged_attention(self, qkv: torch.Tensor, query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
                         block_tables: torch.Tensor, cache_k: torch.Tensor, cache_v: torch.Tensor,
-                        max_query_len: int, max_seq_len: int, out=None, ws=None, stream=None):
-        """Attention of the new tokens (rows of qkv) over their requests' cached keys.
+                        max_query_len: int, max_seq_len: int, out=None, ws=None, stream=None, slot_mapping=None):
+        """Attention of the new tokens (rows of qkv) over their requests' cached keys; with
+        slot_mapping (int32 [T]) the call also writes the new tokens' k and v to their slots.
         Returns (attn in the attention core's output layout, workspace)."""
         c = self.cfg
         T = qkv.shape[0] if self.gathered else qkv.shape[1]
@@ -320,12 +321,16 @@ class TPLinear:
         if ws is None:
             ws = torch.zeros(self.paged_attention_workspace_size(n_reqs, max_query_len, max_seq_len),
                              dtype=torch.uint8, device=qkv.device)
-        for name, a in (("query_start_loc", query_start_loc), ("seq_lens", seq_lens), ("block_tables", block_tables)):
+        for name, a in (("query_start_loc", query_start_loc), ("seq_lens", seq_lens), ("block_tables", block_tables),
+                        ("slot_mapping", slot_mapping)):
+            if a is None and name == "slot_mapping":
+                continue
             if a.dtype != torch.int32 or not a.is_cuda or not a.is_contiguous():
                 raise TypeError(f"{name} must be a contiguous int32 CUDA tensor")
         _check(lib().tp_paged_attention(self.handle, T, _ptr(_bf16(qkv, "qkv")), _ptr(query_start_loc),
                                         _ptr(seq_lens), n_reqs, int(max_query_len), int(max_seq_len),
-                                        _ptr(block_tables), block_tables.shape[1], _ptr(_bf16(cache_k, "cache_k")),
+                                        _ptr(block_tables), block_tables.shape[1],
+                                        _ptr(slot_mapping), _ptr(_bf16(cache_k, "cache_k")),
                                         _ptr(_bf16(cache_v, "cache_v")), nb, bs, _ptr(out), _ptr(ws), ws.numel(),
                                         _stream(stream)))
         return out, ws

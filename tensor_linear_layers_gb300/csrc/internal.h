@@ -90,8 +90,10 @@ struct PagedAttnParams {
   const int* qsl;                    // [n_reqs + 1] new-token offsets
   const int* seq_lens;               // [n_reqs] tokens of each request, new ones included
   const int* block_tables;           // [n_reqs][max_blocks]
-  const __nv_bfloat16* cache_k;      // [t][num_blocks][block_size][kv_per][128]
-  const __nv_bfloat16* cache_v;
+  const int* slots;                  // [T] cache slot of each new token, written before it is read (null: none)
+  long long n_slots;                 // num_blocks * block_size
+  __nv_bfloat16* cache_k;            // [t][num_blocks][block_size][kv_per][128]
+  __nv_bfloat16* cache_v;
   __nv_bfloat16* out;                // shard r, token i at out + r * sstride_out + i * rstride_out
   long long sstride_out;
   int rstride_out;

@@ -155,6 +155,26 @@ __global__ void __launch_bounds__(kAttnThreads)
   const int h0 = g * gq;
   const int nq = n_new * gq;                       // queries of this item
   const long long row_elems = (long long)p.kv_per * kHd;
+  // The new tokens whose positions fall in this split: their k and v heads of (shard r,
+  // kv head g) go to their slots first. No other CTA reads those positions, and this one
+  // reads them back only after the barrier.
+  if (p.slots != nullptr) {
+    const int first = max(0, k0 - (L - n_new)), last = min(n_new, k1 - (L - n_new));   // new tokens [first, last)
+    for (int e = tid; e < (last - first) * 32; e += kAttnThreads) {
+      const int i = first + (e >> 5), which = (e >> 4) & 1, c = e & 15;   // which: 0 k, 1 v
+      const int s = p.slots[q0 + i];
+      if (s < 0) continue;                         // padding token
+      if (s >= p.n_slots) {
+        atomicExch(p.status, kStatusShape);
+        continue;
+      }
+      const __nv_bfloat16* src = p.qkv + (size_t)r * p.sstride_in + (size_t)(q0 + i) * p.rstride_in +
+                                 (p.q_per + which * p.kv_per + g) * kHd + c * 8;
+      __nv_bfloat16* dst = (which ? p.cache_v : p.cache_k) + ((size_t)r * p.n_slots + s) * row_elems + g * kHd + c * 8;
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+    }
+    __syncthreads();
+  }
   float* part = p.partials + (size_t)blockIdx.x * p.q_stride * (kHd + 2);
   // each key's cache row through the block table, one key per thread (blk: its entry, if loaded)
   auto lookup = [&](int c0, int par, bool have_blk, int blk) {

@@ -1041,8 +1041,8 @@ int tp_paged_attention_workspace_size(const tp_linear_t* h, int32_t n_reqs, int3
 
 int tp_paged_attention(tp_linear_t* h, int64_t T, const void* qkv, const int32_t* query_start_loc,
                        const int32_t* seq_lens, int32_t n_reqs, int32_t max_query_len, int32_t max_seq_len,
-                       const int32_t* block_tables, int32_t max_blocks_per_req, const void* cache_k,
-                       const void* cache_v, int64_t num_blocks, int32_t block_size, void* attn_out,
+                       const int32_t* block_tables, int32_t max_blocks_per_req, const int32_t* slot_mapping,
+                       void* cache_k, void* cache_v, int64_t num_blocks, int32_t block_size, void* attn_out,
                        void* workspace, int64_t workspace_bytes, tp_stream_t stream) {
   if (h == nullptr) return fail(TP_ERR_ARG, "handle is null");
   if (h->cfg.kind != TP_BLOCK_ATTN_PROJ) return fail(TP_ERR_ARG, "not an attention handle");
@@ -1067,6 +1067,8 @@ int tp_paged_attention(tp_linear_t* h, int64_t T, const void* qkv, const int32_t
   for (const int32_t* q : {query_start_loc, seq_lens, block_tables})
     if (q == nullptr || (reinterpret_cast<uintptr_t>(q) & 3u) != 0)
       return fail(TP_ERR_ARG, "query_start_loc, seq_lens and block_tables must be 4-byte aligned device arrays");
+  if ((reinterpret_cast<uintptr_t>(slot_mapping) & 3u) != 0)
+    return fail(TP_ERR_ARG, "slot_mapping must be null or a 4-byte aligned device array");
   const PagedPlan pl = paged_plan(h, n_reqs, max_query_len, max_seq_len);
   if (workspace == nullptr || !aligned16(workspace)) return fail(TP_ERR_ARG, "workspace is null or not 16-byte aligned");
   if (workspace_bytes < pl.ws_bytes)
@@ -1081,8 +1083,10 @@ int tp_paged_attention(tp_linear_t* h, int64_t T, const void* qkv, const int32_t
   p.qsl = query_start_loc;
   p.seq_lens = seq_lens;
   p.block_tables = block_tables;
-  p.cache_k = static_cast<const __nv_bfloat16*>(cache_k);
-  p.cache_v = static_cast<const __nv_bfloat16*>(cache_v);
+  p.slots = slot_mapping;
+  p.n_slots = num_blocks * (int64_t)block_size;
+  p.cache_k = static_cast<__nv_bfloat16*>(cache_k);
+  p.cache_v = static_cast<__nv_bfloat16*>(cache_v);
   p.out = static_cast<__nv_bfloat16*>(attn_out);
   p.sstride_out = gath ? h->Ks : T * h->Ks;
   p.rstride_out = (int)(gath ? h->cfg.t * h->Ks : h->Ks);

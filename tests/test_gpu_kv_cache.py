@@ -7,8 +7,10 @@ attention over the GPU's own cache contents, and for the decode case also the
 contiguous attention core on the same rows (the cache must hold exactly the
 sequence). Cases: decode (one new token per request) and chunks of new tokens,
 a request of one token, scattered blocks, kv heads split and replicated, the
-Llama-3-8B-shaped decode batch at full size, the gathered layout, and block
-ids out of range.
+Llama-3-8B-shaped decode batch at full size, the gathered layout, block ids
+and slots out of range. The attention call that writes the new tokens' k and v
+itself must leave the same cache bits and return the same output bits as the
+separate write followed by attention.
 """
 import numpy as np
 import pytest
@@ -43,8 +45,9 @@ def width(nq, nkv, t):
     return (nq // t + 2 * kv_per) * 128
 
 
-def build_case(blk, nq, nkv, t, lens, new, bs, seed):
-    """Cache filled with every request's tokens through the GPU write; returns what the tests need."""
+def build_case(blk, nq, nkv, t, lens, new, bs, seed, write_new=True):
+    """Cache filled with every request's tokens (or only the context before the new ones)
+    through the GPU write; returns what the tests need."""
     rng = np.random.default_rng(seed)
     n_blocks = sum(-(-L // bs) for L in lens) + 5
     perm = rng.permutation(n_blocks)
@@ -60,10 +63,13 @@ def build_case(blk, nq, nkv, t, lens, new, bs, seed):
     slots = np.concatenate([[tables[b, p // bs] * bs + p % bs for p in range(L)] for b, L in enumerate(lens)])
     ck = torch.zeros(blk.kv_cache_shape(n_blocks, bs), dtype=torch.bfloat16, device="cuda")
     cv = torch.zeros_like(ck)
-    ws = blk.kv_cache_write(full.cuda(), torch.from_numpy(slots.astype(np.int32)).cuda(), ck, cv)
+    rows = np.concatenate([np.arange(cu[b] + L - n, cu[b] + L) for b, (L, n) in enumerate(zip(lens, new))])
+    wslots = slots.copy()
+    if not write_new:
+        wslots[rows] = -1
+    ws = blk.kv_cache_write(full.cuda(), torch.from_numpy(wslots.astype(np.int32)).cuda(), ck, cv)
     torch.cuda.synchronize()
     assert int(ws[:4].view(torch.int32).item()) == 0
-    rows = np.concatenate([np.arange(cu[b] + L - n, cu[b] + L) for b, (L, n) in enumerate(zip(lens, new))])
     qkv_new = full[:, rows].contiguous()
     qsl = np.concatenate([[0], np.cumsum(new)]).astype(np.int32)
     return dict(full=full, cu=cu, rows=rows, qkv_new=qkv_new, qsl=qsl, tables=tables, ck=ck, cv=cv, slots=slots)
@@ -150,5 +156,44 @@ def test_block_id_out_of_range_reports_shape_error():
     assert st == tl.TP_ERR_SHAPE
     bad = torch.tensor([c["ck"].shape[1] * bs], dtype=torch.int32, device="cuda")       # one past the cache
     ws = blk.kv_cache_write(c["qkv_new"][:, :1].contiguous().cuda(), bad, c["ck"], c["cv"])
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == tl.TP_ERR_SHAPE
+
+
+@pytest.mark.parametrize("nq,nkv,t,lens,new,bs", [
+    (8, 2, 2, [1, 37, 300, 129], [1, 1, 1, 1], 16),     # decode
+    (4, 4, 2, [90, 17, 400], [5, 17, 3], 16),           # chunks, one whole prefill
+    (8, 2, 2, [270, 50], [30, 2], 16),                  # new tokens on both sides of a split boundary
+    (8, 2, 4, [200, 64], [1, 1], 8),                    # t > nkv: each shard writes its replica
+])
+def test_write_inside_attention_same_bits(nq, nkv, t, lens, new, bs):
+    blk = make_attn(256, nq, nkv, t)
+    c = build_case(blk, nq, nkv, t, lens, new, bs, seed=20 + len(lens), write_new=False)
+    new_slots = c["slots"][c["rows"]].astype(np.int32)
+    new_slots[0] = -1                                   # a padding token writes nothing on either path
+    new_slots = torch.from_numpy(new_slots).cuda()
+    ck2, cv2 = c["ck"].clone(), c["cv"].clone()
+    out_f, ws = blk.paged_attention(c["qkv_new"].cuda(), torch.from_numpy(c["qsl"]).cuda(),
+                                    torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                                    torch.from_numpy(c["tables"]).cuda(), ck2, cv2, max(new), max(lens),
+                                    slot_mapping=new_slots)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 0
+    wk = blk.kv_cache_write(c["qkv_new"].cuda(), new_slots, c["ck"], c["cv"])
+    out_s, st = run_paged(blk, c, lens, new, bs)
+    assert st == 0 and int(wk[:4].view(torch.int32).item()) == 0
+    assert torch.equal(ck2, c["ck"]) and torch.equal(cv2, c["cv"])
+    assert torch.equal(out_f, out_s)
+
+
+def test_write_inside_attention_slot_out_of_range():
+    nq, nkv, t, lens, new, bs = 8, 2, 2, [40, 9], [1, 1], 16
+    blk = make_attn(256, nq, nkv, t)
+    c = build_case(blk, nq, nkv, t, lens, new, bs, seed=5, write_new=False)
+    bad = torch.tensor([c["ck"].shape[1] * bs, int(c["slots"][c["rows"][1]])], dtype=torch.int32, device="cuda")
+    _, ws = blk.paged_attention(c["qkv_new"].cuda(), torch.from_numpy(c["qsl"]).cuda(),
+                                torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                                torch.from_numpy(c["tables"]).cuda(), c["ck"], c["cv"], 1, max(lens),
+                                slot_mapping=bad)
     torch.cuda.synchronize()
     assert int(ws[:4].view(torch.int32).item()) == tl.TP_ERR_SHAPE
