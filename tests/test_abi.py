@@ -201,3 +201,12 @@ def test_moe_config_and_packing(L):
 
 def test_moe_forward_rejects_null_handle(L):
     assert L.tp_moe_forward(None, 4, 2, None, None, None, None, None, 0, None) == tl.TP_ERR_ARG
+
+
+def test_kv_cache_calls_reject_null_handle(L):
+    p = ctypes.c_void_p(0x10000)
+    b = ctypes.c_int64()
+    assert L.tp_kv_cache_write(None, 4, p, p, p, p, 16, 16, p, 16, None) == tl.TP_ERR_ARG
+    assert L.tp_paged_attention_workspace_size(None, 4, 1, 256, ctypes.byref(b)) == tl.TP_ERR_ARG
+    assert L.tp_paged_attention(None, 4, p, p, p, 4, 1, 256, p, 16, None, p, p, 16, 16, p, p, 1 << 20,
+                                None) == tl.TP_ERR_ARG
