@@ -376,9 +376,9 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
-      // x_norm is read by the tensor copies of phase 1 (async proxy)
+      // x_norm is read by the tensor copies of phase 1 (async proxy); the rows of all
+      // epilogue threads are released by the one fence in bar_arrive after the barrier
       fence_proxy_async_global();
-      __threadfence();
       named_bar_sync(1, 128);
       if (et == 0 && blockIdx.x < norm_ctas) bar_arrive(P.bars + 0);
     }
@@ -552,21 +552,26 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, S::kTmemCols);
   }
-  // every wait of this CTA is behind it: the last CTA out resets counters and flags
+  // every wait of this CTA is behind it: the last CTA out resets counters and flags, all
+  // threads at once. The next launch reads them only after this grid has completed
+  // (griddepcontrol.wait, or stream order), so the resets need no fence of their own.
+  volatile int* s_last = reinterpret_cast<volatile int*>(misc + 12);
   if (threadIdx.x == 0) {
     __threadfence();
-    const unsigned old = atomicAdd(P.bars + 1, 1u);
-    if (old == grid - 1) {
-      const int n1 = P.g1.m_tiles, n2 = P.g2.m_tiles;
-      for (int i = 0; i < n1; ++i) {
-        P.hready[i] = 0u;
-        P.cnt1[i] = 0u;
-      }
-      for (int i = 0; i < n2; ++i) P.cnt2[i] = 0u;
+    *s_last = atomicAdd(P.bars + 1, 1u) == grid - 1 ? 1 : 0;
+  }
+  __syncthreads();
+  if (*s_last) {
+    const int n1 = P.g1.m_tiles, n2 = P.g2.m_tiles;
+    for (int i = threadIdx.x; i < n1; i += blockDim.x) {
+      P.hready[i] = 0u;
+      P.cnt1[i] = 0u;
+    }
+    for (int i = threadIdx.x; i < n2; i += blockDim.x) P.cnt2[i] = 0u;
+    if (threadIdx.x == 0) {
       P.bars[0] = 0u;
+      P.bars[1] = 0u;
       P.bars[2] = 0u;
-      __threadfence();
-      atomicExch(P.bars + 1, 0u);
     }
   }
 }
