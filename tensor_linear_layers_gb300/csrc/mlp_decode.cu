@@ -56,6 +56,9 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 4);
   volatile int* s_ok = reinterpret_cast<volatile int*>(misc + 8);
   float* s_red = reinterpret_cast<float*>(misc + 16);  // 4 floats: norm reduction
+  // the down unit this CTA takes at run time, and the barrier that publishes it to the roles
+  const uint32_t unit_bar = smem_u32(misc + 32);
+  volatile int* s_unit = reinterpret_cast<volatile int*>(misc + 40);
   // h tile of a gate_up unit, [token][128 columns] bf16, written out with 16-byte stores
   __nv_bfloat16* s_h = reinterpret_cast<__nv_bfloat16*>(base_ptr + STAGES * S::kStageBytes + S::kBarBytes);
 
@@ -72,6 +75,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(tempty_bar(b), 4);
     }
     mbar_init(done_bar, 1);
+    mbar_init(unit_bar, 1);
     *s_abort = 0;
     fence_barrier_init();
     prefetch_tensormap(&map_x);
@@ -96,9 +100,14 @@ __global__ void __launch_bounds__(192, 1)
       *s_abort = 1;
     }
   };
-  // gate_up units go to CTAs 0, 1, ...; down units to CTAs grid-1, grid-2, ...,
-  // so CTAs without gate_up work start down (and its weight stream) at once
+  // gate_up units go to CTAs 0, 1, ... When there are no more down units than CTAs, each CTA
+  // takes at most one down unit from a counter once its producer has issued its gate_up
+  // work, so the CTAs that finish gate_up first (or have none) take the down units first.
+  // Otherwise down units go to CTAs grid-1, grid-2, ..., so CTAs without gate_up work start
+  // down at once.
+  const bool dyn_down = P.g2.units <= (int)grid;
   auto first_unit = [&](int ph) -> int { return ph == 0 ? (int)blockIdx.x : (int)(grid - 1 - blockIdx.x); };
+  auto step_unit = [&](int ph, int u, int units) -> int { return (ph == 1 && dyn_down) ? units : u + (int)grid; };
   auto krange = [](const GemmParams& p, int u, int& tm, int& kb0, int& kb1) {
     const int tile = u / p.splits;
     const int sp = u - tile * p.splits;
@@ -166,7 +175,18 @@ __global__ void __launch_bounds__(192, 1)
       };
       for (int ph = 0; ph < 2 && ok; ++ph) {
         const GemmParams& p = ph == 0 ? P.g1 : P.g2;
-        for (int u = first_unit(ph); u < p.units && ok; u += grid) {
+        int u0 = first_unit(ph);
+        if (ph == 1 && dyn_down) {
+          // the counter belongs to this launch once the previous one has completed
+          if (!dep_waited) {
+            griddep_wait();
+            dep_waited = true;
+          }
+          u0 = (int)atomicAdd(P.bars + 3, 1u);
+          *s_unit = u0;
+          mbar_arrive(unit_bar);
+        }
+        for (int u = u0; u < p.units && ok; u = step_unit(ph, u, p.units)) {
           int tm, kb0, kb1;
           krange(p, u, tm, kb0, kb1);
           const uint8_t* wsrc = p.w_packed + (size_t)tm * p.nkb * kWBlockBytes;
@@ -229,7 +249,16 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       for (int ph = 0; ph < 2 && ok; ++ph) {
         const GemmParams& p = ph == 0 ? P.g1 : P.g2;
-        for (int u = first_unit(ph); u < p.units && ok; u += grid) {
+        int u0 = first_unit(ph);
+        if (ph == 1 && dyn_down) {
+          if (!mbar_wait_bounded(unit_bar, 0, s_abort, timeout)) {
+            set_abort();
+            ok = false;
+            break;
+          }
+          u0 = *s_unit;
+        }
+        for (int u = u0; u < p.units && ok; u = step_unit(ph, u, p.units)) {
           int tm, kb0, kb1;
           krange(p, u, tm, kb0, kb1);
           if (!mbar_wait_bounded(tempty_bar(buf), acc_phase ^ 1u, s_abort, timeout)) {
@@ -387,7 +416,20 @@ __global__ void __launch_bounds__(192, 1)
     // ---- gate_up units, then down units
     for (int ph = 0; ph < 2 && ok; ++ph) {
       const GemmParams& p = ph == 0 ? P.g1 : P.g2;
-      for (int u = first_unit(ph); u < p.units && ok; u += grid) {
+      int u0 = first_unit(ph);
+      if (ph == 1 && dyn_down) {
+        bool w_ok = true;
+        if (et == 0) {
+          w_ok = mbar_wait_bounded(unit_bar, 0, s_abort, timeout);
+          if (!w_ok) set_abort();
+        }
+        if (!agree(w_ok)) {
+          ok = false;
+          break;
+        }
+        u0 = *s_unit;
+      }
+      for (int u = u0; u < p.units && ok; u = step_unit(ph, u, p.units)) {
         int tm, kb0, kb1;
         krange(p, u, tm, kb0, kb1);
         const int sp = u - tm * p.splits;
@@ -572,6 +614,7 @@ __global__ void __launch_bounds__(192, 1)
       P.bars[0] = 0u;
       P.bars[1] = 0u;
       P.bars[2] = 0u;
+      P.bars[3] = 0u;
     }
   }
 }

@@ -287,6 +287,17 @@ int fused_gate_up_splits(const tp_linear* h) {
   return tiles * 2 >= h->nsm ? 1 : std::max(1, h->nsm / tiles);
 }
 
+// Split count of the down GEMM inside the fused decode block: the stand-alone plan's, capped
+// so that there are no more down units than SMs. Each CTA then takes at most one down unit
+// at run time, in the order the CTAs finish their gate_up work, and every split of a tile is
+// resident at once. (Fewer, larger units, leaving the CTAs that finish gate_up last without
+// down work, measured slower: a unit then needs more bandwidth than one SM draws.)
+int fused_down_splits(const tp_linear* h, int64_t T) {
+  const Plan p = make_plan(h, 1, T);
+  const int tiles = p.m_tiles * p.n_tiles;
+  return std::min(p.splits, std::max(1, h->nsm / std::max(tiles, 1)));
+}
+
 Layout make_layout(const tp_linear* h, int64_t T) {
   Layout L{};
   int64_t off = dyn_off(h);
@@ -854,7 +865,7 @@ int tp_mlp_forward(tp_linear_t* h, int64_t T, const void* x_in, const void* resi
   void* hbuf = ws + L.h;
   if (T <= kFusedMaxT) {
     // decode-shaped step: norm, gate_up, h, down and both reductions in one launch
-    const Plan p1 = make_plan(h, 0, T, fused_gate_up_splits(h)), p2 = make_plan(h, 1, T);
+    const Plan p1 = make_plan(h, 0, T, fused_gate_up_splits(h)), p2 = make_plan(h, 1, T, fused_down_splits(h, T));
     const void* xsrc = norm ? static_cast<const void*>(ws + L.x_norm) : x_in;
     CUtensorMap map_x, map_h;
     if ((rc = make_map(&map_x, xsrc, h->H, T, 1, 1, p1.bn))) return rc;
@@ -1294,7 +1305,7 @@ extern "C" int tp_mlp_forward_no_alloc(tp_linear_t* h, int64_t T, const void* x_
   cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)dyn_off(h), st);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the no-alloc scratch counters");
   void* hbuf = ws + L.h;
-  const Plan p1 = make_plan(h, 0, T, fused_gate_up_splits(h)), p2 = make_plan(h, 1, T);
+  const Plan p1 = make_plan(h, 0, T, fused_gate_up_splits(h)), p2 = make_plan(h, 1, T, fused_down_splits(h, T));
   const void* xsrc = norm ? static_cast<const void*>(ws + L.x_norm) : x_in;
   CUtensorMap map_x, map_h;
   if ((rc = make_map(&map_x, xsrc, h->H, T, 1, 1, p1.bn))) return rc;
