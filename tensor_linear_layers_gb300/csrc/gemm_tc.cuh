@@ -104,10 +104,13 @@ struct MlpDecodeParams {
   const __nv_bfloat16* gamma;    // [H] (norm)
   __nv_bfloat16* res_out;        // [T, H] (norm)
   __nv_bfloat16* x_norm;         // [T, H] workspace (norm)
-  unsigned* bars;                // [0] norm arrivals, [1] CTAs finished, [2] gate_up partials written
+  // Two sets of counters; a launch uses the set its launch count selects and clears the other.
+  unsigned* bars;                // [0] norm arrivals, [2] gate_up partials written, [3] down units taken; set 1 at +4
   unsigned* cnt1;                // per gate_up tile: splits whose partial is written
   unsigned* hready;              // per gate_up tile: 1 once its h columns are written
   unsigned* cnt2;                // per down tile: splits whose partial is written
+  int cset;                      // words from set 0 to set 1 of cnt1 / hready / cnt2
+  unsigned long long* epoch;     // completed launches in the high 32 bits (each CTA adds its share at exit)
   float eps;
   int H;
   int has_norm;

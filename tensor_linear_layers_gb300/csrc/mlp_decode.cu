@@ -17,9 +17,10 @@
 //            of the tile; mlp_out = y, residual_stream = y + residual
 //
 // Between the GEMMs, work flows through per-tile counters and flags in the
-// workspace. Every wait is bounded (status word on
-// timeout); with one CTA per SM every CTA of the grid is resident. The last CTA
-// to finish resets the counters and flags for the next launch.
+// workspace. Every wait is bounded (status word on timeout); with one CTA per SM
+// every CTA of the grid is resident. There are two sets of counters: a launch
+// uses the one its launch count (a word every CTA adds its share to at exit)
+// selects, and clears the other for the next launch.
 #include "gemm_launch.cuh"
 
 namespace tpl {
@@ -108,6 +109,12 @@ __global__ void __launch_bounds__(192, 1)
   const bool dyn_down = P.g2.units <= (int)grid;
   auto first_unit = [&](int ph) -> int { return ph == 0 ? (int)blockIdx.x : (int)(grid - 1 - blockIdx.x); };
   auto step_unit = [&](int ph, int u, int units) -> int { return (ph == 1 && dyn_down) ? units : u + (int)grid; };
+  // The counters of this launch: the set selected by the number of launches completed
+  // before it (read after griddepcontrol.wait). The other set is the next launch's; this
+  // launch clears it, so no CTA has to find out at exit whether it is the last one.
+  auto launch_parity = [&]() -> int {
+    return (int)((*reinterpret_cast<const volatile unsigned long long*>(P.epoch) >> 32) & 1ull);
+  };
   auto krange = [](const GemmParams& p, int u, int& tm, int& kb0, int& kb1) {
     const int tile = u / p.splits;
     const int sp = u - tile * p.splits;
@@ -125,6 +132,15 @@ __global__ void __launch_bounds__(192, 1)
       // before it (griddepcontrol.wait), which comes first whenever an activation
       // copy or a counter of the workspace is needed
       bool dep_waited = false;
+      const unsigned* c_bars = nullptr;     // this launch's counters, known after the dependency wait
+      const unsigned* c_hready = nullptr;
+      auto wait_dep = [&]() {
+        griddep_wait();
+        dep_waited = true;
+        const int par = launch_parity();
+        c_bars = P.bars + 4 * par;
+        c_hready = P.hready + par * P.cset;
+      };
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, last_phase_bits = 0;
@@ -135,10 +151,10 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       auto dep_ready = [&](int dep) -> bool {
         if (dep < 0) {
-          if (!x_ready) x_ready = *reinterpret_cast<const volatile unsigned*>(P.bars) >= norm_ctas;
+          if (!x_ready) x_ready = *reinterpret_cast<const volatile unsigned*>(c_bars) >= norm_ctas;
           return x_ready;
         }
-        return *reinterpret_cast<const volatile unsigned*>(P.hready + dep) >= (unsigned)kItems1;
+        return *reinterpret_cast<const volatile unsigned*>(c_hready + dep) >= (unsigned)kItems1;
       };
       auto issue_front = [&]() {
         const int i = q_head;
@@ -155,10 +171,7 @@ __global__ void __launch_bounds__(192, 1)
       // oldest one while more than `keep` entries remain queued
       auto drain = [&](int keep) -> bool {
         if (q_n <= keep && !dep_waited) return true;
-        if (!dep_waited) {
-          griddep_wait();
-          dep_waited = true;
-        }
+        if (!dep_waited) wait_dep();
         while (q_n > 0) {
           if (dep_ready(q_dep[q_head])) {
             issue_front();
@@ -166,7 +179,7 @@ __global__ void __launch_bounds__(192, 1)
           }
           if (q_n <= keep) return true;
           const int dep = q_dep[q_head];
-          const unsigned* c = dep < 0 ? P.bars : P.hready + dep;
+          const unsigned* c = dep < 0 ? c_bars : c_hready + dep;
           if (!bar_wait(c, dep < 0 ? norm_ctas : (unsigned)kItems1, timeout, s_abort)) return false;
           if (dep < 0) x_ready = true;
           issue_front();
@@ -178,11 +191,8 @@ __global__ void __launch_bounds__(192, 1)
         int u0 = first_unit(ph);
         if (ph == 1 && dyn_down) {
           // the counter belongs to this launch once the previous one has completed
-          if (!dep_waited) {
-            griddep_wait();
-            dep_waited = true;
-          }
-          u0 = (int)atomicAdd(P.bars + 3, 1u);
+          if (!dep_waited) wait_dep();
+          u0 = (int)atomicAdd(const_cast<unsigned*>(c_bars) + 3, 1u);
           *s_unit = u0;
           mbar_arrive(unit_bar);
         }
@@ -227,7 +237,7 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
-      if (!dep_waited) griddep_wait();
+      if (!dep_waited) wait_dep();
       if (ok && !drain(0)) {
         set_abort();
         ok = false;
@@ -323,6 +333,17 @@ __global__ void __launch_bounds__(192, 1)
       return r;
     };
     griddep_wait();
+    const int par = launch_parity();
+    unsigned* const e_bars = P.bars + 4 * par;
+    unsigned* const e_hready = P.hready + par * P.cset;
+    unsigned* const e_cnt2 = P.cnt2 + par * P.cset;
+    {
+      // the other set, used by the launch before this one, starts the next launch at zero
+      unsigned* const o_bars = P.bars + 4 * (par ^ 1);
+      unsigned* const o_cnt = P.cnt1 + (par ^ 1) * P.cset;
+      for (long long i = etid; i < P.cset; i += ethreads) o_cnt[i] = 0u;
+      if (blockIdx.x == 0 && et < 4) o_bars[et] = 0u;
+    }
     // ---- phase 0: residual add + RMSNorm, one row per CTA in turn. The loads of
     // a chunk (a, residual and gamma, up to 8 vectors per thread each) are issued
     // together before anything waits on them, and the rounded residual stays in
@@ -409,7 +430,7 @@ __global__ void __launch_bounds__(192, 1)
       // epilogue threads are released by the one fence in bar_arrive after the barrier
       fence_proxy_async_global();
       named_bar_sync(1, 128);
-      if (et == 0 && blockIdx.x < norm_ctas) bar_arrive(P.bars + 0);
+      if (et == 0 && blockIdx.x < norm_ctas) bar_arrive(e_bars + 0);
     }
 
     float g[CH], uu[CH];
@@ -488,7 +509,7 @@ __global__ void __launch_bounds__(192, 1)
             fence_proxy_async_global();
             __threadfence();
             named_bar_sync(1, 128);
-            if (et == 0) atomicAdd(P.hready + tm, (unsigned)kItems1);
+            if (et == 0) atomicAdd(e_hready + tm, (unsigned)kItems1);
           }
         } else {
           float* part = p.partials + ((size_t)tm * p.splits + sp) * ACC * 128;
@@ -509,7 +530,7 @@ __global__ void __launch_bounds__(192, 1)
             // the whole tile.
             __threadfence();
             named_bar_sync(1, 128);
-            unsigned* cnt = P.cnt2 + tm;
+            unsigned* cnt = e_cnt2 + tm;
             constexpr int items = tile_items<true, KIND_ROW, BN>();
             const bool together = (p.units <= (int)grid) || ((int)grid % p.splits == 0);
             unsigned old = 0;
@@ -548,8 +569,8 @@ __global__ void __launch_bounds__(192, 1)
         named_bar_sync(1, 128);
         bool w1 = true;
         if (et == 0) {
-          bar_arrive(P.bars + 2);
-          w1 = bar_wait(P.bars + 2, grid, timeout, s_abort);
+          bar_arrive(e_bars + 2);
+          w1 = bar_wait(e_bars + 2, grid, timeout, s_abort);
           if (!w1) set_abort();
         }
         if (!agree(w1)) {
@@ -582,7 +603,7 @@ __global__ void __launch_bounds__(192, 1)
           __syncwarp();
           if (lane == 0) {
             __threadfence();
-            atomicAdd(P.hready + x, 32u);
+            atomicAdd(e_hready + x, 32u);
           }
         }
       }
@@ -594,28 +615,11 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, S::kTmemCols);
   }
-  // every wait of this CTA is behind it: the last CTA out resets counters and flags, all
-  // threads at once. The next launch reads them only after this grid has completed
-  // (griddepcontrol.wait, or stream order), so the resets need no fence of their own.
-  volatile int* s_last = reinterpret_cast<volatile int*>(misc + 12);
+  // this CTA's share of the launch count; the grid's shares add up to exactly 2^32, so the high
+  // word counts completed launches whatever grid each launch had (no CTA waits for the sum)
   if (threadIdx.x == 0) {
-    __threadfence();
-    *s_last = atomicAdd(P.bars + 1, 1u) == grid - 1 ? 1 : 0;
-  }
-  __syncthreads();
-  if (*s_last) {
-    const int n1 = P.g1.m_tiles, n2 = P.g2.m_tiles;
-    for (int i = threadIdx.x; i < n1; i += blockDim.x) {
-      P.hready[i] = 0u;
-      P.cnt1[i] = 0u;
-    }
-    for (int i = threadIdx.x; i < n2; i += blockDim.x) P.cnt2[i] = 0u;
-    if (threadIdx.x == 0) {
-      P.bars[0] = 0u;
-      P.bars[1] = 0u;
-      P.bars[2] = 0u;
-      P.bars[3] = 0u;
-    }
+    const unsigned long long share = (1ull << 32) / grid;
+    atomicAdd(P.epoch, blockIdx.x == 0 ? (1ull << 32) - share * (grid - 1) : share);
   }
 }
 

@@ -162,8 +162,9 @@ int make_shard_map(CUtensorMap* m, const void* ptr, int64_t w, int64_t T, int64_
 // ============================================================================ workspace layout
 // header: [0] status word; [64] grid barrier of the column-parallel GEMM;
 // [128] grid barrier of the row-parallel GEMM; [192] counters of the fused
-// decode block. Then the fused block's per-tile counters and flags (fixed size
-// per handle), then the buffers whose size depends on T.
+// decode block (two sets of four words), [224] its launch count (64 bits). Then
+// the fused block's two sets of per-tile counters and flags (fixed size per
+// handle), then the buffers whose size depends on T.
 constexpr int64_t kGbarColOff = 64;
 constexpr int64_t kGbarRowOff = 128;
 constexpr int64_t kDecodeBarsOff = 192;
@@ -208,11 +209,10 @@ struct tp_linear {
 namespace {
 
 // start of the T-dependent part of a forward workspace: after the header and
-// the fused block's per-tile counters (cnt1 and hready per gate_up tile, cnt2
-// per down tile)
-int64_t dyn_off(const tp_linear* h) {
-  return align256(kTileCountersOff + 4 * (2 * (int64_t)h->wt_col + (int64_t)h->wt_row));
-}
+// the fused block's two sets of per-tile counters (cnt1 and hready per gate_up
+// tile, cnt2 per down tile)
+int64_t tile_counter_words(const tp_linear* h) { return 2 * (int64_t)h->wt_col + (int64_t)h->wt_row; }
+int64_t dyn_off(const tp_linear* h) { return align256(kTileCountersOff + 4 * 2 * tile_counter_words(h)); }
 
 struct Plan {
   bool swap;
@@ -892,6 +892,8 @@ int tp_mlp_forward(tp_linear_t* h, int64_t T, const void* x_in, const void* resi
     P.cnt1 = reinterpret_cast<unsigned*>(ws + kTileCountersOff);
     P.hready = P.cnt1 + h->wt_col;
     P.cnt2 = P.hready + h->wt_col;
+    P.cset = (int)tile_counter_words(h);
+    P.epoch = reinterpret_cast<unsigned long long*>(ws + kDecodeBarsOff + 32);
     P.eps = h->cfg.rms_eps;
     P.H = (int)h->H;
     P.has_norm = norm ? 1 : 0;
@@ -1333,6 +1335,8 @@ extern "C" int tp_mlp_forward_no_alloc(tp_linear_t* h, int64_t T, const void* x_
   P.cnt1 = reinterpret_cast<unsigned*>(ws + kTileCountersOff);
   P.hready = P.cnt1 + h->wt_col;
   P.cnt2 = P.hready + h->wt_col;
+  P.cset = (int)tile_counter_words(h);
+  P.epoch = reinterpret_cast<unsigned long long*>(ws + kDecodeBarsOff + 32);
   P.eps = h->cfg.rms_eps;
   P.H = (int)h->H;
   P.has_norm = norm ? 1 : 0;
