@@ -995,7 +995,8 @@ int tp_attention_forward(tp_linear_t* h, int64_t T, const void* qkv, const int32
 }
 
 // Paged attention: splits along each request's keys so that about twelve CTAs per SM are
-// launched, at most 512 splits. Workspace: the status word, then the splits' partial results.
+// launched, at most 512 splits and at most 256 MiB of partial results. Workspace: the status
+// word, then the splits' partial results.
 struct PagedPlan {
   int split_len, n_splits, q_stride;
   int64_t partials_off, ws_bytes;
@@ -1005,8 +1006,12 @@ PagedPlan paged_plan(const tp_linear* h, int n_reqs, int max_query_len, int max_
   const int gq = h->q_per / (h->rep > 1 ? 1 : h->kv_per);
   const int64_t per_split = (int64_t)n_reqs * h->cfg.t * h->kv_per;
   const int max_chunks = (int)ceil_div(std::max(max_seq_len, 1), 128);
+  // the partial results are q_stride * (128 + 2) floats per item: at most 256 MiB of them
+  // unless a single split already needs more (long chunks of new tokens)
+  const int64_t item_bytes = (int64_t)max_query_len * gq * (128 + 2) * 4;
+  const int64_t cap = std::max<int64_t>(1, (int64_t(256) << 20) / std::max<int64_t>(per_split * item_bytes, 1));
   const int want = (int)std::max<int64_t>(
-      1, std::min<int64_t>({max_chunks, 512, ceil_div(12LL * h->nsm, std::max<int64_t>(per_split, 1))}));
+      1, std::min<int64_t>({max_chunks, 512, cap, ceil_div(12LL * h->nsm, std::max<int64_t>(per_split, 1))}));
   pl.split_len = (int)ceil_div(ceil_div(std::max(max_seq_len, 1), want), 128) * 128;
   pl.n_splits = (int)ceil_div(std::max(max_seq_len, 1), pl.split_len);
   pl.q_stride = max_query_len * gq;

@@ -197,3 +197,10 @@ def test_write_inside_attention_slot_out_of_range():
                                 slot_mapping=bad)
     torch.cuda.synchronize()
     assert int(ws[:4].view(torch.int32).item()) == tl.TP_ERR_SHAPE
+
+
+def test_workspace_of_long_chunks_stays_bounded():
+    # a 4096-token chunk of new tokens over 8192 cached ones: fewer splits, not gigabytes of partials
+    blk = make_attn(256, 8, 2, 2)
+    assert blk.paged_attention_workspace_size(1, 4096, 8192) <= 256 * 2**20 + 4096
+    assert blk.paged_attention_workspace_size(32, 1, 4096) < 2**20 * 16      # decode: small
