@@ -6,7 +6,8 @@ softmax and split merge; bf16 output). The reference is the oracle's paged
 attention over the GPU's own cache contents, and for the decode case also the
 contiguous attention core on the same rows (the cache must hold exactly the
 sequence). Cases: decode (one new token per request) and chunks of new tokens,
-a request of one token, scattered blocks, kv heads split and replicated, the
+a request of one token, scattered blocks of 1 to 64 tokens (24 included), t = 1,
+2, 4 and 8 with kv heads split and replicated, the
 Llama-3-8B-shaped decode batch at full size, the gathered layout, block ids
 and slots out of range. The attention call that writes the new tokens' k and v
 itself must leave the same cache bits and return the same output bits as the
@@ -107,6 +108,9 @@ def test_cache_write_is_exact():
     (8, 2, 4, [200, 64], [1, 1], 8),                    # t > nkv: kv head replicated
     (4, 4, 2, [90, 17, 400], [5, 17, 3], 16),           # chunks of new tokens (one whole prefill)
     (16, 2, 1, [1000], [2], 32),                        # groups of 8 q heads, more queries than one pass
+    (32, 8, 8, [300, 5], [1, 1], 24),                   # t = 8, one kv head per shard, blocks of 24
+    (8, 4, 8, [129, 40], [3, 1], 1),                    # t = 8 > nkv: replicated kv heads, blocks of one token
+    (4, 4, 1, [700], [1], 64),                          # t = 1, multi-head (one q head per kv head)
 ])
 def test_paged_attention_matches_oracle(nq, nkv, t, lens, new, bs):
     blk = make_attn(256, nq, nkv, t)
