@@ -381,11 +381,16 @@ const char* tp_last_error(void);
 /*
  * Plan of the GEMM launches a forward call with T tokens would make, for
  * inspection and benchmarks: writes up to 2 entries of
- * {swap_ab, block_n, splits, units, grid} for the column-parallel and the
- * row-parallel GEMM. Returns the number written.
+ * {swap_ab, block_n, splits, units, grid, stages, engine} for the
+ * column-parallel and the row-parallel GEMM. engine: 0 = one CTA per unit
+ * (the other fields describe that launch), 1 = CTA pairs (two-SM MMAs over
+ * 256-token x 256-row tiles, no split-K; an attention handle reports the
+ * launch that runs QKV and o_proj together), 2 = the fused decode-shaped MLP
+ * block (T <= 128, both GEMMs in one launch). The pair choice needs the
+ * device: without one it reports engine 0. Returns the number written.
  */
 typedef struct {
-  int32_t swap_ab, block_n, splits, units, grid, stages;
+  int32_t swap_ab, block_n, splits, units, grid, stages, engine;
 } tp_gemm_plan_t;
 int tp_describe_plan(const tp_linear_t* h, int64_t T, tp_gemm_plan_t* plans, int32_t max_plans);
 

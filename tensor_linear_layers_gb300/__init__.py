@@ -57,7 +57,8 @@ class LayerIO(ctypes.Structure):
 
 class GemmPlan(ctypes.Structure):
     _fields_ = [("swap_ab", ctypes.c_int32), ("block_n", ctypes.c_int32), ("splits", ctypes.c_int32),
-                ("units", ctypes.c_int32), ("grid", ctypes.c_int32), ("stages", ctypes.c_int32)]
+                ("units", ctypes.c_int32), ("grid", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("engine", ctypes.c_int32)]
 
 
 _lib = None

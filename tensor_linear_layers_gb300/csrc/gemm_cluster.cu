@@ -1,12 +1,15 @@
-// Prefill-shaped GEMMs on CTA pairs (thread-block clusters of 2).
+// Prefill-shaped GEMMs on CTA pairs: tcgen05 cta_group::2 (two-SM) MMAs.
 //
-// The two CTAs of a cluster compute adjacent 128-token tiles against the same
-// 256-row weight block. Each CTA loads its own token tile (TMA tensor copy)
-// and half of the 32 KB weight block, multicast into both CTAs' shared memory,
-// so every weight byte leaves L2 once per pair instead of once per CTA. The
-// MMAs stay per CTA (tcgen05 cta_group::1, 128 x 256 accumulators in each
-// CTA's tensor memory); a stage may be refilled only when both CTAs' MMAs have
-// read it, so each MMA commit arrives on the empty barrier of both CTAs.
+// The two CTAs of a cluster of 2 compute one 256-token x 256-weight-row tile
+// together: CTA rank r holds token tile 2 pm + r (128 rows of A) and weight
+// rows [128 r, 128 r + 128) of the 256-row weight block (half of B). One
+// thread of the even CTA issues M = 256, N = 256 MMAs that read A and B from
+// both CTAs' shared memory; each CTA's tensor memory receives its own 128
+// tokens x all 256 weight rows. Every byte of a stage is therefore loaded
+// once per pair, by the CTA that holds it, with plain TMA tensor copies (no
+// multicast); the copies of both CTAs count on the even CTA's full barrier.
+// The MMA commits arrive on both CTAs' empty and accumulator barriers; both
+// CTAs' epilogue warps arrive on the even CTA's accumulator-empty barrier.
 //
 // Same epilogues as the one-CTA engine (gate_up with SiLU*mul, column-parallel
 // store, row-parallel store + residual); no split-K. An optional second,
@@ -15,60 +18,78 @@
 
 namespace tpl {
 
+struct PairShape {
+  static constexpr int kABytes = 128 * 128;   // 128 tokens x 64 bf16 of this CTA
+  static constexpr int kBBytes = 128 * 128;   // this CTA's 128 of the block's 256 weight rows x 64 bf16
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = 7;
+  static constexpr int kAccCols = 256;        // 128 lanes x 256 fp32 columns per accumulator
+  static constexpr int kTmemCols = 512;       // two accumulators
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(256, 256);
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+};
+
 template <int KIND, int KIND2>
 __global__ void __launch_bounds__(192, 1)
-    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_act2,
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_w,
+                        const __grid_constant__ CUtensorMap map_act2, const __grid_constant__ CUtensorMap map_w2,
                         const GemmParams p, const GemmParams p2) {
-  using S = GemmShape<false, KIND, 256>;
-  constexpr int STAGES = S::kStages;
+  using P = PairShape;
+  constexpr int STAGES = P::kStages;
   constexpr int BN = 256;
   constexpr bool kTwo = KIND2 >= 0;
   constexpr uint16_t kBoth = 0x3;
-  constexpr uint32_t kHalfB = kWBlockBytes / 2;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw_addr);
-  const uint32_t bar0 = base + STAGES * S::kStageBytes;
+  const uint32_t bar0 = base + STAGES * P::kStageBytes;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
-  uint8_t* misc = base_ptr + STAGES * S::kStageBytes + 8 * (2 * STAGES + 5);
+  uint8_t* misc = base_ptr + STAGES * P::kStageBytes + 8 * (2 * STAGES + 5);
   volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(misc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 4);
   volatile int* s_ok = reinterpret_cast<volatile int*>(misc + 12);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int rank = (int)cluster_ctarank();          // 0 or 1 within the pair
+  const int rank = (int)(cluster_ctarank() & 1u);   // 0: the CTA that issues the MMAs
+  const bool leader = rank == 0;
   const int cluster = blockIdx.x >> 1;
   const int nclusters = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 2);   // both CTAs' MMAs release a stage
+      mbar_init(full_bar(s), 1);    // the even CTA's expect-tx arrival; both CTAs' bytes
+      mbar_init(empty_bar(s), 1);   // the pair MMA's commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 4);
+      mbar_init(tempty_bar(b), 8);  // four epilogue warps of each CTA
     }
     mbar_init(done_bar, 1);
     *s_abort = 0;
     fence_barrier_init();
     prefetch_tensormap(&map_act);
-    if (kTwo) prefetch_tensormap(&map_act2);
+    prefetch_tensormap(&map_w);
+    if (kTwo) {
+      prefetch_tensormap(&map_act2);
+      prefetch_tensormap(&map_w2);
+    }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(const_cast<uint32_t*>(s_tmem)), S::kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(s_tmem)), P::kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
-  // the peer multicasts into this CTA's stages and barriers: both must be initialised
+  // the peer's copies count on this CTA's barriers and the MMA commits arrive on
+  // the peer's: both CTAs' barriers are initialised before either proceeds
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
@@ -108,7 +129,7 @@ __global__ void __launch_bounds__(192, 1)
   };
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_normal();
       const uint64_t pol_a = policy_evict_last();
@@ -122,28 +143,29 @@ __global__ void __launch_bounds__(192, 1)
         if (!decode(pu, second, tm, tn, pm)) continue;
         const GemmParams& q = second ? p2 : p;
         const CUtensorMap* map = second ? &map_act2 : &map_act;
+        const CUtensorMap* wmap = second ? &map_w2 : &map_w;
         const bool row_kind = second ? (KIND2 == KIND_ROW) : (KIND == KIND_ROW);
-        const uint8_t* wsrc = q.w_packed + (size_t)tn * q.nkb * kWBlockBytes + rank * kHalfB;
+        int blk0 = tn * q.nkb;
         if (q.pair_tiles != nullptr)   // both tiles of a pair belong to the expert of its first
-          wsrc += (size_t)q.tile_expert[q.pair_tiles[2 * pm]] * (size_t)q.expert_wbytes;
+          blk0 += q.tile_expert[q.pair_tiles[2 * pm]] * (int)(q.expert_wbytes / kWBlockBytes);
         for (int kb = 0; kb < q.nkb; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, q.timeout_ns)) {
             fail(q);
             ok = false;
             break;
           }
-          const uint32_t sa = base + stage * S::kStageBytes;
-          const uint32_t sb = sa + S::kABytes;
-          const uint32_t fb = full_bar(stage);
-          // own token tile (16 KB) + both halves of the weight block (2 x 16 KB, one from each CTA)
-          mbar_arrive_expect_tx(fb, S::kStageBytes);
+          const uint32_t sa = base + stage * P::kStageBytes;
+          const uint32_t sb = sa + P::kABytes;
+          const uint32_t fb = mapa_shared(full_bar(stage), 0);
+          // the even CTA expects both CTAs' bytes: its own and the peer's token tile and weight half
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * P::kStageBytes);
           int kx = kb * 64, shard = 0;
           if (row_kind) {
             shard = kb / q.kbs;
             kx = (kb - shard * q.kbs) * 64;
           }
-          tma_load_4d(sa, map, fb, kx, tm * 128, 0, shard, pol_a);
-          bulk_load_multicast(sb + rank * kHalfB, wsrc + (size_t)kb * kWBlockBytes, kHalfB, fb, kBoth, pol_w);
+          tma_load_4d_pair(sa, map, fb, kx, tm * 128, 0, shard, pol_a);
+          tma_load_3d_pair(sb, wmap, fb, 0, rank * 128, blk0 + kb, pol_w);
           issued_mask |= 1u << stage;
           last_phase_bits = (last_phase_bits & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -153,15 +175,22 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       if (!ok) {
-        for (int s = 0; s < STAGES; ++s)
-          if (issued_mask & (1u << s))
-            mbar_wait_bounded(full_bar(s), (last_phase_bits >> s) & 1u, nullptr, kTeardownNs);
+        // let copies in flight land before the CTA exits: the even CTA sees them on its
+        // full barriers; the peer's count there too, so it waits out a fixed bound instead
+        if (leader) {
+          for (int s = 0; s < STAGES; ++s)
+            if (issued_mask & (1u << s))
+              mbar_wait_bounded(full_bar(s), (last_phase_bits >> s) & 1u, nullptr, kTeardownNs);
+        } else {
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
+        }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (leader && lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int buf = 0;
@@ -172,12 +201,12 @@ __global__ void __launch_bounds__(192, 1)
         bool second;
         if (!decode(pu, second, tm, tn, pm)) continue;
         const GemmParams& q = second ? p2 : p;
-        if (!mbar_wait_bounded(tempty_bar(buf), acc_phase ^ 1u, s_abort, q.timeout_ns)) {
+        if (!mbar_wait_bounded_cluster(tempty_bar(buf), acc_phase ^ 1u, s_abort, q.timeout_ns)) {
           fail(q);
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * S::kAccCols;
+        const uint32_t d_tmem = tmem_base + buf * P::kAccCols;
         for (int kb = 0; kb < q.nkb; ++kb) {
           if (!mbar_wait_bounded(full_bar(stage), phase, s_abort, q.timeout_ns)) {
             fail(q);
@@ -185,32 +214,36 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = base + stage * S::kStageBytes;
+          const uint32_t sa = base + stage * P::kStageBytes;
           const uint64_t adesc = smem_desc_k128(sa);
-          const uint64_t bdesc = smem_desc_k128(sa + S::kABytes);
+          const uint64_t bdesc = smem_desc_k128(sa + P::kABytes);
+          if (kb == 0)
+            tc_mma_bf16_pair<false>(d_tmem, adesc, bdesc, P::kIdesc);
+          else
+            tc_mma_bf16_pair<true>(d_tmem, adesc, bdesc, P::kIdesc);
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc_mma_bf16(d_tmem, adesc + (uint64_t)(ks * 2), bdesc + (uint64_t)(ks * 2), S::kIdesc,
-                        (kb > 0 || ks > 0) ? 1u : 0u);
-          tc_commit_multicast(empty_bar(stage), kBoth);
+          for (int ks = 1; ks < 4; ++ks)
+            tc_mma_bf16_pair<true>(d_tmem, adesc + (uint64_t)(ks * 2), bdesc + (uint64_t)(ks * 2), P::kIdesc);
+          tc_commit_pair_multicast(empty_bar(stage), kBoth);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(tfull_bar(buf));
+        tc_commit_pair_multicast(tfull_bar(buf), kBoth);
         if (++buf == 2) {
           buf = 0;
           acc_phase ^= 1u;
         }
       }
-      tc_commit(done_bar);
+      // every issued MMA completes before either CTA frees tensor memory or exits
+      tc_commit_pair(done_bar);
       mbar_wait_bounded(done_bar, 0, nullptr, kTeardownNs);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (both CTAs)
     const int qd = warp & 3;
     const int row = qd * 32 + lane;
     const int et = threadIdx.x - 64;
@@ -233,7 +266,7 @@ __global__ void __launch_bounds__(192, 1)
       named_bar_sync(1, 128);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t acc = lane_addr + buf * S::kAccCols;
+      const uint32_t acc = lane_addr + buf * P::kAccCols;
       auto direct = [&](auto kind_c, const GemmParams& q) {
         constexpr int K = decltype(kind_c)::value;
         using SK = GemmShape<false, K, BN>;
@@ -251,7 +284,7 @@ __global__ void __launch_bounds__(192, 1)
         direct(std::integral_constant<int, KIND>{}, p);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(buf));
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
       if (++buf == 2) {
         buf = 0;
         acc_phase ^= 1u;
@@ -260,19 +293,20 @@ __global__ void __launch_bounds__(192, 1)
   }
 
   __syncthreads();
+  // the even CTA's MMAs are complete and both epilogues have read their accumulators
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, S::kTmemCols);
+    tmem_dealloc_pair(tmem_base, P::kTmemCols);
   }
-  // the peer's multicast copies and MMA commits target this CTA's shared memory:
-  // neither CTA leaves before both are done
+  // neither CTA leaves while the other may still touch its shared or tensor memory
   cluster_sync();
 }
 
 template <int KIND, int KIND2>
-cudaError_t launch_pair(const CUtensorMap& a1, const GemmParams& p1, const CUtensorMap& a2, const GemmParams& p2,
-                        int max_clusters, cudaStream_t st) {
-  using S = GemmShape<false, KIND, 256>;
+cudaError_t launch_pair(const CUtensorMap& a1, const CUtensorMap& w1, const GemmParams& p1, const CUtensorMap& a2,
+                        const CUtensorMap& w2, const GemmParams& p2, int max_clusters, cudaStream_t st) {
+  using P = PairShape;
   auto kernel = tc_gemm_pair_kernel<KIND, KIND2>;
   static std::atomic<uint64_t> attr_done{0};
   int dev = 0;
@@ -280,7 +314,7 @@ cudaError_t launch_pair(const CUtensorMap& a1, const GemmParams& p1, const CUten
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(attr_done.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit, std::memory_order_acq_rel);
   }
@@ -289,7 +323,7 @@ cudaError_t launch_pair(const CUtensorMap& a1, const GemmParams& p1, const CUten
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters);
   cfg.blockDim = dim3(192);
-  cfg.dynamicSmemBytes = S::kSmemBytes;
+  cfg.dynamicSmemBytes = P::kSmemBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -298,8 +332,10 @@ cudaError_t launch_pair(const CUtensorMap& a1, const GemmParams& p1, const CUten
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, a1, a2, p1, p2);
+  return cudaLaunchKernelEx(&cfg, kernel, a1, w1, a2, w2, p1, p2);
 }
+
+int pair_stages() { return PairShape::kStages; }
 
 // Number of 2-CTA clusters of this engine that fit on the device at once (0 if none).
 int pair_max_clusters() {
@@ -308,16 +344,16 @@ int pair_max_clusters() {
   static std::atomic<int> cached[64];
   int v = cached[dev & 63].load();
   if (v != 0) return v > 0 ? v : 0;
-  using S = GemmShape<false, KIND_GATE_UP, 256>;
+  using P = PairShape;
   auto kernel = tc_gemm_pair_kernel<KIND_GATE_UP, -1>;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes) != cudaSuccess) {
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kSmemBytes) != cudaSuccess) {
     cached[dev & 63].store(-1);
     return 0;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
   cfg.blockDim = dim3(192);
-  cfg.dynamicSmemBytes = S::kSmemBytes;
+  cfg.dynamicSmemBytes = P::kSmemBytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -335,17 +371,19 @@ int pair_max_clusters() {
   return n;
 }
 
-cudaError_t launch_gemm_pair(int kind, int kind2, const CUtensorMap& a1, const GemmParams& p1,
-                             const CUtensorMap& a2, const GemmParams& p2, int max_clusters, cudaStream_t st) {
+cudaError_t launch_gemm_pair(int kind, int kind2, const CUtensorMap& a1, const CUtensorMap& w1, const GemmParams& p1,
+                             const CUtensorMap& a2, const CUtensorMap& w2, const GemmParams& p2, int max_clusters,
+                             cudaStream_t st) {
   if (kind2 < 0) {
     switch (kind) {
-      case KIND_GATE_UP: return launch_pair<KIND_GATE_UP, -1>(a1, p1, a1, p1, max_clusters, st);
-      case KIND_COL: return launch_pair<KIND_COL, -1>(a1, p1, a1, p1, max_clusters, st);
-      case KIND_ROW: return launch_pair<KIND_ROW, -1>(a1, p1, a1, p1, max_clusters, st);
+      case KIND_GATE_UP: return launch_pair<KIND_GATE_UP, -1>(a1, w1, p1, a1, w1, p1, max_clusters, st);
+      case KIND_COL: return launch_pair<KIND_COL, -1>(a1, w1, p1, a1, w1, p1, max_clusters, st);
+      case KIND_ROW: return launch_pair<KIND_ROW, -1>(a1, w1, p1, a1, w1, p1, max_clusters, st);
       default: return cudaErrorInvalidValue;
     }
   }
-  if (kind == KIND_COL && kind2 == KIND_ROW) return launch_pair<KIND_COL, KIND_ROW>(a1, p1, a2, p2, max_clusters, st);
+  if (kind == KIND_COL && kind2 == KIND_ROW)
+    return launch_pair<KIND_COL, KIND_ROW>(a1, w1, p1, a2, w2, p2, max_clusters, st);
   return cudaErrorInvalidValue;
 }
 

@@ -30,9 +30,11 @@ cudaError_t launch_gemm_decode_row(int bn, const CUtensorMap& a, const GemmParam
 int gemm_stages_prefill(int kind);
 cudaError_t launch_gemm_prefill_col_row(const CUtensorMap& a1, const GemmParams& p1, const CUtensorMap& a2,
                                         const GemmParams& p2, int grid, cudaStream_t st);
-cudaError_t launch_gemm_pair(int kind, int kind2, const CUtensorMap& a1, const GemmParams& p1,
-                             const CUtensorMap& a2, const GemmParams& p2, int max_clusters, cudaStream_t st);
+cudaError_t launch_gemm_pair(int kind, int kind2, const CUtensorMap& a1, const CUtensorMap& w1, const GemmParams& p1,
+                             const CUtensorMap& a2, const CUtensorMap& w2, const GemmParams& p2, int max_clusters,
+                             cudaStream_t st);
 int pair_max_clusters();
+int pair_stages();
 int gemm_stages_decode_gate_up(int bn);
 int gemm_stages_decode_col(int bn);
 int gemm_stages_decode_row(int bn);
@@ -159,6 +161,26 @@ int make_shard_map(CUtensorMap* m, const void* ptr, int64_t w, int64_t T, int64_
   return TP_OK;
 }
 
+// Tensor map of packed weight blocks for the CTA-pair engine: dims (64 elements,
+// 256 rows, n_blocks), each block 32 KB, boxes of 64 x 128 rows (one half of a
+// block, 16 KB). The blocks are already in the swizzled image the MMA reads, so
+// the copy itself does not swizzle.
+int make_wmap(CUtensorMap* m, const void* ptr, int64_t n_blocks) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[3] = {64u, 256u, (cuuint64_t)n_blocks};
+  const cuuint64_t strides[2] = {128u, (cuuint64_t)kWBlockBytes};
+  const cuuint32_t box[3] = {64u, 128u, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %lld packed weight blocks", (int)r,
+                (long long)n_blocks);
+  return TP_OK;
+}
+
 // ============================================================================ workspace layout
 // header: [0] status word; [64] grid barrier of the column-parallel GEMM;
 // [128] grid barrier of the row-parallel GEMM; [192] counters of the fused
@@ -204,6 +226,8 @@ struct tp_linear {
   void* w_col;
   void* w_row;
   const void* gamma;
+  // the packed blocks of w_col / w_row (all experts) as tensor maps, for the CTA-pair engine
+  CUtensorMap wmap_col, wmap_row;
 };
 
 namespace {
@@ -372,8 +396,9 @@ int check_device(const tp_linear* h) {
   return TP_OK;
 }
 
-// Prefill GEMMs may run on CTA pairs that share each weight block (multicast);
-// TPL_GEMM_PAIR=0 in the environment keeps them on single CTAs.
+// Prefill GEMMs may run on CTA pairs (two-SM MMAs over 256-token tiles, each
+// CTA loading half of every weight block); TPL_GEMM_PAIR=0 in the environment
+// keeps them on single CTAs.
 bool pair_engine_enabled() {
   static const bool on = [] {
     const char* v = std::getenv("TPL_GEMM_PAIR");
@@ -453,7 +478,7 @@ int run_col(const tp_linear* h, int64_t T, const void* x, void* out, void* ws, c
     GemmParams q = p;
     q.splits = 1;
     q.units = p1.units;
-    cudaError_t e = launch_gemm_pair(pl.kind, -1, map_x, q, map_x, q, ncl, st);
+    cudaError_t e = launch_gemm_pair(pl.kind, -1, map_x, h->wmap_col, q, map_x, h->wmap_col, q, ncl, st);
     if (e != cudaSuccess) return cuda_fail(e, "column-parallel GEMM launch (pairs)");
     return TP_OK;
   }
@@ -482,7 +507,7 @@ int run_row(const tp_linear* h, int64_t T, const void* in_shards, const void* re
     GemmParams q = p;
     q.splits = 1;
     q.units = p1.units;
-    cudaError_t e = launch_gemm_pair(pl.kind, -1, map_in, q, map_in, q, ncl, st);
+    cudaError_t e = launch_gemm_pair(pl.kind, -1, map_in, h->wmap_row, q, map_in, h->wmap_row, q, ncl, st);
     if (e != cudaSuccess) return cuda_fail(e, "row-parallel GEMM launch (pairs)");
     return TP_OK;
   }
@@ -516,7 +541,7 @@ int run_col_row_together(const tp_linear* h, int64_t T, const void* x, void* qkv
   const Plan both[2] = {pc, pr};
   cudaError_t e;
   if (prefer_pair(h, both, 2, ncl)) {
-    e = launch_gemm_pair(KIND_COL, KIND_ROW, map_x, p1, map_a, p2, ncl, st);
+    e = launch_gemm_pair(KIND_COL, KIND_ROW, map_x, h->wmap_col, p1, map_a, h->wmap_row, p2, ncl, st);
   } else {
     const int grid = (int)std::min<int64_t>((int64_t)pc.units + pr.units, h->nsm);
     e = launch_gemm_prefill_col_row(map_x, p1, map_a, p2, grid, st);
@@ -721,6 +746,11 @@ int tp_linear_create(const tp_config_t* cfg, const void* const* w_full, int32_t 
     delete h;
     return cuda_fail(e, "weight packing");
   }
+  if ((rc = make_wmap(&h->wmap_col, w_col_packed, n_exp * col_blocks)) ||
+      (rc = make_wmap(&h->wmap_row, w_row_packed, n_exp * row_blocks))) {
+    delete h;
+    return rc;
+  }
   *out = h;
   return ok();
 }
@@ -764,6 +794,26 @@ int tp_describe_plan(const tp_linear_t* h, int64_t T, tp_gemm_plan_t* plans, int
     plans[n].units = pl.units;
     plans[n].grid = pl.grid;
     plans[n].stages = gemm_stages(pl.swap, pl.kind, pl.bn);
+    plans[n].engine = 0;
+    if (h->cfg.kind == TP_BLOCK_MLP && T <= kFusedMaxT) {
+      plans[n].engine = 2;
+    } else if (!pl.swap) {
+      const int ncl = pair_max_clusters();
+      bool pair;
+      if (h->cfg.kind == TP_BLOCK_ATTN_PROJ && T > kFusedMaxT) {
+        const Plan both[2] = {make_plan(h, 0, T, 1), make_plan(h, 1, T, 1)};
+        pair = prefer_pair(h, both, 2, ncl);
+      } else {
+        pair = prefer_pair(h, &pl, 1, ncl);
+      }
+      if (pair) {
+        plans[n].engine = 1;
+        plans[n].splits = 1;
+        plans[n].units = ((pl.m_tiles + 1) / 2) * pl.n_tiles;
+        plans[n].grid = 2 * std::min(plans[n].units, ncl);
+        plans[n].stages = pair_stages();
+      }
+    }
   }
   g_err[0] = '\0';
   return n;
@@ -1207,7 +1257,8 @@ int tp_moe_forward(tp_linear_t* h, int64_t T, int32_t top_k, const void* x, cons
       p.m_tiles = (int)(2 * L.max_pairs);
       p.pair_tiles = pair_tiles;
       p.pair_count = pair_count;
-      e = launch_gemm_pair(pl.kind, -1, map_a, p, map_a, p, ncl, st);
+      const CUtensorMap& wm = which == 0 ? h->wmap_col : h->wmap_row;
+      e = launch_gemm_pair(pl.kind, -1, map_a, wm, p, map_a, wm, p, ncl, st);
     } else {
       e = launch_gemm(false, pl.kind, pl.bn, map_a, p, pl.grid, st);
     }

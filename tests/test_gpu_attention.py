@@ -15,6 +15,7 @@ import torch
 import oracle
 import workloads
 import tensor_linear_layers_gb300 as tl
+from tile_rows import tile_rows
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
@@ -74,13 +75,13 @@ def test_attention_matches_oracle(nq, nkv, t, lens):
     assert status_of(blk.workspace(T)) == 0
 
 
-def test_llama3_8b_full_size_sampled_rows():
+def test_llama3_8b_full_size_every_query_tile():
     w = workloads.WORKLOADS["llama3_8b_attn_core_prefill"]
     blk, _ = make_attn(w.H, w.nq, w.nkv, w.t)
     d = workloads.attn_core_inputs(w)
     out, cu = run(blk, d["qkv"], np.diff(d["cu_seqlens"]))
-    rng = np.random.default_rng(0)
-    rows = sorted(set([0, 1, 127, 128, 129, 255, 256, 2047, 2048, 4094, 4095]) | set(rng.integers(0, 4096, 21)))
+    # the first and last query of every 128-query tile and two between (every work unit's tile)
+    rows = [int(r) for r in tile_rows(4096, 4)]
     ref = oracle.attention_rows(d["qkv"], w.nq, w.nkv, w.hd, w.t, d["cu_seqlens"], rows)
     got = out[:, rows]
     err = rel_err_shards(got, ref)

@@ -18,6 +18,7 @@ import torch
 import oracle
 import workloads
 import tensor_linear_layers_gb300 as tl
+from tile_rows import tile_rows
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
@@ -142,7 +143,8 @@ def test_qwen_ragged_layer_full_size_with_capture():
     rb = workloads.ragged_batch(w)
     attn, mlp, layer = make_layer(w, d, w.T)
     out, cu = run(layer, d, rb["lens"])
-    rows = np.sort(np.concatenate([rb["sel_rows"][:24], [0, w.T - 1]]))
+    # two rows of every 128-token tile, plus rows the capture selects
+    rows = np.unique(np.concatenate([rb["sel_rows"][:24], tile_rows(w.T, 2)]))
     ref = ref_layer(w, d, cu, rows=rows)
     for k in KEYS:
         assert rel_err(out[k][rows], ref[k]) <= TOL, k
@@ -164,16 +166,14 @@ def test_qwen_ragged_layer_full_size_with_capture():
     assert int(cws[:4].view(torch.int32).item()) == 0
 
 
-def test_llama3_8b_layer_full_size_sampled_rows():
-    # rows of the first three query tiles: under causal attention they need only the
-    # first 384 tokens, which keeps the float64 oracle cheap; rows near the end of the
-    # 4096-token sequence are checked for the attention core alone (test_gpu_attention)
+def test_llama3_8b_layer_full_size_every_tile():
+    # the first and last row of every 128-token tile and one between: the rows at the
+    # end of the sequence make the oracle project all 4096 tokens' q, k and v
     w = workloads.WORKLOADS["llama3_8b_layer_prefill"]
     d = workloads.layer_inputs(w)
     attn, mlp, layer = make_layer(w, d, w.T)
     out, cu = run(layer, d, [w.T])
-    rows = [0, 1, 127, 128, 255, 256, 383] + list(np.random.default_rng(1).integers(0, 384, 9))
-    rows = sorted(set(int(r) for r in rows))
+    rows = [int(r) for r in tile_rows(w.T, 3, seed=1)]
     ref = ref_layer(w, d, cu, rows=rows)
     for k in KEYS:
         assert rel_err(out[k][rows], ref[k]) <= TOL, k

@@ -15,6 +15,7 @@ import torch
 import oracle
 import workloads
 import tensor_linear_layers_gb300 as tl
+from tile_rows import moe_tile_tokens
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
@@ -91,12 +92,14 @@ def test_mixtral_decode_full():
     assert status_of(blk, w.T * w.top_k) == 0
 
 
-def test_mixtral_prefill_sampled_tokens():
+def test_mixtral_prefill_every_expert_tile():
     w = workloads.WORKLOADS["mixtral_8x7b_moe_prefill"]
     d = workloads.moe_inputs(w)
     blk = make(w, d)
     y = run(blk, d)
-    rows = np.sort(np.random.default_rng(2).choice(w.T, 40, replace=False))
+    # tokens routed into every 128-row tile of every expert (both tiles of each CTA
+    # pair, each expert's last partial tile)
+    rows = moe_tile_tokens(d["expert_ids"], per_tile=2)
     ref = oracle.moe_block(d["x"][rows], d["expert_ids"][rows], d["gates"][rows], d["w_gate"], d["w_up"],
                            d["w_down"])
     assert rel_err(y[rows], ref) <= TOL

@@ -11,6 +11,7 @@ import torch
 import oracle
 import workloads
 import tensor_linear_layers_gb300 as tl
+from tile_rows import tile_rows
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
@@ -90,6 +91,41 @@ def test_mlp_with_norm_and_residual_stream(T):
     ref = mlp_ref(d, a, residual=r0, norm=True)
     for k in ("mlp_out", "residual_out", "residual_stream"):
         assert rel_err(out[k], ref[k]) <= TOL, k
+    assert status_of(blk.workspace(T)) == 0
+
+
+# ------------------------------------------------------------------ prefill tails on CTA pairs
+
+@pytest.mark.parametrize("T", [1000, 1300, 1421])
+def test_prefill_tails_on_cta_pairs_every_row(T):
+    # 8 token tiles, the last one partial (104 rows); 11 tiles, so the odd CTA of the
+    # last pair has no tile; 12 tiles, the last one 13 rows. Both GEMMs run on CTA
+    # pairs at this shape; every row of every output is compared.
+    H, I, t = 4096, 2048, 4
+    blk, d = make_mlp(H, I, t, norm=True)
+    assert [p["engine"] for p in blk.plan(T)] == [1, 1]
+    a, r0 = workloads.draw((T, H), 13, 0), workloads.draw((T, H), 13, 1)
+    out = blk.mlp_forward(a.cuda(), residual=r0.cuda())
+    ref = mlp_ref(d, a, residual=r0, norm=True)
+    for k in ("mlp_out", "residual_out", "residual_stream"):
+        assert rel_err(out[k], ref[k]) <= TOL, k
+    assert status_of(blk.workspace(T)) == 0
+
+
+@pytest.mark.parametrize("T", [1300, 1421])
+def test_attention_projections_tails_on_cta_pairs_every_row(T):
+    # QKV and o_proj in one CTA-pair launch, odd and even tile counts with partial tiles
+    H, nq, nkv, hd, t = 2048, 16, 4, 128, 2
+    w = workloads.Workload("case", "attn", T=T, H=H, nq=nq, nkv=nkv, hd=hd, t=t, w_std=0.02)
+    d = workloads.attn_inputs(w)
+    cfg = tl.make_config(tl.TP_BLOCK_ATTN_PROJ, t, H, n_q_heads=nq, n_kv_heads=nkv, head_dim=hd)
+    blk = tl.TPLinear(cfg, [d[k].cuda() for k in ("w_q", "w_k", "w_v", "w_o")])
+    assert blk.plan(T)[0]["engine"] == 1
+    qkv, o = blk.attn_proj_forward(d["x"].cuda(), d["attn"].cuda())
+    ref_qkv = oracle.qkv_parallel(f64(d["x"]), f64(d["w_q"]), f64(d["w_k"]), f64(d["w_v"]), nq, nkv, hd, t)
+    ref_o = oracle.o_proj_parallel(f64(d["attn"]), f64(d["w_o"]), t)
+    assert rel_err(qkv, ref_qkv) <= TOL
+    assert rel_err(o, ref_o) <= TOL
     assert status_of(blk.workspace(T)) == 0
 
 
@@ -213,14 +249,14 @@ def test_capture_large_selector_set_uses_global_table():
 
 # ------------------------------------------------------------------ the five workloads at full size
 
-def sample_rows(T, n=12, seed=0):
-    rng = np.random.default_rng(seed)
-    return np.unique(np.concatenate([[0, T - 1], rng.choice(T, min(n, T), replace=False)]))
+# rows compared per 128-token tile at full size: every tile (so both tiles of every
+# CTA pair) and, on the Llama-3-70B-shaped batch, 4 x 64 = 256 rows
+ROWS_PER_TILE = {"llama3_70b_mlp_prefill": 4, "qwen25_7b_ragged_mlp": 8, "llama3_8b_attn_proj_prefill": 4}
 
 
 @pytest.mark.parametrize("name", ["tiny_mlp", "llama3_8b_mlp_decode", "llama3_70b_mlp_prefill",
                                   "qwen25_7b_ragged_mlp"])
-def test_mlp_workload_full_size(name):
+def test_mlp_workload_full_size_every_tile(name):
     w = workloads.WORKLOADS[name]
     d = workloads.mlp_inputs(w)
     cfg = tl.make_config(tl.TP_BLOCK_MLP, w.t, w.H, w.I, rms_eps=w.eps,
@@ -229,7 +265,9 @@ def test_mlp_workload_full_size(name):
                       gamma=None if not w.norm else d["gamma"].cuda())
     out = blk.mlp_forward(d["x"].cuda(), residual=None if d["residual"] is None else d["residual"].cuda())
     assert status_of(blk.workspace(w.T)) == 0
-    rows = sample_rows(w.T) if w.T > 64 else None
+    rows = tile_rows(w.T, ROWS_PER_TILE[name]) if w.T > 128 else None
+    if name == "llama3_70b_mlp_prefill":
+        assert rows.size >= 256
     ref = mlp_ref(d, d["x"], residual=d["residual"], norm=w.norm, rows=rows)
     sel = slice(None) if rows is None else torch.from_numpy(rows)
     for k in ("mlp_out", "residual_out", "residual_stream"):
@@ -252,14 +290,14 @@ def test_mlp_workload_full_size(name):
         assert status_of(ws) == 0
 
 
-def test_attention_workload_full_size():
+def test_attention_workload_full_size_every_tile():
     w = workloads.WORKLOADS["llama3_8b_attn_proj_prefill"]
     d = workloads.attn_inputs(w)
     cfg = tl.make_config(tl.TP_BLOCK_ATTN_PROJ, w.t, w.H, n_q_heads=w.nq, n_kv_heads=w.nkv, head_dim=w.hd)
     blk = tl.TPLinear(cfg, [d[k].cuda() for k in ("w_q", "w_k", "w_v", "w_o")])
     qkv, o = blk.attn_proj_forward(d["x"].cuda(), d["attn"].cuda())
     assert status_of(blk.workspace(w.T)) == 0
-    rows = sample_rows(w.T)
+    rows = tile_rows(w.T, ROWS_PER_TILE[w.name])
     x = f64(d["x"])[rows]
     ref_qkv = oracle.qkv_parallel(x, f64(d["w_q"]), f64(d["w_k"]), f64(d["w_v"]), w.nq, w.nkv, w.hd, w.t)
     ref_o = oracle.o_proj_parallel(f64(d["attn"])[:, rows], f64(d["w_o"]), w.t)
