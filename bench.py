@@ -20,9 +20,11 @@ token batch (weak scaling); there is no collective on the data path.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import os
 import statistics
+import socket
 import subprocess
 import sys
 import threading
@@ -46,8 +48,11 @@ def parse():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
-    ap.add_argument("--rotate", type=int, default=4, help="weight copies rotated across steps")
+    ap.add_argument("--rotate", type=int, default=None,
+                    help="input sets rotated across steps (default: 4, or 1 when the weights are over 1 GB)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="default workload only, without the other workloads under detail.configs")
     return ap.parse_args()
 
 
@@ -264,7 +269,8 @@ class OracleSample:
             self.feat = max(8, min(w.I, feat))
             d = workloads.mlp_inputs(small, T=self.rows)
             cols = np.sort(rng.choice(w.I, self.feat, replace=False))
-            self.args = (f(d["x"]), f(d["w_gate"])[cols], f(d["w_up"])[cols], f(d["w_down"])[:, cols])
+            tc = torch.from_numpy(cols)
+            self.args = (f(d["x"]), f(d["w_gate"][tc]), f(d["w_up"][tc]), f(d["w_down"][:, tc]))
             self.kw = dict(residual=None if d["residual"] is None else f(d["residual"]),
                            gamma=None if d["gamma"] is None else f(d["gamma"]), eps=w.eps, norm=w.norm)
             self.wbytes = 3.0 * w.H * self.feat * 2
@@ -349,6 +355,7 @@ def time_reps(sample: OracleSample, n: int) -> float:
 
 
 def cpu_baseline(w: workloads.Workload, budget_s: float = 12.0):
+    """The oracle on a bounded sample of the workload, timed on this host's cores."""
     decode = work_model(w)[0]
     s = OracleSample(w, feat=2048)
     s.run()
@@ -391,6 +398,9 @@ def config_obj(w: workloads.Workload, n: int, rotate: int, decode: bool):
     elif w.kind == "layer":
         c["l2"] = (f"weights {w.weight_bytes() / 1e9:.2f} GB and the step's intermediates "
                    f"(h alone {2 * w.T * w.I / 1e9:.2f} GB) > 129 MB L2; {rotate} rotating inputs")
+    elif rotate == 1:
+        c["l2"] = (f"weights {w.weight_bytes() / 1e9:.2f} GB and activations {w.activation_bytes() / 1e9:.2f} GB "
+                   f"per step > 129 MB L2 (no rotation needed)")
     else:
         c["l2"] = f"{rotate} rotating weight copies ({rotate * w.weight_bytes() / 1e9:.2f} GB) > 129 MB L2"
     c["parallelism"] = f"replicas x{n}" if n > 1 else "single GPU (t shards on one GPU)"
@@ -420,7 +430,7 @@ def run_reference(args, ws, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
         "steps": K, "warmup": W, "ms_per_step": el / K * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_obj(w, args.gpus, args.rotate, decode),
+        "config": config_obj(w, args.gpus, rotation(w, args.rotate), decode),
         "cpu_baseline": {"value": value, "unit": unit, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
                          "sample": s.describe(K, el)},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -429,6 +439,23 @@ def run_reference(args, ws, rank):
 
 
 # ---------------------------------------------------------------------------- our arm
+# Workloads measured besides the headline one in a default run, each reported
+# under detail.configs with its own roofline, end-to-end and CPU-oracle numbers.
+OTHER_CONFIGS = ("tiny_mlp", "llama3_8b_attn_proj_prefill", "llama3_70b_mlp_prefill", "qwen25_7b_ragged_mlp")
+
+
+def rotation(w: workloads.Workload, requested) -> int:
+    """Input sets rotated across steps so that no step finds its inputs in L2: at
+    least 4, and enough sets to hold twice the 129 MB L2 (at most 64). A workload
+    whose weights alone are over 1 GB (8x the L2) needs none."""
+    if requested is not None:
+        return max(1, requested)
+    per_set = w.weight_bytes() + w.activation_bytes()
+    if w.weight_bytes() >= (1 << 30):
+        return 1
+    return int(min(64, max(4, -(-2 * 129 * 2**20 // max(per_set, 1)))))
+
+
 def run_ours(args, ws, rank, local):
     import tensor_linear_layers_gb300 as tl
     from tensor_linear_layers_gb300 import _build
@@ -436,11 +463,29 @@ def run_ours(args, ws, rank, local):
         _build.build()
     barrier(ws)
     tl.lib()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
+    torch.cuda.set_device(torch.device("cuda", local))
     w = workloads.WORKLOADS[args.workload]
+    line = measure(args, w, ws, rank, local, cpu_budget_s=12.0)
+    if args.workload == DEFAULT_WORKLOAD and not args.headline_only:
+        recs = {}
+        for name in OTHER_CONFIGS:
+            gc.collect()
+            torch.cuda.empty_cache()
+            r = measure(args, workloads.WORKLOADS[name], ws, rank, local, cpu_budget_s=6.0)
+            for k in ("metric", "n_gpus", "higher_is_better", "scaling", "vs_baseline", "dtype", "data"):
+                r.pop(k, None)
+            recs[name] = r
+        line["detail"]["configs"] = recs
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure(args, w: workloads.Workload, ws, rank, local, cpu_budget_s: float):
+    """Times one workload (whole steps, the dominant kernel, end to end) and returns its JSON record."""
+    import tensor_linear_layers_gb300 as tl
+    dev = torch.device("cuda", local)
     decode, flops, wbytes, abytes = work_model(w)
-    R = max(1, args.rotate)
+    R = rotation(w, args.rotate)
     if decode:
         K = args.steps if args.steps is not None else 10000
         W = args.warmup if args.warmup is not None else 100
@@ -470,10 +515,31 @@ def run_ours(args, ws, rank, local):
         wss = [b.workspace(w.T) for b in blocks]
         # T <= 128: the whole block is one fused kernel; larger T: norm + two GEMMs
         launches_per_step = 1 if w.T <= 128 else (1 if w.norm else 0) + 2
+        cap = None
+        if w.capture_frac > 0:
+            # the ragged batch's step ends with the capture of mlp_out and residual_stream
+            # rows for the selected (request, position) keys: match + copy, two launches
+            b = workloads.ragged_batch(w)
+            n_rec = 2 * len(b["sel_keys"])
+            cap = {"rq": torch.from_numpy(b["row_req"]).to(dev), "rp": torch.from_numpy(b["row_pos"]).to(dev),
+                   "keys": torch.from_numpy(b["sel_keys"]).to(dev), "n": n_rec,
+                   "types": [workloads.TENSOR_TYPES["mlp_out"], workloads.TENSOR_TYPES["residual_stream"]],
+                   "ws": torch.zeros(tl.capture_workspace_size(w.T, len(b["sel_keys"])), dtype=torch.uint8,
+                                     device=dev),
+                   "out": [(torch.empty(n_rec, 6, dtype=torch.int32, device=dev),
+                            torch.empty(n_rec, w.H, dtype=torch.bfloat16, device=dev),
+                            torch.zeros(1, dtype=torch.int64, device=dev)) for _ in range(R)]}
+            launches_per_step += 2
+
+        def capture(j, o):
+            tl.capture_rows(cap["rq"], cap["rp"], cap["keys"], [o["mlp_out"], o["residual_stream"]], cap["types"],
+                            0, cap["n"], ws=cap["ws"], out=cap["out"][j])
 
         def step(i):
             j = i % R
             blocks[j].mlp_forward(xs[j], residual=rs[j], out=outs[j], ws=wss[j])
+            if cap is not None:
+                capture(j, outs[j])
 
         def dominant(i):
             j = i % R
@@ -620,7 +686,7 @@ def run_ours(args, ws, rank, local):
     for i in range(W):
         step(i)
     torch.cuda.synchronize()
-    for wsb in wss:
+    for wsb in wss + ([cap["ws"]] if w.kind == "mlp" and cap is not None else []):
         st = int(wsb[:4].view(torch.int32).item())
         if st != 0:
             raise RuntimeError(f"device status {st} after warm-up")
@@ -676,10 +742,18 @@ def run_ours(args, ws, rank, local):
         hout = [torch.empty(dout[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
         eouts = [{k: dout[j][i] for i, k in enumerate(names)} for j in range(R)]
         in_pairs = lambda j: [(hin[j], din[j])]
-        out_pairs = lambda j: [(dout[j], hout[j])]
+        if cap is None:
+            out_pairs = lambda j: [(dout[j], hout[j])]
+        else:
+            # the captured records (headers and rows) come back with the block's outputs
+            hcap = [(torch.empty(cap["out"][0][0].shape, dtype=torch.int32, pin_memory=True),
+                     torch.empty(cap["out"][0][1].shape, dtype=torch.bfloat16, pin_memory=True)) for _ in range(R)]
+            out_pairs = lambda j: [(dout[j], hout[j]), (cap["out"][j][0], hcap[j][0]), (cap["out"][j][1], hcap[j][1])]
 
         def e2e_compute(j):
             blocks[j].mlp_forward(din[j][0], residual=din[j][1] if n_in == 2 else None, out=eouts[j], ws=wss[j])
+            if cap is not None:
+                capture(j, eouts[j])
     elif w.kind == "paged":
         hq = [qkvs[j].cpu().pin_memory() for j in range(R)]
         ho = [torch.empty(aos[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
@@ -770,7 +844,7 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(f0.elapsed_time(f1) / K3, ws) / 1e3
 
-    for wsb in wss:
+    for wsb in wss + ([cap["ws"]] if w.kind == "mlp" and cap is not None else []):
         st = int(wsb[:4].view(torch.int32).item())
         if st != 0:
             raise RuntimeError(f"device status {st} after the timed region")
@@ -839,13 +913,28 @@ def run_ours(args, ws, rank, local):
         },
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+        line["cpu_baseline"] = cpu_baseline(w, cpu_budget_s)
+    return line
+
+
+def free_port() -> int:
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def self_launch(args) -> int:
+    """--gpus N > 1 outside torchrun: start N local ranks of this script with
+    torch.distributed.run (rendezvous on 127.0.0.1) and return their exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+           "--master-addr", "127.0.0.1", "--master-port", str(free_port()), os.path.abspath(__file__)]
+    return subprocess.call(cmd + sys.argv[1:])
 
 
 def main():
     args = parse()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(self_launch(args))
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, ws, rank)

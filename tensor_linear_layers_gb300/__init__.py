@@ -456,13 +456,22 @@ def add_rms_norm(a: torch.Tensor, residual: Optional[torch.Tensor], gamma: torch
 
 def capture_rows(row_req: torch.Tensor, row_pos: torch.Tensor, sel_keys: torch.Tensor,
                  tensors: Sequence[torch.Tensor], tensor_types: Sequence[int], layer: int, capacity: int,
-                 ws: Optional[torch.Tensor] = None, stream=None):
-    """Returns (headers int32 [capacity, 6], rows [capacity, H], n_out int64 device scalar, ws)."""
+                 ws: Optional[torch.Tensor] = None, stream=None, out=None):
+    """Returns (headers int32 [capacity, 6], rows [capacity, H], n_out int64 device scalar, ws).
+
+    out: optional (headers, rows, n_out) tensors to write instead of new ones."""
     T, H = tensors[0].shape
     dev = tensors[0].device
-    hdr = torch.empty(max(capacity, 1), 6, dtype=torch.int32, device=dev)
-    rows = torch.empty(max(capacity, 1), H, dtype=torch.bfloat16, device=dev)
-    n_out = torch.zeros(1, dtype=torch.int64, device=dev)
+    if out is not None:
+        hdr, rows, n_out = out
+        if (hdr.dtype != torch.int32 or hdr.shape[0] < max(capacity, 1) or hdr.shape[1] != 6
+                or rows.dtype != torch.bfloat16 or rows.shape[0] < max(capacity, 1) or rows.shape[1] != H
+                or n_out.dtype != torch.int64 or n_out.numel() < 1):
+            raise ValueError("capture out tensors: int32 [capacity, 6], bf16 [capacity, H], int64 [1]")
+    else:
+        hdr = torch.empty(max(capacity, 1), 6, dtype=torch.int32, device=dev)
+        rows = torch.empty(max(capacity, 1), H, dtype=torch.bfloat16, device=dev)
+        n_out = torch.zeros(1, dtype=torch.int64, device=dev)
     need = capture_workspace_size(T, sel_keys.numel())
     ws = torch.zeros(need, dtype=torch.uint8, device=dev) if ws is None else ws
     arr = (ctypes.c_void_p * len(tensors))(*[_bf16(t, "tensor").data_ptr() for t in tensors])
