@@ -105,12 +105,17 @@ struct MlpDecodeParams {
   __nv_bfloat16* res_out;        // [T, H] (norm)
   __nv_bfloat16* x_norm;         // [T, H] workspace (norm)
   // Two sets of counters; a launch uses the set its launch count selects and clears the other.
-  unsigned* bars;                // [0] norm arrivals, [2] gate_up partials written, [3] down units taken; set 1 at +4
+  unsigned* bars;                // [0] norm arrivals, [1] CTAs that gave up waiting for the gate_up
+                                 // CTAs to start, [3] down units claimed; set 1 at +4
   unsigned* cnt1;                // per gate_up tile: splits whose partial is written
-  unsigned* hready;              // per gate_up tile: 1 once its h columns are written
-  unsigned* cnt2;                // per down tile: splits whose partial is written
+  unsigned* hready;              // per gate_up tile: items of h written (complete at the tile's item count)
+  unsigned* cnt2;                // per down tile: splits whose partial is written (low 16 bits) and the
+                                 // splits that handed their slice of the sum to the last one (bit 16 + split)
   int cset;                      // words from set 0 to set 1 of cnt1 / hready / cnt2
   unsigned long long* epoch;     // completed launches in the high 32 bits (each CTA adds its share at exit)
+  unsigned long long* ticket;    // CTAs started over all launches: a CTA's ticket mod grid is its place in
+                                 // the start order of its launch (never cleared; grid fixed per workspace)
+  int n_norm;                    // CTAs that own norm rows: the first n_norm to start
   float eps;
   int H;
   int has_norm;

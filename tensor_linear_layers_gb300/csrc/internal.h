@@ -78,9 +78,11 @@ cudaError_t launch_gemm(bool swap, int kind, int bn, const CUtensorMap& map_act,
                         int grid, cudaStream_t st);
 int gemm_stages(bool swap, int kind, int bn);
 struct MlpDecodeParams;
-// The fused decode-shaped MLP block (T <= 128): one cooperative launch.
+// The fused decode-shaped MLP block (T <= 128): one launch.
 cudaError_t launch_mlp_decode(int bn, const CUtensorMap& map_x, const CUtensorMap& map_h,
                               const MlpDecodeParams& P, int grid, cudaStream_t st);
+// CTAs of the fused kernel that fit on one SM (0 when it cannot run on this device).
+int mlp_decode_ctas_per_sm(int bn);
 
 // Paged KV cache (kv_cache.cu).
 struct PagedAttnParams {

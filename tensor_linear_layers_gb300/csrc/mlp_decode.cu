@@ -1,30 +1,45 @@
 // Fused decode-shaped MLP block: one persistent launch runs the
 // whole step for T <= 128 tokens.
 //
-//   norm     residual add + RMSNorm of the T rows by the epilogue warps (rows
-//            spread over CTAs); the CTAs that own rows arrive on bars[0]
+//   norm     residual add + RMSNorm of the T rows by the epilogue warps of
+//            the first n_norm CTAs to start; they arrive on bars[0]
 //   gate_up  column-parallel units of 256 weight rows (128 gate + 128 up of
-//            one shard) x a K range; with split-K every split writes its fp32
-//            partial. After one grid-wide wait the CTAs add the partials tile
-//            by tile (split order), in the order the down splits will read h,
-//            write silu(g) * u to h [t][T][I/t] and count finished items in
-//            hready[tile]
-//   down     row-parallel units: K runs over the t shards in turn, so the
-//            shards' partial sums meet in the accumulator. The producer loads
-//            the h columns of a k-block as soon as the gate_up tile that
-//            wrote them is complete, streaming weight blocks meanwhile. The
-//            splits of a down tile (resident together) each add their slice
-//            of the tile; mlp_out = y, residual_stream = y + residual
+//            one shard) x a K range, owned by the CTAs that start next.
+//            Without split-K the epilogue writes silu(g) * u to h [t][T][I/t]
+//            straight from the accumulator; with split-K every split writes
+//            its fp32 partial and the last split of a tile to arrive adds the
+//            tile's partials in split order. hready[tile] counts written items
+//   down     row-parallel units, claimed from a counter: K runs over the t
+//            shards in turn, so the shards' partial sums meet in the
+//            accumulator. The producer loads the h columns of a k-block as
+//            soon as the gate_up tile that wrote them is complete, streaming
+//            weight blocks meanwhile. Each split of a down tile adds its own
+//            slice of the tile's partials once all have arrived; a split that
+//            has waited too long hands its slice to the last one to arrive.
+//            mlp_out = y, residual_stream = y + residual
 //
-// Between the GEMMs, work flows through per-tile counters and flags in the
-// workspace. Every wait is bounded (status word on timeout); with one CTA per SM
-// every CTA of the grid is resident. There are two sets of counters: a launch
-// uses the one its launch count (a word every CTA adds its share to at exit)
-// selects, and clears the other for the next launch.
+// No CTA relies on the whole grid being resident. A CTA's place in the start
+// order of its launch comes from a ticket counter, and it waits only on work
+// owned by a CTA that has already started and that waits on nothing later:
+// gate_up waits for the norm rows of CTAs with earlier tickets; down units are
+// claimed only once every gate_up owner has started (a CTA that cannot claim
+// for a while gives up and exits, freeing its SM; if any CTA gave up or had
+// not started, CTAs keep claiming until no unit is left); and the splits of a
+// down tile never wait on one another without a bound. Every wait is bounded
+// (status word on timeout). There are two sets of counters: a launch uses the
+// one its launch count (a word every CTA adds its share to at exit) selects,
+// and clears the other for the next launch.
 #include "gemm_launch.cuh"
 
 namespace tpl {
 
+
+// How long a CTA waits for the gate_up CTAs to start before it gives up its
+// down work, and how long a down split waits for the other splits of its tile
+// before it hands its slice of the sum to the last one. Neither is an error.
+constexpr unsigned long long kStartPatienceNs = 50000ull;
+constexpr unsigned long long kSplitPatienceNs = 50000ull;
+constexpr int kUnitSlots = 4;   // down units handed from the producer to the MMA and epilogue roles
 
 template <int BN>
 __global__ void __launch_bounds__(192, 1)
@@ -39,8 +54,6 @@ __global__ void __launch_bounds__(192, 1)
   constexpr int CH = S::kCh;
   constexpr int kItems1 = tile_items<true, KIND_GATE_UP, BN>();  // h of a gate_up tile is complete at this count
   const unsigned grid = gridDim.x;
-  // CTAs that own norm rows (row r goes to CTA r % grid); only they arrive on bars[0]
-  const unsigned norm_ctas = (unsigned)min((int)grid, P.g1.T);
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -57,15 +70,27 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 4);
   volatile int* s_ok = reinterpret_cast<volatile int*>(misc + 8);
   float* s_red = reinterpret_cast<float*>(misc + 16);  // 4 floats: norm reduction
-  // the down unit this CTA takes at run time, and the barrier that publishes it to the roles
-  const uint32_t unit_bar = smem_u32(misc + 32);
-  volatile int* s_unit = reinterpret_cast<volatile int*>(misc + 40);
   // h tile of a gate_up unit, [token][128 columns] bf16, written out with 16-byte stores
   __nv_bfloat16* s_h = reinterpret_cast<__nv_bfloat16*>(base_ptr + STAGES * S::kStageBytes + S::kBarBytes);
+  // after the h tile: this CTA's place in the start order, the down-unit hand-off ring
+  uint8_t* xtra = base_ptr + STAGES * S::kStageBytes + S::kBarBytes + BN * 128 * 2;
+  volatile int* s_me = reinterpret_cast<volatile int*>(xtra);
+  volatile unsigned long long* s_tbase = reinterpret_cast<volatile unsigned long long*>(xtra + 8);
+  volatile int* s_unit = reinterpret_cast<volatile int*>(xtra + 16);          // kUnitSlots
+  const uint32_t ufull0 = smem_u32(xtra + 32);                                  // kUnitSlots mbarriers
+  const uint32_t uempty0 = smem_u32(xtra + 64);                                 // kUnitSlots mbarriers
+  volatile unsigned* s_word = reinterpret_cast<volatile unsigned*>(xtra + 96);  // epilogue decisions
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // the ticket first, so that its round trip overlaps the set-up below
+  if (threadIdx.x == 64) {
+    const unsigned long long tk = atomicAdd(P.ticket, 1ull);
+    const unsigned long long me = tk % grid;
+    *s_me = (int)me;
+    *s_tbase = tk - me;
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
@@ -76,7 +101,10 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(tempty_bar(b), 4);
     }
     mbar_init(done_bar, 1);
-    mbar_init(unit_bar, 1);
+    for (int i = 0; i < kUnitSlots; ++i) {
+      mbar_init(ufull0 + 8u * i, 1);
+      mbar_init(uempty0 + 8u * i, 2);   // the MMA issuer and the epilogue
+    }
     *s_abort = 0;
     fence_barrier_init();
     prefetch_tensormap(&map_x);
@@ -91,9 +119,23 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
   const unsigned long long timeout = P.g1.timeout_ns;
-  // A launch that follows on the same stream may be scheduled onto SMs this grid
-  // frees; it touches nothing but constant weights before its griddepcontrol.wait.
+  // Every CTA has taken its ticket before this point, so a launch that follows on
+  // the same stream (and may be scheduled onto SMs this grid frees) takes tickets
+  // only after all of this launch's; it touches nothing but constant weights before
+  // its griddepcontrol.wait.
   if (threadIdx.x == 0) griddep_launch_dependents();
+
+  const int me = *s_me;
+  const unsigned long long tbase = *s_tbase;
+  // roles by start order: norm rows on [0, n_norm), gate_up units on [n_norm, owners_end)
+  const int n_norm = P.n_norm;
+  const int G = P.g1.units, D = P.g2.units;
+  const int owner_span = min(G, (int)grid - n_norm);
+  const int owners_end = n_norm + owner_span;
+  const int g_first = (me >= n_norm && me < owners_end) ? me - n_norm : G;
+  auto started = [&]() -> unsigned long long {
+    return *reinterpret_cast<const volatile unsigned long long*>(P.ticket) - tbase;
+  };
 
   auto set_abort = [&]() {
     if (!*s_abort) {
@@ -101,14 +143,6 @@ __global__ void __launch_bounds__(192, 1)
       *s_abort = 1;
     }
   };
-  // gate_up units go to CTAs 0, 1, ... When there are no more down units than CTAs, each CTA
-  // takes at most one down unit from a counter once its producer has issued its gate_up
-  // work, so the CTAs that finish gate_up first (or have none) take the down units first.
-  // Otherwise down units go to CTAs grid-1, grid-2, ..., so CTAs without gate_up work start
-  // down at once.
-  const bool dyn_down = P.g2.units <= (int)grid;
-  auto first_unit = [&](int ph) -> int { return ph == 0 ? (int)blockIdx.x : (int)(grid - 1 - blockIdx.x); };
-  auto step_unit = [&](int ph, int u, int units) -> int { return (ph == 1 && dyn_down) ? units : u + (int)grid; };
   // The counters of this launch: the set selected by the number of launches completed
   // before it (read after griddepcontrol.wait). The other set is the next launch's; this
   // launch clears it, so no CTA has to find out at exit whether it is the last one.
@@ -132,7 +166,7 @@ __global__ void __launch_bounds__(192, 1)
       // before it (griddepcontrol.wait), which comes first whenever an activation
       // copy or a counter of the workspace is needed
       bool dep_waited = false;
-      const unsigned* c_bars = nullptr;     // this launch's counters, known after the dependency wait
+      unsigned* c_bars = nullptr;           // this launch's counters, known after the dependency wait
       const unsigned* c_hready = nullptr;
       auto wait_dep = [&]() {
         griddep_wait();
@@ -151,7 +185,7 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       auto dep_ready = [&](int dep) -> bool {
         if (dep < 0) {
-          if (!x_ready) x_ready = *reinterpret_cast<const volatile unsigned*>(c_bars) >= norm_ctas;
+          if (!x_ready) x_ready = *reinterpret_cast<const volatile unsigned*>(c_bars) >= (unsigned)n_norm;
           return x_ready;
         }
         return *reinterpret_cast<const volatile unsigned*>(c_hready + dep) >= (unsigned)kItems1;
@@ -180,61 +214,110 @@ __global__ void __launch_bounds__(192, 1)
           if (q_n <= keep) return true;
           const int dep = q_dep[q_head];
           const unsigned* c = dep < 0 ? c_bars : c_hready + dep;
-          if (!bar_wait(c, dep < 0 ? norm_ctas : (unsigned)kItems1, timeout, s_abort)) return false;
+          if (!bar_wait(c, dep < 0 ? (unsigned)n_norm : (unsigned)kItems1, timeout, s_abort)) return false;
           if (dep < 0) x_ready = true;
           issue_front();
         }
         return true;
       };
-      for (int ph = 0; ph < 2 && ok; ++ph) {
+      // the loads of one unit: weight blocks at once, activation halves as their data is ready
+      auto issue_unit = [&](int ph, int u) -> bool {
         const GemmParams& p = ph == 0 ? P.g1 : P.g2;
-        int u0 = first_unit(ph);
-        if (ph == 1 && dyn_down) {
-          // the counter belongs to this launch once the previous one has completed
-          if (!dep_waited) wait_dep();
-          u0 = (int)atomicAdd(const_cast<unsigned*>(c_bars) + 3, 1u);
-          *s_unit = u0;
-          mbar_arrive(unit_bar);
-        }
-        for (int u = u0; u < p.units && ok; u = step_unit(ph, u, p.units)) {
-          int tm, kb0, kb1;
-          krange(p, u, tm, kb0, kb1);
-          const uint8_t* wsrc = p.w_packed + (size_t)tm * p.nkb * kWBlockBytes;
-          for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, timeout)) {
-              set_abort();
-              ok = false;
-              break;
-            }
-            const uint32_t sa = base + stage * S::kStageBytes;
-            const uint32_t fb = full_bar(stage);
-            mbar_arrive_expect_tx(fb, S::kStageBytes);
-            bulk_load(sa, wsrc + (size_t)kb * kWBlockBytes, kWBlockBytes, fb, pol_w);
-            int kx = kb * 64, shard = 0, dep = -1;
-            if (ph == 1) {
-              shard = kb / p.kbs;
-              const int kk = kb - shard * p.kbs;
-              kx = kk * 64;
-              dep = shard * P.g1.nb + (kk * 64) / 128;   // gate_up tile that wrote these h columns
-            }
-            const int slot = (q_head + q_n) % STAGES;
-            q_stage[slot] = stage;
-            q_kx[slot] = kx;
-            q_sh[slot] = shard;
-            q_dep[slot] = dep;
-            ++q_n;
-            if (!drain(STAGES - 1)) {
-              set_abort();
-              ok = false;
-              break;
-            }
-            issued_mask |= 1u << stage;
-            last_phase_bits = (last_phase_bits & ~(1u << stage)) | (phase << stage);
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
+        int tm, kb0, kb1;
+        krange(p, u, tm, kb0, kb1);
+        const uint8_t* wsrc = p.w_packed + (size_t)tm * p.nkb * kWBlockBytes;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, timeout)) return false;
+          const uint32_t sa = base + stage * S::kStageBytes;
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, S::kStageBytes);
+          bulk_load(sa, wsrc + (size_t)kb * kWBlockBytes, kWBlockBytes, fb, pol_w);
+          int kx = kb * 64, shard = 0, dep = -1;
+          if (ph == 1) {
+            shard = kb / p.kbs;
+            const int kk = kb - shard * p.kbs;
+            kx = kk * 64;
+            dep = shard * P.g1.nb + (kk * 64) / 128;   // gate_up tile that wrote these h columns
           }
+          const int slot = (q_head + q_n) % STAGES;
+          q_stage[slot] = stage;
+          q_kx[slot] = kx;
+          q_sh[slot] = shard;
+          q_dep[slot] = dep;
+          ++q_n;
+          if (!drain(STAGES - 1)) return false;
+          issued_mask |= 1u << stage;
+          last_phase_bits = (last_phase_bits & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        return true;
+      };
+      // ---- gate_up units of this CTA
+      for (int u = g_first; u < G && ok; u += owner_span) {
+        if (!issue_unit(0, u)) {
+          set_abort();
+          ok = false;
+        }
+      }
+      // ---- down units, claimed from the launch's counter. A claimed unit waits on h
+      // tiles, so nothing is claimed before every gate_up owner has started; a CTA that
+      // has waited kStartPatienceNs for that gives up its down work (and says so) so
+      // that its SM can take a CTA that has not started. When every CTA of the launch
+      // has started and none gave up, every CTA makes one claim and together they claim
+      // all units (there are no more units than CTAs); otherwise CTAs keep claiming.
+      if (ok && !dep_waited) wait_dep();
+      bool gave_up = false, first = true;
+      int uslot = 0;
+      uint32_t uphase = 0;
+      for (;;) {
+        int u = -1;
+        if (ok && !gave_up) {
+          bool claim = true;
+          if (first) {
+            if (started() < (unsigned long long)owners_end) {
+              const uint64_t t0 = globaltimer_ns();
+              while (started() < (unsigned long long)owners_end && globaltimer_ns() - t0 < kStartPatienceNs)
+                __nanosleep(200);
+              if (started() < (unsigned long long)owners_end) {
+                // announce first, then look again: a CTA that later finds every CTA started
+                // and nobody gone sees this count if this CTA does give up
+                atomicAdd(c_bars + 1, 1u);
+                __threadfence();
+                if (started() < (unsigned long long)owners_end) gave_up = true;
+                else atomicSub(c_bars + 1, 1u);
+              }
+            }
+            claim = !gave_up;
+          } else {
+            const bool all_started = started() >= grid;
+            __threadfence();
+            const bool nobody_gone = *reinterpret_cast<const volatile unsigned*>(c_bars + 1) == 0u;
+            claim = !(all_started && nobody_gone && D <= (int)grid);
+          }
+          if (claim) {
+            u = (int)atomicAdd(c_bars + 3, 1u);
+            if (u >= D) u = -1;
+          }
+          first = false;
+        }
+        if (!mbar_wait_bounded(uempty0 + 8u * uslot, uphase ^ 1u, s_abort, timeout)) {
+          set_abort();
+          ok = false;
+          break;
+        }
+        s_unit[uslot] = u;
+        mbar_arrive(ufull0 + 8u * uslot);
+        if (++uslot == kUnitSlots) {
+          uslot = 0;
+          uphase ^= 1u;
+        }
+        if (u < 0) break;
+        if (!issue_unit(1, u)) {
+          set_abort();
+          ok = false;
         }
       }
       if (!dep_waited) wait_dep();
@@ -257,58 +340,57 @@ __global__ void __launch_bounds__(192, 1)
       int buf = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int ph = 0; ph < 2 && ok; ++ph) {
+      auto mma_unit = [&](int ph, int u) -> bool {
         const GemmParams& p = ph == 0 ? P.g1 : P.g2;
-        int u0 = first_unit(ph);
-        if (ph == 1 && dyn_down) {
-          if (!mbar_wait_bounded(unit_bar, 0, s_abort, timeout)) {
-            set_abort();
-            ok = false;
-            break;
-          }
-          u0 = *s_unit;
-        }
-        for (int u = u0; u < p.units && ok; u = step_unit(ph, u, p.units)) {
-          int tm, kb0, kb1;
-          krange(p, u, tm, kb0, kb1);
-          if (!mbar_wait_bounded(tempty_bar(buf), acc_phase ^ 1u, s_abort, timeout)) {
-            set_abort();
-            ok = false;
-            break;
-          }
+        int tm, kb0, kb1;
+        krange(p, u, tm, kb0, kb1);
+        if (!mbar_wait_bounded(tempty_bar(buf), acc_phase ^ 1u, s_abort, timeout)) return false;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * ACC;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait_bounded(full_bar(stage), phase, s_abort, timeout)) return false;
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + buf * ACC;
-          for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait_bounded(full_bar(stage), phase, s_abort, timeout)) {
-              set_abort();
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t sa = base + stage * S::kStageBytes;
-            const uint64_t adesc = smem_desc_k128(sa);
-            const uint64_t bdesc = smem_desc_k128(sa + S::kABytes);
+          const uint32_t sa = base + stage * S::kStageBytes;
+          const uint64_t adesc = smem_desc_k128(sa);
+          const uint64_t bdesc = smem_desc_k128(sa + S::kABytes);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
+          for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
-              for (int a = 0; a < 2; ++a)
-                tc_mma_bf16(d_tmem + a * BN, adesc + (uint64_t)(a * (128 * 128 >> 4) + ks * 2),
-                            bdesc + (uint64_t)(ks * 2), S::kIdesc, (kb > kb0 || ks > 0) ? 1u : 0u);
-            }
-            tc_commit(empty_bar(stage));
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
+            for (int a = 0; a < 2; ++a)
+              tc_mma_bf16(d_tmem + a * BN, adesc + (uint64_t)(a * (128 * 128 >> 4) + ks * 2),
+                          bdesc + (uint64_t)(ks * 2), S::kIdesc, (kb > kb0 || ks > 0) ? 1u : 0u);
           }
-          if (!ok) break;
-          tc_commit(tfull_bar(buf));
-          if (++buf == 2) {
-            buf = 0;
-            acc_phase ^= 1u;
+          tc_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
+        tc_commit(tfull_bar(buf));
+        if (++buf == 2) {
+          buf = 0;
+          acc_phase ^= 1u;
+        }
+        return true;
+      };
+      for (int u = g_first; u < G && ok; u += owner_span) ok = mma_unit(0, u);
+      int uslot = 0;
+      uint32_t uphase = 0;
+      while (ok) {
+        if (!mbar_wait_bounded(ufull0 + 8u * uslot, uphase, s_abort, timeout)) {
+          ok = false;
+          break;
+        }
+        const int u = s_unit[uslot];
+        mbar_arrive(uempty0 + 8u * uslot);
+        if (++uslot == kUnitSlots) {
+          uslot = 0;
+          uphase ^= 1u;
+        }
+        if (u < 0) break;
+        ok = mma_unit(1, u);
       }
+      if (!ok) set_abort();
       tc_commit(done_bar);
       mbar_wait_bounded(done_bar, 0, nullptr, kTeardownNs);
     }
@@ -332,9 +414,17 @@ __global__ void __launch_bounds__(192, 1)
       named_bar_sync(1, 128);
       return r;
     };
+    auto share = [&](unsigned mine) -> unsigned {
+      if (et == 0) *s_word = mine;
+      named_bar_sync(1, 128);
+      const unsigned r = *s_word;
+      named_bar_sync(1, 128);
+      return r;
+    };
     griddep_wait();
     const int par = launch_parity();
     unsigned* const e_bars = P.bars + 4 * par;
+    unsigned* const e_cnt1 = P.cnt1 + par * P.cset;
     unsigned* const e_hready = P.hready + par * P.cset;
     unsigned* const e_cnt2 = P.cnt2 + par * P.cset;
     {
@@ -344,16 +434,16 @@ __global__ void __launch_bounds__(192, 1)
       for (long long i = etid; i < P.cset; i += ethreads) o_cnt[i] = 0u;
       if (blockIdx.x == 0 && et < 4) o_bars[et] = 0u;
     }
-    // ---- phase 0: residual add + RMSNorm, one row per CTA in turn. The loads of
-    // a chunk (a, residual and gamma, up to 8 vectors per thread each) are issued
-    // together before anything waits on them, and the rounded residual stays in
-    // registers, so a row costs one memory round trip (H <= 8 * 8 * 128 = 8192 in
+    // ---- phase 0: residual add + RMSNorm of the rows of this CTA (the first n_norm CTAs
+    // to start). The loads of a chunk (a, residual and gamma, up to 8 vectors per thread
+    // each) are issued together before anything waits on them, and the rounded residual
+    // stays in registers, so a row costs one memory round trip (H <= 8 * 8 * 128 = 8192 in
     // one chunk; longer rows loop).
-    if (P.has_norm) {
+    if (P.has_norm && me < n_norm) {
       const int H = P.H, nvec = H >> 3;
       constexpr int NV = 8;
       const uint4* gv = reinterpret_cast<const uint4*>(P.gamma);
-      for (int r = blockIdx.x; r < P.g1.T; r += grid) {
+      for (int r = me; r < P.g1.T; r += n_norm) {
         const size_t roff = (size_t)r * H;
         const uint4* av = reinterpret_cast<const uint4*>(P.x_in + roff);
         const uint4* rv = reinterpret_cast<const uint4*>(P.res_in + roff);
@@ -430,183 +520,168 @@ __global__ void __launch_bounds__(192, 1)
       // epilogue threads are released by the one fence in bar_arrive after the barrier
       fence_proxy_async_global();
       named_bar_sync(1, 128);
-      if (et == 0 && blockIdx.x < norm_ctas) bar_arrive(e_bars + 0);
+      if (et == 0) bar_arrive(e_bars + 0);
     }
 
     float g[CH], uu[CH];
-    // ---- gate_up units, then down units
-    for (int ph = 0; ph < 2 && ok; ++ph) {
+    // epilogue of one unit (ph 0: gate_up, 1: down)
+    auto epi_unit = [&](int ph, int u) -> bool {
       const GemmParams& p = ph == 0 ? P.g1 : P.g2;
-      int u0 = first_unit(ph);
-      if (ph == 1 && dyn_down) {
-        bool w_ok = true;
-        if (et == 0) {
-          w_ok = mbar_wait_bounded(unit_bar, 0, s_abort, timeout);
-          if (!w_ok) set_abort();
-        }
-        if (!agree(w_ok)) {
-          ok = false;
-          break;
-        }
-        u0 = *s_unit;
+      int tm, kb0, kb1;
+      krange(p, u, tm, kb0, kb1);
+      const int sp = u - tm * p.splits;
+      bool w_ok = true;
+      if (et == 0) {
+        w_ok = mbar_wait_bounded(tfull_bar(buf), acc_phase, s_abort, timeout);
+        if (!w_ok) set_abort();
       }
-      for (int u = u0; u < p.units && ok; u = step_unit(ph, u, p.units)) {
-        int tm, kb0, kb1;
-        krange(p, u, tm, kb0, kb1);
-        const int sp = u - tm * p.splits;
-        bool w_ok = true;
-        if (et == 0) {
-          w_ok = mbar_wait_bounded(tfull_bar(buf), acc_phase, s_abort, timeout);
-          if (!w_ok) set_abort();
-        }
-        if (!agree(w_ok)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t acc = lane_addr + buf * ACC;
-        if (p.splits == 1) {
-          if (ph == 0) {
-            // silu(g) * u goes to shared memory as [token][column]; the tile is then
-            // written row by row with 16-byte stores (one warp store covers 512 bytes,
-            // where a column per thread would take a store per token)
+      if (!agree(w_ok)) return false;
+      tc_fence_after();
+      const uint32_t acc = lane_addr + buf * ACC;
+      if (++buf == 2) {
+        buf = 0;
+        acc_phase ^= 1u;
+      }
+      const uint32_t this_buf = (buf ^ 1);
+      if (p.splits == 1) {
+        if (ph == 0) {
+          // silu(g) * u goes to shared memory as [token][column]; the tile is then
+          // written row by row with 16-byte stores (one warp store covers 512 bytes,
+          // where a column per thread would take a store per token)
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += CH) {
-              if (CH == 32) { tmem_ld32(acc + c0, g); tmem_ld32(acc + BN + c0, uu); }
-              else { tmem_ld16(acc + c0, g); tmem_ld16(acc + BN + c0, uu); }
-              tc_wait_ld();
-#pragma unroll
-              for (int j = 0; j < CH; ++j) s_h[(c0 + j) * 128 + row] = __float2bfloat16_rn(silu_f(g[j]) * uu[j]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(buf));
-            named_bar_sync(1, 128);
-            const int r = tm / p.nb, i0 = (tm - r * p.nb) * 128;
-            __nv_bfloat16* dst = p.out + (size_t)r * p.T * p.Is + i0;
-            for (int idx = et; idx < p.T * 16; idx += 128) {
-              const int tok = idx >> 4, ch = idx & 15;
-              if (i0 + ch * 8 < p.Is)
-                *reinterpret_cast<uint4*>(dst + (size_t)tok * p.Is + ch * 8) =
-                    *reinterpret_cast<const uint4*>(s_h + tok * 128 + ch * 8);
-            }
-          } else {
-#pragma unroll 1
-            for (int seg = 0; seg < 2; ++seg) {
-#pragma unroll 1
-              for (int c0 = 0; c0 < BN; c0 += CH) {
-                if (CH == 32) tmem_ld32(acc + seg * BN + c0, g); else tmem_ld16(acc + seg * BN + c0, g);
-                tc_wait_ld();
-                emit_vals<true, KIND_ROW, BN, CH>(p, tm, 0, seg, row, c0, g, uu);
-              }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(buf));
-          }
-          if (ph == 0) {
-            // this tile's h columns are complete
-            fence_proxy_async_global();
-            __threadfence();
-            named_bar_sync(1, 128);
-            if (et == 0) atomicAdd(e_hready + tm, (unsigned)kItems1);
-          }
-        } else {
-          float* part = p.partials + ((size_t)tm * p.splits + sp) * ACC * 128;
-#pragma unroll 1
-          for (int c0 = 0; c0 < ACC; c0 += CH) {
-            if (CH == 32) tmem_ld32(acc + c0, g); else tmem_ld16(acc + c0, g);
+          for (int c0 = 0; c0 < BN; c0 += CH) {
+            if (CH == 32) { tmem_ld32(acc + c0, g); tmem_ld32(acc + BN + c0, uu); }
+            else { tmem_ld16(acc + c0, g); tmem_ld16(acc + BN + c0, uu); }
             tc_wait_ld();
 #pragma unroll
-            for (int j = 0; j < CH; ++j) __stcg(part + (size_t)(c0 + j) * 128 + row, g[j]);
+            for (int j = 0; j < CH; ++j) s_h[(c0 + j) * 128 + row] = __float2bfloat16_rn(silu_f(g[j]) * uu[j]);
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar(buf));
-          if (ph == 1) {
-            // down: the splits of a tile are resident at the same time when the
-            // tile's units fall in one wave; each waits for the tile's partials
-            // and adds its own slice. Otherwise the last split to arrive adds
-            // the whole tile.
-            __threadfence();
-            named_bar_sync(1, 128);
-            unsigned* cnt = e_cnt2 + tm;
-            constexpr int items = tile_items<true, KIND_ROW, BN>();
-            const bool together = (p.units <= (int)grid) || ((int)grid % p.splits == 0);
-            unsigned old = 0;
-            if (et == 0) old = atomicAdd(cnt, 1u);
-            int lo = 0, hi = 0;
-            if (together) {
-              bool w2 = true;
-              if (et == 0) {
-                w2 = bar_wait(cnt, (unsigned)p.splits, timeout, s_abort);
-                if (!w2) set_abort();
-              }
-              if (!agree(w2)) {
-                ok = false;
+          if (lane == 0) mbar_arrive(tempty_bar(this_buf));
+          named_bar_sync(1, 128);
+          const int r = tm / p.nb, i0 = (tm - r * p.nb) * 128;
+          __nv_bfloat16* dst = p.out + (size_t)r * p.T * p.Is + i0;
+          for (int idx = et; idx < p.T * 16; idx += 128) {
+            const int tok = idx >> 4, ch = idx & 15;
+            if (i0 + ch * 8 < p.Is)
+              *reinterpret_cast<uint4*>(dst + (size_t)tok * p.Is + ch * 8) =
+                  *reinterpret_cast<const uint4*>(s_h + tok * 128 + ch * 8);
+          }
+          // this tile's h columns are complete
+          fence_proxy_async_global();
+          __threadfence();
+          named_bar_sync(1, 128);
+          if (et == 0) atomicAdd(e_hready + tm, (unsigned)kItems1);
+        } else {
+#pragma unroll 1
+          for (int seg = 0; seg < 2; ++seg) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += CH) {
+              if (CH == 32) tmem_ld32(acc + seg * BN + c0, g); else tmem_ld16(acc + seg * BN + c0, g);
+              tc_wait_ld();
+              emit_vals<true, KIND_ROW, BN, CH>(p, tm, 0, seg, row, c0, g, uu);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(this_buf));
+        }
+        return true;
+      }
+      float* part = p.partials + ((size_t)tm * p.splits + sp) * ACC * 128;
+#pragma unroll 1
+      for (int c0 = 0; c0 < ACC; c0 += CH) {
+        if (CH == 32) tmem_ld32(acc + c0, g); else tmem_ld16(acc + c0, g);
+        tc_wait_ld();
+#pragma unroll
+        for (int j = 0; j < CH; ++j) __stcg(part + (size_t)(c0 + j) * 128 + row, g[j]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(this_buf));
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (ph == 0) {
+        // gate_up split-K: the last split of the tile to arrive adds the tile's partials
+        // (split order) and publishes its h columns; no split waits for another
+        unsigned last = 0;
+        if (et == 0) last = atomicAdd(e_cnt1 + tm, 1u) == (unsigned)(p.splits - 1) ? 1u : 0u;
+        if (share(last)) {
+          __threadfence();
+          reduce_tile_items<true, KIND_GATE_UP, BN>(p, tm, 0, kItems1, et, 128);
+          fence_proxy_async_global();
+          __threadfence();
+          named_bar_sync(1, 128);
+          if (et == 0) atomicAdd(e_hready + tm, (unsigned)kItems1);
+        }
+        return true;
+      }
+      // down split-K: the count word holds the arrivals (low 16 bits) and, in bit
+      // 16 + s, the splits that handed their slice over. Each split adds its own slice
+      // of the tile once all splits have arrived; a split that has waited
+      // kSplitPatienceNs hands its slice to the last split to arrive, which adds its
+      // own slice and every slice handed over before it arrived. Every slice is added
+      // once, in split order, whoever adds it.
+      constexpr int items = tile_items<true, KIND_ROW, BN>();
+      const unsigned S2n = (unsigned)p.splits;
+      unsigned mask = 0;
+      if (et == 0) {
+        unsigned* cnt = e_cnt2 + tm;
+        const unsigned old = atomicAdd(cnt, 1u);
+        if ((old & 0xFFFFu) == S2n - 1u) {
+          mask = (1u << sp) | (old >> 16);
+        } else {
+          const volatile unsigned* vc = cnt;
+          bool all = (*vc & 0xFFFFu) >= S2n;
+          const uint64_t t0 = globaltimer_ns();
+          while (!all && globaltimer_ns() - t0 < kSplitPatienceNs) {
+            __nanosleep(64);
+            all = (*vc & 0xFFFFu) >= S2n;
+          }
+          if (!all) {
+            unsigned w = *vc;
+            for (;;) {
+              if ((w & 0xFFFFu) >= S2n) {
+                all = true;
                 break;
               }
-              lo = (int)((long long)sp * items / p.splits);
-              hi = (int)((long long)(sp + 1) * items / p.splits);
-            } else if (agree(old == (unsigned)(p.splits - 1))) {
-              __threadfence();
-              hi = items;
+              const unsigned prev = atomicCAS(cnt, w, w | (1u << (16 + sp)));
+              if (prev == w) break;      // handed over
+              w = prev;
             }
-            if (hi > lo) reduce_tile_items<true, KIND_ROW, BN>(p, tm, lo, hi, et, 128);
           }
+          if (all) mask = 1u << sp;
         }
-        if (++buf == 2) {
-          buf = 0;
-          acc_phase ^= 1u;
-        }
+        if (mask) __threadfence();
       }
-      if (ph == 0 && ok && P.g1.splits > 1) {
-        // every CTA's gate_up partials are written: wait for all CTAs, then add
-        // them up tile by tile, in the order the down splits will read h
-        // (round-robin over the down splits, nearest k-block first), counting
-        // finished items per tile so that down can start on a tile at once
-        __threadfence();
-        named_bar_sync(1, 128);
-        bool w1 = true;
-        if (et == 0) {
-          bar_arrive(e_bars + 2);
-          w1 = bar_wait(e_bars + 2, grid, timeout, s_abort);
-          if (!w1) set_abort();
-        }
-        if (!agree(w1)) {
-          ok = false;
-          break;
-        }
-        const GemmParams& q1 = P.g1;
-        const GemmParams& q2 = P.g2;
-        const int n1 = q1.m_tiles;
-        auto dep_of = [&](int kb) {
-          const int sh = kb / q2.kbs, kk = kb - sh * q2.kbs;
-          return sh * q1.nb + (kk * 64) / 128;
-        };
-        auto t0 = [&](int s) { return dep_of((int)((long long)s * q2.nkb / q2.splits)); };
-        const int S2 = q2.splits;
-        const int R = n1 / S2 + 2;
-        constexpr int NCG = kItems1 / 128;
-        const long long total = (long long)S2 * R * NCG * 128;
-        for (long long it = (long long)blockIdx.x * 128 + et; it < total; it += (long long)grid * 128) {
-          const int row = (int)(it & 127);
-          const long long rest = it >> 7;
-          const int cg = (int)(rest % NCG);
-          const int n = (int)(rest / NCG);
-          const int r = n / S2, s = n - r * S2;
-          const int x = t0(s) + r;
-          const bool valid = x < n1 && (s == S2 - 1 || x < t0(s + 1));  // same for the whole warp
-          if (!valid) continue;
-          reduce_tile_items<true, KIND_GATE_UP, BN>(q1, x, cg * 128 + row, cg * 128 + row + 1, 0, 1);
-          fence_proxy_async_global();
-          __syncwarp();
-          if (lane == 0) {
-            __threadfence();
-            atomicAdd(e_hready + x, 32u);
-          }
-        }
+      mask = share(mask);
+      for (int s = 0; s < (int)S2n; ++s)
+        if (mask & (1u << s))
+          reduce_tile_items<true, KIND_ROW, BN>(p, tm, (int)((long long)s * items / S2n),
+                                                (int)((long long)(s + 1) * items / S2n), et, 128);
+      return true;
+    };
+    // ---- gate_up units of this CTA, then the down units the producer hands over
+    for (int u = g_first; u < G && ok; u += owner_span) ok = epi_unit(0, u);
+    int uslot = 0;
+    uint32_t uphase = 0;
+    while (ok) {
+      bool w_ok = true;
+      if (et == 0) {
+        w_ok = mbar_wait_bounded(ufull0 + 8u * uslot, uphase, s_abort, timeout);
+        if (!w_ok) set_abort();
       }
+      if (!agree(w_ok)) break;
+      const int u = s_unit[uslot];
+      named_bar_sync(1, 128);
+      if (et == 0) mbar_arrive(uempty0 + 8u * uslot);
+      if (++uslot == kUnitSlots) {
+        uslot = 0;
+        uphase ^= 1u;
+      }
+      if (u < 0) break;
+      ok = epi_unit(1, u);
     }
   }
 
@@ -628,7 +703,7 @@ cudaError_t launch_mlp_decode_bn(const CUtensorMap& mx, const CUtensorMap& mh, c
                                  int grid, cudaStream_t st) {
   using S = GemmShape<true, KIND_GATE_UP, BN>;
   auto kernel = mlp_decode_kernel<BN>;
-  constexpr int kSmem = S::kSmemBytes + BN * 128 * 2;  // ring, barriers, h tile
+  constexpr int kSmem = S::kSmemBytes + BN * 128 * 2 + 128;  // ring, barriers, h tile, tickets and unit slots
   static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
   static std::atomic<uint64_t> attr_done{0};
   int dev = 0;
@@ -645,13 +720,10 @@ cudaError_t launch_mlp_decode_bn(const CUtensorMap& mx, const CUtensorMap& mh, c
   cfg.blockDim = dim3(192);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = st;
-  // One CTA per SM (shared memory) and grid == SM count: every CTA is resident
-  // while nothing else occupies the GPU. Programmatic serialisation lets the next
-  // launch on the stream be scheduled onto SMs this grid frees; it can only be
-  // scheduled once every CTA of this grid has started (griddepcontrol.launch_dependents
-  // is executed by all of them), so each grid still becomes fully resident. Waits
-  // between CTAs are bounded: a grid that could not become resident ends with
-  // TP_ERR_TIMEOUT in the status word instead of hanging.
+  // One CTA per SM (shared memory), grid == SM count. The kernel does not need its
+  // CTAs to be resident together (their roles follow the order in which they start),
+  // so other work may hold SMs meanwhile. Programmatic serialisation lets the next
+  // launch on the stream be scheduled onto SMs this grid frees.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -659,6 +731,34 @@ cudaError_t launch_mlp_decode_bn(const CUtensorMap& mx, const CUtensorMap& mh, c
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, kernel, mx, mh, P);
   return e;
+}
+
+// CTAs of the fused kernel for block_n = BN that fit on one SM (0: it cannot run here).
+template <int BN>
+int mlp_decode_ctas_per_sm_bn() {
+  using S = GemmShape<true, KIND_GATE_UP, BN>;
+  auto kernel = mlp_decode_kernel<BN>;
+  constexpr int kSmem = S::kSmemBytes + BN * 128 * 2 + 128;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 192, kSmem) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+int mlp_decode_ctas_per_sm(int bn) {
+  switch (bn) {
+    case 16: return mlp_decode_ctas_per_sm_bn<16>();
+    case 32: return mlp_decode_ctas_per_sm_bn<32>();
+    case 64: return mlp_decode_ctas_per_sm_bn<64>();
+    case 128: return mlp_decode_ctas_per_sm_bn<128>();
+    default: return 0;
+  }
 }
 
 cudaError_t launch_mlp_decode(int bn, const CUtensorMap& mx, const CUtensorMap& mh, const MlpDecodeParams& P,

@@ -184,9 +184,10 @@ int make_wmap(CUtensorMap* m, const void* ptr, int64_t n_blocks) {
 // ============================================================================ workspace layout
 // header: [0] status word; [64] grid barrier of the column-parallel GEMM;
 // [128] grid barrier of the row-parallel GEMM; [192] counters of the fused
-// decode block (two sets of four words), [224] its launch count (64 bits). Then
-// the fused block's two sets of per-tile counters and flags (fixed size per
-// handle), then the buffers whose size depends on T.
+// decode block (two sets of four words), [224] its launch count (64 bits),
+// [232] its ticket counter (CTAs started, 64 bits). Then the fused block's two
+// sets of per-tile counters and flags (fixed size per handle), then the
+// buffers whose size depends on T.
 constexpr int64_t kGbarColOff = 64;
 constexpr int64_t kGbarRowOff = 128;
 constexpr int64_t kDecodeBarsOff = 192;
@@ -308,7 +309,8 @@ struct Layout {
 // unless there are too few tiles for that.
 int fused_gate_up_splits(const tp_linear* h) {
   const int tiles = h->wt_col;
-  return tiles * 2 >= h->nsm ? 1 : std::max(1, h->nsm / tiles);
+  // with split-K, leave at least 8 CTAs for the norm rows
+  return tiles * 2 >= h->nsm ? 1 : std::max(1, (h->nsm - 8) / tiles);
 }
 
 // Split count of the down GEMM inside the fused decode block: the stand-alone plan's, capped
@@ -880,6 +882,60 @@ int tp_down_forward(tp_linear_t* h, int64_t T, const void* h_in, const void* res
   return ok();
 }
 
+// The fused decode-shaped block (T <= 128) over the workspace `ws` laid out as L:
+// norm, gate_up, h, down and both reductions in one launch. status: where device
+// errors go (null: the workspace's status word).
+int run_fused_decode(const tp_linear* h, int64_t T, char* ws, const Layout& L, const void* x_in,
+                     const void* residual_in, void* residual_out, void* mlp_out, void* residual_stream,
+                     int32_t* status, cudaStream_t st) {
+  const bool norm = (h->cfg.flags & TP_FLAG_HAS_NORM) != 0;
+  const Plan p1 = make_plan(h, 0, T, fused_gate_up_splits(h)), p2 = make_plan(h, 1, T, fused_down_splits(h, T));
+  if (mlp_decode_ctas_per_sm(p1.bn) < 1)
+    return fail(TP_ERR_UNSUPPORTED, "the fused decode block (block_n %d) does not fit on an SM of this device",
+                p1.bn);
+  void* hbuf = ws + L.h;
+  const void* xsrc = norm ? static_cast<const void*>(ws + L.x_norm) : x_in;
+  CUtensorMap map_x, map_h;
+  int rc;
+  if ((rc = make_map(&map_x, xsrc, h->H, T, 1, 1, p1.bn))) return rc;
+  if ((rc = make_map(&map_h, hbuf, h->Ks, T, 1, h->cfg.t, p2.bn))) return rc;
+  MlpDecodeParams P{};
+  P.g1 = base_params(p1, T, ws, L.part_col, kGbarColOff);
+  P.g1.out = static_cast<__nv_bfloat16*>(hbuf);
+  P.g1.Is = (int)h->Is;
+  set_col_out(P.g1, h, T, h->Is, false);   // h stays inside the launch: shard-major
+  P.g1.w_packed = static_cast<const uint8_t*>(h->w_col);
+  P.g2 = base_params(p2, T, ws, L.part_row, kGbarRowOff);
+  P.g2.n_out = (int)h->H;
+  P.g2.ws_out = (int)h->H;
+  P.g2.out = static_cast<__nv_bfloat16*>(mlp_out);
+  P.g2.out2 = static_cast<__nv_bfloat16*>(residual_stream);
+  P.g2.resid = static_cast<const __nv_bfloat16*>(norm ? residual_out : residual_in);
+  P.g2.w_packed = static_cast<const uint8_t*>(h->w_row);
+  if (status != nullptr) P.g1.status = P.g2.status = status;
+  P.x_in = static_cast<const __nv_bfloat16*>(x_in);
+  P.res_in = static_cast<const __nv_bfloat16*>(residual_in);
+  P.gamma = static_cast<const __nv_bfloat16*>(h->gamma);
+  P.res_out = static_cast<__nv_bfloat16*>(residual_out);
+  P.x_norm = reinterpret_cast<__nv_bfloat16*>(ws + L.x_norm);
+  P.bars = reinterpret_cast<unsigned*>(ws + kDecodeBarsOff);
+  P.cnt1 = reinterpret_cast<unsigned*>(ws + kTileCountersOff);
+  P.hready = P.cnt1 + h->wt_col;
+  P.cnt2 = P.hready + h->wt_col;
+  P.cset = (int)tile_counter_words(h);
+  P.epoch = reinterpret_cast<unsigned long long*>(ws + kDecodeBarsOff + 32);
+  P.ticket = reinterpret_cast<unsigned long long*>(ws + kDecodeBarsOff + 40);
+  // the first CTAs to start own the norm rows; the gate_up units go to the CTAs after them
+  const int grid = h->nsm;
+  P.n_norm = norm ? (int)std::max<int64_t>(1, std::min<int64_t>(T, grid - p1.units)) : 0;
+  P.eps = h->cfg.rms_eps;
+  P.H = (int)h->H;
+  P.has_norm = norm ? 1 : 0;
+  const cudaError_t e = launch_mlp_decode(p1.bn, map_x, map_h, P, grid, st);
+  if (e != cudaSuccess) return cuda_fail(e, "fused decode MLP launch");
+  return TP_OK;
+}
+
 int tp_mlp_forward(tp_linear_t* h, int64_t T, const void* x_in, const void* residual_in,
                    void* residual_out, void* mlp_out, void* residual_stream, void* workspace,
                    int64_t workspace_bytes, tp_stream_t stream) {
@@ -915,40 +971,9 @@ int tp_mlp_forward(tp_linear_t* h, int64_t T, const void* x_in, const void* resi
   void* hbuf = ws + L.h;
   if (T <= kFusedMaxT) {
     // decode-shaped step: norm, gate_up, h, down and both reductions in one launch
-    const Plan p1 = make_plan(h, 0, T, fused_gate_up_splits(h)), p2 = make_plan(h, 1, T, fused_down_splits(h, T));
-    const void* xsrc = norm ? static_cast<const void*>(ws + L.x_norm) : x_in;
-    CUtensorMap map_x, map_h;
-    if ((rc = make_map(&map_x, xsrc, h->H, T, 1, 1, p1.bn))) return rc;
-    if ((rc = make_map(&map_h, hbuf, h->Ks, T, 1, h->cfg.t, p2.bn))) return rc;
-    MlpDecodeParams P{};
-    P.g1 = base_params(p1, T, workspace, L.part_col, kGbarColOff);
-    P.g1.out = static_cast<__nv_bfloat16*>(hbuf);
-    P.g1.Is = (int)h->Is;
-    set_col_out(P.g1, h, T, h->Is, false);   // h stays inside the launch: shard-major
-    P.g1.w_packed = static_cast<const uint8_t*>(h->w_col);
-    P.g2 = base_params(p2, T, workspace, L.part_row, kGbarRowOff);
-    P.g2.n_out = (int)h->H;
-    P.g2.ws_out = (int)h->H;
-    P.g2.out = static_cast<__nv_bfloat16*>(mlp_out);
-    P.g2.out2 = static_cast<__nv_bfloat16*>(residual_stream);
-    P.g2.resid = static_cast<const __nv_bfloat16*>(norm ? residual_out : residual_in);
-    P.g2.w_packed = static_cast<const uint8_t*>(h->w_row);
-    P.x_in = static_cast<const __nv_bfloat16*>(x_in);
-    P.res_in = static_cast<const __nv_bfloat16*>(residual_in);
-    P.gamma = static_cast<const __nv_bfloat16*>(h->gamma);
-    P.res_out = static_cast<__nv_bfloat16*>(residual_out);
-    P.x_norm = reinterpret_cast<__nv_bfloat16*>(ws + L.x_norm);
-    P.bars = reinterpret_cast<unsigned*>(ws + kDecodeBarsOff);
-    P.cnt1 = reinterpret_cast<unsigned*>(ws + kTileCountersOff);
-    P.hready = P.cnt1 + h->wt_col;
-    P.cnt2 = P.hready + h->wt_col;
-    P.cset = (int)tile_counter_words(h);
-    P.epoch = reinterpret_cast<unsigned long long*>(ws + kDecodeBarsOff + 32);
-    P.eps = h->cfg.rms_eps;
-    P.H = (int)h->H;
-    P.has_norm = norm ? 1 : 0;
-    cudaError_t e = launch_mlp_decode(p1.bn, map_x, map_h, P, h->nsm, st);
-    if (e != cudaSuccess) return cuda_fail(e, "fused decode MLP launch");
+    if ((rc = run_fused_decode(h, T, ws, L, x_in, residual_in, residual_out, mlp_out, residual_stream, nullptr,
+                               st)))
+      return rc;
     return ok();
   }
   if (norm) {
@@ -1362,42 +1387,9 @@ extern "C" int tp_mlp_forward_no_alloc(tp_linear_t* h, int64_t T, const void* x_
   // left them set, so clear them on every call (a memset, not an allocation)
   cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)dyn_off(h), st);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the no-alloc scratch counters");
-  void* hbuf = ws + L.h;
-  const Plan p1 = make_plan(h, 0, T, fused_gate_up_splits(h)), p2 = make_plan(h, 1, T, fused_down_splits(h, T));
-  const void* xsrc = norm ? static_cast<const void*>(ws + L.x_norm) : x_in;
-  CUtensorMap map_x, map_h;
-  if ((rc = make_map(&map_x, xsrc, h->H, T, 1, 1, p1.bn))) return rc;
-  if ((rc = make_map(&map_h, hbuf, h->Ks, T, 1, h->cfg.t, p2.bn))) return rc;
-  MlpDecodeParams P{};
-  P.g1 = base_params(p1, T, scratch, L.part_col, kGbarColOff);
-  P.g1.out = static_cast<__nv_bfloat16*>(hbuf);
-  P.g1.Is = (int)h->Is;
-  set_col_out(P.g1, h, T, h->Is, false);
-  P.g1.w_packed = static_cast<const uint8_t*>(h->w_col);
-  P.g2 = base_params(p2, T, scratch, L.part_row, kGbarRowOff);
-  P.g2.n_out = (int)h->H;
-  P.g2.ws_out = (int)h->H;
-  P.g2.out = static_cast<__nv_bfloat16*>(mlp_out);
-  P.g2.out2 = static_cast<__nv_bfloat16*>(residual_stream);
-  P.g2.resid = static_cast<const __nv_bfloat16*>(norm ? residual_out : residual_in);
-  P.g2.w_packed = static_cast<const uint8_t*>(h->w_row);
-  if (status_dev != nullptr) P.g1.status = P.g2.status = status_dev;
-  P.x_in = static_cast<const __nv_bfloat16*>(x_in);
-  P.res_in = static_cast<const __nv_bfloat16*>(residual_in);
-  P.gamma = static_cast<const __nv_bfloat16*>(h->gamma);
-  P.res_out = static_cast<__nv_bfloat16*>(residual_out);
-  P.x_norm = reinterpret_cast<__nv_bfloat16*>(ws + L.x_norm);
-  P.bars = reinterpret_cast<unsigned*>(ws + kDecodeBarsOff);
-  P.cnt1 = reinterpret_cast<unsigned*>(ws + kTileCountersOff);
-  P.hready = P.cnt1 + h->wt_col;
-  P.cnt2 = P.hready + h->wt_col;
-  P.cset = (int)tile_counter_words(h);
-  P.epoch = reinterpret_cast<unsigned long long*>(ws + kDecodeBarsOff + 32);
-  P.eps = h->cfg.rms_eps;
-  P.H = (int)h->H;
-  P.has_norm = norm ? 1 : 0;
-  e = launch_mlp_decode(p1.bn, map_x, map_h, P, h->nsm, st);
-  if (e != cudaSuccess) return cuda_fail(e, "fused decode MLP launch (no-alloc)");
+  if ((rc = run_fused_decode(h, T, ws, L, x_in, residual_in, residual_out, mlp_out, residual_stream, status_dev,
+                             st)))
+    return rc;
   return ok();
 }
 
