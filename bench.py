@@ -115,7 +115,12 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
-            time.sleep(0.15)
+            # nvidia-smi's start-up queries the driver heavily: let it deliver its first
+            # sample before the timed region begins
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 5.0:
+                time.sleep(0.01)
+            time.sleep(0.02)
         except (OSError, FileNotFoundError):
             self.proc = None
 
@@ -126,6 +131,10 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        # a short timed region may fall between two samples: take the next one too
+        n0, t0 = len(self.lines), time.time()
+        while len(self.lines) == n0 and time.time() - t0 < 0.5:
+            time.sleep(0.005)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -177,6 +186,16 @@ def max_over_ranks(v: float, ws: int) -> float:
     t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def hold_stream(stream, n_steps: int):
+    """Keep `stream` busy (a bounded spin kernel, about 25 us per step to enqueue, at
+    most 50 ms) while the host enqueues the timed steps, so that the device-timed
+    region measures the steps back to back and not the host's enqueue lag. Nothing
+    of the step runs in it; the end-to-end figure is timed without it."""
+    cycles = int(min(50e-3, 1e-3 + 25e-6 * n_steps) * 2.0e9)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(cycles)
 
 
 # ---------------------------------------------------------------------------- work model
@@ -697,6 +716,7 @@ def measure(args, w: workloads.Workload, ws, rank, local, cpu_budget_s: float):
     barrier(ws)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hold_stream(stream, K)
     e0.record(stream)
     for i in range(K):
         step(i)
@@ -719,6 +739,7 @@ def measure(args, w: workloads.Workload, ws, rank, local, cpu_budget_s: float):
             dominant(i)
         torch.cuda.synchronize()
         d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_stream(stream, K2)
         d0.record(stream)
         for i in range(K2):
             dominant(i)

@@ -30,6 +30,7 @@
 // one its launch count (a word every CTA adds its share to at exit) selects,
 // and clears the other for the next launch.
 #include "gemm_launch.cuh"
+#include <atomic>
 
 namespace tpl {
 
@@ -752,13 +753,23 @@ int mlp_decode_ctas_per_sm_bn() {
 }
 
 int mlp_decode_ctas_per_sm(int bn) {
+  // asked once per device and block_n (the answer cannot change)
+  static std::atomic<int> cached[64][4];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const int slot = bn == 16 ? 0 : bn == 32 ? 1 : bn == 64 ? 2 : bn == 128 ? 3 : -1;
+  if (slot < 0) return 0;
+  const int v = cached[dev & 63][slot].load(std::memory_order_relaxed);
+  if (v != 0) return v > 0 ? v : 0;
+  int n = 0;
   switch (bn) {
-    case 16: return mlp_decode_ctas_per_sm_bn<16>();
-    case 32: return mlp_decode_ctas_per_sm_bn<32>();
-    case 64: return mlp_decode_ctas_per_sm_bn<64>();
-    case 128: return mlp_decode_ctas_per_sm_bn<128>();
-    default: return 0;
+    case 16: n = mlp_decode_ctas_per_sm_bn<16>(); break;
+    case 32: n = mlp_decode_ctas_per_sm_bn<32>(); break;
+    case 64: n = mlp_decode_ctas_per_sm_bn<64>(); break;
+    default: n = mlp_decode_ctas_per_sm_bn<128>(); break;
   }
+  cached[dev & 63][slot].store(n > 0 ? n : -1, std::memory_order_relaxed);
+  return n;
 }
 
 cudaError_t launch_mlp_decode(int bn, const CUtensorMap& mx, const CUtensorMap& mh, const MlpDecodeParams& P,
