@@ -154,12 +154,18 @@ int tp_mlp_forward(tp_linear_t* h, int64_t T, const void* x_in, const void* resi
  *     larger returns TP_ERR_UNSUPPORTED with the size in tp_last_error().
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     The address is kept for the life of the process: it does not survive a
+ *     device or context reset (cudaDeviceReset), after which this entry point
+ *     must not be called.
  *   - Every call shares the one array, which keeps the last call's contents:
  *     calls that may overlap on the GPU (two streams, two handles) race and
- *     must be serialised by the caller. Each call clears the counters it needs
- *     (a memset on `stream`, not an allocation).
+ *     must be serialised by the caller. When the previous call on the device
+ *     came from another handle (or this is the first), the call clears the
+ *     counters first (a memset on `stream`, not an allocation); calls of one
+ *     handle in a row need no clearing.
  *   - status_dev: optional device int32 the caller owns and zeroes; kernels
- *     write a TP_ERR_* code there on a device-side failure. NULL: not reported.
+ *     write a TP_ERR_* code there on a device-side failure. NULL: errors go to a
+ *     word of the shared array and are not reported to the caller.
  * Calls no cudaMalloc, cudaFree or other allocating routine.
  */
 int tp_mlp_forward_no_alloc(tp_linear_t* h, int64_t T, const void* x_in, const void* residual_in,

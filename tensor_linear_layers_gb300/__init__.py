@@ -248,6 +248,9 @@ class TPLinear:
             o["residual_out"] = torch.empty_like(x)
         if residual_stream and residual is not None and "residual_stream" not in o:
             o["residual_stream"] = torch.empty_like(x)
+        if status is not None and (status.dtype != torch.int32 or not status.is_cuda or status.numel() < 1
+                                   or status.device != self.w_col.device):
+            raise ValueError("status must be an int32 CUDA tensor of at least one element on the block's device")
         _check(lib().tp_mlp_forward_no_alloc(self.handle, T, _ptr(_bf16(x, "x")), _ptr(residual),
                                              _ptr(o.get("residual_out")), _ptr(o["mlp_out"]),
                                              _ptr(o.get("residual_stream")), _ptr(status), _stream(stream)))

@@ -229,6 +229,7 @@ struct tp_linear {
   const void* gamma;
   // the packed blocks of w_col / w_row (all experts) as tensor maps, for the CTA-pair engine
   CUtensorMap wmap_col, wmap_row;
+  uint64_t uid;    // unique per handle created in this process (never reused)
 };
 
 namespace {
@@ -692,6 +693,8 @@ int tp_linear_create(const tp_config_t* cfg, const void* const* w_full, int32_t 
   if (h == nullptr) return fail(TP_ERR_ARG, "out of host memory");
   h->cfg = *cfg;
   derive(h);
+  static std::atomic<uint64_t> next_uid{1};
+  h->uid = next_uid.fetch_add(1);
   h->w_col = w_col_packed;
   h->w_row = w_row_packed;
   h->gamma = (cfg->flags & TP_FLAG_HAS_NORM) ? gamma : nullptr;
@@ -1314,6 +1317,8 @@ static __device__ __align__(256) unsigned char g_no_alloc_scratch[kNoAllocScratc
 constexpr int kMaxDevices = 64;
 std::mutex g_no_alloc_mu;
 void* g_no_alloc_ptr[kMaxDevices] = {};
+// handle (uid) whose counters the array holds on each device; 0: none yet
+uint64_t g_no_alloc_owner[kMaxDevices] = {};
 
 // Scratch the fused decode kernel itself uses: the counters, x_norm, h and the
 // split-K partials of its own two plans.
@@ -1334,7 +1339,9 @@ Layout no_alloc_layout(const tp_linear* h, int64_t T) {
   return L;
 }
 
-int no_alloc_scratch(int device, void** out) {
+// The array's device address on `device` (looked up on the first call there) and
+// whether its counters must be cleared because another handle (or none) used it last.
+int no_alloc_scratch(int device, uint64_t uid, void** out, bool* clear) {
   if (device < 0 || device >= kMaxDevices) return fail(TP_ERR_UNSUPPORTED, "device ordinal %d", device);
   std::lock_guard<std::mutex> lock(g_no_alloc_mu);
   if (g_no_alloc_ptr[device] == nullptr) {
@@ -1344,6 +1351,8 @@ int no_alloc_scratch(int device, void** out) {
     g_no_alloc_ptr[device] = ptr;
   }
   *out = g_no_alloc_ptr[device];
+  *clear = g_no_alloc_owner[device] != uid;
+  g_no_alloc_owner[device] = uid;
   return TP_OK;
 }
 }  // namespace
@@ -1380,13 +1389,18 @@ extern "C" int tp_mlp_forward_no_alloc(tp_linear_t* h, int64_t T, const void* x_
                 "tp_mlp_forward_no_alloc: this shape needs %lld bytes of scratch, the fixed scratch holds %lld",
                 (long long)L.total, (long long)kNoAllocScratchBytes);
   void* scratch = nullptr;
-  if ((rc = no_alloc_scratch(h->device, &scratch))) return rc;
+  bool clear = true;
+  if ((rc = no_alloc_scratch(h->device, h->uid, &scratch, &clear))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(scratch);
-  // the phase counters and flags must start at zero; a call that gave up may have
-  // left them set, so clear them on every call (a memset, not an allocation)
-  cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)dyn_off(h), st);
-  if (e != cudaSuccess) return cuda_fail(e, "clearing the no-alloc scratch counters");
+  // The counters start at zero for a handle that did not make the last call here (their
+  // layout is the handle's): a memset, not an allocation. Between calls of one handle
+  // the kernel keeps them consistent itself (each launch clears the set the next one
+  // uses, even a launch that gave up), so those calls keep overlapping one another.
+  if (clear) {
+    const cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)dyn_off(h), st);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the no-alloc scratch counters");
+  }
   if ((rc = run_fused_decode(h, T, ws, L, x_in, residual_in, residual_out, mlp_out, residual_stream, status_dev,
                              st)))
     return rc;
