@@ -106,7 +106,8 @@ struct MlpDecodeParams {
   __nv_bfloat16* x_norm;         // [T, H] workspace (norm)
   // Two sets of counters; a launch uses the set its launch count selects and clears the other.
   unsigned* bars;                // [0] norm arrivals, [1] CTAs that gave up waiting for the gate_up
-                                 // CTAs to start, [3] down units claimed; set 1 at +4
+                                 // CTAs to start, [2] gate_up tiles finished, [3] down units claimed;
+                                 // set 1 at +4
   unsigned* cnt1;                // per gate_up tile: splits whose partial is written
   unsigned* hready;              // per gate_up tile: items of h written (complete at the tile's item count)
   unsigned* cnt2;                // per down tile: splits whose partial is written (low 16 bits) and the

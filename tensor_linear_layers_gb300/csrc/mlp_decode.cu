@@ -184,12 +184,42 @@ __global__ void __launch_bounds__(192, 1)
       int q_head = 0, q_n = 0;
       bool x_ready = !P.has_norm;
       bool ok = true;
+      // gate_up tiles (the first 256) already seen complete, as four 64-bit register
+      // words (no dynamically indexed array: local memory would go to L2, the shared
+      // memory carve-out leaves almost no L1). A down unit reads the h of a dozen tiles,
+      // two k-blocks each: a tile's counter is read until it shows the tile complete, and
+      // with it the count of finished tiles; once that count is full nothing is read.
+      uint64_t rdy0 = 0, rdy1 = 0, rdy2 = 0, rdy3 = 0;
+      bool all_known = false;     // every gate_up tile is finished (bars[2] counts them)
+      const int n_tiles1 = P.g1.m_tiles;
+      auto tile_known = [&](int x) -> bool {
+        const uint64_t w = x < 64 ? rdy0 : x < 128 ? rdy1 : x < 192 ? rdy2 : rdy3;
+        return ((w >> (x & 63)) & 1ull) != 0ull;
+      };
+      auto mark_known = [&](int x) {
+        const uint64_t b = 1ull << (x & 63);
+        if (x < 64) rdy0 |= b;
+        else if (x < 128) rdy1 |= b;
+        else if (x < 192) rdy2 |= b;
+        else rdy3 |= b;
+      };
       auto dep_ready = [&](int dep) -> bool {
         if (dep < 0) {
           if (!x_ready) x_ready = *reinterpret_cast<const volatile unsigned*>(c_bars) >= (unsigned)n_norm;
           return x_ready;
         }
-        return *reinterpret_cast<const volatile unsigned*>(c_hready + dep) >= (unsigned)kItems1;
+        if (dep >= 256) return *reinterpret_cast<const volatile unsigned*>(c_hready + dep) >= (unsigned)kItems1;
+        if (all_known || tile_known(dep)) return true;
+        // the tile's counter and the count of finished tiles, in one round trip
+        const unsigned v = *reinterpret_cast<const volatile unsigned*>(c_hready + dep);
+        const unsigned n_done = *reinterpret_cast<const volatile unsigned*>(c_bars + 2);
+        if (n_done >= (unsigned)n_tiles1) {
+          all_known = true;
+          return true;
+        }
+        if (v < (unsigned)kItems1) return false;
+        mark_known(dep);
+        return true;
       };
       auto issue_front = [&]() {
         const int i = q_head;
@@ -217,6 +247,7 @@ __global__ void __launch_bounds__(192, 1)
           const unsigned* c = dep < 0 ? c_bars : c_hready + dep;
           if (!bar_wait(c, dep < 0 ? (unsigned)n_norm : (unsigned)kItems1, timeout, s_abort)) return false;
           if (dep < 0) x_ready = true;
+          else if (dep < 256) mark_known(dep);
           issue_front();
         }
         return true;
@@ -573,7 +604,10 @@ __global__ void __launch_bounds__(192, 1)
           fence_proxy_async_global();
           __threadfence();
           named_bar_sync(1, 128);
-          if (et == 0) atomicAdd(e_hready + tm, (unsigned)kItems1);
+          if (et == 0) {
+            atomicAdd(e_hready + tm, (unsigned)kItems1);
+            atomicAdd(e_bars + 2, 1u);
+          }
         } else {
 #pragma unroll 1
           for (int seg = 0; seg < 2; ++seg) {
@@ -614,7 +648,10 @@ __global__ void __launch_bounds__(192, 1)
           fence_proxy_async_global();
           __threadfence();
           named_bar_sync(1, 128);
-          if (et == 0) atomicAdd(e_hready + tm, (unsigned)kItems1);
+          if (et == 0) {
+            atomicAdd(e_hready + tm, (unsigned)kItems1);
+            atomicAdd(e_bars + 2, 1u);
+          }
         }
         return true;
       }
