@@ -40,7 +40,23 @@ namespace tpl {
 // before it hands its slice of the sum to the last one. Neither is an error.
 constexpr unsigned long long kStartPatienceNs = 50000ull;
 constexpr unsigned long long kSplitPatienceNs = 50000ull;
-constexpr int kUnitSlots = 4;   // down units handed from the producer to the MMA and epilogue roles
+constexpr int kUnitSlots = 4;
+
+// Wait until *c >= n, reading it with acquire loads; false after timeout_ns or when
+// *abort is set (bounded; a short sleep between reads).
+__device__ __forceinline__ bool poll_acquire(const unsigned* c, unsigned n, unsigned long long timeout_ns,
+                                             const volatile int* abort) {
+  if (ld_acquire(c) >= n) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(32);
+    if (ld_acquire(c) >= n) return true;
+    if ((it & 31u) == 0) {
+      if (abort != nullptr && *abort) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+  }
+}   // down units handed from the producer to the MMA and epilogue roles
 
 template <int BN>
 __global__ void __launch_bounds__(192, 1)
@@ -205,14 +221,14 @@ __global__ void __launch_bounds__(192, 1)
       };
       auto dep_ready = [&](int dep) -> bool {
         if (dep < 0) {
-          if (!x_ready) x_ready = *reinterpret_cast<const volatile unsigned*>(c_bars) >= (unsigned)n_norm;
+          if (!x_ready) x_ready = ld_acquire(c_bars) >= (unsigned)n_norm;
           return x_ready;
         }
-        if (dep >= 256) return *reinterpret_cast<const volatile unsigned*>(c_hready + dep) >= (unsigned)kItems1;
+        if (dep >= 256) return ld_acquire(c_hready + dep) >= (unsigned)kItems1;
         if (all_known || tile_known(dep)) return true;
         // the tile's counter and the count of finished tiles, in one round trip
-        const unsigned v = *reinterpret_cast<const volatile unsigned*>(c_hready + dep);
-        const unsigned n_done = *reinterpret_cast<const volatile unsigned*>(c_bars + 2);
+        const unsigned v = ld_acquire(c_hready + dep);
+        const unsigned n_done = ld_acquire(c_bars + 2);
         if (n_done >= (unsigned)n_tiles1) {
           all_known = true;
           return true;
@@ -245,7 +261,7 @@ __global__ void __launch_bounds__(192, 1)
           if (q_n <= keep) return true;
           const int dep = q_dep[q_head];
           const unsigned* c = dep < 0 ? c_bars : c_hready + dep;
-          if (!bar_wait(c, dep < 0 ? (unsigned)n_norm : (unsigned)kItems1, timeout, s_abort)) return false;
+          if (!poll_acquire(c, dep < 0 ? (unsigned)n_norm : (unsigned)kItems1, timeout, s_abort)) return false;
           if (dep < 0) x_ready = true;
           else if (dep < 256) mark_known(dep);
           issue_front();
@@ -549,10 +565,10 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       // x_norm is read by the tensor copies of phase 1 (async proxy); the rows of all
-      // epilogue threads are released by the one fence in bar_arrive after the barrier
+      // epilogue threads are released by one release-add after the barrier
       fence_proxy_async_global();
       named_bar_sync(1, 128);
-      if (et == 0) bar_arrive(e_bars + 0);
+      if (et == 0) red_release_add(e_bars + 0, 1u);
     }
 
     float g[CH], uu[CH];
@@ -600,13 +616,12 @@ __global__ void __launch_bounds__(192, 1)
               *reinterpret_cast<uint4*>(dst + (size_t)tok * p.Is + ch * 8) =
                   *reinterpret_cast<const uint4*>(s_h + tok * 128 + ch * 8);
           }
-          // this tile's h columns are complete
+          // this tile's h columns are complete (released by one thread after the barrier)
           fence_proxy_async_global();
-          __threadfence();
           named_bar_sync(1, 128);
           if (et == 0) {
-            atomicAdd(e_hready + tm, (unsigned)kItems1);
-            atomicAdd(e_bars + 2, 1u);
+            red_release_add(e_hready + tm, (unsigned)kItems1);
+            red_release_add(e_bars + 2, 1u);
           }
         } else {
 #pragma unroll 1
@@ -635,22 +650,20 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(this_buf));
-      __threadfence();
+      // the partial of every epilogue thread is released by the arrival (acq_rel) after the barrier
       named_bar_sync(1, 128);
       if (ph == 0) {
         // gate_up split-K: the last split of the tile to arrive adds the tile's partials
         // (split order) and publishes its h columns; no split waits for another
         unsigned last = 0;
-        if (et == 0) last = atomicAdd(e_cnt1 + tm, 1u) == (unsigned)(p.splits - 1) ? 1u : 0u;
+        if (et == 0) last = atom_acq_rel_add(e_cnt1 + tm, 1u) == (unsigned)(p.splits - 1) ? 1u : 0u;
         if (share(last)) {
-          __threadfence();
           reduce_tile_items<true, KIND_GATE_UP, BN>(p, tm, 0, kItems1, et, 128);
           fence_proxy_async_global();
-          __threadfence();
           named_bar_sync(1, 128);
           if (et == 0) {
-            atomicAdd(e_hready + tm, (unsigned)kItems1);
-            atomicAdd(e_bars + 2, 1u);
+            red_release_add(e_hready + tm, (unsigned)kItems1);
+            red_release_add(e_bars + 2, 1u);
           }
         }
         return true;
@@ -666,22 +679,22 @@ __global__ void __launch_bounds__(192, 1)
       unsigned mask = 0;
       if (et == 0) {
         unsigned* cnt = e_cnt2 + tm;
-        const unsigned old = atomicAdd(cnt, 1u);
+        const unsigned old = atom_acq_rel_add(cnt, 1u);
         if ((old & 0xFFFFu) == S2n - 1u) {
           mask = (1u << sp) | (old >> 16);
         } else {
-          const volatile unsigned* vc = cnt;
-          bool all = (*vc & 0xFFFFu) >= S2n;
+          bool all = (ld_acquire(cnt) & 0xFFFFu) >= S2n;
           const uint64_t t0 = globaltimer_ns();
           while (!all && globaltimer_ns() - t0 < kSplitPatienceNs) {
             __nanosleep(64);
-            all = (*vc & 0xFFFFu) >= S2n;
+            all = (ld_acquire(cnt) & 0xFFFFu) >= S2n;
           }
           if (!all) {
-            unsigned w = *vc;
+            unsigned w = ld_acquire(cnt);
             for (;;) {
               if ((w & 0xFFFFu) >= S2n) {
                 all = true;
+                __threadfence();
                 break;
               }
               const unsigned prev = atomicCAS(cnt, w, w | (1u << (16 + sp)));
@@ -691,7 +704,6 @@ __global__ void __launch_bounds__(192, 1)
           }
           if (all) mask = 1u << sp;
         }
-        if (mask) __threadfence();
       }
       mask = share(mask);
       for (int s = 0; s < (int)S2n; ++s)
