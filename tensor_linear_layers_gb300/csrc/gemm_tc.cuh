@@ -89,6 +89,9 @@ struct GemmParams {
   // pm < *pair_count exist
   const int* pair_tiles;
   const int* pair_count;
+  // swapped KIND_GATE_UP only: per-token factor the gate and up accumulators are
+  // multiplied by before SiLU*mul (the fused decode block's 1 / rms); null: none
+  const float* inv;
   float* partials;             // split-K fp32 partials [tile][split][col][128 rows]
   unsigned* gbar;              // grid barrier {arrivals, generation}
   int* status;                 // device status word
@@ -103,7 +106,8 @@ struct MlpDecodeParams {
   const __nv_bfloat16* res_in;   // [T, H] or null
   const __nv_bfloat16* gamma;    // [H] (norm)
   __nv_bfloat16* res_out;        // [T, H] (norm)
-  __nv_bfloat16* x_norm;         // [T, H] workspace (norm)
+  __nv_bfloat16* x_norm;         // [T, H] workspace (norm): y = bf16(r * gamma), gate_up's token operand
+  float* inv;                    // [T] workspace (norm): 1 / rms of every row
   // Two sets of counters; a launch uses the set its launch count selects and clears the other.
   unsigned* bars;                // [0] norm arrivals, [1] CTAs that gave up waiting for the gate_up
                                  // CTAs to start, [2] gate_up tiles finished, [3] down units claimed;
@@ -237,7 +241,10 @@ __device__ __forceinline__ void emit_vals(const GemmParams& p, int tm, int tn, i
 #pragma unroll
         for (int j = 0; j < N; ++j) {
           const int tok = tn * BN + c0 + j;
-          if (tok < p.T) dst[(size_t)tok * p.out_rstride] = __float2bfloat16_rn(silu_f(g[j]) * u[j]);
+          if (tok < p.T) {
+            const float iv = p.inv != nullptr ? __ldcg(p.inv + tok) : 1.f;
+            dst[(size_t)tok * p.out_rstride] = __float2bfloat16_rn(silu_f(g[j] * iv) * (u[j] * iv));
+          }
         }
       } else if (KIND == KIND_COL) {
         const int f = tm * 256 + seg * 128 + row;

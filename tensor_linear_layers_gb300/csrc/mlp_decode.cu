@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t ufull0 = smem_u32(xtra + 32);                                  // kUnitSlots mbarriers
   const uint32_t uempty0 = smem_u32(xtra + 64);                                 // kUnitSlots mbarriers
   volatile unsigned* s_word = reinterpret_cast<volatile unsigned*>(xtra + 96);  // epilogue decisions
+  float* s_inv = reinterpret_cast<float*>(xtra + 128);                          // 1 / rms per token (BN)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -110,7 +111,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), 2);   // the producer, and whoever provides the token operand
       mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -150,6 +151,14 @@ __global__ void __launch_bounds__(192, 1)
   const int owner_span = min(G, (int)grid - n_norm);
   const int owners_end = n_norm + owner_span;
   const int g_first = (me >= n_norm && me < owners_end) ? me - n_norm : G;
+  // With the norm, gate_up's token operand is y = bf16(r * gamma), r = bf16(a + r0),
+  // which the norm CTAs write with 1 / rms of every row; the accumulator is scaled by
+  // 1 / rms per token in the epilogue. For T <= 32 the gate_up CTAs do not wait for it
+  // to start: their epilogue warps build the operand of their first k-blocks into the
+  // ring stages themselves (the weights arrive by bulk copy).
+  constexpr bool kBuildX = BN <= 32;
+  constexpr int kBuildKb = STAGES;    // k-blocks of a gate_up unit whose token operand is built here
+  const bool build_x = kBuildX && P.has_norm && P.g1.splits == 1;
   auto started = [&]() -> unsigned long long {
     return *reinterpret_cast<const volatile unsigned long long*>(P.ticket) - tbase;
   };
@@ -278,7 +287,20 @@ __global__ void __launch_bounds__(192, 1)
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, timeout)) return false;
           const uint32_t sa = base + stage * S::kStageBytes;
           const uint32_t fb = full_bar(stage);
+          if (ph == 0 && build_x && kb < kb0 + kBuildKb) {
+            // the epilogue warps write the token operand and make the second arrival
+            mbar_arrive_expect_tx(fb, S::kABytes);
+            bulk_load(sa, wsrc + (size_t)kb * kWBlockBytes, kWBlockBytes, fb, pol_w);
+            issued_mask |= 1u << stage;
+            last_phase_bits = (last_phase_bits & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           mbar_arrive_expect_tx(fb, S::kStageBytes);
+          mbar_arrive(fb);
           bulk_load(sa, wsrc + (size_t)kb * kWBlockBytes, kWBlockBytes, fb, pol_w);
           int kx = kb * 64, shard = 0, dep = -1;
           if (ph == 1) {
@@ -482,11 +504,11 @@ __global__ void __launch_bounds__(192, 1)
       for (long long i = etid; i < P.cset; i += ethreads) o_cnt[i] = 0u;
       if (blockIdx.x == 0 && et < 4) o_bars[et] = 0u;
     }
-    // ---- phase 0: residual add + RMSNorm of the rows of this CTA (the first n_norm CTAs
-    // to start). The loads of a chunk (a, residual and gamma, up to 8 vectors per thread
-    // each) are issued together before anything waits on them, and the rounded residual
-    // stays in registers, so a row costs one memory round trip (H <= 8 * 8 * 128 = 8192 in
-    // one chunk; longer rows loop).
+    // ---- phase 0: the rows of this CTA (the first n_norm CTAs to start): r = bf16(a + r0)
+    // to residual_out, gate_up's token operand y = bf16(r * gamma) to the workspace, and
+    // 1 / rms of r. The loads of a chunk (a, residual and gamma, up to 8 vectors per
+    // thread each) are issued together before anything waits on them, so a row costs one
+    // memory round trip (rows longer than 8 * 8 * 128 = 8192 take more chunks).
     if (P.has_norm && me < n_norm) {
       const int H = P.H, nvec = H >> 3;
       constexpr int NV = 8;
@@ -496,17 +518,16 @@ __global__ void __launch_bounds__(192, 1)
         const uint4* av = reinterpret_cast<const uint4*>(P.x_in + roff);
         const uint4* rv = reinterpret_cast<const uint4*>(P.res_in + roff);
         uint4* ro = reinterpret_cast<uint4*>(P.res_out + roff);
-        uint4* xo = reinterpret_cast<uint4*>(P.x_norm + roff);
-        const bool one_chunk = nvec <= NV * 128;
+        uint4* yo = reinterpret_cast<uint4*>(P.x_norm + roff);
         float ss = 0.f;
-        uint4 a4[NV], r4[NV], g4[NV];
         for (int v0 = 0; v0 < nvec; v0 += NV * 128) {
+          uint4 a4[NV], r4[NV], g4[NV];
 #pragma unroll
           for (int k = 0; k < NV; ++k) {
             const int v = v0 + k * 128 + et;
             if (v < nvec) {
-              a4[k] = __ldg(av + v);
-              r4[k] = __ldg(rv + v);
+              a4[k] = __ldcg(av + v);
+              r4[k] = __ldcg(rv + v);
               g4[k] = __ldg(gv + v);
             }
           }
@@ -516,15 +537,21 @@ __global__ void __launch_bounds__(192, 1)
             if (v < nvec) {
               const __nv_bfloat162* ab = reinterpret_cast<const __nv_bfloat162*>(&a4[k]);
               const __nv_bfloat162* rb = reinterpret_cast<const __nv_bfloat162*>(&r4[k]);
-              __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&a4[k]);  // a4[k] becomes the residual
+              const __nv_bfloat162* gb = reinterpret_cast<const __nv_bfloat162*>(&g4[k]);
+              uint4 o, y;
+              __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+              __nv_bfloat162* yb = reinterpret_cast<__nv_bfloat162*>(&y);
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const float2 fa = __bfloat1622float2(ab[i]), fr = __bfloat1622float2(rb[i]);
                 ob[i] = __floats2bfloat162_rn(fa.x + fr.x, fa.y + fr.y);
                 const float2 q2 = __bfloat1622float2(ob[i]);  // the stored residual is what is normalised
+                const float2 fg = __bfloat1622float2(gb[i]);
                 ss += q2.x * q2.x + q2.y * q2.y;
+                yb[i] = __floats2bfloat162_rn(q2.x * fg.x, q2.y * fg.y);
               }
-              ro[v] = a4[k];
+              ro[v] = o;
+              yo[v] = y;
             }
           }
         }
@@ -532,40 +559,11 @@ __global__ void __launch_bounds__(192, 1)
         for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
         if (lane == 0) s_red[q] = ss;
         named_bar_sync(1, 128);
-        const float inv = rsqrtf((s_red[0] + s_red[1] + s_red[2] + s_red[3]) / (float)H + P.eps);
+        if (et == 0) P.inv[r] = rsqrtf((s_red[0] + s_red[1] + s_red[2] + s_red[3]) / (float)H + P.eps);
         named_bar_sync(1, 128);
-        for (int v0 = 0; v0 < nvec; v0 += NV * 128) {
-          if (!one_chunk) {
-            // rows longer than one chunk: the registers hold the last chunk only
-#pragma unroll
-            for (int k = 0; k < NV; ++k) {
-              const int v = v0 + k * 128 + et;
-              if (v < nvec) {
-                a4[k] = ro[v];   // written by this thread above
-                g4[k] = __ldg(gv + v);
-              }
-            }
-          }
-#pragma unroll
-          for (int k = 0; k < NV; ++k) {
-            const int v = v0 + k * 128 + et;
-            if (v < nvec) {
-              const __nv_bfloat162* rb = reinterpret_cast<const __nv_bfloat162*>(&a4[k]);
-              const __nv_bfloat162* gb = reinterpret_cast<const __nv_bfloat162*>(&g4[k]);
-              uint4 o;
-              __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const float2 fr = __bfloat1622float2(rb[i]), fg = __bfloat1622float2(gb[i]);
-                ob[i] = __floats2bfloat162_rn(fr.x * inv * fg.x, fr.y * inv * fg.y);
-              }
-              xo[v] = o;
-            }
-          }
-        }
       }
-      // x_norm is read by the tensor copies of phase 1 (async proxy); the rows of all
-      // epilogue threads are released by one release-add after the barrier
+      // y is read by the tensor copies of gate_up (async proxy); the rows of all epilogue
+      // threads are released by one release-add after the barrier
       fence_proxy_async_global();
       named_bar_sync(1, 128);
       if (et == 0) red_release_add(e_bars + 0, 1u);
@@ -601,8 +599,16 @@ __global__ void __launch_bounds__(192, 1)
             if (CH == 32) { tmem_ld32(acc + c0, g); tmem_ld32(acc + BN + c0, uu); }
             else { tmem_ld16(acc + c0, g); tmem_ld16(acc + BN + c0, uu); }
             tc_wait_ld();
+            if (P.has_norm) {
 #pragma unroll
-            for (int j = 0; j < CH; ++j) s_h[(c0 + j) * 128 + row] = __float2bfloat16_rn(silu_f(g[j]) * uu[j]);
+              for (int j = 0; j < CH; ++j) {
+                const float iv = s_inv[c0 + j];
+                s_h[(c0 + j) * 128 + row] = __float2bfloat16_rn(silu_f(g[j] * iv) * (uu[j] * iv));
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < CH; ++j) s_h[(c0 + j) * 128 + row] = __float2bfloat16_rn(silu_f(g[j]) * uu[j]);
+            }
           }
           tc_fence_before();
           __syncwarp();
@@ -712,8 +718,116 @@ __global__ void __launch_bounds__(192, 1)
                                                 (int)((long long)(s + 1) * items / S2n), et, 128);
       return true;
     };
+    // ---- the token operand of the first kBuildKb k-blocks of a gate_up unit (build_x):
+    // y = bf16(bf16(a + r0) * gamma), the values the norm CTAs write for the rest, built
+    // by this CTA's epilogue warps straight into the ring stages the producer filled
+    // with those k-blocks' weights, so gate_up starts before the norm rows are published.
+    // Loads run two k-blocks ahead. Each thread owns NC 16-byte chunks (8 features of one
+    // token) of a k-block's [BN tokens][64] tile.
+    constexpr int NC = kBuildX ? BN / 16 : 1;
+    int bstage = 0;
+    uint32_t bphase = 0;
+    auto build_unit = [&](int u) -> bool {
+      int tm, kb0, kb1;
+      krange(P.g1, u, tm, kb0, kb1);
+      const int kbb = min(kb1, kb0 + kBuildKb);
+      const int H = P.H, T = P.g1.T;
+      struct Chunks {
+        uint4 a[NC], r[NC], g[NC];
+      };
+      auto load = [&](int kb, Chunks& c) {
+#pragma unroll
+        for (int m = 0; m < NC; ++m) {
+          const int ci = et + 128 * m, t = ci >> 3, col = kb * 64 + (ci & 7) * 8;
+          if (kb < kbb && t < T && col < H) {
+            c.a[m] = __ldcg(reinterpret_cast<const uint4*>(P.x_in + (size_t)t * H + col));
+            c.r[m] = __ldcg(reinterpret_cast<const uint4*>(P.res_in + (size_t)t * H + col));
+            c.g[m] = __ldg(reinterpret_cast<const uint4*>(P.gamma + col));
+          } else {
+            c.a[m] = c.r[m] = c.g[m] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+      };
+      Chunks c0, c1, c2;
+      load(kb0, c0);
+      load(kb0 + 1, c1);
+      for (int kb = kb0; kb < kbb; ++kb) {
+        load(kb + 2, c2);
+        uint4 y[NC];
+#pragma unroll
+        for (int m = 0; m < NC; ++m) {
+          const __nv_bfloat162* ab = reinterpret_cast<const __nv_bfloat162*>(&c0.a[m]);
+          const __nv_bfloat162* rb = reinterpret_cast<const __nv_bfloat162*>(&c0.r[m]);
+          const __nv_bfloat162* gb = reinterpret_cast<const __nv_bfloat162*>(&c0.g[m]);
+          __nv_bfloat162* yb = reinterpret_cast<__nv_bfloat162*>(&y[m]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 fa = __bfloat1622float2(ab[i]), fr = __bfloat1622float2(rb[i]);
+            const float2 q2 = __bfloat1622float2(__floats2bfloat162_rn(fa.x + fr.x, fa.y + fr.y));
+            const float2 fg = __bfloat1622float2(gb[i]);
+            yb[i] = __floats2bfloat162_rn(q2.x * fg.x, q2.y * fg.y);
+          }
+        }
+        bool w_ok = true;
+        if (et == 0) {
+          w_ok = mbar_wait_bounded(empty_bar(bstage), bphase ^ 1u, s_abort, timeout);
+          if (!w_ok) set_abort();
+        }
+        if (!agree(w_ok)) return false;
+        uint8_t* sb = base_ptr + bstage * S::kStageBytes + S::kABytes;   // [BN rows][128 B], 128-byte swizzle
+#pragma unroll
+        for (int m = 0; m < NC; ++m) {
+          const int ci = et + 128 * m, t = ci >> 3, j = ci & 7;
+          *reinterpret_cast<uint4*>(sb + t * 128 + ((j ^ (t & 7)) << 4)) = y[m];
+        }
+        fence_proxy_async_shared();
+        named_bar_sync(1, 128);
+        if (et == 0) mbar_arrive(full_bar(bstage));
+        if (++bstage == STAGES) {
+          bstage = 0;
+          bphase ^= 1u;
+        }
+        c0 = c1;
+        c1 = c2;
+      }
+      // the unit's other k-blocks are loaded by the producer: advance the ring past them
+      for (int kb = kbb; kb < kb1; ++kb)
+        if (++bstage == STAGES) {
+          bstage = 0;
+          bphase ^= 1u;
+        }
+      return true;
+    };
+    // the gate_up epilogue reads 1 / rms and down's residual epilogue residual_out, both
+    // written by the norm CTAs (which wait on nothing)
+    auto acquire_norm = [&]() -> bool {
+      bool w_ok = true;
+      if (et == 0) {
+        w_ok = poll_acquire(e_bars + 0, (unsigned)n_norm, timeout, s_abort);
+        if (!w_ok) set_abort();
+      }
+      if (!agree(w_ok)) return false;
+      if (et < BN) s_inv[et] = et < P.g1.T ? __ldcg(P.inv + et) : 0.f;
+      named_bar_sync(1, 128);
+      return true;
+    };
+    bool norm_seen = !P.has_norm;
     // ---- gate_up units of this CTA, then the down units the producer hands over
-    for (int u = g_first; u < G && ok; u += owner_span) ok = epi_unit(0, u);
+    for (int u = g_first; u < G && ok; u += owner_span) {
+      if (build_x && !build_unit(u)) {
+        ok = false;
+        break;
+      }
+      if (!norm_seen) {
+        if (!acquire_norm()) {
+          ok = false;
+          break;
+        }
+        norm_seen = true;
+      }
+      ok = epi_unit(0, u);
+    }
+    if (ok && !norm_seen) ok = acquire_norm();
     int uslot = 0;
     uint32_t uphase = 0;
     while (ok) {
@@ -753,7 +867,7 @@ cudaError_t launch_mlp_decode_bn(const CUtensorMap& mx, const CUtensorMap& mh, c
                                  int grid, cudaStream_t st) {
   using S = GemmShape<true, KIND_GATE_UP, BN>;
   auto kernel = mlp_decode_kernel<BN>;
-  constexpr int kSmem = S::kSmemBytes + BN * 128 * 2 + 128;  // ring, barriers, h tile, tickets and unit slots
+  constexpr int kSmem = S::kSmemBytes + BN * 128 * 2 + 128 + BN * 4;  // ring, barriers, h tile, tickets and unit slots, 1/rms
   static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
   static std::atomic<uint64_t> attr_done{0};
   int dev = 0;
@@ -788,7 +902,7 @@ template <int BN>
 int mlp_decode_ctas_per_sm_bn() {
   using S = GemmShape<true, KIND_GATE_UP, BN>;
   auto kernel = mlp_decode_kernel<BN>;
-  constexpr int kSmem = S::kSmemBytes + BN * 128 * 2 + 128;
+  constexpr int kSmem = S::kSmemBytes + BN * 128 * 2 + 128 + BN * 4;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;

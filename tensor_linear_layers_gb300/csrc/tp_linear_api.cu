@@ -301,7 +301,7 @@ Plan make_plan(const tp_linear* h, int which, int64_t T, int force_splits = 0) {
 }
 
 struct Layout {
-  int64_t x_norm, h, part_col, part_row, total;
+  int64_t x_norm, inv, h, part_col, part_row, total;
 };
 
 // Split count of the gate_up GEMM inside the fused decode block. Decode streams
@@ -332,6 +332,8 @@ Layout make_layout(const tp_linear* h, int64_t T) {
   if (mlp && (h->cfg.flags & TP_FLAG_HAS_NORM)) {
     L.x_norm = off;
     off = align256(off + T * h->H * 2);
+    L.inv = off;                       // the fused decode block's 1 / rms per row
+    off = align256(off + T * 4);
   }
   if (mlp) {
     L.h = off;
@@ -921,6 +923,8 @@ int run_fused_decode(const tp_linear* h, int64_t T, char* ws, const Layout& L, c
   P.gamma = static_cast<const __nv_bfloat16*>(h->gamma);
   P.res_out = static_cast<__nv_bfloat16*>(residual_out);
   P.x_norm = reinterpret_cast<__nv_bfloat16*>(ws + L.x_norm);
+  P.inv = norm ? reinterpret_cast<float*>(ws + L.inv) : nullptr;
+  P.g1.inv = P.inv;   // gate_up with split-K scales in the reduction
   P.bars = reinterpret_cast<unsigned*>(ws + kDecodeBarsOff);
   P.cnt1 = reinterpret_cast<unsigned*>(ws + kTileCountersOff);
   P.hready = P.cnt1 + h->wt_col;
@@ -1328,6 +1332,8 @@ Layout no_alloc_layout(const tp_linear* h, int64_t T) {
   if (h->cfg.flags & TP_FLAG_HAS_NORM) {
     L.x_norm = off;
     off = align256(off + T * h->H * 2);
+    L.inv = off;
+    off = align256(off + T * 4);
   }
   L.h = off;
   off = align256(off + (int64_t)h->cfg.t * T * h->Is * 2);
