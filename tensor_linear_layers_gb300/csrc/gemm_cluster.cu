@@ -15,6 +15,7 @@
 // store, row-parallel store + residual); no split-K. An optional second,
 // independent problem shares the launch (the units of both form one list).
 #include "gemm_launch.cuh"
+#include <algorithm>
 
 namespace tpl {
 
@@ -34,7 +35,7 @@ template <int KIND, int KIND2>
 __global__ void __launch_bounds__(192, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_w,
                         const __grid_constant__ CUtensorMap map_act2, const __grid_constant__ CUtensorMap map_w2,
-                        const GemmParams p, const GemmParams p2) {
+                        const GemmParams p, const GemmParams p2, const PairTail tail) {
   using P = PairShape;
   constexpr int STAGES = P::kStages;
   constexpr int BN = 256;
@@ -95,7 +96,32 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem_base = *s_tmem;
 
   const int pu1 = ((p.m_tiles + 1) >> 1) * p.n_tiles;
-  const int pu_all = pu1 + (kTwo ? ((p2.m_tiles + 1) >> 1) * p2.n_tiles : 0);
+  const int pu_all_units = pu1 + (kTwo ? ((p2.m_tiles + 1) >> 1) * p2.n_tiles : 0);
+  // the list the clusters walk: `full` whole units, then rem x s parts of the last units
+  const bool split_tail = tail.s >= 2;
+  const int pu_all = split_tail ? tail.full + tail.rem * tail.s : pu_all_units;
+  // virtual unit -> (pair unit, part, split slot); part -1: whole
+  auto vunit = [&](int v, int& pu, int& part, int& slot) {
+    if (!split_tail || v < tail.full) {
+      pu = v;
+      part = -1;
+      slot = -1;
+      return;
+    }
+    const int w = v - tail.full;
+    slot = w / tail.s;
+    part = w - slot * tail.s;
+    pu = tail.full + slot;
+  };
+  auto krange = [&](const GemmParams& q, int part, int& kb0, int& kb1) {
+    if (part < 0) {
+      kb0 = 0;
+      kb1 = q.nkb;
+    } else {
+      kb0 = (int)((long long)part * q.nkb / tail.s);
+      kb1 = (int)((long long)(part + 1) * q.nkb / tail.s);
+    }
+  };
   // pair unit -> (problem, token tile of this CTA, weight tile); grouped along M
   // pm: the pair of token tiles; grouped problems look the tiles up (false: pair skipped)
   auto decode = [&](int pu, bool& second, int& tm, int& tn, int& pm) -> bool {
@@ -137,18 +163,22 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0, last_phase_bits = 0;
       bool ok = true;
-      for (int pu = cluster; pu < pu_all && ok; pu += nclusters) {
+      for (int v = cluster; v < pu_all && ok; v += nclusters) {
+        int pu, part, slot;
+        vunit(v, pu, part, slot);
         int tm, tn, pm;
         bool second;
         if (!decode(pu, second, tm, tn, pm)) continue;
         const GemmParams& q = second ? p2 : p;
+        int kb_lo, kb_hi;
+        krange(q, part, kb_lo, kb_hi);
         const CUtensorMap* map = second ? &map_act2 : &map_act;
         const CUtensorMap* wmap = second ? &map_w2 : &map_w;
         const bool row_kind = second ? (KIND2 == KIND_ROW) : (KIND == KIND_ROW);
         int blk0 = tn * q.nkb;
         if (q.pair_tiles != nullptr)   // both tiles of a pair belong to the expert of its first
           blk0 += q.tile_expert[q.pair_tiles[2 * pm]] * (int)(q.expert_wbytes / kWBlockBytes);
-        for (int kb = 0; kb < q.nkb; ++kb) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, q.timeout_ns)) {
             fail(q);
             ok = false;
@@ -196,18 +226,22 @@ __global__ void __launch_bounds__(192, 1)
       int buf = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int pu = cluster; pu < pu_all && ok; pu += nclusters) {
+      for (int v = cluster; v < pu_all && ok; v += nclusters) {
+        int pu, part, slot;
+        vunit(v, pu, part, slot);
         int tm, tn, pm;
         bool second;
         if (!decode(pu, second, tm, tn, pm)) continue;
         const GemmParams& q = second ? p2 : p;
+        int kb_lo, kb_hi;
+        krange(q, part, kb_lo, kb_hi);
         if (!mbar_wait_bounded_cluster(tempty_bar(buf), acc_phase ^ 1u, s_abort, q.timeout_ns)) {
           fail(q);
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * P::kAccCols;
-        for (int kb = 0; kb < q.nkb; ++kb) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait_bounded(full_bar(stage), phase, s_abort, q.timeout_ns)) {
             fail(q);
             ok = false;
@@ -217,7 +251,7 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t sa = base + stage * P::kStageBytes;
           const uint64_t adesc = smem_desc_k128(sa);
           const uint64_t bdesc = smem_desc_k128(sa + P::kABytes);
-          if (kb == 0)
+          if (kb == kb_lo)
             tc_mma_bf16_pair<false>(d_tmem, adesc, bdesc, P::kIdesc);
           else
             tc_mma_bf16_pair<true>(d_tmem, adesc, bdesc, P::kIdesc);
@@ -252,7 +286,9 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t acc_phase = 0;
     constexpr int CH = 32;
     float g[CH], uu[CH];
-    for (int pu = cluster; pu < pu_all; pu += nclusters) {
+    for (int v = cluster; v < pu_all; v += nclusters) {
+      int pu, part, slot;
+      vunit(v, pu, part, slot);
       int tm, tn, pm;
       bool second;
       if (!decode(pu, second, tm, tn, pm)) continue;
@@ -278,13 +314,64 @@ __global__ void __launch_bounds__(192, 1)
           emit_vals<false, K, BN, CH>(q, tm, tn, 0, row, c0, g, uu);
         }
       };
-      if (second)
-        direct(std::integral_constant<int, (kTwo ? KIND2 : KIND)>{}, p2);
-      else
-        direct(std::integral_constant<int, KIND>{}, p);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
+      if (part < 0) {
+        if (second)
+          direct(std::integral_constant<int, (kTwo ? KIND2 : KIND)>{}, p2);
+        else
+          direct(std::integral_constant<int, KIND>{}, p);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
+      } else {
+        // a part of a split unit: its fp32 accumulator goes to the workspace (columns
+        // fastest across threads: row `row` of column c at c * 128 + row)
+        float* mine = tail.part + ((size_t)(slot * tail.s + part) * 2 + rank) * (256 * 128);
+#pragma unroll 1
+        for (int c0 = 0; c0 < 256; c0 += CH) {
+          tmem_ld32(acc + c0, g);
+          tc_wait_ld();
+#pragma unroll
+          for (int j = 0; j < CH; ++j) __stcg(mine + (size_t)(c0 + j) * 128 + row, g[j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
+        // the last part to arrive adds the parts in order and applies the epilogue
+        named_bar_sync(1, 128);
+        if (et == 0) *s_ok = atom_acq_rel_add(tail.cnt + slot * 2 + rank, 1u) == (unsigned)(tail.s - 1) ? 1 : 0;
+        named_bar_sync(1, 128);
+        const bool last = *s_ok != 0;
+        named_bar_sync(1, 128);
+        if (last) {
+          if (et == 0) atomicExch(tail.cnt + slot * 2 + rank, 0u);   // ready for the next launch
+          const float* base_p = tail.part + (size_t)slot * tail.s * 2 * (256 * 128) + (size_t)rank * (256 * 128);
+          auto summed = [&](auto kind_c, const GemmParams& q) {
+            constexpr int K = decltype(kind_c)::value;
+            using SK = GemmShape<false, K, BN>;
+#pragma unroll 1
+            for (int c0 = 0; c0 < SK::kNG; c0 += CH) {
+#pragma unroll
+              for (int j = 0; j < CH; ++j) {
+                g[j] = 0.f;
+                if (K == KIND_GATE_UP) uu[j] = 0.f;
+              }
+              for (int pp = 0; pp < tail.s; ++pp) {
+                const float* src = base_p + (size_t)pp * 2 * (256 * 128);
+#pragma unroll
+                for (int j = 0; j < CH; ++j) {
+                  g[j] += __ldcg(src + (size_t)(c0 + j) * 128 + row);
+                  if (K == KIND_GATE_UP) uu[j] += __ldcg(src + (size_t)(SK::kUOff + c0 + j) * 128 + row);
+                }
+              }
+              emit_vals<false, K, BN, CH>(q, tm, tn, 0, row, c0, g, uu);
+            }
+          };
+          if (second)
+            summed(std::integral_constant<int, (kTwo ? KIND2 : KIND)>{}, p2);
+          else
+            summed(std::integral_constant<int, KIND>{}, p);
+        }
+      }
       if (++buf == 2) {
         buf = 0;
         acc_phase ^= 1u;
@@ -303,9 +390,39 @@ __global__ void __launch_bounds__(192, 1)
   cluster_sync();
 }
 
+// How a launch of pu pair units on `clusters` clusters splits its tail (see PairTail):
+// when the last wave would be at most half full, its units are split into
+// s = min(4, clusters / rem) parts. Grouped (expert) problems are not split.
+PairTail plan_pair_tail(int pu, int clusters, bool grouped, float* part, unsigned* cnt) {
+  PairTail t{};
+  t.full = pu;
+  t.s = 1;
+  if (grouped || part == nullptr || cnt == nullptr || clusters < 2 || pu < 1) return t;
+  const int waves = (pu + clusters - 1) / clusters;
+  const int rem = pu - (waves - 1) * clusters;
+  const int s = std::min(4, clusters / rem);
+  if (s < 2) return t;
+  t.full = pu - rem;
+  t.rem = rem;
+  t.s = s;
+  t.part = part;
+  t.cnt = cnt;
+  return t;
+}
+
+// Waves (in whole-unit times) a launch of pu pair units takes on `clusters` clusters,
+// counting a split tail's parts as 1 / s of a unit.
+double pair_waves(int pu, int clusters) {
+  if (clusters < 1 || pu < 1) return 0.0;
+  const PairTail t = plan_pair_tail(pu, clusters, false, reinterpret_cast<float*>(1), reinterpret_cast<unsigned*>(1));
+  if (t.s < 2) return (double)((pu + clusters - 1) / clusters);
+  return (double)(t.full / clusters) + 1.0 / t.s;
+}
+
 template <int KIND, int KIND2>
 cudaError_t launch_pair(const CUtensorMap& a1, const CUtensorMap& w1, const GemmParams& p1, const CUtensorMap& a2,
-                        const CUtensorMap& w2, const GemmParams& p2, int max_clusters, cudaStream_t st) {
+                        const CUtensorMap& w2, const GemmParams& p2, int max_clusters, float* tail_part,
+                        unsigned* tail_cnt, cudaStream_t st) {
   using P = PairShape;
   auto kernel = tc_gemm_pair_kernel<KIND, KIND2>;
   static std::atomic<uint64_t> attr_done{0};
@@ -319,7 +436,9 @@ cudaError_t launch_pair(const CUtensorMap& a1, const CUtensorMap& w1, const Gemm
     attr_done.fetch_or(bit, std::memory_order_acq_rel);
   }
   const int pu = ((p1.m_tiles + 1) / 2) * p1.n_tiles + (KIND2 >= 0 ? ((p2.m_tiles + 1) / 2) * p2.n_tiles : 0);
-  const int clusters = pu < max_clusters ? pu : max_clusters;
+  const PairTail tail = plan_pair_tail(pu, max_clusters, p1.pair_tiles != nullptr, tail_part, tail_cnt);
+  const int vunits = tail.s >= 2 ? tail.full + tail.rem * tail.s : pu;
+  const int clusters = vunits < max_clusters ? vunits : max_clusters;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters);
   cfg.blockDim = dim3(192);
@@ -332,7 +451,7 @@ cudaError_t launch_pair(const CUtensorMap& a1, const CUtensorMap& w1, const Gemm
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, a1, w1, a2, w2, p1, p2);
+  return cudaLaunchKernelEx(&cfg, kernel, a1, w1, a2, w2, p1, p2, tail);
 }
 
 int pair_stages() { return PairShape::kStages; }
@@ -373,18 +492,27 @@ int pair_max_clusters() {
 
 cudaError_t launch_gemm_pair(int kind, int kind2, const CUtensorMap& a1, const CUtensorMap& w1, const GemmParams& p1,
                              const CUtensorMap& a2, const CUtensorMap& w2, const GemmParams& p2, int max_clusters,
-                             cudaStream_t st) {
+                             float* tail_part, unsigned* tail_cnt, cudaStream_t st) {
+  float* tp = tail_part;
+  unsigned* tc = tail_cnt;
   if (kind2 < 0) {
     switch (kind) {
-      case KIND_GATE_UP: return launch_pair<KIND_GATE_UP, -1>(a1, w1, p1, a1, w1, p1, max_clusters, st);
-      case KIND_COL: return launch_pair<KIND_COL, -1>(a1, w1, p1, a1, w1, p1, max_clusters, st);
-      case KIND_ROW: return launch_pair<KIND_ROW, -1>(a1, w1, p1, a1, w1, p1, max_clusters, st);
+      case KIND_GATE_UP: return launch_pair<KIND_GATE_UP, -1>(a1, w1, p1, a1, w1, p1, max_clusters, tp, tc, st);
+      case KIND_COL: return launch_pair<KIND_COL, -1>(a1, w1, p1, a1, w1, p1, max_clusters, tp, tc, st);
+      case KIND_ROW: return launch_pair<KIND_ROW, -1>(a1, w1, p1, a1, w1, p1, max_clusters, tp, tc, st);
       default: return cudaErrorInvalidValue;
     }
   }
   if (kind == KIND_COL && kind2 == KIND_ROW)
-    return launch_pair<KIND_COL, KIND_ROW>(a1, w1, p1, a2, w2, p2, max_clusters, st);
+    return launch_pair<KIND_COL, KIND_ROW>(a1, w1, p1, a2, w2, p2, max_clusters, tp, tc, st);
   return cudaErrorInvalidValue;
+}
+
+// Workspace of a pair launch's split tail on a device with `nsm` SMs: at most nsm / 2
+// parts (one per cluster) of 2 x 128 KB, then the counters.
+int64_t pair_tail_bytes(int nsm) {
+  const int64_t parts = std::max(1, nsm / 2);
+  return parts * 2 * 256 * 128 * 4 + ((parts * 2 * 4 + 255) & ~int64_t(255));
 }
 
 }  // namespace tpl

@@ -98,6 +98,20 @@ struct GemmParams {
   unsigned long long timeout_ns;
 };
 
+// Tail of a CTA-pair launch: the last `rem` pair units of the list are split into `s`
+// parts along K, so that a last wave that would be less than half full runs as s
+// shorter waves' worth of parts on more clusters. Each part writes its fp32 accumulator
+// to `part` (per part and CTA rank: 128 rows x 256 columns); the last part of a unit to
+// arrive (count in `cnt`, per unit and rank, reset by that part) adds the s partials in
+// part order and applies the epilogue. s < 2: no split.
+struct PairTail {
+  int full;          // pair units run whole (the first `full` of the list)
+  int rem;           // units split into parts
+  int s;             // parts per split unit
+  float* part;       // [rem][s][2][256 columns][128 rows] fp32
+  unsigned* cnt;     // [rem][2]
+};
+
 // Parameters of the fused decode-shaped MLP block (mlp_decode.cu).
 struct MlpDecodeParams {
   GemmParams g1;                 // KIND_GATE_UP, swapped operands

@@ -32,7 +32,9 @@ cudaError_t launch_gemm_prefill_col_row(const CUtensorMap& a1, const GemmParams&
                                         const GemmParams& p2, int grid, cudaStream_t st);
 cudaError_t launch_gemm_pair(int kind, int kind2, const CUtensorMap& a1, const CUtensorMap& w1, const GemmParams& p1,
                              const CUtensorMap& a2, const CUtensorMap& w2, const GemmParams& p2, int max_clusters,
-                             cudaStream_t st);
+                             float* tail_part, unsigned* tail_cnt, cudaStream_t st);
+int64_t pair_tail_bytes(int nsm);
+double pair_waves(int pu, int clusters);
 int pair_max_clusters();
 int pair_stages();
 int gemm_stages_decode_gate_up(int bn);
@@ -301,7 +303,7 @@ Plan make_plan(const tp_linear* h, int which, int64_t T, int force_splits = 0) {
 }
 
 struct Layout {
-  int64_t x_norm, inv, h, part_col, part_row, total;
+  int64_t x_norm, inv, h, part_col, part_row, pair_tail, total;
 };
 
 // Split count of the gate_up GEMM inside the fused decode block. Decode streams
@@ -345,8 +347,22 @@ Layout make_layout(const tp_linear* h, int64_t T) {
   off = align256(off + pc);
   L.part_row = off;
   off = align256(off + make_plan(h, 1, T).partial_bytes);
+  if (T > kFusedMaxT) {
+    L.pair_tail = off;   // the CTA-pair launches' split tail: partials, then counters
+    off = align256(off + pair_tail_bytes(h->nsm));
+  }
   L.total = off;
   return L;
+}
+
+// The partials and counters of a pair launch's split tail in workspace `ws` (null: no split).
+float* tail_part(const tp_linear* h, void* ws, const Layout& L) {
+  return L.pair_tail ? reinterpret_cast<float*>(static_cast<char*>(ws) + L.pair_tail) : nullptr;
+}
+unsigned* tail_cnt(const tp_linear* h, void* ws, const Layout& L) {
+  if (!L.pair_tail) return nullptr;
+  const int64_t parts = std::max(1, h->nsm / 2);
+  return reinterpret_cast<unsigned*>(static_cast<char*>(ws) + L.pair_tail + parts * 2 * 256 * 128 * 4);
 }
 
 // Attention core workspace: after the handle's persistent counters and flags,
@@ -429,7 +445,7 @@ bool prefer_pair(const tp_linear* h, const Plan* pls, int n, int ncl) {
     one = (double)ceil_div(pls[0].units, h->nsm) * ((double)pls[0].nkb / pls[0].splits + (pls[0].splits > 1 ? 16.0 : 0.0));
   else
     one = (double)ceil_div(units, h->nsm) * pls[0].nkb;
-  const double pair = (double)ceil_div(pu, ncl) * pls[0].nkb * 0.8;
+  const double pair = pair_waves((int)pu, ncl) * pls[0].nkb * 0.8;
   return pair < one;
 }
 
@@ -483,7 +499,8 @@ int run_col(const tp_linear* h, int64_t T, const void* x, void* out, void* ws, c
     GemmParams q = p;
     q.splits = 1;
     q.units = p1.units;
-    cudaError_t e = launch_gemm_pair(pl.kind, -1, map_x, h->wmap_col, q, map_x, h->wmap_col, q, ncl, st);
+    cudaError_t e = launch_gemm_pair(pl.kind, -1, map_x, h->wmap_col, q, map_x, h->wmap_col, q, ncl,
+                                     tail_part(h, ws, L), tail_cnt(h, ws, L), st);
     if (e != cudaSuccess) return cuda_fail(e, "column-parallel GEMM launch (pairs)");
     return TP_OK;
   }
@@ -512,7 +529,8 @@ int run_row(const tp_linear* h, int64_t T, const void* in_shards, const void* re
     GemmParams q = p;
     q.splits = 1;
     q.units = p1.units;
-    cudaError_t e = launch_gemm_pair(pl.kind, -1, map_in, h->wmap_row, q, map_in, h->wmap_row, q, ncl, st);
+    cudaError_t e = launch_gemm_pair(pl.kind, -1, map_in, h->wmap_row, q, map_in, h->wmap_row, q, ncl,
+                                     tail_part(h, ws, L), tail_cnt(h, ws, L), st);
     if (e != cudaSuccess) return cuda_fail(e, "row-parallel GEMM launch (pairs)");
     return TP_OK;
   }
@@ -546,7 +564,8 @@ int run_col_row_together(const tp_linear* h, int64_t T, const void* x, void* qkv
   const Plan both[2] = {pc, pr};
   cudaError_t e;
   if (prefer_pair(h, both, 2, ncl)) {
-    e = launch_gemm_pair(KIND_COL, KIND_ROW, map_x, h->wmap_col, p1, map_a, h->wmap_row, p2, ncl, st);
+    e = launch_gemm_pair(KIND_COL, KIND_ROW, map_x, h->wmap_col, p1, map_a, h->wmap_row, p2, ncl,
+                         tail_part(h, ws, L), tail_cnt(h, ws, L), st);
   } else {
     const int grid = (int)std::min<int64_t>((int64_t)pc.units + pr.units, h->nsm);
     e = launch_gemm_prefill_col_row(map_x, p1, map_a, p2, grid, st);
@@ -1290,7 +1309,7 @@ int tp_moe_forward(tp_linear_t* h, int64_t T, int32_t top_k, const void* x, cons
       p.pair_tiles = pair_tiles;
       p.pair_count = pair_count;
       const CUtensorMap& wm = which == 0 ? h->wmap_col : h->wmap_row;
-      e = launch_gemm_pair(pl.kind, -1, map_a, wm, p, map_a, wm, p, ncl, st);
+      e = launch_gemm_pair(pl.kind, -1, map_a, wm, p, map_a, wm, p, ncl, nullptr, nullptr, st);
     } else {
       e = launch_gemm(false, pl.kind, pl.bn, map_a, p, pl.grid, st);
     }

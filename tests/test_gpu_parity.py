@@ -96,11 +96,14 @@ def test_mlp_with_norm_and_residual_stream(T):
 
 # ------------------------------------------------------------------ prefill tails on CTA pairs
 
-@pytest.mark.parametrize("T", [1000, 1300, 1421])
+@pytest.mark.parametrize("T", [256, 300, 1000, 1300, 1421])
 def test_prefill_tails_on_cta_pairs_every_row(T):
     # 8 token tiles, the last one partial (104 rows); 11 tiles, so the odd CTA of the
     # last pair has no tile; 12 tiles, the last one 13 rows. Both GEMMs run on CTA
-    # pairs at this shape; every row of every output is compared.
+    # pairs at this shape; every row of every output is compared. With 16 weight tiles
+    # per GEMM a launch's last wave is split along K when it is at most half full: T =
+    # 256 gives 16 pair units in 4 parts each, T = 300 32 units in 2 parts, T = 1300 and
+    # 1421 a 20-unit tail in 3 parts (the last part of a unit adds the parts in order).
     H, I, t = 4096, 2048, 4
     blk, d = make_mlp(H, I, t, norm=True)
     assert [p["engine"] for p in blk.plan(T)] == [1, 1]
