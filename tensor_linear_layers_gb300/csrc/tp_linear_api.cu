@@ -459,7 +459,10 @@ GemmParams base_params(const Plan& pl, int64_t T, void* ws, int64_t part_off, in
   p.nkb = pl.nkb;
   p.kbs = pl.kbs;
   p.nb = pl.nb;
-  p.group_m = 8;
+  // raster groups of 32 token tiles (16 CTA pairs): each weight tile is read from DRAM
+  // once per group while the group's token tiles stay in L2 (Llama-3-70B gate_up: 12.9 GB
+  // of DRAM reads per launch with groups of 8, 8.6 GB with 32; 3.6 % faster)
+  p.group_m = 32;
   char* w = static_cast<char*>(ws);
   p.partials = reinterpret_cast<float*>(w + part_off);
   p.gbar = reinterpret_cast<unsigned*>(w + gbar_off);
