@@ -72,8 +72,9 @@ def kernel_sources_hash() -> str:
     csrc = os.path.join(ROOT, "tensor_linear_layers_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(csrc)):
-        # device code only: the host-side API file does not change what a kernel does
-        if f.endswith((".cu", ".cuh", ".h")) and f != "tp_linear_api.cu":
+        # every source: the host file chooses the plans (rasterisation, splits) that
+        # decide a kernel's DRAM traffic
+        if f.endswith((".cu", ".cuh", ".h")):
             h.update(f.encode())
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(fh.read())
