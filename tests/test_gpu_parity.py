@@ -328,6 +328,21 @@ def test_fused_decode_block_matches_stage_calls(T):
     assert status_of(blk.workspace(T)) == 0
 
 
+@pytest.mark.parametrize("T", [1, 24])
+def test_fused_decode_more_gate_up_tiles_than_sms(T):
+    # I / t = 5120 gives 40 gate_up tiles per shard, 320 in all: more than the SMs, so
+    # the CTAs after the single norm CTA own two or three gate_up tiles each
+    H, I, t = 1024, 40960, 8
+    blk, d = make_mlp(H, I, t, norm=True, seed=3)
+    assert blk.plan(T)[0]["engine"] == 2
+    a, r0 = workloads.draw((T, H), 17, 0), workloads.draw((T, H), 17, 1)
+    out = blk.mlp_forward(a.cuda(), residual=r0.cuda())
+    ref = mlp_ref(d, a, residual=r0, norm=True)
+    for k in ("mlp_out", "residual_out", "residual_stream"):
+        assert rel_err(out[k], ref[k]) <= TOL, k
+    assert status_of(blk.workspace(T)) == 0
+
+
 def test_workspace_bound_covers_every_token_count():
     # one workspace sized for max_tokens must serve every T <= max_tokens
     blk, d = make_mlp(512, 1408, 2, norm=True)
