@@ -109,6 +109,22 @@ __global__ void __launch_bounds__(192, 1)
     *s_me = (int)me;
     *s_tbase = tk - me;
   }
+  // The block's activations (a, the residual and gamma: 2 T H + H elements) are fetched
+  // into L2 while this launch waits for the one before it, so that the norm rows and the
+  // first k-blocks of gate_up's token operand, loaded once the wait ends, do not queue in
+  // HBM behind the weight ring's first fill. Each line is prefetched by one thread of the grid.
+  if (threadIdx.x >= 64) {
+    const long long lines = ((long long)P.g1.T * P.H * 2 + 127) / 128;
+    const long long gl = ((long long)P.H * 2 + 127) / 128;
+    const long long gt = (long long)blockIdx.x * 128 + (threadIdx.x - 64), nt = (long long)grid * 128;
+    const char* a = reinterpret_cast<const char*>(P.x_in);
+    const char* r = reinterpret_cast<const char*>(P.res_in);
+    for (long long i = gt; i < lines; i += nt) {
+      prefetch_l2(a + i * 128);
+      if (r != nullptr) prefetch_l2(r + i * 128);
+    }
+    if (P.has_norm && gt < gl) prefetch_l2(reinterpret_cast<const char*>(P.gamma) + gt * 128);
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 2);   // the producer, and whoever provides the token operand
