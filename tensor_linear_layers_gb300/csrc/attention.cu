@@ -75,14 +75,15 @@ enum {
   U_EMPTY = U_FULL + kUnitSlots,   // read by the two MMA threads and the four softmax warps
   NBARS = U_EMPTY + kUnitSlots
 };
-static_assert(8 * NBARS + 8 + 4 * kUnitSlots <= kBarBytes, "barrier area");
+// barriers, tensor-memory address and abort flag, unit ids, then (16-byte aligned) their entries
+static_assert(8 * NBARS + 8 + 4 * kUnitSlots + 15 + 16 * kUnitSlots <= kBarBytes, "barrier area");
 static_assert(S_FULL <= 32, "copy barriers fit the producer's bit masks");
 
 struct Unit {
   int r, i, g, start, len, qt;
 };
-__device__ __forceinline__ Unit decode_unit(const AttnParams& p, int u) {
-  const int4 pr = p.pairs[u / p.heads];
+// unit u from its work-table entry pr = pairs[u / heads]
+__device__ __forceinline__ Unit decode_unit(const AttnParams& p, int u, int4 pr) {
   const int hh = u - (u / p.heads) * p.heads;
   Unit x;
   x.r = hh / p.q_per;
@@ -159,6 +160,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(misc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 4);
   volatile int* s_units = reinterpret_cast<volatile int*>(misc + 8);  // [kUnitSlots] unit ids, -1 = no more
+  // [kUnitSlots] their work-table entries: the consumers read them here, not from global
+  // memory, where a load would queue behind the output rows a softmax warp has just stored
+  int4* s_pair = reinterpret_cast<int4*>((reinterpret_cast<uintptr_t>(misc + 8 + 4 * kUnitSlots) + 15) & ~uintptr_t(15));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -219,9 +223,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         int u = atomicAdd(p.next_unit, 1);
         if (u >= n_units) u = -1;
         s_units[slot] = u;
-        mbar_arrive(bar(U_FULL + slot));  // releases the id to the consumers
+        const int4 pr = u >= 0 ? p.pairs[u / p.heads] : make_int4(0, 0, 0, 0);
+        s_pair[slot] = pr;
+        mbar_arrive(bar(U_FULL + slot));  // releases the id and its entry to the consumers
         if (u < 0) break;
-        const Unit x = decode_unit(p, u);
+        const Unit x = decode_unit(p, u, pr);
         if (!mbar_wait_bounded(bar(Q_EMPTY), (nu & 1) ^ 1, s_abort, timeout)) {
           ok = false;
           break;
@@ -289,9 +295,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slot = nu % kUnitSlots;
         if (!wait(U_FULL + slot, (nu / kUnitSlots) & 1)) break;
         const int u = s_units[slot];
+        const int4 pr = s_pair[slot];
         mbar_arrive(bar(U_EMPTY + slot));
         if (u < 0) break;
-        const Unit x = decode_unit(p, u);
+        const Unit x = decode_unit(p, u, pr);
         const int n = x.qt + 1;
         if (s_role) {
           if (!wait(Q_FULL, nu & 1)) break;
@@ -365,10 +372,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int slot = nu % kUnitSlots;
       if (!wait_all(U_FULL + slot, (nu / kUnitSlots) & 1)) break;
       const int u = s_units[slot];
+      const int4 pr = s_pair[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(U_EMPTY + slot));
       if (u < 0) break;
-      const Unit x = decode_unit(p, u);
+      const Unit x = decode_unit(p, u, pr);
       const int q_rel = x.qt * 128 + row;
       float m = -INFINITY, l = 0.f;
       for (int kt = 0; kt <= x.qt; ++kt) {
@@ -457,26 +465,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv = 1.0f / l;
       __nv_bfloat16* dst = p.out + (size_t)x.r * p.out_sstride + (size_t)(x.start + q_rel) * p.out_rstride + x.i * 128;
-      float o[32];
-#pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        tmem_ld32(lane_addr + kOCol + c0, o);
-        tc_wait_ld();
-        if (q_rel < x.len) {
-#pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(o[j] * inv, o[j + 1] * inv);
-            v.y = pack_bf16x2(o[j + 2] * inv, o[j + 3] * inv);
-            v.z = pack_bf16x2(o[j + 4] * inv, o[j + 5] * inv);
-            v.w = pack_bf16x2(o[j + 6] * inv, o[j + 7] * inv);
-            *reinterpret_cast<uint4*>(dst + c0 + j) = v;
-          }
-        }
-      }
+      // O comes out of tensor memory whole (into the registers S used) and its buffer is
+      // released before the rows are written.
+      tmem_ld32(lane_addr + kOCol, s);
+      tmem_ld32(lane_addr + kOCol + 32, s + 32);
+      tmem_ld32(lane_addr + kOCol + 64, s + 64);
+      tmem_ld32(lane_addr + kOCol + 96, s + 96);
+      tc_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(O_EMPTY));
+      // Row q of the tile is this thread's: 256 bytes, eight 32-byte chunks. A store in
+      // which each lane writes its own row touches 32 lines; instead each group of four
+      // lanes transposes its 4 x 4 blocks of chunks (two shuffle stages per half row),
+      // after which lane a of the group holds chunk a of the half of all four rows, and a
+      // store has four lanes fill each line it touches (8 lines a store instead of 32).
+      uint32_t w[64];
+#pragma unroll
+      for (int k = 0; k < 64; ++k) w[k] = pack_bf16x2(s[2 * k] * inv, s[2 * k + 1] * inv);
+      const int a = lane & 3;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t* c = w + 32 * h;   // chunks 0..3 of this half: c[8 * i .. 8 * i + 7]
+        // stage 1 (lanes a, a ^ 2): lanes 0, 1 give chunks 2, 3 and take the partner's 0, 1
+        const bool hi2 = (a & 2) != 0;
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int lo = 8 * i + e, up = 8 * (2 + i) + e;
+            const uint32_t got = __shfl_xor_sync(0xffffffffu, hi2 ? c[lo] : c[up], 2);
+            if (hi2) c[lo] = got; else c[up] = got;
+          }
+        // stage 2 (lanes a, a ^ 1), in each pair of chunks: even lanes give the second,
+        // odd lanes the first
+        const bool odd = (a & 1) != 0;
+#pragma unroll
+        for (int i = 0; i < 4; i += 2)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int lo = 8 * i + e, up = 8 * (i + 1) + e;
+            const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? c[lo] : c[up], 1);
+            if (odd) c[lo] = got; else c[up] = got;
+          }
+        // c[8 k ..] is now chunk 4 h + a of row q - a + k
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (q_rel - a + k < x.len) {
+            __nv_bfloat16* d = dst + (k - a) * p.out_rstride + (4 * h + a) * 16;
+            const uint32_t* v = c + 8 * k;
+            if (p.out_align32) {
+              st_global_v8(d, *reinterpret_cast<const uint32_t(*)[8]>(v));
+            } else {
+              *reinterpret_cast<uint4*>(d) = make_uint4(v[0], v[1], v[2], v[3]);
+              *reinterpret_cast<uint4*>(d + 8) = make_uint4(v[4], v[5], v[6], v[7]);
+            }
+          }
+        }
+      }
     }
   }
 

@@ -63,6 +63,7 @@ struct AttnParams {
   unsigned long long timeout_ns;
   int T, q_per, kv_per, rep, group, heads;  // group = nq / nkv, heads = t * q_per
   float scale_log2;        // log2(e) / sqrt(hd)
+  int out_align32;         // out is 32-byte aligned (rows are then written with 32-byte stores)
 };
 // Builds the (sequence, q tile) table from cu_seqlens (device) into `pairs` and
 // runs the attention kernel on `grid` CTAs; map_qkv covers qkv as

@@ -1078,6 +1078,7 @@ int tp_attention_forward(tp_linear_t* h, int64_t T, const void* qkv, const int32
   p.n_pairs = reinterpret_cast<const int*>(ws + dyn_off(h) + 256);
   p.next_unit = reinterpret_cast<int*>(ws + dyn_off(h) + 260);
   p.out = static_cast<__nv_bfloat16*>(attn_out);
+  p.out_align32 = (reinterpret_cast<uintptr_t>(attn_out) & 31u) == 0 ? 1 : 0;
   p.out_sstride = gathered(h) ? h->Ks : T * h->Ks;
   p.out_rstride = (int)(gathered(h) ? h->cfg.t * h->Ks : h->Ks);
   p.status = t_status != nullptr ? t_status : reinterpret_cast<int*>(ws);

@@ -6,7 +6,8 @@ for the P V product; bf16 output). The cases cover several 128-query tiles,
 ragged tails, one-token and exact-tile sequences, kv heads split and
 replicated (t > nkv), plain multi-head (group of one), the Llama-3-8B-shaped
 4096-token sequence at full size (sampled rows), the ragged Qwen-shaped batch
-in full, determinism, bad offsets and the QKV -> attention -> o_proj chain.
+in full, determinism, an output only 16-byte aligned, bad offsets and the QKV ->
+attention -> o_proj chain.
 """
 import numpy as np
 import pytest
@@ -107,6 +108,21 @@ def test_run_twice_same_bits():
     a, _ = run(blk, qkv, lens)
     b, _ = run(blk, qkv, lens)
     assert torch.equal(a, b)
+
+
+def test_output_only_16_byte_aligned_same_bits():
+    # rows go out with 32-byte stores when the output is 32-byte aligned and with
+    # 16-byte stores otherwise; both must write the same values
+    blk, _ = make_attn(256, 8, 2, 2)
+    lens = [300, 45, 200]
+    qkv = workloads.draw((2, 545, qkv_width(8, 2, 2)), 12, 0)
+    a, cu = run(blk, qkv, lens)
+    big = torch.full((a.numel() + 8,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = big[8:].view(a.shape)
+    assert out.data_ptr() % 32 == 16
+    blk.attention_forward(qkv.cuda(), cu, int(max(lens)), out=out)
+    assert torch.equal(a, out)
+    assert status_of(blk.workspace(545)) == 0
 
 
 def test_bad_offsets_report_shape_error():
