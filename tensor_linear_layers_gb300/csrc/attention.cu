@@ -106,6 +106,9 @@ __global__ void attn_prep_kernel(const int* cu, int n_seqs, int T, int max_tiles
   extern __shared__ int off[];  // [max_tiles]
   __shared__ int s_bad;
   const int tid = threadIdx.x;
+  // the attention grid may be scheduled now: it sets itself up, then waits for this
+  // grid to complete before it reads the table
+  if (tid == 0) griddep_launch_dependents();
   if (tid == 0) {
     s_bad = (cu[0] != 0 || cu[n_seqs] != T) ? 1 : 0;
     *next_unit = 0;
@@ -185,6 +188,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(const_cast<uint32_t*>(s_tmem)), kTmemCols);
     tmem_relinquish();
   }
+  // launched behind the table's preparation (programmatic dependent launch): the set-up
+  // above overlaps it; the table, the unit counter and qkv are read only after this
+  griddep_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -549,8 +555,17 @@ cudaError_t launch_attention(const CUtensorMap& map_qkv, const AttnParams& p, co
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit, std::memory_order_acq_rel);
   }
-  attn_fwd_kernel<<<grid, kThreads, kAttnSmem, st>>>(map_qkv, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kAttnSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_fwd_kernel, map_qkv, p);
 }
 
 }  // namespace tpl
