@@ -264,11 +264,143 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// One launch for small selector sets (the table in shared memory) and T <= 64 * 256:
+// every CTA builds the selector table and matches all T rows itself (a few KB, from
+// L2), so no CTA waits for another and no list of matched rows goes through global
+// memory; then each CTA copies records j = blockIdx.x, blockIdx.x + gridDim.x, ... and
+// writes their headers. Thread t owns rows [t R, (t + 1) R), so a block-wide scan of
+// the per-thread hit counts gives every match its place in batch-row order.
+constexpr int kCapFusedThreads = 256;
+constexpr int kCapFusedMaxRowsPerThread = 64;   // one 64-bit hit mask per thread
+
+__global__ void __launch_bounds__(kCapFusedThreads)
+    capture_fused_kernel(int T, int H, const int32_t* __restrict__ row_req, const int32_t* __restrict__ row_pos,
+                         const int64_t* __restrict__ sel, int n_sel, int cap_log2, CaptureMeta meta,
+                         int64_t capacity, int64_t* n_out_dev, int* status) {
+  extern __shared__ uint64_t cap_smem[];
+  uint64_t* table = cap_smem;                                               // 1 << cap_log2 slots
+  int32_t* s_match = reinterpret_cast<int32_t*>(cap_smem + (1u << cap_log2));  // T entries
+  __shared__ int s_has_empty;
+  __shared__ int s_warp[kCapFusedThreads / 32];
+  const uint32_t cap = 1u << cap_log2;
+  const uint32_t mask = cap - 1u;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int R = (T + kCapFusedThreads - 1) / kCapFusedThreads;
+  const int r0 = min(T, tid * R), r1 = min(T, r0 + R);
+  if (tid == 0) s_has_empty = 0;
+  for (uint32_t i = tid; i < cap; i += kCapFusedThreads) table[i] = kEmpty;
+  __syncthreads();
+  for (int i = tid; i < n_sel; i += kCapFusedThreads) {
+    const uint64_t key = static_cast<uint64_t>(sel[i]);
+    if (key == kEmpty) {
+      s_has_empty = 1;
+      continue;
+    }
+    uint32_t h = static_cast<uint32_t>(mix64(key)) & mask;
+    for (uint32_t probe = 0; probe < cap; ++probe) {
+      const unsigned long long prev = atomicCAS(reinterpret_cast<unsigned long long*>(table + h), kEmpty, key);
+      if (prev == kEmpty || prev == key) break;
+      h = (h + 1u) & mask;
+    }
+  }
+  __syncthreads();
+  // this thread's rows: hit bits, eight rows' keys loaded at a time
+  uint64_t hits = 0;
+  for (int c = r0; c < r1; c += 8) {
+    int rq[8], ps[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (c + u < r1) {
+        rq[u] = row_req[c + u];
+        ps[u] = row_pos[c + u];
+      }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (c + u < r1) {
+        const uint64_t key = row_key(rq[u], ps[u]);
+        bool hit = false;
+        if (key == kEmpty) {
+          hit = s_has_empty != 0;
+        } else {
+          uint32_t h = static_cast<uint32_t>(mix64(key)) & mask;
+          for (uint32_t probe = 0; probe < cap; ++probe) {
+            const uint64_t v = table[h];
+            if (v == key) {
+              hit = true;
+              break;
+            }
+            if (v == kEmpty) break;
+            h = (h + 1u) & mask;
+          }
+        }
+        if (hit) hits |= 1ull << (c + u - r0);
+      }
+  }
+  // exclusive scan of the hit counts over the block (thread order = row order)
+  const int cnt = __popcll(hits);
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) s_warp[wid] = incl;
+  __syncthreads();
+  int before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kCapFusedThreads / 32; ++w) {
+    const int v = s_warp[w];
+    if (w < wid) before += v;
+    total += v;
+  }
+  int o = before + incl - cnt;
+  for (uint64_t b = hits; b != 0ull; b &= b - 1ull) s_match[o++] = r0 + __ffsll(static_cast<long long>(b)) - 1;
+  __syncthreads();
+  const int n_match = total;
+  const int64_t n_rec = static_cast<int64_t>(meta.n_tensors) * n_match;
+  if (blockIdx.x == 0 && tid == 0) {
+    *n_out_dev = n_rec;
+    if (n_rec > capacity) atomicCAS(status, 0, kStatusCapacity);
+  }
+  const int64_t n_write = n_rec < capacity ? n_rec : capacity;
+  const int nvec = H >> 3;
+  __nv_bfloat16* rows_out = static_cast<__nv_bfloat16*>(meta.rows_out);
+  for (int64_t j = blockIdx.x; j < n_write; j += gridDim.x) {
+    const int k = static_cast<int>(j / n_match);
+    const int m = static_cast<int>(j - static_cast<int64_t>(k) * n_match);
+    const int row = s_match[m];
+    if (tid == 0) {
+      int32_t* hd = meta.hdr + j * 6;
+      hd[0] = row_req[row];
+      hd[1] = row_pos[row];
+      hd[2] = meta.types[k];
+      hd[3] = meta.layer;
+      hd[4] = row;
+      hd[5] = 0;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(meta.tensors[k] + (size_t)row * H);
+    uint4* dst = reinterpret_cast<uint4*>(rows_out + (size_t)j * H);
+    for (int v = tid; v < nvec; v += kCapFusedThreads) dst[v] = __ldg(src + v);
+  }
+}
+
 cudaError_t launch_capture(int T, int H, const int32_t* row_req, const int32_t* row_pos,
                            const int64_t* sel, int n_sel, uint64_t* gtable, int cap_log2,
                            size_t table_smem, const CaptureMeta& meta, int64_t capacity,
                            int64_t* n_out_dev, int32_t* match_rows, int32_t* n_match_ws, int* status,
                            int copy_grid, cudaStream_t st) {
+  // small selector sets: one launch (table and match list in each CTA's shared memory)
+  const size_t fused_smem = table_smem + 4 * (size_t)T;
+  if (gtable == nullptr && T <= kCapFusedThreads * kCapFusedMaxRowsPerThread && fused_smem <= 160 * 1024) {
+    if (fused_smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(capture_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(fused_smem));
+      if (e != cudaSuccess) return e;
+    }
+    capture_fused_kernel<<<copy_grid, kCapFusedThreads, fused_smem, st>>>(T, H, row_req, row_pos, sel, n_sel,
+                                                                          cap_log2, meta, capacity, n_out_dev, status);
+    return cudaGetLastError();
+  }
   if (table_smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(capture_match_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,

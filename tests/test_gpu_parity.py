@@ -233,6 +233,31 @@ def test_capture_overflow_reports_capacity():
     assert hdr[:4, 4].cpu().tolist() == [0, 1, 2, 3]
 
 
+@pytest.mark.parametrize("T", [300, 20000])
+def test_capture_all_ones_key_on_both_paths(T):
+    # A row of request -1 at position -1 has the all-ones key, which is also the table's
+    # empty-slot marker. T = 300 runs the single-launch capture (each CTA matches every
+    # row); T = 20000 is past its 64 rows per thread and runs the two-kernel one.
+    H = 64
+    row_req = torch.arange(T, dtype=torch.int32) % 97
+    row_pos = torch.arange(T, dtype=torch.int32) // 97
+    row_req[5] = -1
+    row_pos[5] = -1
+    A = workloads.draw((T, H), 5, 0)
+    rng = np.random.default_rng(4)
+    rows_sel = rng.choice(T, 150, replace=False)
+    sel = np.concatenate([oracle.pack_key(row_req.numpy()[rows_sel], row_pos.numpy()[rows_sel]),
+                          oracle.pack_key([-1], [-1])])
+    hdr, rows, n_out, ws = tl.capture_rows(row_req.cuda(), row_pos.cuda(), torch.from_numpy(sel).cuda(),
+                                           [A.cuda()], [1], 3, capacity=T)
+    rh, rr = oracle.capture_rows(row_req.numpy(), row_pos.numpy(), sel, [A.float().numpy()], [1], 3)
+    n = int(n_out.item())
+    assert n == len(rh) and 5 in rh[:, 4].tolist()
+    assert np.array_equal(hdr[:n, :5].cpu().numpy(), rh)
+    assert torch.equal(rows[:n].cpu().float(), torch.from_numpy(rr).float())
+    assert status_of(ws) == 0
+
+
 def test_capture_large_selector_set_uses_global_table():
     T, H = 5000, 64
     row_req = torch.arange(T, dtype=torch.int32) // 100
