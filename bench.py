@@ -491,6 +491,10 @@ def run_ours(args, ws, rank, local):
         for name in OTHER_CONFIGS:
             gc.collect()
             torch.cuda.empty_cache()
+            # and the pinned host blocks the caching host allocator keeps: reused by the next
+            # workload's transfer buffers they left its end-to-end copies at a fraction of
+            # their speed (ragged Qwen block 1050-1430 instead of 558 us per step)
+            getattr(torch._C, "_host_emptyCache", lambda: None)()
             r = measure(args, workloads.WORKLOADS[name], ws, rank, local, cpu_budget_s=6.0)
             for k in ("metric", "n_gpus", "higher_is_better", "scaling", "vs_baseline", "dtype", "data"):
                 r.pop(k, None)
@@ -538,7 +542,7 @@ def measure(args, w: workloads.Workload, ws, rank, local, cpu_budget_s: float):
         cap = None
         if w.capture_frac > 0:
             # the ragged batch's step ends with the capture of mlp_out and residual_stream
-            # rows for the selected (request, position) keys: match + copy, two launches
+            # rows for the selected (request, position) keys
             b = workloads.ragged_batch(w)
             n_rec = 2 * len(b["sel_keys"])
             cap = {"rq": torch.from_numpy(b["row_req"]).to(dev), "rp": torch.from_numpy(b["row_pos"]).to(dev),
@@ -549,7 +553,12 @@ def measure(args, w: workloads.Workload, ws, rank, local, cpu_budget_s: float):
                    "out": [(torch.empty(n_rec, 6, dtype=torch.int32, device=dev),
                             torch.empty(n_rec, w.H, dtype=torch.bfloat16, device=dev),
                             torch.zeros(1, dtype=torch.int64, device=dev)) for _ in range(R)]}
-            launches_per_step += 2
+            # one launch while the selector table and the match list fit in shared memory
+            # (the library's choice), else a match and a copy launch
+            lg = 6
+            while (1 << lg) < 2 * len(b["sel_keys"]):
+                lg += 1
+            launches_per_step += 1 if (lg <= 13 and w.T <= 16384 and (8 << lg) + 4 * w.T <= 160 * 1024) else 2
 
         def capture(j, o):
             tl.capture_rows(cap["rq"], cap["rp"], cap["keys"], [o["mlp_out"], o["residual_stream"]], cap["types"],
@@ -750,102 +759,124 @@ def measure(args, w: workloads.Workload, ws, rank, local, cpu_budget_s: float):
 
     # ---- end to end through the public API from pinned host buffers. Every step copies its
     # inputs in and its results out; the copies run on two copy streams, ordered by events,
-    # so that step i's compute overlaps step i+1's input copy and step i-1's result copy
-    # (R buffer sets rotate; a set is refilled only after the compute and the read-back of
-    # its previous step).
+    # so that step i's compute overlaps step i+1's input copy and step i-1's result copy.
+    # E >= 3 sets of activation buffers rotate (a set is refilled only after the compute and
+    # the read-back of its previous step); the weights and workspaces rotate with R as in
+    # the timed region (steps run one after another on the compute stream, so set e uses
+    # weight copy e % R).
     K3 = min(K, 500 if decode else 10)
+    E = max(R, 3)
+
+    def extend(lst, make):
+        return list(lst) + [make() for _ in range(len(lst), E)]
     if w.kind == "mlp":
         # x and residual in one device buffer, the outputs in another: one copy each way
         names = list(outs[0].keys())
         n_in = 2 if rs[0] is not None else 1
-        din = [torch.empty((n_in, w.T, w.H), dtype=torch.bfloat16, device=dev) for _ in range(R)]
-        dout = [torch.empty((len(names), w.T, w.H), dtype=torch.bfloat16, device=dev) for _ in range(R)]
-        hin = [torch.stack([xs[j]] + ([rs[j]] if n_in == 2 else [])).cpu().pin_memory() for j in range(R)]
-        hout = [torch.empty(dout[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
-        eouts = [{k: dout[j][i] for i, k in enumerate(names)} for j in range(R)]
+        din = [torch.empty((n_in, w.T, w.H), dtype=torch.bfloat16, device=dev) for _ in range(E)]
+        dout = [torch.empty((len(names), w.T, w.H), dtype=torch.bfloat16, device=dev) for _ in range(E)]
+        hin = [torch.stack([xs[j % R]] + ([rs[j % R]] if n_in == 2 else [])).cpu().pin_memory() for j in range(E)]
+        hout = [torch.empty(dout[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(E)]
+        eouts = [{k: dout[j][i] for i, k in enumerate(names)} for j in range(E)]
         in_pairs = lambda j: [(hin[j], din[j])]
         if cap is None:
             out_pairs = lambda j: [(dout[j], hout[j])]
         else:
             # the captured records (headers and rows) come back with the block's outputs
+            ecap = extend(cap["out"], lambda: tuple(torch.empty_like(t) for t in cap["out"][0]))
             hcap = [(torch.empty(cap["out"][0][0].shape, dtype=torch.int32, pin_memory=True),
-                     torch.empty(cap["out"][0][1].shape, dtype=torch.bfloat16, pin_memory=True)) for _ in range(R)]
-            out_pairs = lambda j: [(dout[j], hout[j]), (cap["out"][j][0], hcap[j][0]), (cap["out"][j][1], hcap[j][1])]
+                     torch.empty(cap["out"][0][1].shape, dtype=torch.bfloat16, pin_memory=True)) for _ in range(E)]
+            out_pairs = lambda j: [(dout[j], hout[j]), (ecap[j][0], hcap[j][0]), (ecap[j][1], hcap[j][1])]
 
         def e2e_compute(j):
-            blocks[j].mlp_forward(din[j][0], residual=din[j][1] if n_in == 2 else None, out=eouts[j], ws=wss[j])
+            blocks[j % R].mlp_forward(din[j][0], residual=din[j][1] if n_in == 2 else None, out=eouts[j],
+                                      ws=wss[j % R])
             if cap is not None:
-                capture(j, eouts[j])
+                tl.capture_rows(cap["rq"], cap["rp"], cap["keys"], [eouts[j]["mlp_out"], eouts[j]["residual_stream"]],
+                                cap["types"], 0, cap["n"], ws=cap["ws"], out=ecap[j])
     elif w.kind == "paged":
-        hq = [qkvs[j].cpu().pin_memory() for j in range(R)]
-        ho = [torch.empty(aos[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
-        in_pairs = lambda j: [(hq[j], qkvs[j])]
-        out_pairs = lambda j: [(aos[j], ho[j])]
+        eq = extend(qkvs, lambda: torch.empty_like(qkvs[0]))
+        eo = extend(aos, lambda: torch.empty_like(aos[0]))
+        hq = [qkvs[j % R].cpu().pin_memory() for j in range(E)]
+        ho = [torch.empty(aos[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(E)]
+        in_pairs = lambda j: [(hq[j], eq[j])]
+        out_pairs = lambda j: [(eo[j], ho[j])]
 
         def e2e_compute(j):
-            ck, cv = caches[j]
-            blocks[0].paged_attention(qkvs[j], qsl, lens_d, tables_d, ck, cv, 1, max(lens), out=aos[j], ws=pws,
+            ck, cv = caches[j % R]
+            blocks[0].paged_attention(eq[j], qsl, lens_d, tables_d, ck, cv, 1, max(lens), out=eo[j], ws=pws,
                                       slot_mapping=new_slots)
     elif w.kind == "moe":
-        hx = [xs[j].cpu().pin_memory() for j in range(R)]
+        ex = extend(xs, lambda: torch.empty_like(xs[0]))
+        eo = extend(outs, lambda: torch.empty_like(outs[0]))
+        hx = [xs[j % R].cpu().pin_memory() for j in range(E)]
         hid = ids.cpu().pin_memory()
         hg = gts.cpu().pin_memory()
-        ho = [torch.empty(xs[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
-        eids = [ids.clone() for _ in range(R)]
-        egts = [gts.clone() for _ in range(R)]
-        in_pairs = lambda j: [(hx[j], xs[j]), (hid, eids[j]), (hg, egts[j])]
-        out_pairs = lambda j: [(outs[j], ho[j])]
+        ho = [torch.empty(xs[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(E)]
+        eids = [ids.clone() for _ in range(E)]
+        egts = [gts.clone() for _ in range(E)]
+        in_pairs = lambda j: [(hx[j], ex[j]), (hid, eids[j]), (hg, egts[j])]
+        out_pairs = lambda j: [(eo[j], ho[j])]
 
         def e2e_compute(j):
-            blocks[0].moe_forward(xs[j], eids[j], egts[j], out=outs[j], ws=wss[0])
+            blocks[0].moe_forward(ex[j], eids[j], egts[j], out=eo[j], ws=wss[0])
     elif w.kind == "layer":
-        hx = [xs[j].cpu().pin_memory() for j in range(R)]
-        hr = [rs[j].cpu().pin_memory() for j in range(R)]
+        ex = extend(xs, lambda: torch.empty_like(xs[0]))
+        er = extend(rs, lambda: torch.empty_like(rs[0]))
+        eo = extend(outs, lambda: {k: torch.empty_like(v) for k, v in outs[0].items()})
+        hx = [xs[j % R].cpu().pin_memory() for j in range(E)]
+        hr = [rs[j % R].cpu().pin_memory() for j in range(E)]
         # the layer's result as the next layer takes it: (hidden = mlp_out, residual = r2)
-        hm = [torch.empty(xs[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
-        hres = [torch.empty(xs[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
-        in_pairs = lambda j: [(hx[j], xs[j]), (hr[j], rs[j])]
-        out_pairs = lambda j: [(outs[j]["mlp_out"], hm[j]), (outs[j]["residual_mlp"], hres[j])]
+        hm = [torch.empty(xs[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(E)]
+        hres = [torch.empty(xs[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(E)]
+        in_pairs = lambda j: [(hx[j], ex[j]), (hr[j], er[j])]
+        out_pairs = lambda j: [(eo[j]["mlp_out"], hm[j]), (eo[j]["residual_mlp"], hres[j])]
 
         def e2e_compute(j):
-            layer.forward(xs[j], rs[j], cu, max_len, out=outs[j], ws=wss[0])
+            layer.forward(ex[j], er[j], cu, max_len, out=eo[j], ws=wss[0])
     elif w.kind == "attn_core":
-        hq = [qkvs[j].cpu().pin_memory() for j in range(R)]
-        ho = [torch.empty(aos[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
-        in_pairs = lambda j: [(hq[j], qkvs[j])]
-        out_pairs = lambda j: [(aos[j], ho[j])]
+        eq = extend(qkvs, lambda: torch.empty_like(qkvs[0]))
+        eo = extend(aos, lambda: torch.empty_like(aos[0]))
+        hq = [qkvs[j % R].cpu().pin_memory() for j in range(E)]
+        ho = [torch.empty(aos[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(E)]
+        in_pairs = lambda j: [(hq[j], eq[j])]
+        out_pairs = lambda j: [(eo[j], ho[j])]
 
         def e2e_compute(j):
-            blocks[0].attention_forward(qkvs[j], cu, max_len, out=aos[j], ws=wss[0])
+            blocks[0].attention_forward(eq[j], cu, max_len, out=eo[j], ws=wss[0])
     else:
-        hx = [xs[j].cpu().pin_memory() for j in range(R)]
-        hA = [As[j].cpu().pin_memory() for j in range(R)]
-        hq = [torch.empty(qkvs[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
-        hoo = [torch.empty(oos[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
-        in_pairs = lambda j: [(hx[j], xs[j]), (hA[j], As[j])]
-        out_pairs = lambda j: [(qkvs[j], hq[j]), (oos[j], hoo[j])]
+        ex = extend(xs, lambda: torch.empty_like(xs[0]))
+        eA = extend(As, lambda: torch.empty_like(As[0]))
+        eq = extend(qkvs, lambda: torch.empty_like(qkvs[0]))
+        eo = extend(oos, lambda: torch.empty_like(oos[0]))
+        hx = [xs[j % R].cpu().pin_memory() for j in range(E)]
+        hA = [As[j % R].cpu().pin_memory() for j in range(E)]
+        hq = [torch.empty(qkvs[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(E)]
+        hoo = [torch.empty(oos[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(E)]
+        in_pairs = lambda j: [(hx[j], ex[j]), (hA[j], eA[j])]
+        out_pairs = lambda j: [(eq[j], hq[j]), (eo[j], hoo[j])]
 
         def e2e_compute(j):
-            blocks[j].attn_proj_forward(xs[j], As[j], qkv_out=qkvs[j], o_out=oos[j], ws=wss[j])
+            blocks[j % R].attn_proj_forward(ex[j], eA[j], qkv_out=eq[j], o_out=eo[j], ws=wss[j % R])
     h2d = sum(hsrc.numel() * hsrc.element_size() for hsrc, _ in in_pairs(0))
     d2h = sum(hdst.numel() * hdst.element_size() for _, hdst in out_pairs(0))
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(R)]
-    ev_comp = [torch.cuda.Event() for _ in range(R)]
-    ev_out = [torch.cuda.Event() for _ in range(R)]
+    ev_in = [torch.cuda.Event() for _ in range(E)]
+    ev_comp = [torch.cuda.Event() for _ in range(E)]
+    ev_out = [torch.cuda.Event() for _ in range(E)]
 
     def e2e_run(n, start_ev=None):
         if start_ev is not None:
             s_in.wait_event(start_ev)           # no copy of the timed steps starts before the timer
         for i in range(n):
-            j = i % R
-            s_in.wait_event(ev_comp[j])         # the set's inputs were consumed by step i - R
+            j = i % E
+            s_in.wait_event(ev_comp[j])         # the set's inputs were consumed by step i - E
             with torch.cuda.stream(s_in):
                 for hsrc, ddst in in_pairs(j):
                     ddst.copy_(hsrc, non_blocking=True)
             ev_in[j].record(s_in)
             stream.wait_event(ev_in[j])
-            stream.wait_event(ev_out[j])        # the set's results were read back after step i - R
+            stream.wait_event(ev_out[j])        # the set's results were read back after step i - E
             e2e_compute(j)
             ev_comp[j].record(stream)
             s_out.wait_event(ev_comp[j])
