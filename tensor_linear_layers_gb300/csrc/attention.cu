@@ -271,17 +271,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Warp 6 issues S = Q K^T, warp 1 O += P V. Each shares its sub-partition with a
     // softmax warp, so every instruction saved keeps the tensor pipe fed: descriptors
     // are built once, a k-step adds a constant, ring positions advance without division.
+    // The whole warp runs the loop (waits, unit ids, descriptors) and one elected lane
+    // issues each group of MMAs with its commits: operands computed by a converged warp
+    // are warp-uniform, where computed under a branch on the lane index they are not,
+    // and each MMA then costs more to issue than its 64 cycles on the tensor pipe.
     // Ordering between the two goes through mbarriers: S_FULL (S done) -> softmax ->
     // PV_READY (P written, V in) -> P V -> S_READY (buffer free for the S three tiles
     // later, with its K).
-    if (lane == 0) {
+    {
       const bool s_role = warp == kSWarp;
       bool ok = true;
       auto wait = [&](int b, uint32_t ph) -> bool {
-        if (mbar_wait_bounded(bar(b), ph, s_abort, timeout)) return true;
-        set_abort();
-        ok = false;
-        return false;
+        bool w = mbar_wait_bounded(bar(b), ph, s_abort, timeout);
+        w = __all_sync(0xffffffffu, w);
+        if (!w) {
+          if (lane == 0) set_abort();
+          ok = false;
+        }
+        return w;
       };
       auto advance = [](int& i, uint32_t& ph, int n) {
         if (++i == n) {
@@ -302,7 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait(U_FULL + slot, (nu / kUnitSlots) & 1)) break;
         const int u = s_units[slot];
         const int4 pr = s_pair[slot];
-        mbar_arrive(bar(U_EMPTY + slot));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(U_EMPTY + slot));
         if (u < 0) break;
         const Unit x = decode_unit(p, u, pr);
         const int n = x.qt + 1;
@@ -314,15 +322,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint64_t kd = k_desc0 + (uint64_t)st * kTileDesc;
             const uint32_t d = tmem_base + buf * 128;
-            tc_mma_bf16_c<false>(d, q_desc, kd, kIdescS);
+            if (elect_one()) {
+              tc_mma_bf16_c<false>(d, q_desc, kd, kIdescS);
 #pragma unroll
-            for (int k = 1; k < 8; ++k) {
-              const uint64_t o = (uint64_t)(((k >> 2) * (kTileBytes / 2) + (k & 3) * 32) >> 4);
-              tc_mma_bf16_c<true>(d, q_desc + o, kd + o, kIdescS);
+              for (int k = 1; k < 8; ++k) {
+                const uint64_t o = (uint64_t)(((k >> 2) * (kTileBytes / 2) + (k & 3) * 32) >> 4);
+                tc_mma_bf16_c<true>(d, q_desc + o, kd + o, kIdescS);
+              }
+              tc_commit(bar(K_EMPTY + st));
+              tc_commit(bar(S_FULL + buf));
+              if (j == n - 1) tc_commit(bar(Q_EMPTY));
             }
-            tc_commit(bar(K_EMPTY + st));
-            tc_commit(bar(S_FULL + buf));
-            if (j == n - 1) tc_commit(bar(Q_EMPTY));
+            __syncwarp();
             advance(st, st_ph, kStages);
             advance(buf, buf_ph, kSBufs);
           }
@@ -333,29 +344,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint64_t vd = v_desc0 + (uint64_t)st * kTileDesc;
             const uint32_t pa = tmem_base + buf * 128;
-            // 16 keys = two 8-row groups of V (2048 B) and 8 columns of P
-            if (j == 0)
-              tc_mma_bf16_ta_c<false>(tmem_base + kOCol, pa, vd, kIdescO);
-            else
-              tc_mma_bf16_ta_c<true>(tmem_base + kOCol, pa, vd, kIdescO);
+            if (elect_one()) {
+              // 16 keys = two 8-row groups of V (2048 B) and 8 columns of P
+              if (j == 0)
+                tc_mma_bf16_ta_c<false>(tmem_base + kOCol, pa, vd, kIdescO);
+              else
+                tc_mma_bf16_ta_c<true>(tmem_base + kOCol, pa, vd, kIdescO);
 #pragma unroll
-            for (int k = 1; k < 8; ++k)
-              tc_mma_bf16_ta_c<true>(tmem_base + kOCol, pa + k * 8, vd + (uint64_t)(k * (2048 >> 4)), kIdescO);
-            tc_commit(bar(V_EMPTY + st));   // V consumed; O holds this tile (softmax rescale)
-            tc_commit(bar(S_READY + st));   // the buffer's P is consumed
+              for (int k = 1; k < 8; ++k)
+                tc_mma_bf16_ta_c<true>(tmem_base + kOCol, pa + k * 8, vd + (uint64_t)(k * (2048 >> 4)), kIdescO);
+              tc_commit(bar(V_EMPTY + st));   // V consumed; O holds this tile (softmax rescale)
+              tc_commit(bar(S_READY + st));   // the buffer's P is consumed
+              if (j == n - 1) tc_commit(bar(O_DONE));
+            }
+            __syncwarp();
             advance(st, st_ph, kStages);
             advance(buf, buf_ph, kSBufs);
           }
-          if (!ok) break;
-          tc_commit(bar(O_DONE));
         }
       }
-      // this thread's MMAs complete before tensor memory is released
+      // this warp's MMAs complete before tensor memory is released
       const int done = s_role ? DONE_S : DONE;
-      tc_commit(bar(done));
+      if (elect_one()) tc_commit(bar(done));
+      __syncwarp();
       mbar_wait_bounded(bar(done), 0, nullptr, kTeardownNs);
+      __syncwarp();
     }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     const int q4 = warp & 3;

@@ -440,6 +440,18 @@ constexpr uint32_t kIdescBMnMajor = 1u << 16;
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// True in exactly one active lane of a converged warp (PTX elect.sync). Code that
+// runs with the whole warp and issues from the elected lane keeps its operands
+// warp-uniform, which a branch on the lane index does not.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(e));
+  return e != 0;
+}
 __device__ __forceinline__ void griddep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
