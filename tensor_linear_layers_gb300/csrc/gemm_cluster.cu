@@ -220,7 +220,9 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
-    if (leader && lane == 0) {
+    // The whole warp runs the loop and one elected lane issues each k-block's MMAs
+    // with their commit, so descriptors and tensor-memory addresses stay warp-uniform.
+    if (leader) {
       int stage = 0;
       uint32_t phase = 0;
       int buf = 0;
@@ -235,15 +237,15 @@ __global__ void __launch_bounds__(192, 1)
         const GemmParams& q = second ? p2 : p;
         int kb_lo, kb_hi;
         krange(q, part, kb_lo, kb_hi);
-        if (!mbar_wait_bounded_cluster(tempty_bar(buf), acc_phase ^ 1u, s_abort, q.timeout_ns)) {
-          fail(q);
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(tempty_bar(buf), acc_phase ^ 1u, s_abort, q.timeout_ns))) {
+          if (lane == 0) fail(q);
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * P::kAccCols;
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
-          if (!mbar_wait_bounded(full_bar(stage), phase, s_abort, q.timeout_ns)) {
-            fail(q);
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(full_bar(stage), phase, s_abort, q.timeout_ns))) {
+            if (lane == 0) fail(q);
             ok = false;
             break;
           }
@@ -251,28 +253,35 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t sa = base + stage * P::kStageBytes;
           const uint64_t adesc = smem_desc_k128(sa);
           const uint64_t bdesc = smem_desc_k128(sa + P::kABytes);
-          if (kb == kb_lo)
-            tc_mma_bf16_pair<false>(d_tmem, adesc, bdesc, P::kIdesc);
-          else
-            tc_mma_bf16_pair<true>(d_tmem, adesc, bdesc, P::kIdesc);
+          if (elect_one()) {
+            if (kb == kb_lo)
+              tc_mma_bf16_pair<false>(d_tmem, adesc, bdesc, P::kIdesc);
+            else
+              tc_mma_bf16_pair<true>(d_tmem, adesc, bdesc, P::kIdesc);
 #pragma unroll
-          for (int ks = 1; ks < 4; ++ks)
-            tc_mma_bf16_pair<true>(d_tmem, adesc + (uint64_t)(ks * 2), bdesc + (uint64_t)(ks * 2), P::kIdesc);
-          tc_commit_pair_multicast(empty_bar(stage), kBoth);
+            for (int ks = 1; ks < 4; ++ks)
+              tc_mma_bf16_pair<true>(d_tmem, adesc + (uint64_t)(ks * 2), bdesc + (uint64_t)(ks * 2), P::kIdesc);
+            tc_commit_pair_multicast(empty_bar(stage), kBoth);
+          }
+          __syncwarp();
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit_pair_multicast(tfull_bar(buf), kBoth);
+        // elect.sync picks the same lane for the same mask, so this commit follows the
+        // MMAs above
+        if (elect_one()) tc_commit_pair_multicast(tfull_bar(buf), kBoth);
+        __syncwarp();
         if (++buf == 2) {
           buf = 0;
           acc_phase ^= 1u;
         }
       }
       // every issued MMA completes before either CTA frees tensor memory or exits
-      tc_commit_pair(done_bar);
+      if (elect_one()) tc_commit_pair(done_bar);
+      __syncwarp();
       mbar_wait_bounded(done_bar, 0, nullptr, kTeardownNs);
     }
     __syncwarp();
@@ -392,15 +401,16 @@ __global__ void __launch_bounds__(192, 1)
 
 // How a launch of pu pair units on `clusters` clusters splits its tail (see PairTail):
 // when the last wave would be at most half full, its units are split into
-// s = min(4, clusters / rem) parts. Grouped (expert) problems are not split.
-PairTail plan_pair_tail(int pu, int clusters, bool grouped, float* part, unsigned* cnt) {
+// s = min(4, clusters / rem, max_s) parts, max_s the fewest k-blocks of a problem (every
+// part keeps at least one). Grouped (expert) problems are not split.
+PairTail plan_pair_tail(int pu, int clusters, bool grouped, float* part, unsigned* cnt, int max_s) {
   PairTail t{};
   t.full = pu;
   t.s = 1;
   if (grouped || part == nullptr || cnt == nullptr || clusters < 2 || pu < 1) return t;
   const int waves = (pu + clusters - 1) / clusters;
   const int rem = pu - (waves - 1) * clusters;
-  const int s = std::min(4, clusters / rem);
+  const int s = std::min(std::min(4, clusters / rem), max_s);
   if (s < 2) return t;
   t.full = pu - rem;
   t.rem = rem;
@@ -414,7 +424,7 @@ PairTail plan_pair_tail(int pu, int clusters, bool grouped, float* part, unsigne
 // counting a split tail's parts as 1 / s of a unit.
 double pair_waves(int pu, int clusters) {
   if (clusters < 1 || pu < 1) return 0.0;
-  const PairTail t = plan_pair_tail(pu, clusters, false, reinterpret_cast<float*>(1), reinterpret_cast<unsigned*>(1));
+  const PairTail t = plan_pair_tail(pu, clusters, false, reinterpret_cast<float*>(1), reinterpret_cast<unsigned*>(1), 4);
   if (t.s < 2) return (double)((pu + clusters - 1) / clusters);
   return (double)(t.full / clusters) + 1.0 / t.s;
 }
@@ -436,7 +446,8 @@ cudaError_t launch_pair(const CUtensorMap& a1, const CUtensorMap& w1, const Gemm
     attr_done.fetch_or(bit, std::memory_order_acq_rel);
   }
   const int pu = ((p1.m_tiles + 1) / 2) * p1.n_tiles + (KIND2 >= 0 ? ((p2.m_tiles + 1) / 2) * p2.n_tiles : 0);
-  const PairTail tail = plan_pair_tail(pu, max_clusters, p1.pair_tiles != nullptr, tail_part, tail_cnt);
+  const int min_nkb = KIND2 >= 0 ? std::min(p1.nkb, p2.nkb) : p1.nkb;
+  const PairTail tail = plan_pair_tail(pu, max_clusters, p1.pair_tiles != nullptr, tail_part, tail_cnt, min_nkb);
   const int vunits = tail.s >= 2 ? tail.full + tail.rem * tail.s : pu;
   const int clusters = vunits < max_clusters ? vunits : max_clusters;
   cudaLaunchConfig_t cfg = {};

@@ -600,12 +600,21 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop and one elected lane issues each k-block's MMAs with
+    // their commit, so descriptors and tensor-memory addresses stay warp-uniform
+    // (elect.sync picks the same lane for the same mask: every commit follows the MMAs).
+    {
       int stage = 0;
       uint32_t phase = 0;
       int buf = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      auto timed_out = [&]() {
+        if (lane == 0 && !*s_abort) {
+          atomicExch(p.status, kStatusTimeout);
+          *s_abort = 1;
+        }
+      };
       for (int ug = blockIdx.x; ug < units_all && ok; ug += gridDim.x) {
         int tm, tn, sp;
         bool second;
@@ -614,21 +623,15 @@ __global__ void __launch_bounds__(192, 1)
         if (!SWAP && q.tile_expert != nullptr && tm >= *q.m_valid) continue;
         const int kb0 = (int)((long long)sp * q.nkb / q.splits);
         const int kb1 = (int)((long long)(sp + 1) * q.nkb / q.splits);
-        if (!mbar_wait_bounded(tempty_bar(buf), acc_phase ^ 1u, s_abort, p.timeout_ns)) {
-          if (!*s_abort) {
-            atomicExch(p.status, kStatusTimeout);
-            *s_abort = 1;
-          }
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(tempty_bar(buf), acc_phase ^ 1u, s_abort, p.timeout_ns))) {
+          timed_out();
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * S::kAccCols;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait_bounded(full_bar(stage), phase, s_abort, p.timeout_ns)) {
-            if (!*s_abort) {
-              atomicExch(p.status, kStatusTimeout);
-              *s_abort = 1;
-            }
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(full_bar(stage), phase, s_abort, p.timeout_ns))) {
+            timed_out();
             ok = false;
             break;
           }
@@ -637,29 +640,34 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t sb = sa + S::kABytes;
           const uint64_t adesc = smem_desc_k128(sa);
           const uint64_t bdesc = smem_desc_k128(sb);
+          if (elect_one()) {
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
+            for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
-            for (int a = 0; a < NA; ++a) {
-              tc_mma_bf16(d_tmem + a * BN, adesc + (uint64_t)(a * (128 * 128 >> 4) + ks * 2),
-                          bdesc + (uint64_t)(ks * 2), S::kIdesc, (kb > kb0 || ks > 0) ? 1u : 0u);
+              for (int a = 0; a < NA; ++a) {
+                tc_mma_bf16(d_tmem + a * BN, adesc + (uint64_t)(a * (128 * 128 >> 4) + ks * 2),
+                            bdesc + (uint64_t)(ks * 2), S::kIdesc, (kb > kb0 || ks > 0) ? 1u : 0u);
+              }
             }
+            tc_commit(empty_bar(stage));
           }
-          tc_commit(empty_bar(stage));
+          __syncwarp();
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(tfull_bar(buf));
+        if (elect_one()) tc_commit(tfull_bar(buf));
+        __syncwarp();
         if (++buf == 2) {
           buf = 0;
           acc_phase ^= 1u;
         }
       }
       // all issued MMAs complete before tensor memory is released
-      tc_commit(done_bar);
+      if (elect_one()) tc_commit(done_bar);
+      __syncwarp();
       mbar_wait_bounded(done_bar, 0, nullptr, kTeardownNs);
     }
     __syncwarp();

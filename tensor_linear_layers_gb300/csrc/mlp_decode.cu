@@ -420,39 +420,49 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop and one elected lane issues each k-block's MMAs with
+    // their commit, so descriptors and tensor-memory addresses stay warp-uniform
+    // (elect.sync picks the same lane for the same mask: every commit follows the MMAs).
+    {
       int stage = 0;
       uint32_t phase = 0;
       int buf = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      auto wait_all = [&](uint32_t b, uint32_t ph) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait_bounded(b, ph, s_abort, timeout));
+      };
       auto mma_unit = [&](int ph, int u) -> bool {
         const GemmParams& p = ph == 0 ? P.g1 : P.g2;
         int tm, kb0, kb1;
         krange(p, u, tm, kb0, kb1);
-        if (!mbar_wait_bounded(tempty_bar(buf), acc_phase ^ 1u, s_abort, timeout)) return false;
+        if (!wait_all(tempty_bar(buf), acc_phase ^ 1u)) return false;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * ACC;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait_bounded(full_bar(stage), phase, s_abort, timeout)) return false;
+          if (!wait_all(full_bar(stage), phase)) return false;
           tc_fence_after();
           const uint32_t sa = base + stage * S::kStageBytes;
           const uint64_t adesc = smem_desc_k128(sa);
           const uint64_t bdesc = smem_desc_k128(sa + S::kABytes);
+          if (elect_one()) {
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
+            for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
-            for (int a = 0; a < 2; ++a)
-              tc_mma_bf16(d_tmem + a * BN, adesc + (uint64_t)(a * (128 * 128 >> 4) + ks * 2),
-                          bdesc + (uint64_t)(ks * 2), S::kIdesc, (kb > kb0 || ks > 0) ? 1u : 0u);
+              for (int a = 0; a < 2; ++a)
+                tc_mma_bf16(d_tmem + a * BN, adesc + (uint64_t)(a * (128 * 128 >> 4) + ks * 2),
+                            bdesc + (uint64_t)(ks * 2), S::kIdesc, (kb > kb0 || ks > 0) ? 1u : 0u);
+            }
+            tc_commit(empty_bar(stage));
           }
-          tc_commit(empty_bar(stage));
+          __syncwarp();
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        tc_commit(tfull_bar(buf));
+        if (elect_one()) tc_commit(tfull_bar(buf));
+        __syncwarp();
         if (++buf == 2) {
           buf = 0;
           acc_phase ^= 1u;
@@ -463,12 +473,13 @@ __global__ void __launch_bounds__(192, 1)
       int uslot = 0;
       uint32_t uphase = 0;
       while (ok) {
-        if (!mbar_wait_bounded(ufull0 + 8u * uslot, uphase, s_abort, timeout)) {
+        if (!wait_all(ufull0 + 8u * uslot, uphase)) {
           ok = false;
           break;
         }
         const int u = s_unit[uslot];
-        mbar_arrive(uempty0 + 8u * uslot);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(uempty0 + 8u * uslot);
         if (++uslot == kUnitSlots) {
           uslot = 0;
           uphase ^= 1u;
@@ -476,8 +487,9 @@ __global__ void __launch_bounds__(192, 1)
         if (u < 0) break;
         ok = mma_unit(1, u);
       }
-      if (!ok) set_abort();
-      tc_commit(done_bar);
+      if (!ok && lane == 0) set_abort();
+      if (elect_one()) tc_commit(done_bar);
+      __syncwarp();
       mbar_wait_bounded(done_bar, 0, nullptr, kTeardownNs);
     }
     __syncwarp();
