@@ -15,19 +15,25 @@
 //            run side by side and share its K/V tiles in L2
 //   warp 0   TMA: the Q tile (two 64-column boxes, 128-byte swizzle), then
 //            K and V tiles of 128 keys into a 3-stage ring
-//   warp 6   tcgen05.mma: S = Q K^T into one of three tensor-memory buffers,
+//   warp 2   tcgen05.mma: S = Q K^T into one of three tensor-memory buffers,
 //            up to three key tiles ahead of O += P V
 //   warp 1   tcgen05.mma: O += P V, once the softmax has written P. P is written by the softmax into
 //            the buffer its S came from (bf16 pairs, the tensor-memory A
 //            operand), so P never passes through shared memory; V is read
 //            MN-major straight from its [key][hd] tile. A buffer is reused
 //            once the P V that read it has completed
-//   warps 2-5 softmax, one query row per thread: the row of S from tensor
+//   warps 4-7 softmax, one query row per thread: the row of S from tensor
 //            memory, causal / sequence-end mask, running max and sum in the
 //            exp2 domain, P = 2^(s*c - m) as bf16 back into tensor memory. O
 //            is rescaled in tensor memory only when the row max grows by more
 //            than 2^8 (until then the stale max keeps every p <= 256); at the
-//            end O / l goes to global memory as bf16
+//            end of a unit the row sum l goes to the epilogue warps through
+//            shared memory and the next unit starts at once
+//   warps 8-11 epilogue: once the unit's last P V has completed, O out of tensor
+//            memory (the buffer is released at once), O / l to global memory as
+//            bf16, while the softmax warps work on the next unit
+//   warp 3   idle; warps 0-3 run on 56 registers, the softmax warps on 232 and
+//            the epilogue warps on 216
 //
 // Every wait is bounded (status word TP_ERR_TIMEOUT on timeout).
 #include <cuda_bf16.h>
@@ -50,10 +56,16 @@ constexpr int kKOff = kTileBytes;
 constexpr int kVOff = kKOff + kStages * kTileBytes;
 constexpr int kBarOff = kVOff + kStages * kTileBytes;
 constexpr int kBarBytes = 512;
-constexpr int kAttnSmem = 1024 + kBarOff + kBarBytes;
+// row sums from the softmax to the epilogue warps: [2 units in flight][128 rows] fp32
+constexpr int kLOff = kBarOff + kBarBytes;
+constexpr int kAttnSmem = 1024 + kLOff + 2 * 128 * 4;
+static_assert(kAttnSmem <= 232448, "shared memory of one CTA");
 constexpr int kUnitSlots = 4;                // units the producer may hand out ahead of the consumers
-constexpr int kSWarp = 6;                    // issues the S = Q K^T MMAs (warp 1 issues P V)
-constexpr int kThreads = 32 * (kSWarp + 1);
+constexpr int kSWarp = 2;                    // issues the S = Q K^T MMAs (warp 1 issues P V)
+constexpr int kThreads = 384;                // three warpgroups: copies and MMAs, softmax, epilogue
+constexpr int kOtherRegs = 56, kSoftRegs = 232, kEpiRegs = 216;
+static_assert(128 * (kOtherRegs + kSoftRegs + kEpiRegs) <= kThreads * 168,
+              "register split within the launch's 168 a thread");
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128);
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 128) | kIdescBMnMajor;
 constexpr int kTmemCols = 512;               // S/P buffers [0,128) [128,256) [256,384), O [384,512)
@@ -72,8 +84,10 @@ enum {
   S_FULL = V_EMPTY + kStages,      // S of a buffer computed
   O_DONE = S_FULL + kSBufs, O_EMPTY, DONE, DONE_S,
   U_FULL,                          // a unit id published by the producer
-  U_EMPTY = U_FULL + kUnitSlots,   // read by the two MMA threads and the four softmax warps
-  NBARS = U_EMPTY + kUnitSlots
+  U_EMPTY = U_FULL + kUnitSlots,   // read by the two MMA warps, the softmax and the epilogue warps
+  L_FULL = U_EMPTY + kUnitSlots,   // a unit's row sums written (per unit parity)
+  L_EMPTY = L_FULL + 2,            // and read by the epilogue warps
+  NBARS = L_EMPTY + 2
 };
 // barriers, tensor-memory address and abort flag, unit ids, then (16-byte aligned) their entries
 static_assert(8 * NBARS + 8 + 4 * kUnitSlots + 15 + 16 * kUnitSlots <= kBarBytes, "barrier area");
@@ -172,8 +186,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int b = 0; b < NBARS; ++b) {
       int count = 1;
-      if (b == O_EMPTY) count = 4;                          // the four softmax warps
-      if (b >= U_EMPTY) count = 6;                          // and the two MMA threads
+      if (b == O_EMPTY) count = 4;                          // the four epilogue warps
+      if (b >= U_EMPTY && b < U_EMPTY + kUnitSlots) count = 10;  // 2 MMA, 4 softmax, 4 epilogue warps
+      if (b >= L_FULL) count = 4;                           // the four softmax / epilogue warps
       if (b >= S_READY && b < S_READY + kStages) count = 2;  // producer + P V commit
       if (b >= PV_READY && b < PV_READY + kStages) count = 5;  // producer + four softmax warps
       mbar_init(bar(b), count);
@@ -204,178 +219,186 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_normal();
-      uint32_t full_mask = 0, full_phase = 0;  // bit b: barrier b has a copy in flight, its phase
-      auto issued = [&](int b, uint32_t ph) {
-        full_mask |= 1u << b;
-        full_phase = (full_phase & ~(1u << b)) | (ph << b);
-      };
-      auto load_tile = [&](uint32_t dst, int b, int col, int row, int r) {
-        mbar_arrive_expect_tx(bar(b), kTileBytes);
-        tma_load_4d(dst, &map_qkv, bar(b), col, row, r, 0, pol);
-        tma_load_4d(dst + kTileBytes / 2, &map_qkv, bar(b), col + 64, row, r, 0, pol);
-      };
-      bool ok = true;
-      int kv = 0;
-      for (int nu = 0; ok; ++nu) {
-        const int slot = nu % kUnitSlots;
-        if (!mbar_wait_bounded(bar(U_EMPTY + slot), ((nu / kUnitSlots) & 1) ^ 1, s_abort, timeout)) {
-          ok = false;
-          break;
-        }
-        int u = atomicAdd(p.next_unit, 1);
-        if (u >= n_units) u = -1;
-        s_units[slot] = u;
-        const int4 pr = u >= 0 ? p.pairs[u / p.heads] : make_int4(0, 0, 0, 0);
-        s_pair[slot] = pr;
-        mbar_arrive(bar(U_FULL + slot));  // releases the id and its entry to the consumers
-        if (u < 0) break;
-        const Unit x = decode_unit(p, u, pr);
-        if (!mbar_wait_bounded(bar(Q_EMPTY), (nu & 1) ^ 1, s_abort, timeout)) {
-          ok = false;
-          break;
-        }
-        load_tile(base + kQOff, Q_FULL, x.i * 128, x.start + x.qt * 128, x.r);
-        issued(Q_FULL, nu & 1);
-        const int kcol = (p.q_per + x.g) * 128, vcol = (p.q_per + p.kv_per + x.g) * 128;
-        for (int kt = 0; kt <= x.qt; ++kt, ++kv) {
-          const int st = kv % kStages;
-          const uint32_t ph = (kv / kStages) & 1;
-          if (!mbar_wait_bounded(bar(K_EMPTY + st), ph ^ 1, s_abort, timeout)) {
+  if (warp < 4) {
+    // copies and MMAs (warp 3 idle) on few registers, so that the softmax and epilogue
+    // warps can have more; each budget is set by a whole warpgroup and governs the
+    // code it dominates
+    regs_dec<kOtherRegs>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        const uint64_t pol = policy_evict_normal();
+        uint32_t full_mask = 0, full_phase = 0;  // bit b: barrier b has a copy in flight, its phase
+        auto issued = [&](int b, uint32_t ph) {
+          full_mask |= 1u << b;
+          full_phase = (full_phase & ~(1u << b)) | (ph << b);
+        };
+        auto load_tile = [&](uint32_t dst, int b, int col, int row, int r) {
+          mbar_arrive_expect_tx(bar(b), kTileBytes);
+          tma_load_4d(dst, &map_qkv, bar(b), col, row, r, 0, pol);
+          tma_load_4d(dst + kTileBytes / 2, &map_qkv, bar(b), col + 64, row, r, 0, pol);
+        };
+        bool ok = true;
+        int kv = 0;
+        for (int nu = 0; ok; ++nu) {
+          const int slot = nu % kUnitSlots;
+          if (!mbar_wait_bounded(bar(U_EMPTY + slot), ((nu / kUnitSlots) & 1) ^ 1, s_abort, timeout)) {
             ok = false;
             break;
           }
-          load_tile(base + kKOff + st * kTileBytes, S_READY + st, kcol, x.start + kt * 128, x.r);
-          issued(S_READY + st, ph);
-          if (!mbar_wait_bounded(bar(V_EMPTY + st), ph ^ 1, s_abort, timeout)) {
+          int u = atomicAdd(p.next_unit, 1);
+          if (u >= n_units) u = -1;
+          s_units[slot] = u;
+          const int4 pr = u >= 0 ? p.pairs[u / p.heads] : make_int4(0, 0, 0, 0);
+          s_pair[slot] = pr;
+          mbar_arrive(bar(U_FULL + slot));  // releases the id and its entry to the consumers
+          if (u < 0) break;
+          const Unit x = decode_unit(p, u, pr);
+          if (!mbar_wait_bounded(bar(Q_EMPTY), (nu & 1) ^ 1, s_abort, timeout)) {
             ok = false;
             break;
           }
-          load_tile(base + kVOff + st * kTileBytes, PV_READY + st, vcol, x.start + kt * 128, x.r);
-          issued(PV_READY + st, ph);
+          load_tile(base + kQOff, Q_FULL, x.i * 128, x.start + x.qt * 128, x.r);
+          issued(Q_FULL, nu & 1);
+          const int kcol = (p.q_per + x.g) * 128, vcol = (p.q_per + p.kv_per + x.g) * 128;
+          for (int kt = 0; kt <= x.qt; ++kt, ++kv) {
+            const int st = kv % kStages;
+            const uint32_t ph = (kv / kStages) & 1;
+            if (!mbar_wait_bounded(bar(K_EMPTY + st), ph ^ 1, s_abort, timeout)) {
+              ok = false;
+              break;
+            }
+            load_tile(base + kKOff + st * kTileBytes, S_READY + st, kcol, x.start + kt * 128, x.r);
+            issued(S_READY + st, ph);
+            if (!mbar_wait_bounded(bar(V_EMPTY + st), ph ^ 1, s_abort, timeout)) {
+              ok = false;
+              break;
+            }
+            load_tile(base + kVOff + st * kTileBytes, PV_READY + st, vcol, x.start + kt * 128, x.r);
+            issued(PV_READY + st, ph);
+          }
+        }
+        if (!ok) {
+          set_abort();
+          // no copy into this CTA's shared memory may outlive it
+          for (int b = 0; b < S_FULL; ++b)
+            if (full_mask & (1u << b)) mbar_wait_bounded(bar(b), (full_phase >> b) & 1u, nullptr, kTeardownNs);
         }
       }
-      if (!ok) {
-        set_abort();
-        // no copy into this CTA's shared memory may outlive it
-        for (int b = 0; b < S_FULL; ++b)
-          if (full_mask & (1u << b)) mbar_wait_bounded(bar(b), (full_phase >> b) & 1u, nullptr, kTeardownNs);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1 || warp == kSWarp) {
-    // ------------------------------------------------------------ MMA issuers
-    // Warp 6 issues S = Q K^T, warp 1 O += P V. Each shares its sub-partition with a
-    // softmax warp, so every instruction saved keeps the tensor pipe fed: descriptors
-    // are built once, a k-step adds a constant, ring positions advance without division.
-    // The whole warp runs the loop (waits, unit ids, descriptors) and one elected lane
-    // issues each group of MMAs with its commits: operands computed by a converged warp
-    // are warp-uniform, where computed under a branch on the lane index they are not,
-    // and each MMA then costs more to issue than its 64 cycles on the tensor pipe.
-    // Ordering between the two goes through mbarriers: S_FULL (S done) -> softmax ->
-    // PV_READY (P written, V in) -> P V -> S_READY (buffer free for the S three tiles
-    // later, with its K).
-    {
-      const bool s_role = warp == kSWarp;
-      bool ok = true;
-      auto wait = [&](int b, uint32_t ph) -> bool {
-        bool w = mbar_wait_bounded(bar(b), ph, s_abort, timeout);
-        w = __all_sync(0xffffffffu, w);
-        if (!w) {
-          if (lane == 0) set_abort();
-          ok = false;
-        }
-        return w;
-      };
-      auto advance = [](int& i, uint32_t& ph, int n) {
-        if (++i == n) {
-          i = 0;
-          ph ^= 1u;
-        }
-      };
-      // stage i's descriptor is stage 0's plus i tiles in the address field (address >> 4,
-      // 14 bits; every shared address here is below 256 KB, so the field never carries)
-      constexpr uint64_t kTileDesc = kTileBytes >> 4;
-      const uint64_t q_desc = smem_desc_k128(base + kQOff);
-      const uint64_t k_desc0 = smem_desc_k128(base + kKOff);
-      const uint64_t v_desc0 = smem_desc_mn128(base + kVOff, kTileBytes / 2);
-      int st = 0, buf = 0;        // K/V stage and S/P buffer of the next MMA group
-      uint32_t st_ph = 0, buf_ph = 0;
-      for (int nu = 0; ok; ++nu) {
-        const int slot = nu % kUnitSlots;
-        if (!wait(U_FULL + slot, (nu / kUnitSlots) & 1)) break;
-        const int u = s_units[slot];
-        const int4 pr = s_pair[slot];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(U_EMPTY + slot));
-        if (u < 0) break;
-        const Unit x = decode_unit(p, u, pr);
-        const int n = x.qt + 1;
-        if (s_role) {
-          if (!wait(Q_FULL, nu & 1)) break;
-          for (int j = 0; j < n; ++j) {
-            // K is in and the P V that last read this buffer has completed
-            if (!wait(S_READY + st, st_ph)) break;
-            tc_fence_after();
-            const uint64_t kd = k_desc0 + (uint64_t)st * kTileDesc;
-            const uint32_t d = tmem_base + buf * 128;
-            if (elect_one()) {
-              tc_mma_bf16_c<false>(d, q_desc, kd, kIdescS);
-#pragma unroll
-              for (int k = 1; k < 8; ++k) {
-                const uint64_t o = (uint64_t)(((k >> 2) * (kTileBytes / 2) + (k & 3) * 32) >> 4);
-                tc_mma_bf16_c<true>(d, q_desc + o, kd + o, kIdescS);
+      __syncwarp();
+    } else if (warp == 1 || warp == kSWarp) {
+      // ------------------------------------------------------------ MMA issuers
+      // Warp 2 issues S = Q K^T, warp 1 O += P V. Each shares its sub-partition with a
+      // softmax warp, so every instruction saved keeps the tensor pipe fed: descriptors
+      // are built once, a k-step adds a constant, ring positions advance without division.
+      // The whole warp runs the loop (waits, unit ids, descriptors) and one elected lane
+      // issues each group of MMAs with its commits: operands computed by a converged warp
+      // are warp-uniform, where computed under a branch on the lane index they are not,
+      // and each MMA then costs more to issue than its 64 cycles on the tensor pipe.
+      // Ordering between the two goes through mbarriers: S_FULL (S done) -> softmax ->
+      // PV_READY (P written, V in) -> P V -> S_READY (buffer free for the S three tiles
+      // later, with its K).
+      {
+        const bool s_role = warp == kSWarp;
+        bool ok = true;
+        auto wait = [&](int b, uint32_t ph) -> bool {
+          bool w = mbar_wait_bounded(bar(b), ph, s_abort, timeout);
+          w = __all_sync(0xffffffffu, w);
+          if (!w) {
+            if (lane == 0) set_abort();
+            ok = false;
+          }
+          return w;
+        };
+        auto advance = [](int& i, uint32_t& ph, int n) {
+          if (++i == n) {
+            i = 0;
+            ph ^= 1u;
+          }
+        };
+        // stage i's descriptor is stage 0's plus i tiles in the address field (address >> 4,
+        // 14 bits; every shared address here is below 256 KB, so the field never carries)
+        constexpr uint64_t kTileDesc = kTileBytes >> 4;
+        const uint64_t q_desc = smem_desc_k128(base + kQOff);
+        const uint64_t k_desc0 = smem_desc_k128(base + kKOff);
+        const uint64_t v_desc0 = smem_desc_mn128(base + kVOff, kTileBytes / 2);
+        int st = 0, buf = 0;        // K/V stage and S/P buffer of the next MMA group
+        uint32_t st_ph = 0, buf_ph = 0;
+        for (int nu = 0; ok; ++nu) {
+          const int slot = nu % kUnitSlots;
+          if (!wait(U_FULL + slot, (nu / kUnitSlots) & 1)) break;
+          const int u = s_units[slot];
+          const int4 pr = s_pair[slot];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(U_EMPTY + slot));
+          if (u < 0) break;
+          const Unit x = decode_unit(p, u, pr);
+          const int n = x.qt + 1;
+          if (s_role) {
+            if (!wait(Q_FULL, nu & 1)) break;
+            for (int j = 0; j < n; ++j) {
+              // K is in and the P V that last read this buffer has completed
+              if (!wait(S_READY + st, st_ph)) break;
+              tc_fence_after();
+              const uint64_t kd = k_desc0 + (uint64_t)st * kTileDesc;
+              const uint32_t d = tmem_base + buf * 128;
+              if (elect_one()) {
+                tc_mma_bf16_c<false>(d, q_desc, kd, kIdescS);
+  #pragma unroll
+                for (int k = 1; k < 8; ++k) {
+                  const uint64_t o = (uint64_t)(((k >> 2) * (kTileBytes / 2) + (k & 3) * 32) >> 4);
+                  tc_mma_bf16_c<true>(d, q_desc + o, kd + o, kIdescS);
+                }
+                tc_commit(bar(K_EMPTY + st));
+                tc_commit(bar(S_FULL + buf));
+                if (j == n - 1) tc_commit(bar(Q_EMPTY));
               }
-              tc_commit(bar(K_EMPTY + st));
-              tc_commit(bar(S_FULL + buf));
-              if (j == n - 1) tc_commit(bar(Q_EMPTY));
+              __syncwarp();
+              advance(st, st_ph, kStages);
+              advance(buf, buf_ph, kSBufs);
             }
-            __syncwarp();
-            advance(st, st_ph, kStages);
-            advance(buf, buf_ph, kSBufs);
-          }
-        } else {
-          for (int j = 0; j < n; ++j) {
-            if (!wait(PV_READY + st, st_ph)) break;  // V is in and P written
-            if (j == 0 && !wait(O_EMPTY, (nu & 1) ^ 1)) break;
-            tc_fence_after();
-            const uint64_t vd = v_desc0 + (uint64_t)st * kTileDesc;
-            const uint32_t pa = tmem_base + buf * 128;
-            if (elect_one()) {
-              // 16 keys = two 8-row groups of V (2048 B) and 8 columns of P
-              if (j == 0)
-                tc_mma_bf16_ta_c<false>(tmem_base + kOCol, pa, vd, kIdescO);
-              else
-                tc_mma_bf16_ta_c<true>(tmem_base + kOCol, pa, vd, kIdescO);
-#pragma unroll
-              for (int k = 1; k < 8; ++k)
-                tc_mma_bf16_ta_c<true>(tmem_base + kOCol, pa + k * 8, vd + (uint64_t)(k * (2048 >> 4)), kIdescO);
-              tc_commit(bar(V_EMPTY + st));   // V consumed; O holds this tile (softmax rescale)
-              tc_commit(bar(S_READY + st));   // the buffer's P is consumed
-              if (j == n - 1) tc_commit(bar(O_DONE));
+          } else {
+            for (int j = 0; j < n; ++j) {
+              if (!wait(PV_READY + st, st_ph)) break;  // V is in and P written
+              if (j == 0 && !wait(O_EMPTY, (nu & 1) ^ 1)) break;
+              tc_fence_after();
+              const uint64_t vd = v_desc0 + (uint64_t)st * kTileDesc;
+              const uint32_t pa = tmem_base + buf * 128;
+              if (elect_one()) {
+                // 16 keys = two 8-row groups of V (2048 B) and 8 columns of P
+                if (j == 0)
+                  tc_mma_bf16_ta_c<false>(tmem_base + kOCol, pa, vd, kIdescO);
+                else
+                  tc_mma_bf16_ta_c<true>(tmem_base + kOCol, pa, vd, kIdescO);
+  #pragma unroll
+                for (int k = 1; k < 8; ++k)
+                  tc_mma_bf16_ta_c<true>(tmem_base + kOCol, pa + k * 8, vd + (uint64_t)(k * (2048 >> 4)), kIdescO);
+                tc_commit(bar(V_EMPTY + st));   // V consumed; O holds this tile (softmax rescale)
+                tc_commit(bar(S_READY + st));   // the buffer's P is consumed
+                if (j == n - 1) tc_commit(bar(O_DONE));
+              }
+              __syncwarp();
+              advance(st, st_ph, kStages);
+              advance(buf, buf_ph, kSBufs);
             }
-            __syncwarp();
-            advance(st, st_ph, kStages);
-            advance(buf, buf_ph, kSBufs);
           }
         }
+        // this warp's MMAs complete before tensor memory is released
+        const int done = s_role ? DONE_S : DONE;
+        if (elect_one()) tc_commit(bar(done));
+        __syncwarp();
+        mbar_wait_bounded(bar(done), 0, nullptr, kTeardownNs);
+        __syncwarp();
       }
-      // this warp's MMAs complete before tensor memory is released
-      const int done = s_role ? DONE_S : DONE;
-      if (elect_one()) tc_commit(bar(done));
-      __syncwarp();
-      mbar_wait_bounded(bar(done), 0, nullptr, kTeardownNs);
-      __syncwarp();
     }
-  } else {
-    // ------------------------------------------------------------ softmax + epilogue
+  } else if (warp < 8) {
+    regs_inc<kSoftRegs>();
+    // ------------------------------------------------------------ softmax
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;  // query row of the tile = tensor-memory lane
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16);
     const float c = p.scale_log2;
+    float* xl = reinterpret_cast<float*>(base_ptr + kLOff);
     int sc = 0;  // S tiles consumed (= P tiles produced)
     bool ok = true;
     auto wait_all = [&](int b, uint32_t ph) -> bool {
@@ -481,7 +504,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(PV_READY + b));
         ++sc;
       }
-      if (!ok || !wait_all(O_DONE, nu & 1)) break;
+      if (!ok) break;
+      // the row sums go to the epilogue warps; the next unit starts at once
+      const int lp = nu & 1;
+      if (!wait_all(L_EMPTY + lp, ((nu >> 1) & 1) ^ 1)) break;
+      xl[lp * 128 + row] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L_FULL + lp));
+    }
+  } else {
+    regs_inc<kEpiRegs>();
+    // ------------------------------------------------------------ epilogue
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;  // query row of the tile = tensor-memory lane
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16);
+    const float* xl = reinterpret_cast<const float*>(base_ptr + kLOff);
+    bool ok = true;
+    auto wait_all = [&](int b, uint32_t ph) -> bool {
+      bool w = mbar_wait_bounded(bar(b), ph, s_abort, timeout);
+      w = __all_sync(0xffffffffu, w);
+      if (!w) {
+        if (lane == 0) set_abort();
+        ok = false;
+      }
+      return w;
+    };
+    float s[128];
+    for (int nu = 0; ok; ++nu) {
+      const int slot = nu % kUnitSlots;
+      if (!wait_all(U_FULL + slot, (nu / kUnitSlots) & 1)) break;
+      const int u = s_units[slot];
+      const int4 pr = s_pair[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(U_EMPTY + slot));
+      if (u < 0) break;
+      const Unit x = decode_unit(p, u, pr);
+      const int q_rel = x.qt * 128 + row;
+      const int lp = nu & 1;
+      if (!wait_all(L_FULL + lp, (nu >> 1) & 1)) break;
+      const float l = xl[lp * 128 + row];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L_EMPTY + lp));
+      if (!wait_all(O_DONE, nu & 1)) break;
       tc_fence_after();
       const float inv = 1.0f / l;
       __nv_bfloat16* dst = p.out + (size_t)x.r * p.out_sstride + (size_t)(x.start + q_rel) * p.out_rstride + x.i * 128;
