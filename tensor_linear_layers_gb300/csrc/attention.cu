@@ -631,6 +631,12 @@ cudaError_t launch_attention(const CUtensorMap& map_qkv, const AttnParams& p, co
   if (!(attr_done.load(std::memory_order_acquire) & bit)) {
     e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
     if (e != cudaSuccess) return e;
+    // The warpgroups' register budgets (setmaxnreg) come out of the registers the CTA is
+    // launched with; were the kernel built with fewer, an increase would wait forever.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, attn_fwd_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * kThreads < 128 * (kOtherRegs + kSoftRegs + kEpiRegs)) return cudaErrorInvalidConfiguration;
     attr_done.fetch_or(bit, std::memory_order_acq_rel);
   }
   cudaLaunchConfig_t cfg = {};
