@@ -115,6 +115,21 @@ def test_prefill_tails_on_cta_pairs_every_row(T):
     assert status_of(blk.workspace(T)) == 0
 
 
+@pytest.mark.parametrize("H,T", [(128, 256), (128, 300), (192, 256)])
+def test_prefill_split_tail_never_exceeds_k_blocks(H, T):
+    # gate_up's K is H: 2 or 3 k-blocks of 64. Its 4 pair units (2I = 1024 weight rows)
+    # fill a small part of one wave, so the wave is split along K, into at most as many
+    # parts as there are k-blocks: a part with an empty K range would hand its stale
+    # accumulator to the reduction. Every row of the output is compared.
+    blk, d = make_mlp(H, 512, 1)
+    assert blk.plan(T)[0]["engine"] == 1
+    a = workloads.draw((T, H), 17, 0)
+    out = blk.mlp_forward(a.cuda())
+    ref = mlp_ref(d, a)
+    assert rel_err(out["mlp_out"], ref["mlp_out"]) <= TOL
+    assert status_of(blk.workspace(T)) == 0
+
+
 @pytest.mark.parametrize("T", [1300, 1421])
 def test_attention_projections_tails_on_cta_pairs_every_row(T):
     # QKV and o_proj in one CTA-pair launch, odd and even tile counts with partial tiles
